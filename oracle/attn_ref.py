@@ -1,0 +1,382 @@
+"""Float64 CPU oracle for fused scaled-dot-product attention, forward and backward.
+
+TEST INFRASTRUCTURE ONLY.  This module is the correctness reference for the
+CUDA library in ``bwd_tcgen05_tma_gb300``.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline / reference arm of
+``bench.py`` may import it.  The product path never calls it, and it shares no
+code, helper, table or constant with the CUDA path.
+
+What it computes (all in float64 on bf16-valued inputs):
+
+* Layout resolution: the packed-QKV ("3HD"), packed-KV ("HD_2HD") and separate
+  ("HD_HD_HD") layouts, where the K and V slices of a packed buffer start one
+  and two head-blocks after Q, and the V slice of a packed KV buffer is offset
+  by ``num_gqa_groups * v_head_dim`` elements (TransformerEngine PR #2358 "[JAX]
+  Make all jax attention calls use non-packed common calls": the pointer
+  arithmetic sequence diagram and the review of the KV-packed stride).
+* Segment metadata: segment ids with 0 meaning padding, segment positions that
+  restart in each segment and may be derived from the ids
+  (TransformerEngine PR #2692 "[JAX] Fix batcher in FusedAttn primitive for
+  when seg ids bdims != seg pos bdims", Description), or ragged offsets
+  (cu_seqlens).
+* The attention itself, as the plain definition.  For batch b, query head h
+  with KV head g = h // (Hq // Hkv), query i and key j::
+
+      valid(i, j) = id_q[i] == id_kv[j] != 0  and (not causal or pos_kv[j] <= pos_q[i])
+      S_ij   = scale * <Q_i, K_j> + bias_ij          over valid pairs, -inf elsewhere
+      P_ij   = exp(S_ij - m_i) / l_i,  m_i = max_j S_ij,  l_i = sum_j exp(S_ij - m_i)
+      O_i    = sum_j P_ij V_j,  LSE_i = m_i + ln l_i    (O_i = 0, LSE_i = -inf if no valid j)
+
+  and the closed-form backward for a given dO::
+
+      dP_ij = <dO_i, V_j>,  D_i = sum_j P_ij dP_ij,  dS_ij = P_ij (dP_ij - D_i)
+      dQ_i  = scale * sum_j dS_ij K_j
+      dK_j  = scale * sum_{h in group(g)} sum_i dS_ij Q_i
+      dV_j  = sum_{h in group(g)} sum_i P_ij dO_i
+      dBias = dS summed over every axis the bias is broadcast along
+
+  The outputs and gradient set follow the fused-attention backward diagram of
+  TransformerEngine PR #3516 "[JAX] Align fused attn backward output gradient
+  sharding and other test strengthening" (saved O plus incoming dO give the
+  Q/K/V and optional bias gradients); Q and KV metadata may differ (same page,
+  Changes 3-4); gradients of a KV head sum over the query heads that share it
+  (maxdiffusion PR #485, Summary: dK/dV held across Q blocks and GQA heads);
+  the bias gradient is reduced over its broadcast axes (PR #3516, Change 6).
+
+Rows are processed one block of queries at a time and each block only touches
+the keys that are valid for at least one of its rows; since every softmax row is
+independent and masked keys contribute exactly zero, this is still the plain
+definition, not a reformulation.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+LAYOUTS = ("3HD", "HD_2HD", "HD_HD_HD")
+
+# --------------------------------------------------------------------------
+# Layout resolution
+# --------------------------------------------------------------------------
+
+
+def unpack_layout(layout, buffers, B, Sq, Skv, Hq, Hkv, d_qk, d_v):
+    """Return float64 views Q [B,Sq,Hq,d_qk], K [B,Skv,Hkv,d_qk], V [B,Skv,Hkv,d_v].
+
+    ``buffers`` holds the raw token-major arrays of the layout:
+
+    * "3HD":      {"qkv": [B*Sq, Hq*d_qk + Hkv*d_qk + Hkv*d_v]} -- each token row
+      packs the Q heads, then the K heads, then the V heads.  With Hq == Hkv and
+      d_qk == d_v this is the [T, 3, H, D] packing with K one head-block and V
+      two head-blocks after Q (PR #2358, pointer arithmetic for NVTE_3HD).
+      Requires Sq == Skv (PR #2358, the q_max_seqlen == kv_max_seqlen check).
+    * "HD_2HD":   {"q": [B*Sq, Hq*d_qk], "kv": [B*Skv, 2, Hkv, d_v]} -- the V
+      slice starts Hkv*d_v elements after the K slice (PR #2358, KV-packed stride
+      review); requires d_qk == d_v.
+    * "HD_HD_HD": {"q": ..., "k": ..., "v": ...} separate arrays.
+    """
+    if layout == "3HD":
+        if Sq != Skv:
+            raise ValueError("3HD needs equal query and key/value lengths")
+        qkv = np.asarray(buffers["qkv"], dtype=np.float64).reshape(B * Sq, -1)
+        if qkv.shape[1] != Hq * d_qk + Hkv * d_qk + Hkv * d_v:
+            raise ValueError("3HD row width mismatch")
+        q = qkv[:, : Hq * d_qk]
+        k = qkv[:, Hq * d_qk : Hq * d_qk + Hkv * d_qk]
+        v = qkv[:, Hq * d_qk + Hkv * d_qk :]
+    elif layout == "HD_2HD":
+        if d_qk != d_v:
+            raise ValueError("HD_2HD needs qk_head_dim == v_head_dim")
+        q = np.asarray(buffers["q"], dtype=np.float64).reshape(B * Sq, -1)
+        kv = np.asarray(buffers["kv"], dtype=np.float64).reshape(B * Skv, 2 * Hkv * d_v)
+        k = kv[:, : Hkv * d_v]
+        v = kv[:, Hkv * d_v :]
+    elif layout == "HD_HD_HD":
+        q = np.asarray(buffers["q"], dtype=np.float64)
+        k = np.asarray(buffers["k"], dtype=np.float64)
+        v = np.asarray(buffers["v"], dtype=np.float64)
+    else:
+        raise ValueError(f"unknown layout {layout!r}")
+    return (
+        q.reshape(B, Sq, Hq, d_qk),
+        k.reshape(B, Skv, Hkv, d_qk),
+        v.reshape(B, Skv, Hkv, d_v),
+    )
+
+
+def pack_grads(layout, dq, dk, dv):
+    """Pack gradients into the same token-major layout as the inputs
+    (the gradient of each packed slice lands where that slice was read)."""
+    B, Sq, Hq, d_qk = dq.shape
+    _, Skv, Hkv, d_v = dv.shape
+    if layout == "3HD":
+        return {
+            "dqkv": np.concatenate(
+                [dq.reshape(B * Sq, -1), dk.reshape(B * Skv, -1), dv.reshape(B * Skv, -1)],
+                axis=1,
+            )
+        }
+    if layout == "HD_2HD":
+        return {
+            "dq": dq.reshape(B * Sq, -1),
+            "dkv": np.concatenate([dk.reshape(B * Skv, -1), dv.reshape(B * Skv, -1)], axis=1),
+        }
+    return {"dq": dq, "dk": dk, "dv": dv}
+
+
+# --------------------------------------------------------------------------
+# Segment metadata
+# --------------------------------------------------------------------------
+
+
+def derive_segment_pos(segment_ids):
+    """Positions restarting at 0 at the first token of every run of equal ids
+    (what from_segment_ids_and_pos generates when only ids are given, PR #2692,
+    Description).  Works row by row on a [B, S] array."""
+    ids = np.asarray(segment_ids)
+    pos = np.zeros(ids.shape, dtype=np.int64)
+    for b in range(ids.shape[0]):
+        p = 0
+        for t in range(ids.shape[1]):
+            if t > 0 and ids[b, t] != ids[b, t - 1]:
+                p = 0
+            pos[b, t] = p
+            p += 1
+    return pos
+
+
+def metadata_from_cu_seqlens(cu_seqlens, total):
+    """Ragged offsets -> ([1, total] ids, [1, total] pos).  Segment k covers
+    tokens cu[k] .. cu[k+1]-1 and gets id k+1; tokens at or past cu[n] are
+    padding (id 0); equal consecutive offsets describe an empty segment."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    ids = np.zeros((1, total), dtype=np.int64)
+    pos = np.zeros((1, total), dtype=np.int64)
+    for k in range(len(cu) - 1):
+        lo, hi = int(cu[k]), int(cu[k + 1])
+        ids[0, lo:hi] = k + 1
+        pos[0, lo:hi] = np.arange(hi - lo)
+    return ids, pos
+
+
+def dense_metadata(B, S):
+    """Dense BSHD rows without segments: every token valid, position = index."""
+    return np.ones((B, S), dtype=np.int64), np.tile(np.arange(S, dtype=np.int64), (B, 1))
+
+
+def valid_pairs(id_q, pos_q, id_kv, pos_kv, causal):
+    """Boolean [Sq, Skv] mask of one batch row: same nonzero segment and, when
+    causal, key position not after the query position."""
+    id_q = np.asarray(id_q)[:, None]
+    id_kv = np.asarray(id_kv)[None, :]
+    m = (id_q == id_kv) & (id_q != 0)
+    if causal:
+        m &= np.asarray(pos_kv)[None, :] <= np.asarray(pos_q)[:, None]
+    return m
+
+
+def count_valid_pairs(id_q, pos_q, id_kv, pos_kv, causal):
+    """Exact number of unmasked (i, j) pairs per head summed over batch rows."""
+    return int(sum(valid_pairs(id_q[b], pos_q[b], id_kv[b], pos_kv[b], causal).sum()
+                   for b in range(np.asarray(id_q).shape[0])))
+
+
+# --------------------------------------------------------------------------
+# The attention definition
+# --------------------------------------------------------------------------
+
+
+def _bias_index(bias_shape, b, h):
+    bb, bh = bias_shape[0], bias_shape[1]
+    return (b if bb > 1 else 0), (h if bh > 1 else 0)
+
+
+def _rows_softmax(q_rows, k_b, mask_rows, scale, bias_rows):
+    """Scores and probabilities of a block of query rows over the keys valid
+    for at least one of them.  Returns (cols, S, P, m, l)."""
+    cols = np.nonzero(mask_rows.any(axis=0))[0]
+    R = q_rows.shape[0]
+    if cols.size == 0:
+        return cols, np.zeros((R, 0)), np.zeros((R, 0)), np.full(R, -np.inf), np.zeros(R)
+    s = scale * (q_rows @ k_b[cols].T)
+    if bias_rows is not None:
+        s = s + bias_rows[:, cols]
+    s = np.where(mask_rows[:, cols], s, -np.inf)
+    m = s.max(axis=1)
+    finite = np.isfinite(m)
+    e = np.zeros_like(s)
+    e[finite] = np.exp(s[finite] - m[finite, None])
+    l = e.sum(axis=1)
+    p = np.zeros_like(e)
+    p[finite] = e[finite] / l[finite, None]
+    return cols, s, p, m, l
+
+
+def attention_forward(q, k, v, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=None,
+                      row_block=256):
+    """O [B,Sq,Hq,d_v] and LSE [B,Hq,Sq] (natural log) by the definition above."""
+    B, Sq, Hq, _ = q.shape
+    _, Skv, Hkv, d_v = v.shape
+    group = Hq // Hkv
+    o = np.zeros((B, Sq, Hq, d_v))
+    lse = np.full((B, Hq, Sq), -np.inf)
+    for b in range(B):
+        mask = valid_pairs(id_q[b], pos_q[b], id_kv[b], pos_kv[b], causal)
+        for h in range(Hq):
+            g = h // group
+            for r0 in range(0, Sq, row_block):
+                r1 = min(Sq, r0 + row_block)
+                br = None
+                if bias is not None:
+                    bi, hi = _bias_index(bias.shape, b, h)
+                    br = bias[bi, hi, r0:r1]
+                cols, _, p, m, l = _rows_softmax(q[b, r0:r1, h], k[b, :, g], mask[r0:r1],
+                                                 scale, br)
+                if cols.size == 0:
+                    continue
+                o[b, r0:r1, h] = p @ v[b, cols, g]
+                fin = np.isfinite(m)
+                lse[b, h, r0:r1][fin] = m[fin] + np.log(l[fin])
+    return o, lse
+
+
+def attention_backward(q, k, v, do, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=None,
+                       row_block=256):
+    """Closed-form gradients (dQ, dK, dV, dBias or None) for the incoming dO.
+
+    The probabilities are recomputed here from Q, K, V (and bias), so the
+    backward depends on nothing but the definition.  dBias has the shape of the
+    bias and sums dS over every axis the bias broadcasts along."""
+    B, Sq, Hq, _ = q.shape
+    _, Skv, Hkv, _ = v.shape
+    group = Hq // Hkv
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    dbias = None if bias is None else np.zeros(bias.shape)
+    for b in range(B):
+        mask = valid_pairs(id_q[b], pos_q[b], id_kv[b], pos_kv[b], causal)
+        for h in range(Hq):
+            g = h // group
+            for r0 in range(0, Sq, row_block):
+                r1 = min(Sq, r0 + row_block)
+                br = None
+                if bias is not None:
+                    bi, hi = _bias_index(bias.shape, b, h)
+                    br = bias[bi, hi, r0:r1]
+                cols, _, p, _, _ = _rows_softmax(q[b, r0:r1, h], k[b, :, g], mask[r0:r1],
+                                                 scale, br)
+                if cols.size == 0:
+                    continue
+                do_r = do[b, r0:r1, h]
+                dp = do_r @ v[b, cols, g].T
+                D = (p * dp).sum(axis=1)
+                ds = p * (dp - D[:, None])
+                dq[b, r0:r1, h] = scale * (ds @ k[b, cols, g])
+                dk[b, cols, g] += scale * (ds.T @ q[b, r0:r1, h])
+                dv[b, cols, g] += p.T @ do_r
+                if dbias is not None:
+                    dbias[bi, hi, r0:r1][:, cols] += ds
+    return dq, dk, dv, dbias
+
+
+# --------------------------------------------------------------------------
+# Sampled evaluation for full-size checks
+# --------------------------------------------------------------------------
+
+
+def forward_rows(q, k, v, id_q, pos_q, id_kv, pos_kv, causal, scale, b, h, rows, bias=None):
+    """O and LSE of the listed query rows of (b, h) only."""
+    Hq, Hkv = q.shape[2], v.shape[2]
+    g = h // (Hq // Hkv)
+    rows = np.asarray(rows)
+    mask = valid_pairs(id_q[b][rows], pos_q[b][rows], id_kv[b], pos_kv[b], causal)
+    br = None
+    if bias is not None:
+        bi, hi = _bias_index(bias.shape, b, h)
+        br = bias[bi, hi, rows]
+    cols, _, p, m, l = _rows_softmax(q[b, rows, h], k[b, :, g], mask, scale, br)
+    o = np.zeros((rows.size, v.shape[3]))
+    lse = np.full(rows.size, -np.inf)
+    if cols.size:
+        o = p @ v[b, cols, g]
+        fin = np.isfinite(m)
+        lse[fin] = m[fin] + np.log(l[fin])
+    return o, lse
+
+
+def backward_dq_rows(q, k, v, do, id_q, pos_q, id_kv, pos_kv, causal, scale, b, h, rows,
+                     bias=None):
+    """dQ of the listed query rows of (b, h) only (each row needs only its own
+    softmax row, so this is exact)."""
+    Hq, Hkv = q.shape[2], v.shape[2]
+    g = h // (Hq // Hkv)
+    rows = np.asarray(rows)
+    mask = valid_pairs(id_q[b][rows], pos_q[b][rows], id_kv[b], pos_kv[b], causal)
+    br = None
+    if bias is not None:
+        bi, hi = _bias_index(bias.shape, b, h)
+        br = bias[bi, hi, rows]
+    cols, _, p, _, _ = _rows_softmax(q[b, rows, h], k[b, :, g], mask, scale, br)
+    out = np.zeros((rows.size, q.shape[3]))
+    if cols.size:
+        dp = do[b, rows, h] @ v[b, cols, g].T
+        D = (p * dp).sum(axis=1)
+        out = scale * ((p * (dp - D[:, None])) @ k[b, cols, g])
+    return out
+
+
+def backward_dkdv_cols(q, k, v, do, id_q, pos_q, id_kv, pos_kv, causal, scale, b, g, cols,
+                       bias=None):
+    """dK and dV of the listed key rows of (b, kv-head g).  Every query row that
+    attends to one of them is recomputed in full (its softmax needs all of its
+    keys), so the result is exact, not an approximation."""
+    Hq, Hkv = q.shape[2], v.shape[2]
+    group = Hq // Hkv
+    cols = np.asarray(cols)
+    dk = np.zeros((cols.size, k.shape[3]))
+    dv = np.zeros((cols.size, v.shape[3]))
+    sel = valid_pairs(id_q[b], pos_q[b], id_kv[b][cols], pos_kv[b][cols], causal)
+    rows = np.nonzero(sel.any(axis=1))[0]
+    if rows.size == 0:
+        return dk, dv
+    mask = valid_pairs(id_q[b][rows], pos_q[b][rows], id_kv[b], pos_kv[b], causal)
+    for h in range(g * group, (g + 1) * group):
+        br = None
+        if bias is not None:
+            bi, hi = _bias_index(bias.shape, b, h)
+            br = bias[bi, hi, rows]
+        kc, _, p, _, _ = _rows_softmax(q[b, rows, h], k[b, :, g], mask, scale, br)
+        dp = do[b, rows, h] @ v[b, kc, g].T
+        D = (p * dp).sum(axis=1)
+        ds = p * (dp - D[:, None])
+        where = {int(c): n for n, c in enumerate(kc)}
+        for t, c in enumerate(cols):
+            n = where.get(int(c))
+            if n is None:
+                continue
+            dk[t] += scale * (ds[:, n] @ q[b, rows, h])
+            dv[t] += p[:, n] @ do[b, rows, h]
+    return dk, dv
+
+
+# --------------------------------------------------------------------------
+# Comparison metric
+# --------------------------------------------------------------------------
+
+
+def rel_frobenius(x, ref):
+    """||x - ref||_F / ||ref||_F over the given elements (0 when both vanish)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref.ravel())
+    num = np.linalg.norm((x - ref).ravel())
+    if den == 0.0:
+        return 0.0 if num == 0.0 else np.inf
+    return float(num / den)
+
+
+def attention_flops(n_valid_pairs_all_heads, d_qk, d_v):
+    """Algorithmic FLOPs: forward 2*P*(d_qk + d_v); backward 2*P*(3*d_qk + 2*d_v)
+    (the five-GEMM count including the recomputed Q K^T)."""
+    P = n_valid_pairs_all_heads
+    return 2.0 * P * (d_qk + d_v), 2.0 * P * (3 * d_qk + 2 * d_v)
