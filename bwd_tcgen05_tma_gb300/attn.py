@@ -1,0 +1,189 @@
+"""ctypes binding of the attention C ABI (``include/attn.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library ``libattn_sm103.so``.  PyTorch supplies device memory and the stream.
+Loading fails loudly (RuntimeError) when the library is missing; there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libattn_sm103.so")
+
+ATTN_PARAMS_VERSION = 1
+
+LAYOUTS = {"3HD": 0, "HD_2HD": 1, "HD_HD_HD": 2}
+FORMATS = {"BSHD": 0, "THD_SEGMENTS": 1, "THD_CU_SEQLENS": 2}
+MASKS = {"NONE": 0, "CAUSAL": 1, "PADDING": 2, "PADDING_CAUSAL": 3}
+DQ_MODES = {"atomic": 0, "deterministic": 1}
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+          3: "ATTN_ERR_SHAPE_MISMATCH", 4: "ATTN_ERR_WORKSPACE_TOO_SMALL", 5: "ATTN_ERR_CUDA",
+          6: "ATTN_ERR_DEVICE_TIMEOUT"}
+EXPORTED = ("attn_abi_version", "attn_status_string", "attn_fwd_workspace_size",
+            "attn_bwd_workspace_size", "attn_resolve_layout", "attn_fwd", "attn_bwd",
+            "attn_read_status")
+
+c_i32, c_i64, c_f32, c_vp, c_sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                   ctypes.c_void_p, ctypes.c_size_t)
+
+
+class attn_params_t(ctypes.Structure):
+    _fields_ = [
+        ("struct_version", c_i32), ("fmt", c_i32), ("layout", c_i32), ("mask", c_i32),
+        ("dq_mode", c_i32),
+        ("B", c_i32), ("Sq", c_i32), ("Skv", c_i32), ("Hq", c_i32), ("Hkv", c_i32),
+        ("d_qk", c_i32), ("d_v", c_i32),
+        ("scale", c_f32),
+        ("q", c_vp), ("k", c_vp), ("v", c_vp),
+        ("q_seg_ids", c_vp), ("q_seg_pos", c_vp), ("kv_seg_ids", c_vp), ("kv_seg_pos", c_vp),
+        ("q_ids_dims", c_i64 * 2), ("q_pos_dims", c_i64 * 2), ("kv_ids_dims", c_i64 * 2),
+        ("kv_pos_dims", c_i64 * 2),
+        ("cu_seqlens_q", c_vp), ("cu_seqlens_kv", c_vp), ("num_segments", c_i32),
+        ("bias", c_vp), ("bias_b", c_i32), ("bias_h", c_i32),
+        ("force_general_path", c_i32),
+    ]
+
+
+class attn_stats_t(ctypes.Structure):
+    _fields_ = [("status", c_i32), ("path", c_i32), ("reason", c_i32), ("dq_mode", c_i32),
+                ("tile_pairs", c_i64)]
+
+
+class attn_resolved_t(ctypes.Structure):
+    _fields_ = [("q", c_vp), ("k", c_vp), ("v", c_vp), ("q_token_stride", c_i64),
+                ("k_token_stride", c_i64), ("v_token_stride", c_i64), ("dq", c_vp), ("dk", c_vp),
+                ("dv", c_vp)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the CUDA library (built by ``bwd_tcgen05_tma_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA attention library not built: {path} is missing "
+                           "(run bwd_tcgen05_tma_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(attn_params_t)
+    lib.attn_abi_version.restype = c_i32
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_status_string.argtypes = [c_i32]
+    lib.attn_fwd_workspace_size.restype = c_sz
+    lib.attn_fwd_workspace_size.argtypes = [P]
+    lib.attn_bwd_workspace_size.restype = c_sz
+    lib.attn_bwd_workspace_size.argtypes = [P]
+    lib.attn_resolve_layout.restype = c_i32
+    lib.attn_resolve_layout.argtypes = [P, c_vp, c_vp, c_vp, ctypes.POINTER(attn_resolved_t)]
+    lib.attn_fwd.restype = c_i32
+    lib.attn_fwd.argtypes = [P, c_vp, c_vp, c_vp, c_sz, c_vp]
+    lib.attn_bwd.restype = c_i32
+    lib.attn_bwd.argtypes = [P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]
+    lib.attn_read_status.restype = c_i32
+    lib.attn_read_status.argtypes = [c_vp, c_vp, ctypes.POINTER(attn_stats_t)]
+    if lib.attn_abi_version() != ATTN_PARAMS_VERSION:
+        raise RuntimeError("attention library ABI version mismatch")
+    _lib = lib
+    return lib
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        name = STATUS.get(code, str(code))
+        msg = load_library().attn_status_string(code).decode()
+        super().__init__(f"{what}: {name} ({msg})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(getattr(stream, "cuda_stream", stream))
+
+
+def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, k=None, v=None,
+                q_seg_ids=None, q_seg_pos=None, kv_seg_ids=None, kv_seg_pos=None,
+                cu_seqlens_q=None, cu_seqlens_kv=None, bias=None, dq_mode="deterministic",
+                force_general_path=False):
+    """Fill an ``attn_params_t`` from tensors (any object with data_ptr/shape)."""
+    p = attn_params_t()
+    p.struct_version = ATTN_PARAMS_VERSION
+    p.fmt = FORMATS[fmt]
+    p.layout = LAYOUTS[layout]
+    p.mask = MASKS[mask]
+    p.dq_mode = DQ_MODES[dq_mode]
+    p.B, p.Sq, p.Skv, p.Hq, p.Hkv, p.d_qk, p.d_v = B, Sq, Skv, Hq, Hkv, d_qk, d_v
+    p.scale = float(scale)
+    p.q, p.k, p.v = _ptr(q), _ptr(k), _ptr(v)
+    for name, t in (("q_seg_ids", q_seg_ids), ("q_seg_pos", q_seg_pos), ("kv_seg_ids", kv_seg_ids),
+                    ("kv_seg_pos", kv_seg_pos)):
+        setattr(p, name, _ptr(t))
+        if t is not None:
+            dims = tuple(t.shape)
+            if len(dims) == 1:
+                dims = (1,) + dims
+            key = {"q_seg_ids": "q_ids_dims", "q_seg_pos": "q_pos_dims",
+                   "kv_seg_ids": "kv_ids_dims", "kv_seg_pos": "kv_pos_dims"}[name]
+            arr = getattr(p, key)
+            arr[0] = int(dims[-2]) if len(dims) >= 2 else 1
+            arr[1] = int(dims[-1])
+            if len(dims) > 2:  # extra leading dims: a mismatch the library reports
+                arr[0] = -1
+    p.cu_seqlens_q, p.cu_seqlens_kv = _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv)
+    p.num_segments = 0 if cu_seqlens_q is None else int(cu_seqlens_q.shape[0]) - 1
+    p.bias = _ptr(bias)
+    if bias is not None:
+        p.bias_b, p.bias_h = int(bias.shape[0]), int(bias.shape[1])
+    p.force_general_path = 1 if force_general_path else 0
+    return p
+
+
+def attn_fwd_workspace_size(p):
+    return int(load_library().attn_fwd_workspace_size(ctypes.byref(p)))
+
+
+def attn_bwd_workspace_size(p):
+    return int(load_library().attn_bwd_workspace_size(ctypes.byref(p)))
+
+
+def attn_resolve_layout(p, dq=None, dk=None, dv=None):
+    r = attn_resolved_t()
+    s = load_library().attn_resolve_layout(ctypes.byref(p), dq, dk, dv, ctypes.byref(r))
+    if s != 0:
+        raise AttnError(s, "attn_resolve_layout")
+    return r
+
+
+def attn_fwd(p, o, lse, ws, stream=None):
+    """Enqueue the forward on `stream` (default: torch's current stream)."""
+    s = load_library().attn_fwd(ctypes.byref(p), _ptr(o), _ptr(lse), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream))
+    if s != 0:
+        raise AttnError(s, "attn_fwd")
+
+
+def attn_bwd(p, o, d_o, lse, dq, dk, dv, dbias, ws, stream=None):
+    """Enqueue the backward on `stream` (default: torch's current stream)."""
+    s = load_library().attn_bwd(ctypes.byref(p), _ptr(o), _ptr(d_o), _ptr(lse), _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(dbias), _ptr(ws), ws.numel() * ws.element_size(),
+                                _stream(stream))
+    if s != 0:
+        raise AttnError(s, "attn_bwd")
+
+
+def attn_read_status(ws, stream=None):
+    """Synchronise and return (status, attn_stats_t) of the last call on `ws`."""
+    st = attn_stats_t()
+    s = load_library().attn_read_status(_ptr(ws), _stream(stream), ctypes.byref(st))
+    return s, st

@@ -1,0 +1,400 @@
+// Host side of the C ABI: argument validation, packed-layout resolution,
+// workspace planning, TMA descriptor encoding and kernel launches.
+//
+// Layout resolution follows TransformerEngine PR #2358 ("[JAX] Make all jax
+// attention calls use non-packed common calls"): a packed QKV buffer yields K
+// one head-block and V two head-blocks after Q, and the V slice of a packed KV
+// buffer starts num_gqa_groups * v_head_dim elements after K (the page's
+// review of the KV-packed stride).  With grouped query heads the 3HD token row
+// holds Hq query heads, then Hkv key heads, then Hkv value heads.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.cuh"
+
+namespace attn {
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Plan {
+  size_t hdr, q_id, q_pos, seg_lo, seg_hi, kv_id, kv_pos, kv_seg_lo, kv_seg_hi;
+  size_t q_chunk, kv_chunk, q_range, kv_range;
+  size_t fwd_total;
+  size_t lse2, dvec, dq_acc, dbias_acc;
+  size_t bwd_total;
+};
+
+bool effective_atomic(const attn_params_t* p) {
+  return p->dq_mode == ATTN_DQ_ATOMIC && p->d_qk <= 128;
+}
+
+bool dbias_needs_acc(const attn_params_t* p) {
+  return p->bias != nullptr && ((p->bias_b == 1 && p->B > 1) || (p->bias_h == 1 && p->Hq > 1));
+}
+
+Plan make_plan(const attn_params_t* p) {
+  Plan pl{};
+  const size_t B = p->B, Sq = p->Sq, Skv = p->Skv;
+  const size_t nqc = (Sq + kChunk - 1) / kChunk, nkc = (Skv + kChunk - 1) / kChunk;
+  const size_t nqt = (Sq + kTile - 1) / kTile, nkt = (Skv + kTile - 1) / kTile;
+  size_t o = 0;
+  pl.hdr = o; o = up(o + sizeof(WsHeader));
+  pl.q_id = o; o = up(o + B * Sq * 4);
+  pl.q_pos = o; o = up(o + B * Sq * 4);
+  pl.seg_lo = o; o = up(o + B * Sq * 4);
+  pl.seg_hi = o; o = up(o + B * Sq * 4);
+  pl.kv_id = o; o = up(o + B * Skv * 4);
+  pl.kv_pos = o; o = up(o + B * Skv * 4);
+  pl.kv_seg_lo = o; o = up(o + B * Skv * 4);
+  pl.kv_seg_hi = o; o = up(o + B * Skv * 4);
+  pl.q_chunk = o; o = up(o + B * nqc * sizeof(ChunkInfo));
+  pl.kv_chunk = o; o = up(o + B * nkc * sizeof(ChunkInfo));
+  pl.q_range = o; o = up(o + B * nqt * sizeof(int2));
+  pl.kv_range = o; o = up(o + B * nkt * sizeof(int2));
+  pl.fwd_total = o;
+  pl.lse2 = o; o = up(o + B * p->Hq * Sq * 4);
+  pl.dvec = o; o = up(o + B * p->Hq * Sq * 4);
+  pl.dq_acc = o;
+  if (effective_atomic(p)) o = up(o + B * Sq * p->Hq * (size_t)p->d_qk * 4);
+  pl.dbias_acc = o;
+  if (dbias_needs_acc(p)) o = up(o + (size_t)p->bias_b * p->bias_h * Sq * Skv * 4);
+  pl.bwd_total = o;
+  return pl;
+}
+
+attn_status_t validate(const attn_params_t* p) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  if (p->struct_version != ATTN_PARAMS_VERSION) return ATTN_ERR_INVALID_ARG;
+  if (p->fmt < 0 || p->fmt > 2 || p->layout < 0 || p->layout > 2 || p->mask < 0 || p->mask > 3 ||
+      p->dq_mode < 0 || p->dq_mode > 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (p->B <= 0 || p->Sq <= 0 || p->Skv <= 0 || p->Hq <= 0 || p->Hkv <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if ((int64_t)p->B * p->Sq >= (1ll << 31) || (int64_t)p->B * p->Skv >= (1ll << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  if (p->Hq % p->Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(p->scale > 0.f) || p->scale != p->scale) return ATTN_ERR_INVALID_ARG;
+  if (p->d_qk != 64 && p->d_qk != 128 && p->d_qk != 192) return ATTN_ERR_UNSUPPORTED;
+  if (p->d_v != 64 && p->d_v != 128) return ATTN_ERR_UNSUPPORTED;
+  // packed-layout rules (PR #2358: the 3HD check q_max_seqlen == kv_max_seqlen and
+  // the KV-packed requirement qk_head_dim == v_head_dim)
+  if (p->layout == ATTN_LAYOUT_3HD && p->Sq != p->Skv) return ATTN_ERR_SHAPE_MISMATCH;
+  if (p->layout == ATTN_LAYOUT_HD_2HD && p->d_qk != p->d_v) return ATTN_ERR_SHAPE_MISMATCH;
+  if (!p->q || !aligned16(p->q)) return ATTN_ERR_INVALID_ARG;
+  if (p->layout != ATTN_LAYOUT_3HD && (!p->k || !aligned16(p->k))) return ATTN_ERR_INVALID_ARG;
+  if (p->layout == ATTN_LAYOUT_HD_HD_HD && (!p->v || !aligned16(p->v))) return ATTN_ERR_INVALID_ARG;
+  // sequence description
+  if (p->fmt == ATTN_FMT_THD_SEGMENTS && (!p->q_seg_ids || !p->kv_seg_ids))
+    return ATTN_ERR_INVALID_ARG;
+  if (p->fmt == ATTN_FMT_THD_CU_SEQLENS) {
+    if (p->B != 1 || !p->cu_seqlens_q || !p->cu_seqlens_kv || p->num_segments < 0)
+      return ATTN_ERR_INVALID_ARG;
+  }
+  if (p->fmt != ATTN_FMT_THD_CU_SEQLENS) {
+    // ids and positions of one side must agree in shape with each other and with [B, S]
+    // (PR #2692: segment_pos must carry the same leading dims as segment_ids)
+    const bool qi = p->q_seg_ids != nullptr, ki = p->kv_seg_ids != nullptr;
+    if (qi != ki) return ATTN_ERR_INVALID_ARG;
+    if ((p->q_seg_pos != nullptr) != (p->kv_seg_pos != nullptr)) return ATTN_ERR_INVALID_ARG;
+    if ((p->q_seg_pos && !qi)) return ATTN_ERR_INVALID_ARG;
+    if (qi) {
+      if (p->q_ids_dims[0] != p->B || p->q_ids_dims[1] != p->Sq) return ATTN_ERR_SHAPE_MISMATCH;
+      if (p->kv_ids_dims[0] != p->B || p->kv_ids_dims[1] != p->Skv) return ATTN_ERR_SHAPE_MISMATCH;
+      if (p->q_seg_pos) {
+        if (p->q_pos_dims[0] != p->q_ids_dims[0] || p->q_pos_dims[1] != p->q_ids_dims[1])
+          return ATTN_ERR_SHAPE_MISMATCH;
+        if (p->kv_pos_dims[0] != p->kv_ids_dims[0] || p->kv_pos_dims[1] != p->kv_ids_dims[1])
+          return ATTN_ERR_SHAPE_MISMATCH;
+      }
+    }
+  }
+  if (p->bias) {
+    if (!aligned16(p->bias)) return ATTN_ERR_INVALID_ARG;
+    if (!(p->bias_b == 1 || p->bias_b == p->B) || !(p->bias_h == 1 || p->bias_h == p->Hq))
+      return ATTN_ERR_SHAPE_MISMATCH;
+  }
+  return ATTN_OK;
+}
+
+attn_status_t resolve(const attn_params_t* p, void* dq, void* dk, void* dv, attn_resolved_t* r) {
+  const char* q = static_cast<const char*>(p->q);
+  const int64_t Hq = p->Hq, Hkv = p->Hkv, dqk = p->d_qk, dvv = p->d_v;
+  std::memset(r, 0, sizeof(*r));
+  switch (p->layout) {
+    case ATTN_LAYOUT_3HD: {
+      const int64_t W = Hq * dqk + Hkv * dqk + Hkv * dvv;
+      r->q = q;
+      r->k = q + Hq * dqk * 2;
+      r->v = q + (Hq * dqk + Hkv * dqk) * 2;
+      r->q_token_stride = r->k_token_stride = r->v_token_stride = W;
+      if (dq) {
+        char* d = static_cast<char*>(dq);
+        r->dq = d;
+        r->dk = d + Hq * dqk * 2;
+        r->dv = d + (Hq * dqk + Hkv * dqk) * 2;
+      }
+      break;
+    }
+    case ATTN_LAYOUT_HD_2HD: {
+      const char* k = static_cast<const char*>(p->k);
+      r->q = q;
+      r->k = k;
+      r->v = k + Hkv * dvv * 2;  // stride from v_head_dim
+      r->q_token_stride = Hq * dqk;
+      r->k_token_stride = r->v_token_stride = 2 * Hkv * dvv;
+      r->dq = dq;
+      if (dk) {
+        r->dk = dk;
+        r->dv = static_cast<char*>(dk) + Hkv * dvv * 2;
+      }
+      break;
+    }
+    default:
+      r->q = q;
+      r->k = p->k;
+      r->v = p->v;
+      r->q_token_stride = Hq * dqk;
+      r->k_token_stride = Hkv * dqk;
+      r->v_token_stride = Hkv * dvv;
+      r->dq = dq;
+      r->dk = dk;
+      r->dv = dv;
+  }
+  return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a token-major tensor: dims {D, H, T}, box {64, 1, rows}.
+bool make_map(CUtensorMap* m, const void* base, int D, int H, int64_t T, int64_t tok_stride,
+              int rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)tok_stride * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cache[64] = {0};
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+void fill_common(KernelArgs& a, const attn_params_t* p, char* ws, const Plan& pl) {
+  a.B = p->B; a.Sq = p->Sq; a.Skv = p->Skv; a.Hq = p->Hq; a.Hkv = p->Hkv;
+  a.d_qk = p->d_qk; a.d_v = p->d_v;
+  a.causal = (p->mask == ATTN_MASK_CAUSAL || p->mask == ATTN_MASK_PADDING_CAUSAL) ? 1 : 0;
+  a.scale = p->scale;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.n_qt = (p->Sq + kTile - 1) / kTile;
+  a.n_kt = (p->Skv + kTile - 1) / kTile;
+  a.n_qt64 = (p->Sq + kBwdQ - 1) / kBwdQ;
+  a.hdr = reinterpret_cast<WsHeader*>(ws + pl.hdr);
+  a.q_id = reinterpret_cast<int32_t*>(ws + pl.q_id);
+  a.q_pos = reinterpret_cast<int32_t*>(ws + pl.q_pos);
+  a.seg_lo = reinterpret_cast<int32_t*>(ws + pl.seg_lo);
+  a.seg_hi = reinterpret_cast<int32_t*>(ws + pl.seg_hi);
+  a.kv_id = reinterpret_cast<int32_t*>(ws + pl.kv_id);
+  a.kv_pos = reinterpret_cast<int32_t*>(ws + pl.kv_pos);
+  a.kv_seg_lo = reinterpret_cast<int32_t*>(ws + pl.kv_seg_lo);
+  a.kv_seg_hi = reinterpret_cast<int32_t*>(ws + pl.kv_seg_hi);
+  a.q_chunk = reinterpret_cast<ChunkInfo*>(ws + pl.q_chunk);
+  a.kv_chunk = reinterpret_cast<ChunkInfo*>(ws + pl.kv_chunk);
+  a.q_tile_range = reinterpret_cast<int2*>(ws + pl.q_range);
+  a.kv_tile_range = reinterpret_cast<int2*>(ws + pl.kv_range);
+  a.bias = static_cast<const bf16*>(p->bias);
+  a.bias_b = p->bias_b;
+  a.bias_h = p->bias_h;
+}
+
+attn_status_t run_meta(const KernelArgs& a, const attn_params_t* p, cudaStream_t st) {
+  const bool seg = p->fmt != ATTN_FMT_THD_CU_SEQLENS && p->q_seg_ids != nullptr;
+  const cudaError_t e =
+      launch_meta(a, p->fmt == ATTN_FMT_THD_CU_SEQLENS ? 2 : (seg ? 1 : 0),
+                  seg ? p->q_seg_ids : nullptr, seg ? p->q_seg_pos : nullptr,
+                  seg ? p->kv_seg_ids : nullptr, seg ? p->kv_seg_pos : nullptr,
+                  p->cu_seqlens_q, p->cu_seqlens_kv, p->num_segments, p->force_general_path, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int32_t attn_abi_version(void) { return ATTN_PARAMS_VERSION; }
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_SHAPE_MISMATCH: return "shape mismatch";
+    case ATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t attn_fwd_workspace_size(const attn_params_t* p) {
+  if (validate(p) != ATTN_OK) return 0;
+  return make_plan(p).fwd_total;
+}
+
+size_t attn_bwd_workspace_size(const attn_params_t* p) {
+  if (validate(p) != ATTN_OK) return 0;
+  return make_plan(p).bwd_total;
+}
+
+attn_status_t attn_resolve_layout(const attn_params_t* p, void* dq, void* dk, void* dv,
+                                  attn_resolved_t* out) {
+  const attn_status_t s = validate(p);
+  if (s != ATTN_OK) return s;
+  if (!out) return ATTN_ERR_INVALID_ARG;
+  return resolve(p, dq, dk, dv, out);
+}
+
+attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, size_t ws_bytes,
+                       void* stream) {
+  attn_status_t s = validate(p);
+  if (s != ATTN_OK) return s;
+  if (!o || !lse || !ws || !aligned16(o) || (reinterpret_cast<uintptr_t>(ws) % kAlign))
+    return ATTN_ERR_INVALID_ARG;
+  const Plan pl = make_plan(p);
+  if (ws_bytes < pl.fwd_total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  attn_resolved_t r;
+  resolve(p, nullptr, nullptr, nullptr, &r);
+  if (!aligned16(r.k) || !aligned16(r.v) || (r.q_token_stride % 8) || (r.k_token_stride % 8) ||
+      (r.v_token_stride % 8))
+    return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  KernelArgs a;
+  std::memset(&a, 0, sizeof(a));
+  fill_common(a, p, static_cast<char*>(ws), pl);
+  if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
+      !make_map(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
+      !make_map(&a.tm_v, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile))
+    return ATTN_ERR_CUDA;
+  a.o = static_cast<bf16*>(o);
+  a.lse = lse;
+  if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
+  if (launch_fwd(a, sm_count(), st) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, const float* lse,
+                       void* dq, void* dk, void* dv, void* dbias, void* ws, size_t ws_bytes,
+                       void* stream) {
+  attn_status_t s = validate(p);
+  if (s != ATTN_OK) return s;
+  if (!o || !d_o || !lse || !ws || !aligned16(o) || !aligned16(d_o) ||
+      (reinterpret_cast<uintptr_t>(ws) % kAlign))
+    return ATTN_ERR_INVALID_ARG;
+  if (!dq || !aligned16(dq)) return ATTN_ERR_INVALID_ARG;
+  if (p->layout != ATTN_LAYOUT_3HD && (!dk || !aligned16(dk))) return ATTN_ERR_INVALID_ARG;
+  if (p->layout == ATTN_LAYOUT_HD_HD_HD && (!dv || !aligned16(dv))) return ATTN_ERR_INVALID_ARG;
+  if (dbias && !p->bias) return ATTN_ERR_INVALID_ARG;
+  if (dbias && !aligned16(dbias)) return ATTN_ERR_INVALID_ARG;
+  const Plan pl = make_plan(p);
+  if (ws_bytes < pl.bwd_total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  attn_resolved_t r;
+  resolve(p, dq, dk, dv, &r);
+  if (!aligned16(r.k) || !aligned16(r.v) || (r.q_token_stride % 8) || (r.k_token_stride % 8) ||
+      (r.v_token_stride % 8))
+    return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  KernelArgs a;
+  std::memset(&a, 0, sizeof(a));
+  fill_common(a, p, w, pl);
+  a.o_in = static_cast<const bf16*>(o);
+  a.d_o = static_cast<const bf16*>(d_o);
+  a.lse_in = lse;
+  a.lse2 = reinterpret_cast<float*>(w + pl.lse2);
+  a.Dvec = reinterpret_cast<float*>(w + pl.dvec);
+  const bool atomic = effective_atomic(p);
+  a.dq_acc = atomic ? reinterpret_cast<float*>(w + pl.dq_acc) : nullptr;
+  a.dq = static_cast<bf16*>(const_cast<void*>(r.dq));
+  a.dk = static_cast<bf16*>(const_cast<void*>(r.dk));
+  a.dv = static_cast<bf16*>(const_cast<void*>(r.dv));
+  a.dq_stride = r.q_token_stride;
+  a.dk_stride = r.k_token_stride;
+  a.dv_stride = r.v_token_stride;
+  a.dbias = static_cast<bf16*>(dbias);
+  a.dbias_mode = dbias ? (dbias_needs_acc(p) ? 2 : 1) : 0;
+  a.dbias_acc = (a.dbias_mode == 2) ? reinterpret_cast<float*>(w + pl.dbias_acc) : nullptr;
+  a.dkdv_batch_loop = (a.dbias_mode == 2 && p->bias_b == 1 && p->B > 1) ? 1 : 0;
+  a.dkdv_head_loop = (a.dbias_mode == 2 && p->bias_h == 1 && p->Hkv > 1) ? 1 : 0;
+  if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
+  if (launch_bwd_pre(a, atomic ? 1 : 0, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  // dK/dV pass: query tiles of 64 rows
+  if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kBwdQ) ||
+      !make_map(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
+      !make_map(&a.tm_v, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
+      !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
+                kBwdQ))
+    return ATTN_ERR_CUDA;
+  const int nsm = sm_count();
+  if (launch_bwd_dkdv(a, atomic, nsm, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (atomic) {
+    if (launch_dq_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  } else {
+    if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
+        !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
+                  kTile))
+      return ATTN_ERR_CUDA;
+    if (launch_bwd_dq(a, nsm, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  if (a.dbias_mode == 2 && launch_dbias_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status_t attn_read_status(const void* ws, void* stream, attn_stats_t* stats) {
+  if (!ws) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (stats) {
+    stats->status = h.status;
+    stats->path = h.path;
+    stats->reason = h.reason;
+    stats->dq_mode = h.dq_mode;
+    stats->tile_pairs = h.tile_pairs;
+  }
+  return h.status == 0 ? ATTN_OK : static_cast<attn_status_t>(h.status);
+}
+
+}  // extern "C"

@@ -1,0 +1,1158 @@
+// Backward pass: dQ, dK, dV (and dBias) from O, dO and the forward's LSE.
+//
+//   bwd_pre      D = rowsum(dO * O) per (batch row, head, query) and LSE in
+//                log2 units; zeroes the fp32 accumulators it is asked to.
+//   dkdv         one persistent CTA per SM; a work item is one 128-row KV tile
+//                of one KV head (and, when a broadcast bias gradient has to be
+//                reduced, of every batch row / head sharing that bias slice).
+//                The CTA loops *sequentially* over the query heads of the
+//                group and every 64-row query tile that can see the KV tile,
+//                accumulating dK and dV in tensor memory.  No accumulation
+//                depends on the order in which CTAs run, which is the
+//                grid-order hazard of the maxdiffusion PR #485 review (dK/dV
+//                initialised and written by whichever grid step happens to run
+//                first / last); the fused single-pass structure (KV outer,
+//                queries and GQA heads inner, dK/dV held across them) follows
+//                that page's Summary.
+//                Per query tile:  S^T = K Q^T,  P^T = exp2(S^T - LSE),
+//                dP^T = V dO^T,  dS^T = P^T (dP^T - D),  dV += P^T dO,
+//                dK += dS^T Q,  and in atomic-dQ mode dQ^T = K^T dS^T, added to an
+//                fp32 buffer with red.global.add.
+//   dq           deterministic dQ: one 128-row query tile per work item, KV
+//                tiles visited in a fixed order, dQ accumulated in tensor
+//                memory (recomputes S and dP: two more GEMMs than atomic mode).
+//   dq_convert   fp32 dQ accumulator -> bf16 in the caller's layout.
+//   dbias_convert fp32 broadcast-bias gradient -> bf16.
+//
+// Gradient formulas: TransformerEngine PR #3516 (fused-attention backward:
+// Q/K/V and optional bias gradients from the saved output and dO); dK/dV of a
+// KV head sum over the query heads sharing it (maxdiffusion PR #485, Summary);
+// the bias gradient is summed over the axes the bias is broadcast along.
+#include <cmath>
+
+#include "attn_internal.cuh"
+
+namespace attn {
+namespace {
+using namespace sm103;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// =========================================================== preprocess
+template <int DV>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const KernelArgs a, int dq_mode_used) {
+  constexpr int LPR = DV / 8;    // lanes per (token, head) row
+  constexpr int RPW = 32 / LPR;  // rows per warp
+  const int64_t nrows = (int64_t)a.B * a.Sq * a.Hq;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, l = lane % LPR;
+  const int64_t wg = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r0 = wg * RPW; r0 < nrows; r0 += nw * RPW) {
+    const int64_t row = r0 + sub;  // (b * Sq + i) * Hq + h
+    float acc = 0.f;
+    if (row < nrows) {
+      const uint4 o = ld_nc_v4(a.o_in + row * DV + l * 8);
+      const uint4 d = ld_nc_v4(a.d_o + row * DV + l * 8);
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), acc);
+        acc = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(dw[e] & 0xFFFF0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (l == 0 && row < nrows) {
+      const int64_t tok = row / a.Hq;
+      const int h = static_cast<int>(row - tok * a.Hq);
+      const int b = static_cast<int>(tok / a.Sq);
+      const int i = static_cast<int>(tok - (int64_t)b * a.Sq);
+      const int64_t idx = ((int64_t)b * a.Hq + h) * a.Sq + i;
+      a.Dvec[idx] = acc;
+      const float lse = a.lse_in[idx];
+      a.lse2[idx] = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.hdr->dq_mode = dq_mode_used;
+}
+
+// =========================================================== converts
+__global__ void dq_convert_kernel(const KernelArgs a) {
+  const int64_t per_tok = (int64_t)a.Hq * a.d_qk / 8;  // groups of 8 elements
+  const int64_t n = (int64_t)a.B * a.Sq * per_tok;
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tok = v / per_tok;
+    const int64_t e = (v - tok * per_tok) * 8;  // h * d_qk + d
+    const float4 x0 = *reinterpret_cast<const float4*>(a.dq_acc + tok * a.Hq * a.d_qk + e);
+    const float4 x1 = *reinterpret_cast<const float4*>(a.dq_acc + tok * a.Hq * a.d_qk + e + 4);
+    uint4 o;
+    o.x = pack_bf16x2(x0.x, x0.y);
+    o.y = pack_bf16x2(x0.z, x0.w);
+    o.z = pack_bf16x2(x1.x, x1.y);
+    o.w = pack_bf16x2(x1.z, x1.w);
+    *reinterpret_cast<uint4*>(a.dq + tok * a.dq_stride + e) = o;
+  }
+}
+
+__global__ void dbias_convert_kernel(const KernelArgs a) {
+  const int64_t n = (int64_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n;
+       v += (int64_t)gridDim.x * blockDim.x)
+    a.dbias[v] = __float2bfloat16_rn(a.dbias_acc[v]);
+}
+
+// =========================================================== dK / dV pass
+template <int DQK, int DV>
+struct DkdvLayout {
+  static constexpr int kKBytes = kTile * DQK * 2;
+  static constexpr int kVBytes = kTile * DV * 2;
+  static constexpr int kQBytes = kBwdQ * DQK * 2;  // one 64-row query tile
+  static constexpr int kOBytes = kBwdQ * DV * 2;
+  static constexpr int kPBytes = kTile * kBwdQ * 2;
+  static constexpr int kStageBytes = kQBytes + kOBytes;
+  static constexpr int kFixed = kKBytes + kVBytes + 2 * kPBytes;
+  static constexpr int kStages = (kFixed + 3 * kStageBytes <= 200 * 1024) ? 3 : 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKBytes;
+  static constexpr int kPOff = kKBytes + kVBytes;
+  static constexpr int kDSOff = kPOff + kPBytes;
+  static constexpr int kStageOff = kDSOff + kPBytes;
+  static constexpr int kVecOff = kStageOff + kStages * kStageBytes;  // 1 KB per stage
+  static constexpr int kBarOff = kVecOff + kStages * 1024;
+  static constexpr int kBytes = kBarOff + 512;
+  static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
+  static constexpr uint32_t kColDV = 0;
+  static constexpr uint32_t kColDK = 128;
+  static constexpr uint32_t kColS = (DQK > 128) ? 320 : 256;
+  static constexpr uint32_t kColDP = kColS + 64;
+  static constexpr uint32_t kColDQ = 384;  // two 64-column buffers (d_qk <= 128 only)
+};
+
+struct DkdvBars {
+  uint64_t kv_full, kv_empty, s_full, s_free, dp_full, dp_free, p_ready, p_free, ds_ready,
+      ds_free, acc_full, acc_empty, drain;
+  uint64_t dq_full[2], dq_free[2];
+  uint64_t qd_full[3], qd_empty[3];
+};
+
+struct StageVec {  // per query tile: log2-LSE, D, and (general path) ids / positions
+  float lse2[kBwdQ];
+  float D[kBwdQ];
+  int32_t qid[kBwdQ];
+  int32_t qpos[kBwdQ];
+};
+
+// Work item -> (KV tile, batch range, KV-head range).
+struct DkdvItem {
+  int t, b0, b1, g0, g1;
+};
+
+__device__ __forceinline__ int dkdv_n_items(const KernelArgs& a) {
+  const int nb = a.dkdv_batch_loop ? 1 : a.B;
+  const int ng = a.dkdv_head_loop ? 1 : a.Hkv;
+  return a.n_kt * nb * ng;
+}
+
+__device__ __forceinline__ DkdvItem dkdv_item(const KernelArgs& a, int idx) {
+  const int nb = a.dkdv_batch_loop ? 1 : a.B;
+  const int ng = a.dkdv_head_loop ? 1 : a.Hkv;
+  DkdvItem it;
+  it.t = idx / (nb * ng);  // KV tile 0 first: it sees the most causal query tiles
+  const int rem = idx - it.t * nb * ng;
+  const int bi = rem / ng, gi = rem - (rem / ng) * ng;
+  it.b0 = a.dkdv_batch_loop ? 0 : bi;
+  it.b1 = a.dkdv_batch_loop ? a.B : bi + 1;
+  it.g0 = a.dkdv_head_loop ? 0 : gi;
+  it.g1 = a.dkdv_head_loop ? a.Hkv : gi + 1;
+  return it;
+}
+
+// Query range of KV tile t of row b; returns the number of 64-row query tiles.
+__device__ __forceinline__ int dkdv_q_tiles(const KernelArgs& a, int b, int t, int& q_lo) {
+  const int2 r = a.kv_tile_range[b * a.n_kt + t];
+  q_lo = r.x;
+  return (r.y > r.x) ? (r.y - r.x + kBwdQ - 1) / kBwdQ : 0;
+}
+
+template <int DQK, int DV, bool ATOMIC, bool HAS_BIAS, int DBIAS>
+__global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ KernelArgs a) {
+  using L = DkdvLayout<DQK, DV>;
+  constexpr int NS = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  DkdvBars* bars = reinterpret_cast<DkdvBars*>(sm + L::kBarOff);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(DkdvBars));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  StageVec* vec = reinterpret_cast<StageVec*>(sm + L::kVecOff);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_items = dkdv_n_items(a);
+  const int G = a.Hq / a.Hkv;
+
+  if (tid == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 128);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 128);
+    mbar_init(&bars->p_ready, 128);
+    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->ds_ready, 128);
+    mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, 128);
+    mbar_init(&bars->drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->dq_full[s], 1);
+      mbar_init(&bars->dq_free[s], 128);
+    }
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&bars->qd_full[s], 1 + 64);
+      mbar_init(&bars->qd_empty[s], 1 + 128);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool general = path_general(a);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&a.tm_q);
+      prefetch_tensormap(&a.tm_k);
+      prefetch_tensormap(&a.tm_v);
+      prefetch_tensormap(&a.tm_do);
+      uint32_t st = 0, kvc = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+        const DkdvItem w = dkdv_item(a, idx);
+        for (int b = w.b0; b < w.b1 && ok; ++b) {
+          for (int g = w.g0; g < w.g1 && ok; ++g) {
+            int q_lo;
+            const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
+            if (nq == 0) continue;
+            if (kvc > 0 && !(ok = mbar_wait(&bars->kv_empty, (kvc - 1) & 1))) break;
+            const int krow = b * a.Skv + w.t * kTile;
+            mbar_arrive_expect_tx(&bars->kv_full, L::kKBytes + L::kVBytes);
+#pragma unroll
+            for (int c = 0; c < DQK / 64; ++c)
+              tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
+#pragma unroll
+            for (int c = 0; c < DV / 64; ++c)
+              tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
+            ++kvc;
+            for (int hh = 0; hh < G && ok; ++hh) {
+              const int h = g * G + hh;
+              for (int s = 0; s < nq; ++s, ++st) {
+                const int stage = st % NS;
+                if (st >= (uint32_t)NS &&
+                    !(ok = mbar_wait(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
+                  break;
+                const int qrow = b * a.Sq + q_lo + s * kBwdQ;
+                uint8_t* qs = sm + L::kStageOff + stage * L::kStageBytes;
+                mbar_arrive_expect_tx(&bars->qd_full[stage], L::kStageBytes);
+#pragma unroll
+                for (int c = 0; c < DQK / 64; ++c)
+                  tma_load_3d(qs + c * 8192, &a.tm_q, &bars->qd_full[stage], c * 64, h, qrow);
+#pragma unroll
+                for (int c = 0; c < DV / 64; ++c)
+                  tma_load_3d(qs + L::kQBytes + c * 8192, &a.tm_do, &bars->qd_full[stage], c * 64,
+                              h, qrow);
+              }
+            }
+          }
+        }
+      }
+      if (!ok) {
+        report_timeout(a, 0x110);
+        *abort_flag = 1;
+      }
+      if (*abort_flag) {
+        if (kvc > 0) mbar_wait(&bars->kv_full, (kvc - 1) & 1, 100000000ull);
+        for (uint32_t u = (st > (uint32_t)NS ? st - NS : 0u); u < st; ++u)
+          mbar_wait(&bars->qd_full[u % NS], (u / NS) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ vector loader
+    const int t = tid - 64;
+    uint32_t st = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      const DkdvItem w = dkdv_item(a, idx);
+      for (int b = w.b0; b < w.b1 && ok; ++b) {
+        for (int g = w.g0; g < w.g1 && ok; ++g) {
+          int q_lo;
+          const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
+          for (int hh = 0; hh < G && ok && nq > 0; ++hh) {
+            const int h = g * G + hh;
+            for (int s = 0; s < nq; ++s, ++st) {
+              const int stage = st % NS;
+              if (st >= (uint32_t)NS &&
+                  !(ok = mbar_wait_warp(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
+                break;
+              const int i = q_lo + s * kBwdQ + t;
+              const bool in = i < a.Sq;
+              const int64_t vi = ((int64_t)b * a.Hq + h) * a.Sq + i;
+              vec[stage].lse2[t] = in ? a.lse2[vi] : INFINITY;
+              vec[stage].D[t] = in ? a.Dvec[vi] : 0.f;
+              if (general) {
+                vec[stage].qid[t] = in ? a.q_id[(int64_t)b * a.Sq + i] : -1;
+                vec[stage].qpos[t] = in ? a.q_pos[(int64_t)b * a.Sq + i] : 0;
+              }
+              mbar_arrive(&bars->qd_full[stage]);
+            }
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(a, 0x120 + warp);
+      *abort_flag = 1;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, kBwdQ, false, false);
+      constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, false, true);
+      constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, false, true);
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, kBwdQ, true, true);
+      const uint32_t k_addr = smem_u32(sm + L::kKOff), v_addr = smem_u32(sm + L::kVOff);
+      const uint32_t p_addr = smem_u32(sm + L::kPOff), ds_addr = smem_u32(sm + L::kDSOff);
+      uint32_t st = 0, kvc = 0, gc = 0;
+      bool ok = true;
+      auto stage_addr = [&](uint32_t x) {
+        return smem_u32(sm + L::kStageOff + (x % NS) * L::kStageBytes);
+      };
+      auto issue_s = [&](uint32_t x) -> bool {  // S^T = K Q^T
+        if (!mbar_wait(&bars->qd_full[x % NS], (x / NS) & 1)) return false;
+        if (x > 0 && !mbar_wait(&bars->s_free, (x - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t q_addr = stage_addr(x);
+#pragma unroll
+        for (int ks = 0; ks < DQK / 16; ++ks)
+          mma_ss(tmem + L::kColS,
+                 sdesc_sw128(k_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                 sdesc_sw128(q_addr + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id_s, ks > 0);
+        mma_commit(&bars->s_full);
+        return true;
+      };
+      auto issue_dp = [&](uint32_t x) -> bool {  // dP^T = V dO^T
+        if (x > 0 && !mbar_wait(&bars->dp_free, (x - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t o_addr = stage_addr(x) + L::kQBytes;
+#pragma unroll
+        for (int ks = 0; ks < DV / 16; ++ks)
+          mma_ss(tmem + L::kColDP,
+                 sdesc_sw128(v_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                 sdesc_sw128(o_addr + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id_s, ks > 0);
+        mma_commit(&bars->dp_full);
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+        const DkdvItem w = dkdv_item(a, idx);
+        for (int b = w.b0; b < w.b1 && ok; ++b) {
+          for (int g = w.g0; g < w.g1 && ok; ++g) {
+            int q_lo;
+            const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
+            if (nq == 0) continue;
+            const uint32_t nsteps = (uint32_t)nq * G;
+            if (!(ok = mbar_wait(&bars->kv_full, kvc & 1))) break;
+            ++kvc;
+            if (!(ok = issue_s(st))) break;
+            if (!(ok = issue_dp(st))) break;
+            for (uint32_t u = 0; u < nsteps; ++u) {
+              const uint32_t cur = st + u;
+              if (u + 1 < nsteps && !(ok = issue_s(cur + 1))) break;
+              if (!(ok = mbar_wait(&bars->p_ready, cur & 1))) break;
+              if (u == 0 && gc > 0 && !(ok = mbar_wait(&bars->acc_empty, (gc - 1) & 1))) break;
+              tc_fence_after();
+              const uint32_t qa = stage_addr(cur), oa = qa + L::kQBytes;
+#pragma unroll
+              for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dV += P^T dO
+                mma_ss(tmem + L::kColDV, sdesc_sw128(p_addr + ks * 32, 16, 1024),
+                       sdesc_sw128(oa + ks * 2048, 8192, 1024), id_dv, (u > 0 || ks > 0));
+              mma_commit(&bars->p_free);
+              if (u + 1 < nsteps && !(ok = issue_dp(cur + 1))) break;
+              if (!(ok = mbar_wait(&bars->ds_ready, cur & 1))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dK += dS^T Q
+                mma_ss(tmem + L::kColDK, sdesc_sw128(ds_addr + ks * 32, 16, 1024),
+                       sdesc_sw128(qa + ks * 2048, 8192, 1024), id_dk, (u > 0 || ks > 0));
+              if constexpr (ATOMIC) {  // dQ^T = K^T dS^T
+                const uint32_t buf = cur & 1;
+                if (cur >= 2 && !(ok = mbar_wait(&bars->dq_free[buf], ((cur >> 1) - 1) & 1))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks)
+                  mma_ss(tmem + L::kColDQ + buf * 64, sdesc_sw128(k_addr + ks * 2048, 16384, 1024),
+                         sdesc_sw128(ds_addr + ks * 2048, 8192, 1024), id_dq, ks > 0);
+                mma_commit(&bars->dq_full[buf]);
+              }
+              mma_commit(&bars->ds_free);
+              mma_commit(&bars->qd_empty[cur % NS]);
+            }
+            if (!ok) break;
+            mma_commit(&bars->acc_full);
+            mma_commit(&bars->kv_empty);
+            ++gc;
+            st += nsteps;
+          }
+        }
+      }
+      if (!ok) {
+        report_timeout(a, 0x130);
+        *abort_flag = 1;
+      }
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, 200000000ull);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ P / dS warps
+    const int j = tid - 128;  // KV row of the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t p_addr = smem_u32(sm + L::kPOff), ds_addr = smem_u32(sm + L::kDSOff);
+    const int nqc = (a.Sq + kChunk - 1) / kChunk;
+    uint32_t st = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      const DkdvItem w = dkdv_item(a, idx);
+      const int kj = w.t * kTile + j;
+      const bool row_ok = kj < a.Skv;
+      for (int b = w.b0; b < w.b1 && ok; ++b) {
+        for (int g = w.g0; g < w.g1 && ok; ++g) {
+          int q_lo;
+          const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
+          if (nq == 0) continue;
+          const int64_t gk = (int64_t)b * a.Skv + kj;
+          int qlo = 0, qhi = 0, my_id = 0, my_pos = 0;
+          if (row_ok) {
+            if (!general) {
+              const int sl = a.kv_seg_lo[gk], sh = a.kv_seg_hi[gk];
+              qlo = a.causal ? max(kj, sl) : sl;
+              qhi = sh;
+            } else {
+              my_id = a.kv_id[gk];
+              my_pos = a.kv_pos[gk];
+            }
+          }
+          for (int hh = 0; hh < G && ok; ++hh) {
+            const int h = g * G + hh;
+            const int bb = a.bias_b > 1 ? b : 0, bh = a.bias_h > 1 ? h : 0;
+            const int64_t bias_base = ((int64_t)bb * a.bias_h + bh) * a.Sq;
+            for (int s = 0; s < nq; ++s, ++st) {
+              const uint32_t cur = st;
+              const int stage = cur % NS;
+              const int q0 = q_lo + s * kBwdQ;
+              float x[kBwdQ];
+              if (!(ok = mbar_wait_warp(&bars->qd_full[stage], (cur / NS) & 1))) break;
+              if (!(ok = mbar_wait_warp(&bars->s_full, cur & 1))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int q = 0; q < kBwdQ / 32; ++q) {
+                uint32_t u[32];
+                tmem_ld32x32b_x32(tmem + lane_base + L::kColS + q * 32, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
+              }
+              tc_fence_before();
+              mbar_arrive(&bars->s_free);
+              const StageVec& V = vec[stage];
+              if (HAS_BIAS && row_ok) {
+                const bf16* bp = a.bias + (bias_base + q0) * a.Skv + kj;
+#pragma unroll 8
+                for (int c = 0; c < kBwdQ; ++c)
+                  if (q0 + c < a.Sq) x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
+              }
+              bool full;
+              if (!general) {
+                full = row_ok && q0 >= qlo && q0 + kBwdQ <= qhi;
+              } else {
+                full = false;
+                if (row_ok && my_id != 0 && q0 + kBwdQ <= a.Sq) {
+                  const ChunkInfo ci = a.q_chunk[b * nqc + q0 / kChunk];
+                  full = ci.uniform && ci.min_id == my_id && (!a.causal || ci.min_pos >= my_pos);
+                }
+              }
+#pragma unroll
+              for (int c = 0; c < kBwdQ; ++c) {
+                bool valid = true;
+                if (!full) {
+                  if (!general) valid = (q0 + c >= qlo) && (q0 + c < qhi);
+                  else valid = V.qid[c] == my_id && my_id != 0 && (!a.causal || my_pos <= V.qpos[c]);
+                }
+                x[c] = valid ? ex2_approx(x[c] - V.lse2[c]) : 0.f;
+              }
+              // P^T row j -> shared memory (K-major, 128-byte swizzle)
+              if (cur > 0 && !(ok = mbar_wait_warp(&bars->p_free, (cur - 1) & 1))) break;
+#pragma unroll
+              for (int u8 = 0; u8 < 8; ++u8) {
+                const float* p8 = x + u8 * 8;
+                st_shared_v4(p_addr + j * 128 + ((u8 ^ (j & 7)) << 4), pack_bf16x2(p8[0], p8[1]),
+                             pack_bf16x2(p8[2], p8[3]), pack_bf16x2(p8[4], p8[5]),
+                             pack_bf16x2(p8[6], p8[7]));
+              }
+              fence_proxy_async_smem();
+              mbar_arrive(&bars->p_ready);
+              // dS^T = P^T (dP^T - D)
+              if (!(ok = mbar_wait_warp(&bars->dp_full, cur & 1))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int q = 0; q < kBwdQ / 32; ++q) {
+                uint32_t u[32];
+                tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + q * 32, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  const int c = q * 32 + e;
+                  x[c] = x[c] * (__uint_as_float(u[e]) - V.D[c]);
+                }
+              }
+              tc_fence_before();
+              mbar_arrive(&bars->dp_free);
+              if (cur > 0 && !(ok = mbar_wait_warp(&bars->ds_free, (cur - 1) & 1))) break;
+#pragma unroll
+              for (int u8 = 0; u8 < 8; ++u8) {
+                const float* p8 = x + u8 * 8;
+                st_shared_v4(ds_addr + j * 128 + ((u8 ^ (j & 7)) << 4), pack_bf16x2(p8[0], p8[1]),
+                             pack_bf16x2(p8[2], p8[3]), pack_bf16x2(p8[4], p8[5]),
+                             pack_bf16x2(p8[6], p8[7]));
+              }
+              fence_proxy_async_smem();
+              mbar_arrive(&bars->ds_ready);
+              if (DBIAS != 0 && row_ok) {
+                if (DBIAS == 1) {
+                  bf16* dp = a.dbias + (bias_base + q0) * a.Skv + kj;
+#pragma unroll 8
+                  for (int c = 0; c < kBwdQ; ++c)
+                    if (q0 + c < a.Sq) dp[(int64_t)c * a.Skv] = __float2bfloat16_rn(x[c]);
+                } else {
+                  float* dp = a.dbias_acc + (bias_base + q0) * a.Skv + kj;
+#pragma unroll 8
+                  for (int c = 0; c < kBwdQ; ++c)
+                    if (q0 + c < a.Sq) dp[(int64_t)c * a.Skv] += x[c];
+                }
+              }
+              mbar_arrive(&bars->qd_empty[stage]);
+            }
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(a, 0x140 + (warp & 3));
+      *abort_flag = 1;
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+    const int j = tid - 256;  // TMEM lane: KV row for dK/dV, head-dim index for dQ^T
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t st = 0, gc = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      const DkdvItem w = dkdv_item(a, idx);
+      const int kj = w.t * kTile + j;
+      const bool row_ok = kj < a.Skv;
+      for (int b = w.b0; b < w.b1 && ok; ++b) {
+        for (int g = w.g0; g < w.g1 && ok; ++g) {
+          int q_lo;
+          const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
+          bf16* dv_row = a.dv + ((int64_t)b * a.Skv + kj) * a.dv_stride + (int64_t)g * DV;
+          bf16* dk_row = a.dk + ((int64_t)b * a.Skv + kj) * a.dk_stride + (int64_t)g * DQK;
+          if (nq == 0) {
+            if (row_ok) {
+#pragma unroll
+              for (int c = 0; c < DV; c += 8)
+                *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+              for (int c = 0; c < DQK; c += 8)
+                *reinterpret_cast<uint4*>(dk_row + c) = make_uint4(0, 0, 0, 0);
+            }
+            continue;
+          }
+          if constexpr (ATOMIC) {
+            for (int hh = 0; hh < G && ok; ++hh) {
+              const int h = g * G + hh;
+              for (int s = 0; s < nq; ++s, ++st) {
+                const uint32_t buf = st & 1;
+                if (!(ok = mbar_wait_warp(&bars->dq_full[buf], (st >> 1) & 1))) break;
+                tc_fence_after();
+                uint32_t u0[32], u1[32];
+                tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + buf * 64, u0);
+                tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + buf * 64 + 32, u1);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&bars->dq_free[buf]);
+                if (j < DQK) {
+                  const int q0 = q_lo + s * kBwdQ;
+                  float* base = a.dq_acc + (((int64_t)b * a.Sq + q0) * a.Hq + h) * DQK + j;
+                  const int64_t rs = (int64_t)a.Hq * DQK;
+                  const int nv = min(kBwdQ, a.Sq - q0);
+#pragma unroll
+                  for (int c = 0; c < 32; ++c)
+                    if (c < nv) red_add_f32(base + c * rs, __uint_as_float(u0[c]) * a.scale);
+#pragma unroll
+                  for (int c = 0; c < 32; ++c)
+                    if (32 + c < nv) red_add_f32(base + (32 + c) * rs, __uint_as_float(u1[c]) * a.scale);
+                }
+              }
+            }
+            if (!ok) break;
+          }
+          if (!(ok = mbar_wait_warp(&bars->acc_full, gc & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < DV / 32; ++q) {
+            uint32_t u[32];
+            tmem_ld32x32b_x32(tmem + lane_base + L::kColDV + q * 32, u);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+                v.y = pack_bf16x2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
+                v.z = pack_bf16x2(__uint_as_float(u[c + 4]), __uint_as_float(u[c + 5]));
+                v.w = pack_bf16x2(__uint_as_float(u[c + 6]), __uint_as_float(u[c + 7]));
+                *reinterpret_cast<uint4*>(dv_row + q * 32 + c) = v;
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < DQK / 32; ++q) {
+            uint32_t u[32];
+            tmem_ld32x32b_x32(tmem + lane_base + L::kColDK + q * 32, u);
+            tmem_ld_wait();
+            if (row_ok) {
+              const float sc = a.scale;
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(u[c]) * sc, __uint_as_float(u[c + 1]) * sc);
+                v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * sc, __uint_as_float(u[c + 3]) * sc);
+                v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * sc, __uint_as_float(u[c + 5]) * sc);
+                v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * sc, __uint_as_float(u[c + 7]) * sc);
+                *reinterpret_cast<uint4*>(dk_row + q * 32 + c) = v;
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&bars->acc_empty);
+          ++gc;
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(a, 0x150 + (warp & 3));
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =========================================================== deterministic dQ pass
+template <int DQK, int DV>
+struct DqLayout {
+  static constexpr int kQBytes = kTile * DQK * 2;
+  static constexpr int kOBytes = kTile * DV * 2;
+  static constexpr int kKBytes = kTile * DQK * 2;
+  static constexpr int kVBytes = kTile * DV * 2;
+  static constexpr int kSBytes = kTile * kTile * 2;
+  static constexpr int kBase = kQBytes + kOBytes + kSBytes;
+  static constexpr int kLimit = 224 * 1024;
+  static constexpr int kKStages = (kBase + 2 * kKBytes + kVBytes <= kLimit) ? 2 : 1;
+  static constexpr int kVStages = (kBase + kKStages * kKBytes + 2 * kVBytes <= kLimit) ? 2 : 1;
+  static constexpr int kQOff = 0;
+  static constexpr int kOOff = kQBytes;
+  static constexpr int kSOff = kQBytes + kOBytes;
+  static constexpr int kKOff = kSOff + kSBytes;
+  static constexpr int kVOff = kKOff + kKStages * kKBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kVBytes;
+  static constexpr int kBytes = kBarOff + 256;
+  static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+};
+
+struct DqBars {
+  uint64_t q_full, q_empty, s_full, s_free, dp_full, dp_free, ds_ready, ds_free, acc_full,
+      acc_empty, drain;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+};
+
+template <int DQK, int DV, bool HAS_BIAS>
+__global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ KernelArgs a) {
+  using L = DqLayout<DQK, DV>;
+  constexpr int KS = L::kKStages, VS = L::kVStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  DqBars* bars = reinterpret_cast<DqBars*>(sm + L::kBarOff);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(DqBars));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_items = a.B * a.n_qt * a.Hq;
+
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 128);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 128);
+    mbar_init(&bars->ds_ready, 128);
+    mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, 128);
+    mbar_init(&bars->drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool general = path_general(a);
+
+  auto item_of = [&](int idx, int& b, int& t, int& h, int& kv_lo, int& n) {
+    const int per_t = a.B * a.Hq;
+    const int t_rev = idx / per_t, rem = idx - t_rev * per_t;
+    t = a.n_qt - 1 - t_rev;
+    b = rem / a.Hq;
+    h = rem - b * a.Hq;
+    const int2 r = a.q_tile_range[b * a.n_qt + t];
+    kv_lo = r.x;
+    n = (r.y > r.x) ? (r.y - r.x + kTile - 1) / kTile : 0;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tensormap(&a.tm_q);
+      prefetch_tensormap(&a.tm_k);
+      prefetch_tensormap(&a.tm_v);
+      prefetch_tensormap(&a.tm_do);
+      uint32_t kt = 0, it = 0, k_loads = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+        int b, t, h, kv_lo, n;
+        item_of(idx, b, t, h, kv_lo, n);
+        if (n == 0) continue;
+        if (it > 0 && !(ok = mbar_wait(&bars->q_empty, (it - 1) & 1))) break;
+        const int qrow = b * a.Sq + t * kTile;
+        mbar_arrive_expect_tx(&bars->q_full, L::kQBytes + L::kOBytes);
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->q_full, c * 64, h, qrow);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_3d(sm + L::kOOff + c * 16384, &a.tm_do, &bars->q_full, c * 64, h, qrow);
+        ++it;
+        const int g = h / (a.Hq / a.Hkv);
+        for (int j = 0; j < n; ++j, ++kt) {
+          const int krow = b * a.Skv + kv_lo + j * kTile;
+          const int ks = kt % KS, vs = kt % VS;
+          if (kt >= (uint32_t)KS && !(ok = mbar_wait(&bars->k_empty[ks], ((kt / KS) - 1) & 1)))
+            break;
+          mbar_arrive_expect_tx(&bars->k_full[ks], L::kKBytes);
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c)
+            tma_load_3d(sm + L::kKOff + ks * L::kKBytes + c * 16384, &a.tm_k, &bars->k_full[ks],
+                        c * 64, g, krow);
+          ++k_loads;
+          if (kt >= (uint32_t)VS && !(ok = mbar_wait(&bars->v_empty[vs], ((kt / VS) - 1) & 1)))
+            break;
+          mbar_arrive_expect_tx(&bars->v_full[vs], L::kVBytes);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_3d(sm + L::kVOff + vs * L::kVBytes + c * 16384, &a.tm_v, &bars->v_full[vs],
+                        c * 64, g, krow);
+        }
+      }
+      if (!ok) {
+        report_timeout(a, 0x210);
+        *abort_flag = 1;
+      }
+      if (*abort_flag) {
+        if (it > 0) mbar_wait(&bars->q_full, (it - 1) & 1, 100000000ull);
+        for (uint32_t u = (k_loads > 2u ? k_loads - 2u : 0u); u < k_loads; ++u)
+          mbar_wait(&bars->k_full[u % KS], (u / KS) & 1, 100000000ull);
+        for (uint32_t u = (kt > 2u ? kt - 2u : 0u); u < kt; ++u)
+          mbar_wait(&bars->v_full[u % VS], (u / VS) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, false, true);
+      const uint32_t q_addr = smem_u32(sm + L::kQOff), o_addr = smem_u32(sm + L::kOOff);
+      const uint32_t s_addr = smem_u32(sm + L::kSOff);
+      uint32_t kt = 0, it = 0;
+      bool ok = true;
+      auto issue_s = [&](uint32_t k) -> bool {  // S = Q K^T
+        const int ks_ = k % KS;
+        if (!mbar_wait(&bars->k_full[ks_], (k / KS) & 1)) return false;
+        if (k > 0 && !mbar_wait(&bars->s_free, (k - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sm + L::kKOff + ks_ * L::kKBytes);
+#pragma unroll
+        for (int ks = 0; ks < DQK / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(tmem + L::kColS, sdesc_sw128(q_addr + off, 16, 1024),
+                 sdesc_sw128(k_addr + off, 16, 1024), id_s, ks > 0);
+        }
+        mma_commit(&bars->s_full);
+        return true;
+      };
+      auto issue_dp = [&](uint32_t k) -> bool {  // dP = dO V^T
+        const int vs = k % VS;
+        if (!mbar_wait(&bars->v_full[vs], (k / VS) & 1)) return false;
+        if (k > 0 && !mbar_wait(&bars->dp_free, (k - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sm + L::kVOff + vs * L::kVBytes);
+#pragma unroll
+        for (int ks = 0; ks < DV / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(tmem + L::kColDP, sdesc_sw128(o_addr + off, 16, 1024),
+                 sdesc_sw128(v_addr + off, 16, 1024), id_s, ks > 0);
+        }
+        mma_commit(&bars->dp_full);
+        mma_commit(&bars->v_empty[vs]);
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+        int b, t, h, kv_lo, n;
+        item_of(idx, b, t, h, kv_lo, n);
+        if (n == 0) continue;
+        if (!(ok = mbar_wait(&bars->q_full, it & 1))) break;
+        if (!(ok = issue_s(kt)) || !(ok = issue_dp(kt))) break;
+        for (int j = 0; j < n; ++j) {
+          const uint32_t k = kt + j;
+          const bool more = j + 1 < n;
+          if (KS >= 2 && more) {
+            if (!(ok = issue_s(k + 1)) || !(ok = issue_dp(k + 1))) break;
+          }
+          if (!more) mma_commit(&bars->q_empty);  // last S / dP of the item issued
+          if (!(ok = mbar_wait(&bars->ds_ready, k & 1))) break;
+          if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->acc_empty, (it - 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sm + L::kKOff + (k % KS) * L::kKBytes);
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)  // dQ += dS K
+            mma_ss(tmem + L::kColDQ,
+                   sdesc_sw128(s_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                   sdesc_sw128(k_addr + ks * 2048, 16384, 1024), id_dq, (j > 0 || ks > 0));
+          mma_commit(&bars->ds_free);
+          mma_commit(&bars->k_empty[k % KS]);
+          if (KS == 1 && more) {
+            if (!(ok = issue_s(k + 1)) || !(ok = issue_dp(k + 1))) break;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bars->acc_full);
+        kt += n;
+        ++it;
+      }
+      if (!ok) {
+        report_timeout(a, 0x230);
+        *abort_flag = 1;
+      }
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    const int r = tid - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = smem_u32(sm + L::kSOff);
+    uint32_t kt = 0, it = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      int b, t, h, kv_lo, n;
+      item_of(idx, b, t, h, kv_lo, n);
+      const int i = t * kTile + r;
+      const bool row_ok = i < a.Sq;
+      const int64_t grow = (int64_t)b * a.Sq + i;
+      bf16* dq_row = a.dq + grow * a.dq_stride + (int64_t)h * DQK;
+      if (n == 0) {
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < DQK; c += 8)
+            *reinterpret_cast<uint4*>(dq_row + c) = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      int rlo = 0, rhi = 0, my_id = 0, my_pos = 0;
+      float lse2 = INFINITY, Di = 0.f;
+      if (row_ok) {
+        if (!general) {
+          const int sl = a.seg_lo[grow], sh = a.seg_hi[grow];
+          rlo = sl;
+          rhi = a.causal ? min(i + 1, sh) : sh;
+        } else {
+          my_id = a.q_id[grow];
+          my_pos = a.q_pos[grow];
+        }
+        const int64_t vi = ((int64_t)b * a.Hq + h) * a.Sq + i;
+        lse2 = a.lse2[vi];
+        Di = a.Dvec[vi];
+      }
+      const bf16* bias_row = nullptr;
+      if (HAS_BIAS && row_ok) {
+        const int bb = a.bias_b > 1 ? b : 0, bh = a.bias_h > 1 ? h : 0;
+        bias_row = a.bias + (((int64_t)bb * a.bias_h + bh) * a.Sq + i) * a.Skv;
+      }
+      for (int j = 0; j < n; ++j) {
+        const uint32_t k = kt + j;
+        const int k0 = kv_lo + j * kTile;
+        float x[kTile];
+        if (!(ok = mbar_wait_warp(&bars->s_full, k & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < kTile / 32; ++q) {
+          uint32_t u[32];
+          tmem_ld32x32b_x32(tmem + lane_base + L::kColS + q * 32, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->s_free);
+        if (HAS_BIAS && row_ok) {
+          const bf16* bp = bias_row + k0;
+          const int nv = min(kTile, a.Skv - k0);
+#pragma unroll 8
+          for (int c = 0; c < kTile; ++c)
+            if (c < nv) x[c] += __bfloat162float(bp[c]) * kLog2e;
+        }
+        bool full;
+        if (!general) {
+          full = (k0 >= rlo) && (k0 + kTile <= rhi);
+        } else {
+          full = false;
+          if (k0 + kTile <= a.Skv && my_id != 0) {
+            const int nkc = (a.Skv + kChunk - 1) / kChunk;
+            const ChunkInfo c0 = a.kv_chunk[b * nkc + k0 / kChunk];
+            const ChunkInfo c1 = a.kv_chunk[b * nkc + k0 / kChunk + 1];
+            full = c0.uniform && c1.uniform && c0.min_id == my_id && c1.min_id == my_id &&
+                   (!a.causal || max(c0.max_pos, c1.max_pos) <= my_pos);
+          }
+        }
+        if (!full) {
+          const int32_t* kid = a.kv_id + (int64_t)b * a.Skv + k0;
+          const int32_t* kpos = a.kv_pos + (int64_t)b * a.Skv + k0;
+          const int nv = min(kTile, a.Skv - k0);
+#pragma unroll
+          for (int c = 0; c < kTile; ++c) {
+            bool v;
+            if (!general) v = (k0 + c >= rlo) && (k0 + c < rhi);
+            else
+              v = c < nv && __ldg(kid + c) == my_id && my_id != 0 &&
+                  (!a.causal || __ldg(kpos + c) <= my_pos);
+            if (!v) x[c] = -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) x[c] = ex2_approx(x[c] - lse2);
+        if (!(ok = mbar_wait_warp(&bars->dp_full, k & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < kTile / 32; ++q) {
+          uint32_t u[32];
+          tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + q * 32, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[q * 32 + e] *= (__uint_as_float(u[e]) - Di);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->dp_free);
+        if (k > 0 && !(ok = mbar_wait_warp(&bars->ds_free, (k - 1) & 1))) break;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+          for (int u8 = 0; u8 < 8; ++u8) {
+            const float* p8 = x + cc * 64 + u8 * 8;
+            st_shared_v4(s_addr + cc * 16384 + r * 128 + ((u8 ^ (r & 7)) << 4),
+                         pack_bf16x2(p8[0], p8[1]), pack_bf16x2(p8[2], p8[3]),
+                         pack_bf16x2(p8[4], p8[5]), pack_bf16x2(p8[6], p8[7]));
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->ds_ready);
+      }
+      if (!ok) break;
+      if (!(ok = mbar_wait_warp(&bars->acc_full, it & 1))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < DQK / 32; ++q) {
+        uint32_t u[32];
+        tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + q * 32, u);
+        tmem_ld_wait();
+        if (row_ok) {
+          const float sc = a.scale;
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(u[c]) * sc, __uint_as_float(u[c + 1]) * sc);
+            v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * sc, __uint_as_float(u[c + 3]) * sc);
+            v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * sc, __uint_as_float(u[c + 5]) * sc);
+            v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * sc, __uint_as_float(u[c + 7]) * sc);
+            *reinterpret_cast<uint4*>(dq_row + q * 32 + c) = v;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->acc_empty);
+      kt += n;
+      ++it;
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(a, 0x240 + (warp & 3));
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =========================================================== launchers
+template <typename K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int DQK, int DV, bool AT, bool HB, int DB>
+cudaError_t dkdv_go(const KernelArgs& a, int nsm, cudaStream_t st) {
+  using L = DkdvLayout<DQK, DV>;
+  auto kern = dkdv_kernel<DQK, DV, AT, HB, DB>;
+  cudaError_t e = set_smem(kern, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int nb = a.dkdv_batch_loop ? 1 : a.B, ng = a.dkdv_head_loop ? 1 : a.Hkv;
+  const int items = a.n_kt * nb * ng;
+  const int grid = items < nsm ? items : nsm;
+  kern<<<grid, 384, L::kAlloc, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DQK, int DV, bool AT>
+cudaError_t dkdv_bias(const KernelArgs& a, int nsm, cudaStream_t st) {
+  if (!a.bias) return dkdv_go<DQK, DV, AT, false, 0>(a, nsm, st);
+  if (a.dbias_mode == 0) return dkdv_go<DQK, DV, AT, true, 0>(a, nsm, st);
+  if (a.dbias_mode == 1) return dkdv_go<DQK, DV, AT, true, 1>(a, nsm, st);
+  return dkdv_go<DQK, DV, AT, true, 2>(a, nsm, st);
+}
+
+template <int DQK, int DV>
+cudaError_t dq_go(const KernelArgs& a, int nsm, cudaStream_t st) {
+  using L = DqLayout<DQK, DV>;
+  auto kern = a.bias ? dq_kernel<DQK, DV, true> : dq_kernel<DQK, DV, false>;
+  cudaError_t e = set_smem(kern, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int items = a.B * a.n_qt * a.Hq;
+  const int grid = items < nsm ? items : nsm;
+  kern<<<grid, 256, L::kAlloc, st>>>(a);
+  return cudaGetLastError();
+}
+
+int blocks_for(int64_t n, int per_block) {
+  const int64_t b = (n + per_block - 1) / per_block;
+  return static_cast<int>(b < 4096 ? (b > 0 ? b : 1) : 4096);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st) {
+  cudaError_t e;
+  if (zero_dq_acc) {
+    e = cudaMemsetAsync(a.dq_acc, 0, (size_t)a.B * a.Sq * a.Hq * a.d_qk * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  const size_t nb = (size_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
+  if (a.dbias_mode == 1) {
+    e = cudaMemsetAsync(a.dbias, 0, nb * sizeof(bf16), st);
+    if (e != cudaSuccess) return e;
+  } else if (a.dbias_mode == 2) {
+    e = cudaMemsetAsync(a.dbias_acc, 0, nb * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t rows = (int64_t)a.B * a.Sq * a.Hq;
+  const int mode = zero_dq_acc ? 0 : 1;
+  if (a.d_v == 64)
+    bwd_pre_kernel<64><<<blocks_for(rows, 8 * 4), 256, 0, st>>>(a, mode);
+  else
+    bwd_pre_kernel<128><<<blocks_for(rows, 8 * 2), 256, 0, st>>>(a, mode);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic, int nsm, cudaStream_t st) {
+#define DKDV_CASE(DQ, DVV)                                                                  \
+  if (a.d_qk == DQ && a.d_v == DVV)                                                         \
+    return atomic ? dkdv_bias<DQ, DVV, true>(a, nsm, st) : dkdv_bias<DQ, DVV, false>(a, nsm, st);
+  DKDV_CASE(64, 64)
+  DKDV_CASE(64, 128)
+  DKDV_CASE(128, 64)
+  DKDV_CASE(128, 128)
+#undef DKDV_CASE
+  if (a.d_qk == 192 && !atomic) {
+    if (a.d_v == 64) return dkdv_bias<192, 64, false>(a, nsm, st);
+    if (a.d_v == 128) return dkdv_bias<192, 128, false>(a, nsm, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_dq(const KernelArgs& a, int nsm, cudaStream_t st) {
+  if (a.d_v == 64) {
+    if (a.d_qk == 64) return dq_go<64, 64>(a, nsm, st);
+    if (a.d_qk == 128) return dq_go<128, 64>(a, nsm, st);
+    if (a.d_qk == 192) return dq_go<192, 64>(a, nsm, st);
+  } else if (a.d_v == 128) {
+    if (a.d_qk == 64) return dq_go<64, 128>(a, nsm, st);
+    if (a.d_qk == 128) return dq_go<128, 128>(a, nsm, st);
+    if (a.d_qk == 192) return dq_go<192, 128>(a, nsm, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dq_convert(const KernelArgs& a, cudaStream_t st) {
+  const int64_t n = (int64_t)a.B * a.Sq * a.Hq * a.d_qk / 8;
+  dq_convert_kernel<<<blocks_for(n, 256), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dbias_convert(const KernelArgs& a, cudaStream_t st) {
+  const int64_t n = (int64_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
+  dbias_convert_kernel<<<blocks_for(n, 256), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

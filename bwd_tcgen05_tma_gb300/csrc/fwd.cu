@@ -1,0 +1,487 @@
+// Forward pass: O = softmax(scale * Q K^T + bias, masked) V and LSE, per
+// 128-row query tile of one (batch row, query head).
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 0      TMA producer: Q tile once per work item, K/V tiles through a
+//               ring of shared-memory stages;
+//   warp 1      allocates tensor memory; lane 0 issues the tcgen05 MMAs
+//               S = Q K^T (into one of two TMEM S buffers) and O += P V
+//               (O accumulates in TMEM);
+//   warps 4-7   softmax warpgroup: thread r owns query row r (TMEM lane r):
+//               reads S, applies scale/bias/mask, keeps the running max and
+//               sum, writes bf16 P to shared memory, and at the end scales O
+//               by 1/l and stores O and LSE.
+// S(j+1) is issued before P(j) V(j), so the tensor core works on the next
+// score tile while the softmax warps exponentiate the current one.  O is only
+// rescaled when the running max grows by more than 2^8 (in log2 units); below
+// that the stale max is kept for both P and l, which leaves O / l exact.
+//
+// Outputs and semantics: TransformerEngine PR #3516 diagram (fused-attention
+// forward feeding the backward with O and the softmax statistics); rows with
+// no valid key get O = 0, LSE = -inf.
+#include <cmath>
+
+#include "attn_internal.cuh"
+
+namespace attn {
+namespace {
+using namespace sm103;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int DQK, int DV>
+struct FwdLayout {
+  static constexpr int kQBytes = kTile * DQK * 2;
+  static constexpr int kKBytes = kTile * DQK * 2;
+  static constexpr int kVBytes = kTile * DV * 2;
+  static constexpr int kPBytes = kTile * kTile * 2;
+  // K and V have separate rings: K(j) is free once S(j) is done, V(j) once P(j) V(j) is.
+  static constexpr int kKStages = 2;
+  static constexpr int kVStages = (kQBytes + 2 * kKBytes + 2 * kVBytes + kPBytes <= 210 * 1024) ? 2 : 1;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + kKStages * kKBytes;
+  static constexpr int kPOff = kVOff + kVStages * kVBytes;
+  static constexpr int kBarOff = kPOff + kPBytes;
+  static constexpr int kBytes = kBarOff + 256;
+  // at least ~116 KB so two CTAs never share an SM (each allocates all of TMEM)
+  static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;    // two S buffers: [0,128) and [128,256)
+  static constexpr uint32_t kColO = 256;  // O: [256, 256+DV)
+};
+
+struct Bars {
+  uint64_t q_full, q_empty, p_full, pv_done, o_empty, drain;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_empty[2];
+};
+
+struct FwdItem {
+  int b, t, h, kv_lo, kv_hi, n;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const KernelArgs& a, int idx) {
+  const int per_t = a.B * a.Hq;
+  const int t_rev = idx / per_t, rem = idx - t_rev * per_t;
+  FwdItem it;
+  it.t = a.n_qt - 1 - t_rev;  // longest causal rows first
+  it.b = rem / a.Hq;
+  it.h = rem - it.b * a.Hq;
+  const int2 r = a.q_tile_range[it.b * a.n_qt + it.t];
+  it.kv_lo = r.x;
+  it.kv_hi = r.y;
+  it.n = (r.y > r.x) ? (r.y - r.x + kTile - 1) / kTile : 0;
+  return it;
+}
+
+// Adds bias[i, k0 + c] * log2(e) to x[c] for c < nvalid (row pointer given).
+__device__ __forceinline__ void add_bias_row(float (&x)[kTile], const bf16* row, int nvalid) {
+  const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
+#pragma unroll
+  for (int c = 0; c < kTile; c += 8) {
+    if (vec && c + 8 <= nvalid) {
+      const uint4 u = ld_nc_v4(row + c);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[c + 2 * e] += __uint_as_float(w[e] << 16) * kLog2e;
+        x[c + 2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u) * kLog2e;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (c + e < nvalid) x[c + e] += __bfloat162float(row[c + e]) * kLog2e;
+    }
+  }
+}
+
+template <int DQK, int DV, bool HAS_BIAS>
+__global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ KernelArgs a) {
+  using L = FwdLayout<DQK, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  Bars* bars = reinterpret_cast<Bars*>(sm + L::kBarOff);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(Bars));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_items = a.B * a.n_qt * a.Hq;
+
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->o_empty, 128);
+    mbar_init(&bars->drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_empty[s], 128);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool general = path_general(a);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&a.tm_q);
+      prefetch_tensormap(&a.tm_k);
+      prefetch_tensormap(&a.tm_v);
+      uint32_t kt = 0, it = 0, q_loads = 0, k_loads = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+        const FwdItem w = fwd_item(a, idx);
+        if (w.n == 0) continue;
+        if (it > 0 && !(ok = mbar_wait(&bars->q_empty, (it - 1) & 1))) break;
+        ++q_loads;
+        mbar_arrive_expect_tx(&bars->q_full, L::kQBytes);
+        const int qrow = w.b * a.Sq + w.t * kTile;
+#pragma unroll
+        for (int c = 0; c < DQK / 64; ++c)
+          tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->q_full, c * 64, w.h, qrow);
+        const int g = w.h / (a.Hq / a.Hkv);
+        for (int j = 0; j < w.n; ++j, ++kt) {
+          const int krow = w.b * a.Skv + w.kv_lo + j * kTile;
+          const int ks = kt % L::kKStages, vs = kt % L::kVStages;
+          if (kt >= (uint32_t)L::kKStages &&
+              !(ok = mbar_wait(&bars->k_empty[ks], ((kt / L::kKStages) - 1) & 1)))
+            break;
+          uint8_t* kst = sm + L::kKOff + ks * L::kKBytes;
+          mbar_arrive_expect_tx(&bars->k_full[ks], L::kKBytes);
+#pragma unroll
+          for (int c = 0; c < DQK / 64; ++c)
+            tma_load_3d(kst + c * 16384, &a.tm_k, &bars->k_full[ks], c * 64, g, krow);
+          ++k_loads;
+          if (kt >= (uint32_t)L::kVStages &&
+              !(ok = mbar_wait(&bars->v_empty[vs], ((kt / L::kVStages) - 1) & 1)))
+            break;
+          uint8_t* vst = sm + L::kVOff + vs * L::kVBytes;
+          mbar_arrive_expect_tx(&bars->v_full[vs], L::kVBytes);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_3d(vst + c * 16384, &a.tm_v, &bars->v_full[vs], c * 64, g, krow);
+        }
+        if (!ok) break;
+        ++it;
+      }
+      if (!ok) {
+        report_timeout(a, 0x10);
+        *abort_flag = 1;
+      }
+      // let every copy this thread issued land before the CTA can exit
+      if (*abort_flag) {
+        if (q_loads > 0) mbar_wait(&bars->q_full, (q_loads - 1) & 1, 100000000ull);
+        for (uint32_t u = (k_loads > 2u ? k_loads - 2u : 0u); u < k_loads; ++u)
+          mbar_wait(&bars->k_full[u % L::kKStages], (u / L::kKStages) & 1, 100000000ull);
+        for (uint32_t u = (kt > 2u ? kt - 2u : 0u); u < kt; ++u)
+          mbar_wait(&bars->v_full[u % L::kVStages], (u / L::kVStages) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, DV, false, true);
+      const uint32_t q_addr = smem_u32(sm + L::kQOff);
+      const uint32_t p_addr = smem_u32(sm + L::kPOff);
+      uint32_t kt = 0, it = 0;
+      bool ok = true;
+      auto issue_s = [&](uint32_t k) -> bool {
+        const int s = k % L::kKStages, sb = k & 1;
+        if (!mbar_wait(&bars->k_full[s], (k / L::kKStages) & 1)) return false;
+        if (k >= 2 && !mbar_wait(&bars->s_empty[sb], ((k >> 1) - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sm + L::kKOff + s * L::kKBytes);
+#pragma unroll
+        for (int ks = 0; ks < DQK / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(tmem + L::kColS + sb * kTile, sdesc_sw128(q_addr + off, 16, 1024),
+                 sdesc_sw128(k_addr + off, 16, 1024), idesc_s, ks > 0);
+        }
+        mma_commit(&bars->s_full[sb]);
+        mma_commit(&bars->k_empty[s]);
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+        const FwdItem w = fwd_item(a, idx);
+        if (w.n == 0) continue;
+        if (!(ok = mbar_wait(&bars->q_full, it & 1))) break;
+        if (!(ok = issue_s(kt))) break;
+        for (int j = 0; j < w.n; ++j) {
+          const uint32_t k = kt + j;
+          if (j + 1 < w.n) {
+            if (!(ok = issue_s(k + 1))) break;
+          } else {
+            mma_commit(&bars->q_empty);  // every S MMA of this item has been issued
+          }
+          if (!(ok = mbar_wait(&bars->p_full, k & 1))) break;
+          if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->o_empty, (it - 1) & 1))) break;
+          const int s = k % L::kVStages;
+          if (!(ok = mbar_wait(&bars->v_full[s], (k / L::kVStages) & 1))) break;
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(sm + L::kVOff + s * L::kVBytes);
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks) {
+            const uint32_t poff = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(tmem + L::kColO, sdesc_sw128(p_addr + poff, 16, 1024),
+                   sdesc_sw128(v_addr + ks * 2048, 16384, 1024), idesc_o, (j > 0 || ks > 0));
+          }
+          mma_commit(&bars->pv_done);
+          mma_commit(&bars->v_empty[s]);
+        }
+        if (!ok) break;
+        kt += w.n;
+        ++it;
+      }
+      if (!ok) {
+        report_timeout(a, 0x20);
+        *abort_flag = 1;
+      }
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int r = tid - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t p_addr = smem_u32(sm + L::kPOff);
+    uint32_t kt = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      const FwdItem w = fwd_item(a, idx);
+      const int i = w.t * kTile + r;
+      const bool row_ok = i < a.Sq;
+      const int64_t grow = (int64_t)w.b * a.Sq + i;
+      bf16* orow = a.o + (grow * a.Hq + w.h) * DV;
+      float* lse_out = a.lse + ((int64_t)w.b * a.Hq + w.h) * a.Sq + i;
+      if (w.n == 0) {
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < DV; c += 8)
+            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+          *lse_out = -INFINITY;
+        }
+        continue;
+      }
+      int rlo = 0, rhi = 0, my_id = 0, my_pos = 0;
+      if (row_ok) {
+        if (!general) {
+          const int sl = a.seg_lo[grow], sh = a.seg_hi[grow];
+          rlo = sl;
+          rhi = a.causal ? min(i + 1, sh) : sh;
+        } else {
+          my_id = a.q_id[grow];
+          my_pos = a.q_pos[grow];
+        }
+      }
+      const bf16* bias_row = nullptr;
+      if (HAS_BIAS && row_ok) {
+        const int bb = a.bias_b > 1 ? w.b : 0, bh = a.bias_h > 1 ? w.h : 0;
+        bias_row = a.bias + (((int64_t)bb * a.bias_h + bh) * a.Sq + i) * a.Skv;
+      }
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < w.n; ++j) {
+        const uint32_t k = kt + j;
+        const int sb = k & 1;
+        const int k0 = w.kv_lo + j * kTile;
+        float x[kTile];
+        if (!(ok = mbar_wait_warp(&bars->s_full[sb], (k >> 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < kTile / 32; ++q) {
+          uint32_t u[32];
+          tmem_ld32x32b_x32(tmem + lane_base + L::kColS + sb * kTile + q * 32, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->s_empty[sb]);
+        if (HAS_BIAS && row_ok) add_bias_row(x, bias_row + k0, min(kTile, a.Skv - k0));
+        // mask
+        bool full;
+        if (!general) {
+          full = (k0 >= rlo) && (k0 + kTile <= rhi);
+        } else {
+          full = false;
+          if (k0 + kTile <= a.Skv && my_id != 0) {
+            const int nkc = (a.Skv + kChunk - 1) / kChunk;
+            const ChunkInfo c0 = a.kv_chunk[w.b * nkc + k0 / kChunk];
+            const ChunkInfo c1 = a.kv_chunk[w.b * nkc + k0 / kChunk + 1];
+            full = c0.uniform && c1.uniform && c0.min_id == my_id && c1.min_id == my_id &&
+                   (!a.causal || max(c0.max_pos, c1.max_pos) <= my_pos);
+          }
+        }
+        if (!full) {
+          if (!general) {
+#pragma unroll
+            for (int c = 0; c < kTile; ++c)
+              if (k0 + c < rlo || k0 + c >= rhi) x[c] = -INFINITY;
+          } else {
+            const int32_t* kid = a.kv_id + (int64_t)w.b * a.Skv + k0;
+            const int32_t* kpos = a.kv_pos + (int64_t)w.b * a.Skv + k0;
+            const int nv = min(kTile, a.Skv - k0);
+#pragma unroll
+            for (int c = 0; c < kTile; c += 4) {
+              int ids4[4], pos4[4];
+              if (c + 4 <= nv && ((reinterpret_cast<uintptr_t>(kid + c) & 15u) == 0)) {
+                const int4 t1 = __ldg(reinterpret_cast<const int4*>(kid + c));
+                const int4 t2 = __ldg(reinterpret_cast<const int4*>(kpos + c));
+                ids4[0] = t1.x; ids4[1] = t1.y; ids4[2] = t1.z; ids4[3] = t1.w;
+                pos4[0] = t2.x; pos4[1] = t2.y; pos4[2] = t2.z; pos4[3] = t2.w;
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  ids4[e] = (c + e < nv) ? __ldg(kid + c + e) : -1;
+                  pos4[e] = (c + e < nv) ? __ldg(kpos + c + e) : 0;
+                }
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const bool v = ids4[e] == my_id && my_id != 0 && (!a.causal || pos4[e] <= my_pos);
+                if (!v) x[c + e] = -INFINITY;
+              }
+            }
+          }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, x[c]);
+        const float m_new = fmaxf(m_ref, mx);
+        // P(j-1) V(j-1) must be finished before O is touched or P is overwritten
+        if (j > 0 && !(ok = mbar_wait_warp(&bars->pv_done, (k - 1) & 1))) break;
+        tc_fence_after();
+        if (m_new > m_ref + kRescaleThreshold) {
+          if (j > 0 && m_ref > -INFINITY) {
+            const float f = ex2_approx(m_ref - m_new);
+            l *= f;
+#pragma unroll
+            for (int q = 0; q < DV / 32; ++q) {
+              uint32_t u[32];
+              const uint32_t ta = tmem + lane_base + L::kColO + q * 32;
+              tmem_ld32x32b_x32(ta, u);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
+              tmem_st32x32b_x32(ta, u);
+            }
+            tmem_st_wait();
+          }
+          m_ref = m_new;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) {
+          x[c] = ex2_approx(x[c] - m_use);
+          rs += x[c];
+        }
+        l += rs;
+        // P row r -> shared memory, K-major with the 128-byte swizzle
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float* p8 = x + cc * 64 + u * 8;
+            st_shared_v4(p_addr + cc * 16384 + r * 128 + ((u ^ (r & 7)) << 4),
+                         pack_bf16x2(p8[0], p8[1]), pack_bf16x2(p8[2], p8[3]),
+                         pack_bf16x2(p8[4], p8[5]), pack_bf16x2(p8[6], p8[7]));
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);
+      }
+      if (!ok) break;
+      // epilogue: O / l and LSE
+      if (!(ok = mbar_wait_warp(&bars->pv_done, (kt + w.n - 1) & 1))) break;
+      tc_fence_after();
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+      for (int q = 0; q < DV / 32; ++q) {
+        uint32_t u[32];
+        tmem_ld32x32b_x32(tmem + lane_base + L::kColO + q * 32, u);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(u[c + 0]) * inv_l, __uint_as_float(u[c + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * inv_l, __uint_as_float(u[c + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * inv_l, __uint_as_float(u[c + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * inv_l, __uint_as_float(u[c + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + q * 32 + c) = v;
+          }
+        }
+      }
+      if (row_ok) *lse_out = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      tc_fence_before();
+      mbar_arrive(&bars->o_empty);
+      kt += w.n;
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(a, 0x30 + (warp & 3));
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int DQK, int DV, bool HB>
+cudaError_t launch_fwd_t(const KernelArgs& a, int num_sms, cudaStream_t st) {
+  using L = FwdLayout<DQK, DV>;
+  auto kern = fwd_kernel<DQK, DV, HB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int n_items = a.B * a.n_qt * a.Hq;
+  const int grid = n_items < num_sms ? n_items : num_sms;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, 256, L::kAlloc, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DQK, int DV>
+cudaError_t launch_fwd_b(const KernelArgs& a, int num_sms, cudaStream_t st) {
+  return a.bias ? launch_fwd_t<DQK, DV, true>(a, num_sms, st)
+                : launch_fwd_t<DQK, DV, false>(a, num_sms, st);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const KernelArgs& a, int num_sms, cudaStream_t st) {
+  if (a.d_v == 64) {
+    if (a.d_qk == 64) return launch_fwd_b<64, 64>(a, num_sms, st);
+    if (a.d_qk == 128) return launch_fwd_b<128, 64>(a, num_sms, st);
+    if (a.d_qk == 192) return launch_fwd_b<192, 64>(a, num_sms, st);
+  } else if (a.d_v == 128) {
+    if (a.d_qk == 64) return launch_fwd_b<64, 128>(a, num_sms, st);
+    if (a.d_qk == 128) return launch_fwd_b<128, 128>(a, num_sms, st);
+    if (a.d_qk == 192) return launch_fwd_b<192, 128>(a, num_sms, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

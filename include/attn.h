@@ -1,0 +1,208 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused scaled-dot-product attention
+ * library: forward (O, LSE) and backward (dQ, dK, dV, dBias).
+ *
+ * The operations follow the fused-attention forward/backward pair of the
+ * TransformerEngine pages: the unified nvte_fused_attn_fwd / nvte_fused_attn_bwd
+ * calls that take separate Q/K/V pointers after the packed layouts have been
+ * resolved ("[JAX] Make all jax attention calls use non-packed common calls",
+ * PR #2358: description and pointer-arithmetic sequence diagram), the backward
+ * that turns the saved forward output plus the incoming output gradient into
+ * Q/K/V and optional bias gradients ("[JAX] Align fused attn backward output
+ * gradient sharding and other test strengthening", PR #3516: diagram), with
+ * THD sequences described by segment ids and positions ("[JAX] Fix batcher in
+ * FusedAttn primitive ...", PR #2692: Description) or ragged offsets.
+ *
+ * Mathematics.  For batch row b, query head h, KV head g = h / (Hq / Hkv),
+ * query i and key j:
+ *   valid(i,j) = id_q[i] == id_kv[j] != 0 && (!causal || pos_kv[j] <= pos_q[i])
+ *   S_ij = scale * Q_i . K_j + bias_ij          (masked pairs: -inf)
+ *   P = softmax_j(S),  O_i = sum_j P_ij V_j,  LSE_i = ln sum_j exp(S_ij)
+ *   dP_ij = dO_i . V_j,  D_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i = scale sum_j dS_ij K_j;  dK_j = scale sum_{h in g} sum_i dS_ij Q_i
+ *   dV_j = sum_{h in g} sum_i P_ij dO_i;  dBias = dS summed over broadcast axes
+ * A query row with no valid key gets O = 0, LSE = -inf and dQ = 0; gradients
+ * of keys no query attends to are exactly 0.
+ *
+ * Conventions.
+ *  - Every tensor is caller-owned device memory (including the workspace).
+ *    The library never allocates, frees or synchronises, except
+ *    attn_read_status(), which synchronises the given stream.
+ *  - All work is enqueued on the caller's stream (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream).
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns a status and launches nothing.  No call aborts.
+ *  - Element type of Q/K/V/O/dO/bias and of all gradients: bf16.  LSE: fp32.
+ *  - Token-major memory: a BSHD tensor [B, S, H, D] is B*S token rows; a THD
+ *    tensor with B rows of S tokens uses the same addressing (row b, token t
+ *    is token row b*S + t).  With cu_seqlens, B = 1 and S = total tokens.
+ *  - Pointers must be 16-byte aligned.
+ */
+#ifndef GB300_ATTN_H_
+#define GB300_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_PARAMS_VERSION 1
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,         /* null/misaligned pointer, bad enum, bad size */
+  ATTN_ERR_UNSUPPORTED = 2,         /* valid request this build does not implement */
+  ATTN_ERR_SHAPE_MISMATCH = 3,      /* segment ids/pos (or Q/KV) shapes disagree */
+  ATTN_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the *_workspace_size() value */
+  ATTN_ERR_CUDA = 5,                /* a CUDA runtime call failed (launch, attribute) */
+  ATTN_ERR_DEVICE_TIMEOUT = 6       /* a kernel wait ran past its limit (read via
+                                       attn_read_status) */
+} attn_status_t;
+
+/* Q/K/V memory layouts (PR #2358, NVTE_3HD / NVTE_HD_2HD / NVTE_HD_HD_HD).
+ *  3HD:      one buffer, token row = [Hq*d_qk Q | Hkv*d_qk K | Hkv*d_v V]; with
+ *            Hq == Hkv and d_qk == d_v this is [T, 3, H, D].  Needs Sq == Skv.
+ *            q points at the buffer; k and v are ignored.
+ *  HD_2HD:   q [T_q, Hq, d_qk]; k points at a [T_kv, 2, Hkv, d_v] buffer whose
+ *            V slice starts Hkv*d_v elements after K.  Needs d_qk == d_v.
+ *            v is ignored.
+ *  HD_HD_HD: separate q [T_q,Hq,d_qk], k [T_kv,Hkv,d_qk], v [T_kv,Hkv,d_v]. */
+typedef enum { ATTN_LAYOUT_3HD = 0, ATTN_LAYOUT_HD_2HD = 1, ATTN_LAYOUT_HD_HD_HD = 2 } attn_layout_t;
+
+/* Sequence description.
+ *  BSHD:            dense rows; segment ids optional (0 = padding).
+ *  THD_SEGMENTS:    rows packed with segments given by ids [B,S] (0 = padding)
+ *                   and positions [B,S] (NULL: derived on the device as the
+ *                   offset inside each run of equal ids).
+ *  THD_CU_SEQLENS:  B = 1; ragged offsets int32[num_segments+1]; segment k of Q
+ *                   pairs with segment k of KV; tokens past the last offset
+ *                   are padding. */
+typedef enum { ATTN_FMT_BSHD = 0, ATTN_FMT_THD_SEGMENTS = 1, ATTN_FMT_THD_CU_SEQLENS = 2 } attn_format_t;
+
+/* Causal masking compares segment positions (pos_kv <= pos_q); without
+ * segments the position is the token index (top-left alignment).  The PADDING
+ * variants only document that segment metadata is present; padding (id 0) is
+ * always masked. */
+typedef enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_PADDING = 2,
+  ATTN_MASK_PADDING_CAUSAL = 3
+} attn_mask_t;
+
+/* dQ accumulation: ATOMIC adds fp32 partial products per KV tile into an fp32
+ * workspace (run-to-run order may vary in the last bits); DETERMINISTIC runs a
+ * separate pass per query tile that visits KV tiles in a fixed order
+ * (bit-reproducible).  dK, dV and dBias are bit-reproducible in both modes. */
+typedef enum { ATTN_DQ_ATOMIC = 0, ATTN_DQ_DETERMINISTIC = 1 } attn_dq_mode_t;
+
+typedef struct {
+  int32_t struct_version; /* = ATTN_PARAMS_VERSION */
+  int32_t fmt;            /* attn_format_t */
+  int32_t layout;         /* attn_layout_t */
+  int32_t mask;           /* attn_mask_t */
+  int32_t dq_mode;        /* attn_dq_mode_t (backward only) */
+  int32_t B, Sq, Skv, Hq, Hkv, d_qk, d_v;
+  /* Supported head dims: d_qk in {64, 128, 192}, d_v in {64, 128};
+   * Hq a multiple of Hkv. */
+  float scale;  /* softmax scale, applied to Q.K before the bias is added */
+  const void* q;
+  const void* k;
+  const void* v;
+  /* Segment metadata, int32 [B,S] each (THD_SEGMENTS, or BSHD with padding).
+   * The *_dims pairs state each array's shape as the caller sees it; ids and
+   * positions of one side must agree with each other and with (B, S). */
+  const int32_t* q_seg_ids;
+  const int32_t* q_seg_pos;
+  const int32_t* kv_seg_ids;
+  const int32_t* kv_seg_pos;
+  int64_t q_ids_dims[2], q_pos_dims[2], kv_ids_dims[2], kv_pos_dims[2];
+  /* Ragged offsets (THD_CU_SEQLENS): int32[num_segments + 1], non-decreasing,
+   * starting at 0, last entry <= Sq (resp. Skv). */
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_kv;
+  int32_t num_segments;
+  /* Optional post-scale bias, bf16 [bias_b, bias_h, Sq, Skv] with
+   * bias_b in {1, B} and bias_h in {1, Hq}; NULL for none. */
+  const void* bias;
+  int32_t bias_b, bias_h;
+  int32_t force_general_path; /* testing knob: skip the fast metadata path */
+} attn_params_t;
+
+/* Which metadata path the device chose (read back by attn_read_status). */
+typedef enum {
+  ATTN_PATH_FAST = 0,   /* Q and KV metadata identical with standard positions:
+                           masks from segment boundaries only */
+  ATTN_PATH_GENERAL = 1 /* per-token id/position comparison */
+} attn_path_t;
+
+typedef enum {
+  ATTN_REASON_DENSE = 0,             /* BSHD without segment ids */
+  ATTN_REASON_METADATA_MATCH = 1,    /* fast: Q/KV ids and positions equal */
+  ATTN_REASON_FORCED = 2,            /* general: force_general_path */
+  ATTN_REASON_LENGTHS_DIFFER = 3,    /* general: Sq != Skv */
+  ATTN_REASON_IDS_DIFFER = 4,        /* general: Q/KV segment ids differ */
+  ATTN_REASON_POS_DIFFER = 5,        /* general: Q/KV positions differ */
+  ATTN_REASON_POS_NONSTANDARD = 6,   /* general: positions do not restart at 0
+                                        and count up inside each segment */
+  ATTN_REASON_CU_SEQLENS_DIFFER = 7  /* general: Q/KV ragged offsets differ */
+} attn_path_reason_t;
+
+typedef struct {
+  int32_t status;        /* attn_status_t of the device side (timeouts) */
+  int32_t path;          /* attn_path_t of the last call using this workspace */
+  int32_t reason;        /* attn_path_reason_t */
+  int32_t dq_mode;       /* dQ mode actually used by the last backward */
+  int64_t tile_pairs;    /* (query tile, KV tile) pairs scheduled by the last call */
+} attn_stats_t;
+
+/* Workspace bytes the forward / backward needs for these parameters (0 on
+ * invalid parameters).  The workspace must be 256-byte aligned. */
+size_t attn_fwd_workspace_size(const attn_params_t* p);
+size_t attn_bwd_workspace_size(const attn_params_t* p);
+
+/* Forward.  o: bf16 [B*Sq, Hq, d_v] token-major; lse: fp32 [B, Hq, Sq]
+ * (natural log; -inf for rows without a valid key). */
+attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* Backward.  o and lse are the forward's outputs, d_o is bf16 like o.
+ * Gradients are written in the input layout:
+ *   3HD:      dq -> the packed dQKV buffer (dk, dv ignored);
+ *   HD_2HD:   dq [T_q,Hq,d_qk]; dk -> packed dKV [T_kv,2,Hkv,d_v] (dv ignored);
+ *   HD_HD_HD: dq, dk, dv separate.
+ * dbias: bf16 like the bias (NULL: not computed; must be NULL without bias).
+ * Every element of every gradient is written (padding rows get exact 0). */
+attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, const float* lse,
+                       void* dq, void* dk, void* dv, void* dbias, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* Synchronises `stream`, then reads the device-side status and path record of
+ * the last call that used `ws`.  stats may be NULL. */
+attn_status_t attn_read_status(const void* ws, void* stream, attn_stats_t* stats);
+
+const char* attn_status_string(attn_status_t s);
+
+/* Layout resolution (host only, no device access): element offsets of the K
+ * and V slices from the pointers given and the token-row strides, in
+ * elements.  Returns ATTN_OK or the validation error of the parameters. */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  int64_t q_token_stride, k_token_stride, v_token_stride;
+  const void* dq;
+  const void* dk;
+  const void* dv;
+} attn_resolved_t;
+attn_status_t attn_resolve_layout(const attn_params_t* p, void* dq, void* dk, void* dv,
+                                  attn_resolved_t* out);
+
+int32_t attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300_ATTN_H_ */

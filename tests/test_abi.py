@@ -1,0 +1,130 @@
+"""Host-side C ABI checks (no GPU needed): the library builds and loads, every
+symbol the header declares is exported, and validation, layout resolution and
+workspace sizing behave as documented.  Only host-only entry points are
+called; pointers are fake addresses that the library never dereferences."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bwd_tcgen05_tma_gb300 import attn as A
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bwd_tcgen05_tma_gb300 import build
+
+    build.build()
+    return A.load_library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert set(names) == set(A.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def params(**kw):
+    d = dict(layout="HD_HD_HD", fmt="BSHD", mask="CAUSAL", B=2, Sq=256, Skv=256, Hq=8, Hkv=2,
+             d_qk=128, d_v=128, scale=0.088)
+    d.update(kw)
+    p = A.attn_params_t()
+    p.struct_version = A.ATTN_PARAMS_VERSION
+    p.fmt, p.layout, p.mask = A.FORMATS[d["fmt"]], A.LAYOUTS[d["layout"]], A.MASKS[d["mask"]]
+    p.dq_mode = 1
+    p.B, p.Sq, p.Skv, p.Hq, p.Hkv, p.d_qk, p.d_v = (d[k] for k in
+                                                     ("B", "Sq", "Skv", "Hq", "Hkv", "d_qk", "d_v"))
+    p.scale = d["scale"]
+    p.q, p.k, p.v = FAKE, FAKE + (1 << 24), FAKE + (2 << 24)
+    return p
+
+
+def test_workspace_sizes(lib):
+    p = params()
+    f, b = A.attn_fwd_workspace_size(p), A.attn_bwd_workspace_size(p)
+    assert 0 < f < b and f % 256 == 0 and b % 256 == 0
+    p.dq_mode = 0  # atomic: fp32 dQ accumulator in the workspace
+    assert A.attn_bwd_workspace_size(p) >= b + 2 * 256 * 8 * 128 * 4
+    bad = params(d_qk=96)
+    assert A.attn_fwd_workspace_size(bad) == 0
+
+
+def test_resolve_3hd_gqa_offsets(lib):
+    """3HD with Hq=32, Hkv=8, D=128: K at Hq*D elements, V at (Hq+Hkv)*D, token
+    stride (Hq+2*Hkv)*D; the gradient buffer is resolved the same way."""
+    p = params(layout="3HD", Hq=32, Hkv=8)
+    r = A.attn_resolve_layout(p, FAKE * 2, None, None)
+    assert r.k - r.q == 32 * 128 * 2
+    assert r.v - r.q == (32 + 8) * 128 * 2
+    assert r.q_token_stride == r.k_token_stride == r.v_token_stride == 48 * 128
+    assert r.dk - r.dq == 32 * 128 * 2 and r.dv - r.dq == 40 * 128 * 2
+
+
+def test_resolve_kv_packed_uses_v_head_dim(lib):
+    """HD_2HD: V starts Hkv * v_head_dim elements after K (the corrected stride)."""
+    p = params(layout="HD_2HD", Hq=64, Hkv=8, d_qk=128, d_v=128)
+    r = A.attn_resolve_layout(p, FAKE * 2, FAKE * 3, None)
+    assert r.v - r.k == 8 * 128 * 2
+    assert r.k_token_stride == r.v_token_stride == 2 * 8 * 128
+    assert r.q_token_stride == 64 * 128
+    assert r.dv - r.dk == 8 * 128 * 2
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(layout="3HD", Sq=256, Skv=384), 3),          # 3HD needs Sq == Skv
+    (dict(layout="HD_2HD", d_qk=192, d_v=128), 3),     # KV-packed needs equal head dims
+    (dict(d_qk=96), 2),                                 # unsupported head dim
+    (dict(Hq=6, Hkv=4), 1),                             # Hq not a multiple of Hkv
+    (dict(B=0), 1),
+    (dict(scale=0.0), 1),
+])
+def test_validation_codes(lib, kw, code):
+    p = params(**kw)
+    r = A.attn_resolved_t()
+    assert lib.attn_resolve_layout(ctypes.byref(p), None, None, None, ctypes.byref(r)) == code
+
+
+def test_segment_shape_agreement(lib):
+    """ids and pos must carry the same shape (the batcher bug of the pages:
+    ids with an extra leading dim, pos without)."""
+    p = params(fmt="THD_SEGMENTS")
+    p.q_seg_ids = p.kv_seg_ids = FAKE
+    p.q_seg_pos = p.kv_seg_pos = FAKE
+    for arr in (p.q_ids_dims, p.kv_ids_dims, p.q_pos_dims, p.kv_pos_dims):
+        arr[0], arr[1] = 2, 256
+    r = A.attn_resolved_t()
+    assert lib.attn_resolve_layout(ctypes.byref(p), None, None, None, ctypes.byref(r)) == 0
+    p.q_pos_dims[0] = 1  # pos [1,256] against ids [2,256]
+    assert lib.attn_resolve_layout(ctypes.byref(p), None, None, None, ctypes.byref(r)) == 3
+    p.q_pos_dims[0] = 2
+    p.kv_ids_dims[1] = 255
+    assert lib.attn_resolve_layout(ctypes.byref(p), None, None, None, ctypes.byref(r)) == 3
+
+
+def test_fwd_rejects_before_launch(lib):
+    """Invalid calls return a status without touching the device."""
+    p = params()
+    ws_need = A.attn_fwd_workspace_size(p)
+    s = lib.attn_fwd(ctypes.byref(p), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                     ctypes.c_void_p(FAKE * 4), ctypes.c_size_t(ws_need - 256), None)
+    assert s == 4
+    s = lib.attn_fwd(ctypes.byref(p), ctypes.c_void_p(FAKE + 8), ctypes.c_void_p(FAKE),
+                     ctypes.c_void_p(FAKE * 4), ctypes.c_size_t(ws_need), None)
+    assert s == 1  # misaligned output
+    s = lib.attn_bwd(ctypes.byref(p), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                     ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                     ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE * 4),
+                     ctypes.c_size_t(A.attn_bwd_workspace_size(p)), None)
+    assert s == 1  # dbias without a bias
+    assert lib.attn_status_string(6) == b"device-side wait timed out"
