@@ -138,21 +138,37 @@ def check_forward(case, ref, o_dev, lse_dev):
     return eo, el
 
 
+def structural_masks(case):
+    """Per batch row: valid-pair matrix, queries without keys, keys without queries."""
+    from conftest import oracle_metadata
+    from oracle import attn_ref as R
+
+    qi, qp, ki, kp = oracle_metadata(case)
+    valid = np.stack([R.valid_pairs(qi[b], qp[b], ki[b], kp[b], case.causal)
+                      for b in range(case.B)])
+    return valid, ~valid.any(axis=2), ~valid.any(axis=1)
+
+
 def check_backward(case, ref, grads, dbias_dev):
     dq, dk, dv = unpack_grads(case, grads)
+    valid, q_dead, k_dead = structural_masks(case)
     out = {}
-    for name, x, r in (("dq", dq, ref["dq"]), ("dk", dk, ref["dk"]), ("dv", dv, ref["dv"])):
+    for name, x, r, dead in (("dq", dq, ref["dq"], q_dead), ("dk", dk, ref["dk"], k_dead),
+                             ("dv", dv, ref["dv"], k_dead)):
         assert np.all(np.isfinite(x)), f"{name} has non-finite values (unwritten elements?)"
         e = rel(x, r)
         out[name] = e
         assert e <= TOL_GRAD, f"{name} rel err {e}"
-        zero = np.all(r == 0, axis=-1)
-        assert np.all(x[zero] == 0.0), f"{name}: rows with no contribution must be exactly 0"
+        assert np.all(x[dead] == 0.0), f"{name}: tokens without a valid pair must get exactly 0"
     if dbias_dev is not None:
         db = dbias_dev.float().cpu().numpy()
         assert np.all(np.isfinite(db))
         e = rel(db, ref["dbias"])
         out["dbias"] = e
         assert e <= TOL_DBIAS, f"dbias rel err {e}"
-        assert np.all(db[ref["dbias"] == 0] == 0.0)
+        # pairs that are invalid in every (batch row, head) summed into an element
+        inval_all = ~valid.any(axis=0) if db.shape[0] == 1 else ~valid
+        inval = np.broadcast_to(inval_all[:, None] if inval_all.ndim == 3 else inval_all[None, None],
+                                db.shape)
+        assert np.all(db[inval] == 0.0), "dBias must be exactly 0 at masked pairs"
     return out

@@ -119,3 +119,112 @@ def test_cu_seqlens_format():
     o, lse = d.forward()
     assert d.fwd_stats.path == 0
     check_forward(base, _ref(base), o, lse)
+
+
+# ----------------------------------------------------------------- backward
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("dq_mode", ["deterministic", "atomic"])
+def test_backward_matches_oracle(name, dq_mode):
+    from gpu_util import DevCase, check_backward
+
+    case = CASES[name]()
+    ref = _ref(case)
+    d = DevCase(case, dq_mode=dq_mode)
+    d.forward()
+    g, db = d.backward()
+    check_backward(case, ref, g, db)
+    expect = 1 if (dq_mode == "deterministic" or case.d_qk > 128) else 0
+    assert d.bwd_stats.dq_mode == expect
+
+
+@pytest.mark.parametrize("name", ["thd_gqa_3hd", "cross_bias_192", "tiny"])
+def test_backward_general_path(name):
+    from gpu_util import DevCase, check_backward
+
+    case = CASES[name]()
+    d = DevCase(case, dq_mode="atomic", force_general=True)
+    d.forward()
+    g, db = d.backward()
+    assert d.bwd_stats.path == 1
+    check_backward(case, _ref(case), g, db)
+
+
+@pytest.mark.parametrize("bias_shape", [(2, 2, 300, 520), (1, 1, 300, 520), (2, 1, 300, 520)])
+def test_bias_shapes_and_reduction(bias_shape):
+    """dBias per batch/head, and reduced over broadcast batch and head axes."""
+    from gpu_util import DevCase, check_backward, check_forward
+
+    case = I.synth("xb", B=2, Sq=300, Skv=520, Hq=4, Hkv=2, d_qk=128, d_v=128,
+                   layout="HD_HD_HD", fmt="THD_SEGMENTS", causal=False, seed=31, seg=(60, 200),
+                   kv_seg=(60, 300), bias_shape=(bias_shape[0], 4 if bias_shape[1] == 2 else 1,
+                                                 300, 520))
+    ref = _ref(case)
+    d = DevCase(case, dq_mode="deterministic")
+    o, lse = d.forward()
+    check_forward(case, ref, o, lse)
+    g, db = d.backward()
+    check_backward(case, ref, g, db)
+
+
+def test_deterministic_mode_bit_reproducible():
+    from gpu_util import DevCase
+
+    case = CASES["thd_gqa_3hd"]()
+    d = DevCase(case, dq_mode="deterministic")
+    d.forward()
+    g1, _ = d.backward()
+    g1 = {k: v.clone() for k, v in g1.items()}
+    g2, _ = d.backward()
+    for k in g1:
+        assert torch.equal(g1[k].view(torch.int16), g2[k].view(torch.int16)), k
+
+
+def test_dkdv_dbias_bit_reproducible_in_atomic_mode():
+    from gpu_util import DevCase, unpack_grads
+
+    case = I.synth("xb", B=2, Sq=300, Skv=520, Hq=2, Hkv=2, d_qk=128, d_v=128,
+                   layout="HD_HD_HD", fmt="THD_SEGMENTS", causal=False, seed=32, seg=(60, 200),
+                   kv_seg=(60, 300), bias_shape=(1, 2, 300, 520))
+    d = DevCase(case, dq_mode="atomic")
+    d.forward()
+    g1, db1 = d.backward()
+    g1 = {k: v.clone() for k, v in g1.items()}
+    db1 = db1.clone()
+    g2, db2 = d.backward()
+    assert torch.equal(g1["dk"].view(torch.int16), g2["dk"].view(torch.int16))
+    assert torch.equal(g1["dv"].view(torch.int16), g2["dv"].view(torch.int16))
+    assert torch.equal(db1.view(torch.int16), db2.view(torch.int16))
+
+
+def test_padding_garbage_isolation():
+    """1000.0 in every padded KV position: outputs and real gradients are
+    bit-identical to the clean run, and padded tokens get exactly zero grads."""
+    from gpu_util import DevCase
+
+    case = I.synth("pad", B=2, Sq=700, Skv=700, Hq=2, Hkv=1, d_qk=128, d_v=128,
+                   layout="HD_HD_HD", fmt="THD_SEGMENTS", causal=True, seed=33, seg=(50, 300),
+                   pad_frac=0.1)
+    clean = DevCase(case)
+    o1, l1 = clean.forward()
+    o1, l1 = o1.clone(), l1.clone()
+    g1, _ = clean.backward()
+    g1 = {k: v.clone() for k, v in g1.items()}
+    pad = case.kv_ids == 0
+    assert pad.sum() > 0
+    dirty = I.synth("pad", B=2, Sq=700, Skv=700, Hq=2, Hkv=1, d_qk=128, d_v=128,
+                    layout="HD_HD_HD", fmt="THD_SEGMENTS", causal=True, seed=33, seg=(50, 300),
+                    pad_frac=0.1)
+    dirty.buffers["k"][pad] = 1000.0
+    dirty.buffers["v"][pad] = 1000.0
+    dd = DevCase(dirty)
+    o2, l2 = dd.forward()
+    g2, _ = dd.backward()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+    padt = torch.from_numpy(pad).cuda()
+    for k in ("dk", "dv"):
+        assert torch.all(g2[k][padt] == 0)
+        assert torch.equal(g1[k].view(torch.int16), g2[k].view(torch.int16))
+    assert torch.equal(g1["dq"].view(torch.int16), g2["dq"].view(torch.int16))
