@@ -24,7 +24,9 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           6: "ATTN_ERR_DEVICE_TIMEOUT"}
 EXPORTED = ("attn_abi_version", "attn_status_string", "attn_fwd_workspace_size",
             "attn_bwd_workspace_size", "attn_resolve_layout", "attn_fwd", "attn_bwd",
-            "attn_read_status")
+            "attn_read_status", "attn_set_trace_events", "attn_event_create",
+            "attn_event_destroy", "attn_event_elapsed_ms")
+TRACE_SLOTS = ("meta", "fwd", "bwd_pre", "dkdv", "dq", "dbias")
 
 c_i32, c_i64, c_f32, c_vp, c_sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                    ctypes.c_void_p, ctypes.c_size_t)
@@ -86,6 +88,14 @@ def load_library(path: str = LIB_PATH):
     lib.attn_bwd.argtypes = [P, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]
     lib.attn_read_status.restype = c_i32
     lib.attn_read_status.argtypes = [c_vp, c_vp, ctypes.POINTER(attn_stats_t)]
+    lib.attn_set_trace_events.restype = c_i32
+    lib.attn_set_trace_events.argtypes = [ctypes.POINTER(c_vp)]
+    lib.attn_event_create.restype = c_i32
+    lib.attn_event_create.argtypes = [ctypes.POINTER(c_vp)]
+    lib.attn_event_destroy.restype = c_i32
+    lib.attn_event_destroy.argtypes = [c_vp]
+    lib.attn_event_elapsed_ms.restype = c_i32
+    lib.attn_event_elapsed_ms.argtypes = [c_vp, c_vp, ctypes.POINTER(ctypes.c_float)]
     if lib.attn_abi_version() != ATTN_PARAMS_VERSION:
         raise RuntimeError("attention library ABI version mismatch")
     _lib = lib
@@ -187,3 +197,40 @@ def attn_read_status(ws, stream=None):
     st = attn_stats_t()
     s = load_library().attn_read_status(_ptr(ws), _stream(stream), ctypes.byref(st))
     return s, st
+
+
+class Event:
+    """A CUDA timing event owned by this object (created through the library)."""
+
+    def __init__(self):
+        h = c_vp()
+        s = load_library().attn_event_create(ctypes.byref(h))
+        if s != 0:
+            raise AttnError(s, "attn_event_create")
+        self.handle = h.value
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.attn_event_destroy(self.handle)
+            self.handle = None
+
+
+def attn_event_elapsed_ms(start, end):
+    """Milliseconds between two recorded events, or None if either is unrecorded."""
+    ms = ctypes.c_float()
+    s = load_library().attn_event_elapsed_ms(start.handle, end.handle, ctypes.byref(ms))
+    return float(ms.value) if s == 0 else None
+
+
+def attn_set_trace_events(events):
+    """events: None, or a sequence of 2 * len(TRACE_SLOTS) Event objects (or None)
+    as (start, end) per slot.  The caller keeps the events alive."""
+    lib = load_library()
+    if events is None:
+        return lib.attn_set_trace_events(None)
+    arr = (c_vp * (2 * len(TRACE_SLOTS)))()
+    for i, e in enumerate(events):
+        arr[i] = None if e is None else c_vp(e.handle)
+    s = lib.attn_set_trace_events(arr)
+    if s != 0:
+        raise AttnError(s, "attn_set_trace_events")

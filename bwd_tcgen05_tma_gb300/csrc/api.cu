@@ -236,13 +236,25 @@ void fill_common(KernelArgs& a, const attn_params_t* p, char* ws, const Plan& pl
   a.bias_h = p->bias_h;
 }
 
+thread_local cudaEvent_t g_trace[2 * ATTN_TRACE_SLOTS] = {};
+thread_local bool g_trace_on = false;
+
+// Records the start (end = false) or end event of a trace slot, if tracing.
+void trace(int slot, bool end, cudaStream_t st) {
+  if (!g_trace_on) return;
+  cudaEvent_t e = g_trace[2 * slot + (end ? 1 : 0)];
+  if (e) cudaEventRecord(e, st);
+}
+
 attn_status_t run_meta(const KernelArgs& a, const attn_params_t* p, cudaStream_t st) {
   const bool seg = p->fmt != ATTN_FMT_THD_CU_SEQLENS && p->q_seg_ids != nullptr;
+  trace(ATTN_TRACE_META, false, st);
   const cudaError_t e =
       launch_meta(a, p->fmt == ATTN_FMT_THD_CU_SEQLENS ? 2 : (seg ? 1 : 0),
                   seg ? p->q_seg_ids : nullptr, seg ? p->q_seg_pos : nullptr,
                   seg ? p->kv_seg_ids : nullptr, seg ? p->kv_seg_pos : nullptr,
                   p->cu_seqlens_q, p->cu_seqlens_kv, p->num_segments, p->force_general_path, st);
+  trace(ATTN_TRACE_META, true, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -254,6 +266,43 @@ using namespace attn;
 extern "C" {
 
 int32_t attn_abi_version(void) { return ATTN_PARAMS_VERSION; }
+
+attn_status_t attn_event_create(void** event) {
+  if (!event) return ATTN_ERR_INVALID_ARG;
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return ATTN_ERR_CUDA;
+  *event = e;
+  return ATTN_OK;
+}
+
+attn_status_t attn_event_destroy(void* event) {
+  if (!event) return ATTN_ERR_INVALID_ARG;
+  return cudaEventDestroy(static_cast<cudaEvent_t>(event)) == cudaSuccess ? ATTN_OK
+                                                                           : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_event_elapsed_ms(const void* start, const void* end, float* ms) {
+  if (!start || !end || !ms) return ATTN_ERR_INVALID_ARG;
+  const cudaError_t e = cudaEventElapsedTime(
+      ms, static_cast<cudaEvent_t>(const_cast<void*>(start)),
+      static_cast<cudaEvent_t>(const_cast<void*>(end)));
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error state of this query
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+attn_status_t attn_set_trace_events(void* const* events) {
+  if (!events) {
+    g_trace_on = false;
+    for (auto& e : g_trace) e = nullptr;
+    return ATTN_OK;
+  }
+  for (int i = 0; i < 2 * ATTN_TRACE_SLOTS; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+  g_trace_on = true;
+  return ATTN_OK;
+}
 
 const char* attn_status_string(attn_status_t s) {
   switch (s) {
@@ -310,7 +359,9 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
   a.o = static_cast<bf16*>(o);
   a.lse = lse;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
+  trace(ATTN_TRACE_FWD, false, st);
   if (launch_fwd(a, sm_count(), st) != cudaSuccess) return ATTN_ERR_CUDA;
+  trace(ATTN_TRACE_FWD, true, st);
   return ATTN_OK;
 }
 
@@ -358,7 +409,9 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   a.dkdv_batch_loop = (a.dbias_mode == 2 && p->bias_b == 1 && p->B > 1) ? 1 : 0;
   a.dkdv_head_loop = (a.dbias_mode == 2 && p->bias_h == 1 && p->Hkv > 1) ? 1 : 0;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
+  trace(ATTN_TRACE_BWD_PRE, false, st);
   if (launch_bwd_pre(a, atomic ? 1 : 0, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  trace(ATTN_TRACE_BWD_PRE, true, st);
   // dK/dV pass: query tiles of 64 rows
   if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kBwdQ) ||
       !make_map(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
@@ -367,7 +420,10 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
                 kBwdQ))
     return ATTN_ERR_CUDA;
   const int nsm = sm_count();
+  trace(ATTN_TRACE_DKDV, false, st);
   if (launch_bwd_dkdv(a, atomic, nsm, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  trace(ATTN_TRACE_DKDV, true, st);
+  trace(ATTN_TRACE_DQ, false, st);
   if (atomic) {
     if (launch_dq_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
   } else {
@@ -377,7 +433,12 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
       return ATTN_ERR_CUDA;
     if (launch_bwd_dq(a, nsm, st) != cudaSuccess) return ATTN_ERR_CUDA;
   }
-  if (a.dbias_mode == 2 && launch_dbias_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  trace(ATTN_TRACE_DQ, true, st);
+  if (a.dbias_mode == 2) {
+    trace(ATTN_TRACE_DBIAS, false, st);
+    if (launch_dbias_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
+    trace(ATTN_TRACE_DBIAS, true, st);
+  }
   return ATTN_OK;
 }
 

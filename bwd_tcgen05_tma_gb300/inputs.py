@@ -33,11 +33,18 @@ import numpy as np
 
 
 def bf16_bits(x):
-    """float32 array -> uint16 bf16 bit patterns, round to nearest even."""
+    """float32 array -> uint16 bf16 bit patterns, round to nearest even
+    (NaN -> the canonical quiet NaN)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return r.astype(np.uint16)
+    u = x.view(np.uint32)
+    r = u + np.uint32(0x7FFF)
+    r += (u >> np.uint32(16)) & np.uint32(1)
+    r >>= np.uint32(16)
+    out = r.astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = 0x7FC0
+    return out
 
 
 def bf16_to_f32(bits):

@@ -200,6 +200,33 @@ typedef struct {
 attn_status_t attn_resolve_layout(const attn_params_t* p, void* dq, void* dk, void* dv,
                                   attn_resolved_t* out);
 
+/* Kernel-level timing (tracing).  `events` points to 2 * ATTN_TRACE_SLOTS
+ * cudaEvent_t handles created by the caller (start, end of each slot), or is
+ * NULL to switch tracing off.  While set (per host thread), every attn_fwd /
+ * attn_bwd call records each slot's start event before the first launch of
+ * that stage and its end event after the last one, on the call's stream.  A
+ * slot whose handles are NULL is skipped.  The handles are copied; the caller
+ * keeps ownership. */
+#define ATTN_TRACE_SLOTS 6
+typedef enum {
+  ATTN_TRACE_META = 0,     /* segment-metadata kernels */
+  ATTN_TRACE_FWD = 1,      /* forward kernel */
+  ATTN_TRACE_BWD_PRE = 2,  /* D = rowsum(dO*O), accumulator zeroing */
+  ATTN_TRACE_DKDV = 3,     /* dK/dV pass (with atomic dQ) */
+  ATTN_TRACE_DQ = 4,       /* deterministic dQ pass or dQ conversion */
+  ATTN_TRACE_DBIAS = 5     /* broadcast dBias conversion */
+} attn_trace_slot_t;
+attn_status_t attn_set_trace_events(void* const* events);
+
+/* Thin wrappers over the CUDA runtime's timing events for callers without a
+ * CUDA binding of their own (e.g. ctypes).  attn_event_create makes a timing
+ * event on the current device (caller owns it; release with
+ * attn_event_destroy).  attn_event_elapsed_ms returns ATTN_ERR_CUDA if either
+ * event has not completed or was never recorded. */
+attn_status_t attn_event_create(void** event);
+attn_status_t attn_event_destroy(void* event);
+attn_status_t attn_event_elapsed_ms(const void* start, const void* end, float* ms);
+
 int32_t attn_abi_version(void);
 
 #ifdef __cplusplus
