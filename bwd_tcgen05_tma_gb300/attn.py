@@ -25,7 +25,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
 EXPORTED = ("attn_abi_version", "attn_status_string", "attn_fwd_workspace_size",
             "attn_bwd_workspace_size", "attn_resolve_layout", "attn_fwd", "attn_bwd",
             "attn_read_status", "attn_set_trace_events", "attn_event_create",
-            "attn_event_destroy", "attn_event_elapsed_ms")
+            "attn_event_destroy", "attn_event_elapsed_ms", "attn_fwd_noalloc")
+FWD_NOALLOC_SCRATCH_BYTES = 4 << 20
 TRACE_SLOTS = ("meta", "fwd", "bwd_pre", "dkdv", "dq", "dbias")
 
 c_i32, c_i64, c_f32, c_vp, c_sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
@@ -90,6 +91,8 @@ def load_library(path: str = LIB_PATH):
     lib.attn_read_status.argtypes = [c_vp, c_vp, ctypes.POINTER(attn_stats_t)]
     lib.attn_set_trace_events.restype = c_i32
     lib.attn_set_trace_events.argtypes = [ctypes.POINTER(c_vp)]
+    lib.attn_fwd_noalloc.restype = c_i32
+    lib.attn_fwd_noalloc.argtypes = [P, c_vp, c_vp, c_vp]
     lib.attn_event_create.restype = c_i32
     lib.attn_event_create.argtypes = [ctypes.POINTER(c_vp)]
     lib.attn_event_destroy.restype = c_i32
@@ -181,6 +184,15 @@ def attn_fwd(p, o, lse, ws, stream=None):
                                 ws.numel() * ws.element_size(), _stream(stream))
     if s != 0:
         raise AttnError(s, "attn_fwd")
+
+
+def attn_fwd_noalloc(p, o, lse, stream=None):
+    """Forward without a workspace: the library's fixed device scratch array is
+    used instead (no allocation).  For callers that cannot allocate device
+    memory at run time.  Overlapping calls on the GPU race on that array."""
+    s = load_library().attn_fwd_noalloc(ctypes.byref(p), _ptr(o), _ptr(lse), _stream(stream))
+    if s != 0:
+        raise AttnError(s, "attn_fwd_noalloc")
 
 
 def attn_bwd(p, o, d_o, lse, dq, dk, dv, dbias, ws, stream=None):

@@ -459,3 +459,56 @@ attn_status_t attn_read_status(const void* ws, void* stream, attn_stats_t* stats
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward without a caller-supplied workspace.
+//
+// Some callers cannot allocate device memory when they run attention: plugin
+// hosts that hand a kernel its inputs and outputs but no workspace, runtimes
+// that plan all device memory at initialisation and forbid allocation
+// afterwards, and latency-critical loops where cudaMalloc's implicit device
+// synchronisation is not acceptable.  For them the forward's scratch (the
+// normalised segment metadata, chunk summaries and tile ranges) lives in one
+// fixed array in device memory that this library owns for the lifetime of the
+// process on every GPU that loads it.
+namespace attn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // = ATTN_FWD_NOALLOC_SCRATCH_BYTES
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device.  In host
+// code the symbol name is only a host-side stand-in, never a device pointer.
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[256] = {};
+
+attn_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+      return ATTN_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" attn_status_t attn_fwd_noalloc(const attn_params_t* p, void* o, float* lse,
+                                          void* stream) {
+  attn_status_t s = validate(p);
+  if (s != ATTN_OK) return s;
+  if (!o || !lse || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  const Plan pl = make_plan(p);
+  if (pl.fwd_total > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  if ((s = noalloc_scratch(&ws)) != ATTN_OK) return s;
+  // The header (status word, counters) is cleared by the metadata launch
+  // itself; every other scratch array is fully written before it is read.
+  return attn_fwd(p, o, lse, ws, kNoAllocScratchBytes, stream);
+}

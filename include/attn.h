@@ -227,6 +227,30 @@ attn_status_t attn_event_create(void** event);
 attn_status_t attn_event_destroy(void* event);
 attn_status_t attn_event_elapsed_ms(const void* start, const void* end, float* ms);
 
+/* Forward with no caller workspace and no allocation.  The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate device
+ * memory when they run attention: plugin hosts that pass a kernel its inputs
+ * and outputs but no workspace, runtimes that plan all device memory at start-up
+ * and forbid allocation later, and latency-critical loops that cannot accept
+ * cudaMalloc's implicit device synchronisation.
+ *
+ * Same arguments and outputs as attn_fwd, minus the workspace.  The scratch is
+ * a fixed device array of ATTN_FWD_NOALLOC_SCRATCH_BYTES inside this library,
+ * held on every GPU that loads the library until the process exits.  Calls
+ * whose attn_fwd_workspace_size() exceeds that size return
+ * ATTN_ERR_WORKSPACE_TOO_SMALL and launch nothing (the forward needs about
+ * 16.5 bytes per query token and per key token, so B*Sq + B*Skv up to roughly
+ * 250k tokens fit).
+ *  - The first call on each device looks the array's device address up (this
+ *    may load the module); make that first call before any stream capture.
+ *  - Every call uses the same array.  Calls that overlap on the GPU (e.g. on
+ *    two streams without ordering between them) race on it; order them.
+ *  - Device-side status (attn_read_status) cannot be read for this call: it
+ *    needs the workspace pointer, which the caller does not have.
+ * No cudaMalloc/cudaFree or allocating library routine is called. */
+#define ATTN_FWD_NOALLOC_SCRATCH_BYTES (4u << 20)
+attn_status_t attn_fwd_noalloc(const attn_params_t* p, void* o, float* lse, void* stream);
+
 int32_t attn_abi_version(void);
 
 #ifdef __cplusplus
