@@ -25,7 +25,57 @@ struct WsHeader {
   int64_t tile_pairs;  // scheduled (query tile, KV tile) pairs
   int32_t mismatch;    // bit0 ids differ, bit1 pos differ, bit2 nonstandard pos
   int32_t where;       // debug: which wait timed out (role * 16 + barrier)
+  int32_t next_item[4];  // work-item counters of the persistent kernels (zeroed per call)
 };
+
+// Dynamic work distribution inside a persistent CTA: one thread claims items
+// from a global counter and hands them to every role of the CTA, in order,
+// through a small ring in shared memory (-1 ends the stream).
+constexpr int kItemRing = 4;
+struct ItemRing {
+  uint64_t full[kItemRing];
+  uint64_t empty[kItemRing];
+  int32_t item[kItemRing];
+};
+
+__device__ __forceinline__ void ring_init(ItemRing* r, uint32_t consumers) {
+  for (int i = 0; i < kItemRing; ++i) {
+    sm103::mbar_init(&r->full[i], 1);
+    sm103::mbar_init(&r->empty[i], consumers);
+  }
+}
+
+// Producer side: claim the next item (or -1 once exhausted) and publish it as
+// the n-th entry of the ring.  Returns false if the wait for a free slot timed out.
+__device__ __forceinline__ bool ring_push(ItemRing* r, uint32_t n, int32_t* counter, int n_items,
+                                          int32_t& item) {
+  const int s = n % kItemRing;
+  if (n >= (uint32_t)kItemRing && !sm103::mbar_wait(&r->empty[s], ((n / kItemRing) - 1) & 1))
+    return false;
+  const int32_t v = atomicAdd(counter, 1);
+  item = (v < n_items) ? v : -1;
+  *reinterpret_cast<volatile int32_t*>(&r->item[s]) = item;
+  sm103::mbar_arrive(&r->full[s]);  // release: the item is visible to waiters
+  return true;
+}
+
+// Consumer side (every consuming thread): read the n-th entry.  Warp-uniform.
+__device__ __forceinline__ bool ring_pop(ItemRing* r, uint32_t n, int32_t& item) {
+  const int s = n % kItemRing;
+  if (!sm103::mbar_wait_warp(&r->full[s], (n / kItemRing) & 1)) return false;
+  item = *reinterpret_cast<volatile int32_t*>(&r->item[s]);
+  sm103::mbar_arrive(&r->empty[s]);
+  return true;
+}
+
+// Single-thread consumer variant (MMA issuer).
+__device__ __forceinline__ bool ring_pop1(ItemRing* r, uint32_t n, int32_t& item) {
+  const int s = n % kItemRing;
+  if (!sm103::mbar_wait(&r->full[s], (n / kItemRing) & 1)) return false;
+  item = *reinterpret_cast<volatile int32_t*>(&r->item[s]);
+  sm103::mbar_arrive(&r->empty[s]);
+  return true;
+}
 
 // Summary of 64 consecutive tokens of one batch row.
 struct ChunkInfo {
@@ -95,6 +145,87 @@ struct KernelArgs {
   int dkdv_batch_loop;  // 1: one dK/dV work item loops over every batch row
   int dkdv_head_loop;   // 1: one dK/dV work item loops over every KV head
 };
+
+// Opt-in timeline for pipeline debugging (-DATTN_TIMELINE builds only): the
+// first threads of each role in CTA 0 append (event, step, SM clock) records.
+#ifdef ATTN_TIMELINE
+// Slot = event * 2048 + step: plain stores, no round trip on the critical path.
+constexpr int kTimelineSteps = 2048;
+constexpr int kTimelineCap = 64 * kTimelineSteps;
+static __device__ unsigned long long g_timeline[kTimelineCap];  // one copy per translation unit
+#define ATTN_TL(ev, step)                                                                    \
+  do {                                                                                       \
+    if (blockIdx.x == 0 && (step) < kTimelineSteps)                                          \
+      g_timeline[(ev) * kTimelineSteps + (step)] = (unsigned long long)clock64();            \
+  } while (0)
+#else
+#define ATTN_TL(ev, step) \
+  do {                    \
+  } while (0)
+#endif
+
+// Bit c set for lo <= c < hi, c in [0, 64).  Masks are applied with selects on
+// these bits so the element loops stay branch-free.
+__device__ __forceinline__ uint64_t range_bits64(int lo, int hi) {
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > 64 ? 64 : hi;
+  if (hi <= lo) return 0ull;
+  const uint64_t upper = (hi >= 64) ? ~0ull : ((1ull << hi) - 1ull);
+  const uint64_t lower = (lo <= 0) ? 0ull : ((1ull << lo) - 1ull);
+  return upper & ~lower;
+}
+
+__device__ __forceinline__ bool path_general(const KernelArgs& a);
+
+// Validity of the 128 keys [k0, k0 + 128) of batch row b for one query row, as
+// two 64-bit masks.  Fast path: the row's key range [rlo, rhi).  General path:
+// same nonzero segment id and, if causal, key position <= query position.
+__device__ __forceinline__ void kv_valid_bits(const KernelArgs& a, bool general, int b, int k0,
+                                              int rlo, int rhi, int my_id, int my_pos,
+                                              uint64_t (&vb)[2]) {
+  if (!general) {
+    vb[0] = range_bits64(rlo - k0, rhi - k0);
+    vb[1] = range_bits64(rlo - k0 - 64, rhi - k0 - 64);
+    return;
+  }
+  vb[0] = vb[1] = 0ull;
+  if (my_id == 0) return;
+  const int nkc = (a.Skv + kChunk - 1) / kChunk;
+  if (k0 + kTile <= a.Skv && (k0 % kChunk) == 0) {
+    const ChunkInfo c0 = a.kv_chunk[b * nkc + k0 / kChunk];
+    const ChunkInfo c1 = a.kv_chunk[b * nkc + k0 / kChunk + 1];
+    if (c0.uniform && c1.uniform && c0.min_id == my_id && c1.min_id == my_id &&
+        (!a.causal || max(c0.max_pos, c1.max_pos) <= my_pos)) {
+      vb[0] = vb[1] = ~0ull;
+      return;
+    }
+  }
+  const int32_t* kid = a.kv_id + (int64_t)b * a.Skv + k0;
+  const int32_t* kpos = a.kv_pos + (int64_t)b * a.Skv + k0;
+  const int nv = min(kTile, a.Skv - k0);
+  const bool vec = ((reinterpret_cast<uintptr_t>(kid) & 15u) == 0);
+#pragma unroll
+  for (int c = 0; c < kTile; c += 4) {
+    int ids[4], pss[4];
+    if (vec && c + 4 <= nv) {
+      const int4 t1 = __ldg(reinterpret_cast<const int4*>(kid + c));
+      const int4 t2 = __ldg(reinterpret_cast<const int4*>(kpos + c));
+      ids[0] = t1.x; ids[1] = t1.y; ids[2] = t1.z; ids[3] = t1.w;
+      pss[0] = t2.x; pss[1] = t2.y; pss[2] = t2.z; pss[3] = t2.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ids[e] = (c + e < nv) ? __ldg(kid + c + e) : -1;
+        pss[e] = (c + e < nv) ? __ldg(kpos + c + e) : 0;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool v = (ids[e] == my_id) & (!a.causal | (pss[e] <= my_pos));
+      vb[(c + e) >> 6] |= static_cast<uint64_t>(v) << ((c + e) & 63);
+    }
+  }
+}
 
 __device__ __forceinline__ bool path_general(const KernelArgs& a) {
   return *reinterpret_cast<const volatile int32_t*>(&a.hdr->path) != 0;

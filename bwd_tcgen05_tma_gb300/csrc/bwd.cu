@@ -159,9 +159,11 @@ __device__ __forceinline__ DkdvItem dkdv_item(const KernelArgs& a, int idx) {
   const int nb = a.dkdv_batch_loop ? 1 : a.B;
   const int ng = a.dkdv_head_loop ? 1 : a.Hkv;
   DkdvItem it;
-  it.t = idx / (nb * ng);  // KV tile 0 first: it sees the most causal query tiles
-  const int rem = idx - it.t * nb * ng;
-  const int bi = rem / ng, gi = rem - (rem / ng) * ng;
+  // (batch row, KV head)-major: CTAs running at the same time work on KV tiles
+  // of the same head and re-read the same Q / dO tiles from L2
+  const int combo = idx / a.n_kt;
+  it.t = idx - combo * a.n_kt;
+  const int bi = combo / ng, gi = combo - (combo / ng) * ng;
   it.b0 = a.dkdv_batch_loop ? 0 : bi;
   it.b1 = a.dkdv_batch_loop ? a.B : bi + 1;
   it.g0 = a.dkdv_head_loop ? 0 : gi;
@@ -187,6 +189,7 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(DkdvBars));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   StageVec* vec = reinterpret_cast<StageVec*>(sm + L::kVecOff);
+  ItemRing* ring = reinterpret_cast<ItemRing*>(sm + L::kBarOff + 256);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = dkdv_n_items(a);
@@ -214,6 +217,7 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
       mbar_init(&bars->qd_full[s], 1 + 64);
       mbar_init(&bars->qd_empty[s], 1 + 128);
     }
+    ring_init(ring, 1 + 64 + 128 + 128);  // MMA, vector loader, P/dS warps, epilogue
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -236,7 +240,11 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
       prefetch_tensormap(&a.tm_do);
       uint32_t st = 0, kvc = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[1], n_items, idx)) ||
+            idx < 0)
+          break;
         const DkdvItem w = dkdv_item(a, idx);
         for (int b = w.b0; b < w.b1 && ok; ++b) {
           for (int g = w.g0; g < w.g1 && ok; ++g) {
@@ -270,6 +278,7 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
                 for (int c = 0; c < DV / 64; ++c)
                   tma_load_3d(qs + L::kQBytes + c * 8192, &a.tm_do, &bars->qd_full[stage], c * 64,
                               h, qrow);
+                ATTN_TL(1, st);
               }
             }
           }
@@ -290,7 +299,11 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
     const int t = tid - 64;
     uint32_t st = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
+          idx < 0)
+        break;
       const DkdvItem w = dkdv_item(a, idx);
       for (int b = w.b0; b < w.b1 && ok; ++b) {
         for (int g = w.g0; g < w.g1 && ok; ++g) {
@@ -313,6 +326,7 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
                 vec[stage].qpos[t] = in ? a.q_pos[(int64_t)b * a.Sq + i] : 0;
               }
               mbar_arrive(&bars->qd_full[stage]);
+              if (t == 0) ATTN_TL(3, st);
             }
           }
         }
@@ -329,39 +343,48 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
       constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, false, true);
       constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, false, true);
       constexpr uint32_t id_dq = idesc_bf16_f32(128, kBwdQ, true, true);
-      const uint32_t k_addr = smem_u32(sm + L::kKOff), v_addr = smem_u32(sm + L::kVOff);
-      const uint32_t p_addr = smem_u32(sm + L::kPOff), ds_addr = smem_u32(sm + L::kDSOff);
+      // operand descriptors are built once; each MMA only adds a constant offset
+      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);      // K, K-major
+      const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);   // K^T, MN-major
+      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
+      const uint64_t p_km = sdesc_sw128(smem_u32(sm + L::kPOff), 16, 1024);
+      const uint64_t ds_km = sdesc_sw128(smem_u32(sm + L::kDSOff), 16, 1024);
+      const uint64_t ds_mn = sdesc_sw128(smem_u32(sm + L::kDSOff), 8192, 1024);
+      const uint64_t st_km = sdesc_sw128(smem_u32(sm + L::kStageOff), 16, 1024);   // Q / dO tiles
+      const uint64_t st_mn = sdesc_sw128(smem_u32(sm + L::kStageOff), 8192, 1024);
       uint32_t st = 0, kvc = 0, gc = 0;
       bool ok = true;
-      auto stage_addr = [&](uint32_t x) {
-        return smem_u32(sm + L::kStageOff + (x % NS) * L::kStageBytes);
+      auto stage_off16 = [&](uint32_t x) -> uint32_t {
+        return static_cast<uint32_t>(((x % NS) * L::kStageBytes) >> 4);
       };
       auto issue_s = [&](uint32_t x) -> bool {  // S^T = K Q^T
         if (!mbar_wait(&bars->qd_full[x % NS], (x / NS) & 1)) return false;
         if (x > 0 && !mbar_wait(&bars->s_free, (x - 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t q_addr = stage_addr(x);
+        const uint64_t qd = st_km + stage_off16(x);
 #pragma unroll
         for (int ks = 0; ks < DQK / 16; ++ks)
-          mma_ss(tmem + L::kColS,
-                 sdesc_sw128(k_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                 sdesc_sw128(q_addr + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id_s, ks > 0);
+          mma_ss(tmem + L::kColS, k_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                 qd + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id_s, ks > 0);
         mma_commit(&bars->s_full);
+        ATTN_TL(10, x);
         return true;
       };
       auto issue_dp = [&](uint32_t x) -> bool {  // dP^T = V dO^T
         if (x > 0 && !mbar_wait(&bars->dp_free, (x - 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t o_addr = stage_addr(x) + L::kQBytes;
+        const uint64_t od = st_km + stage_off16(x) + (L::kQBytes >> 4);
 #pragma unroll
         for (int ks = 0; ks < DV / 16; ++ks)
-          mma_ss(tmem + L::kColDP,
-                 sdesc_sw128(v_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                 sdesc_sw128(o_addr + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), id_s, ks > 0);
+          mma_ss(tmem + L::kColDP, v_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                 od + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id_s, ks > 0);
         mma_commit(&bars->dp_full);
+        ATTN_TL(11, x);
         return true;
       };
-      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
         const DkdvItem w = dkdv_item(a, idx);
         for (int b = w.b0; b < w.b1 && ok; ++b) {
           for (int g = w.g0; g < w.g1 && ok; ++g) {
@@ -377,33 +400,37 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               const uint32_t cur = st + u;
               if (u + 1 < nsteps && !(ok = issue_s(cur + 1))) break;
               if (!(ok = mbar_wait(&bars->p_ready, cur & 1))) break;
+              ATTN_TL(12, cur);
               if (u == 0 && gc > 0 && !(ok = mbar_wait(&bars->acc_empty, (gc - 1) & 1))) break;
               tc_fence_after();
-              const uint32_t qa = stage_addr(cur), oa = qa + L::kQBytes;
+              const uint64_t q_mn = st_mn + stage_off16(cur);
+              const uint64_t o_mn = q_mn + (L::kQBytes >> 4);
 #pragma unroll
               for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dV += P^T dO
-                mma_ss(tmem + L::kColDV, sdesc_sw128(p_addr + ks * 32, 16, 1024),
-                       sdesc_sw128(oa + ks * 2048, 8192, 1024), id_dv, (u > 0 || ks > 0));
+                mma_ss(tmem + L::kColDV, p_km + ((ks * 32) >> 4), o_mn + ((ks * 2048) >> 4), id_dv,
+                       (u > 0 || ks > 0));
               mma_commit(&bars->p_free);
               if (u + 1 < nsteps && !(ok = issue_dp(cur + 1))) break;
               if (!(ok = mbar_wait(&bars->ds_ready, cur & 1))) break;
+              ATTN_TL(14, cur);
               tc_fence_after();
 #pragma unroll
               for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dK += dS^T Q
-                mma_ss(tmem + L::kColDK, sdesc_sw128(ds_addr + ks * 32, 16, 1024),
-                       sdesc_sw128(qa + ks * 2048, 8192, 1024), id_dk, (u > 0 || ks > 0));
+                mma_ss(tmem + L::kColDK, ds_km + ((ks * 32) >> 4), q_mn + ((ks * 2048) >> 4), id_dk,
+                       (u > 0 || ks > 0));
               if constexpr (ATOMIC) {  // dQ^T = K^T dS^T
                 const uint32_t buf = cur & 1;
                 if (cur >= 2 && !(ok = mbar_wait(&bars->dq_free[buf], ((cur >> 1) - 1) & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                  mma_ss(tmem + L::kColDQ + buf * 64, sdesc_sw128(k_addr + ks * 2048, 16384, 1024),
-                         sdesc_sw128(ds_addr + ks * 2048, 8192, 1024), id_dq, ks > 0);
+                  mma_ss(tmem + L::kColDQ + buf * 64, k_mn + ((ks * 2048) >> 4),
+                         ds_mn + ((ks * 2048) >> 4), id_dq, ks > 0);
                 mma_commit(&bars->dq_full[buf]);
               }
               mma_commit(&bars->ds_free);
               mma_commit(&bars->qd_empty[cur % NS]);
+              ATTN_TL(15, cur);
             }
             if (!ok) break;
             mma_commit(&bars->acc_full);
@@ -428,7 +455,11 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
     const int nqc = (a.Sq + kChunk - 1) / kChunk;
     uint32_t st = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
+          idx < 0)
+        break;
       const DkdvItem w = dkdv_item(a, idx);
       const int kj = w.t * kTile + j;
       const bool row_ok = kj < a.Skv;
@@ -458,8 +489,11 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               const int stage = cur % NS;
               const int q0 = q_lo + s * kBwdQ;
               float x[kBwdQ];
+              if (j == 0) ATTN_TL(20, cur);
               if (!(ok = mbar_wait_warp(&bars->qd_full[stage], (cur / NS) & 1))) break;
+              if (j == 0) ATTN_TL(26, cur);
               if (!(ok = mbar_wait_warp(&bars->s_full, cur & 1))) break;
+              if (j == 0) ATTN_TL(21, cur);
               tc_fence_after();
 #pragma unroll
               for (int q = 0; q < kBwdQ / 32; ++q) {
@@ -471,34 +505,56 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               }
               tc_fence_before();
               mbar_arrive(&bars->s_free);
+              if (j == 0) ATTN_TL(40, cur);
               const StageVec& V = vec[stage];
               if (HAS_BIAS && row_ok) {
                 const bf16* bp = a.bias + (bias_base + q0) * a.Skv + kj;
-#pragma unroll 8
+#pragma unroll
                 for (int c = 0; c < kBwdQ; ++c)
                   if (q0 + c < a.Sq) x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
               }
-              bool full;
+              // validity of the 64 query columns for this key row, as a bitmask
+              uint64_t vbits;
               if (!general) {
-                full = row_ok && q0 >= qlo && q0 + kBwdQ <= qhi;
+                vbits = row_ok ? range_bits64(qlo - q0, qhi - q0) : 0ull;
               } else {
-                full = false;
+                vbits = 0ull;
+                bool full = false;
                 if (row_ok && my_id != 0 && q0 + kBwdQ <= a.Sq) {
                   const ChunkInfo ci = a.q_chunk[b * nqc + q0 / kChunk];
                   full = ci.uniform && ci.min_id == my_id && (!a.causal || ci.min_pos >= my_pos);
                 }
+                if (full) {
+                  vbits = ~0ull;
+                } else if (row_ok && my_id != 0) {
+#pragma unroll
+                  for (int c = 0; c < kBwdQ; c += 4) {
+                    const int4 id4 = *reinterpret_cast<const int4*>(&V.qid[c]);
+                    const int4 ps4 = *reinterpret_cast<const int4*>(&V.qpos[c]);
+                    const int ids[4] = {id4.x, id4.y, id4.z, id4.w};
+                    const int pss[4] = {ps4.x, ps4.y, ps4.z, ps4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const bool v = (ids[e] == my_id) & (!a.causal | (my_pos <= pss[e]));
+                      vbits |= static_cast<uint64_t>(v) << (c + e);
+                    }
+                  }
+                }
               }
 #pragma unroll
-              for (int c = 0; c < kBwdQ; ++c) {
-                bool valid = true;
-                if (!full) {
-                  if (!general) valid = (q0 + c >= qlo) && (q0 + c < qhi);
-                  else valid = V.qid[c] == my_id && my_id != 0 && (!a.causal || my_pos <= V.qpos[c]);
+              for (int c = 0; c < kBwdQ; c += 4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(&V.lse2[c]);
+                const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float p = ex2_approx(x[c + e] - ls[e]);
+                  x[c + e] = ((vbits >> (c + e)) & 1ull) ? p : 0.f;
                 }
-                x[c] = valid ? ex2_approx(x[c] - V.lse2[c]) : 0.f;
               }
+              if (j == 0) ATTN_TL(41, cur);
               // P^T row j -> shared memory (K-major, 128-byte swizzle)
               if (cur > 0 && !(ok = mbar_wait_warp(&bars->p_free, (cur - 1) & 1))) break;
+              if (j == 0) ATTN_TL(42, cur);
 #pragma unroll
               for (int u8 = 0; u8 < 8; ++u8) {
                 const float* p8 = x + u8 * 8;
@@ -508,8 +564,10 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               }
               fence_proxy_async_smem();
               mbar_arrive(&bars->p_ready);
+              if (j == 0) ATTN_TL(22, cur);
               // dS^T = P^T (dP^T - D)
               if (!(ok = mbar_wait_warp(&bars->dp_full, cur & 1))) break;
+              if (j == 0) ATTN_TL(23, cur);
               tc_fence_after();
 #pragma unroll
               for (int q = 0; q < kBwdQ / 32; ++q) {
@@ -517,9 +575,13 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
                 tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + q * 32, u);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
+                for (int e = 0; e < 32; e += 4) {
                   const int c = q * 32 + e;
-                  x[c] = x[c] * (__uint_as_float(u[e]) - V.D[c]);
+                  const float4 d4 = *reinterpret_cast<const float4*>(&V.D[c]);
+                  x[c] = x[c] * (__uint_as_float(u[e]) - d4.x);
+                  x[c + 1] = x[c + 1] * (__uint_as_float(u[e + 1]) - d4.y);
+                  x[c + 2] = x[c + 2] * (__uint_as_float(u[e + 2]) - d4.z);
+                  x[c + 3] = x[c + 3] * (__uint_as_float(u[e + 3]) - d4.w);
                 }
               }
               tc_fence_before();
@@ -534,15 +596,16 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               }
               fence_proxy_async_smem();
               mbar_arrive(&bars->ds_ready);
+              if (j == 0) ATTN_TL(24, cur);
               if (DBIAS != 0 && row_ok) {
                 if (DBIAS == 1) {
                   bf16* dp = a.dbias + (bias_base + q0) * a.Skv + kj;
-#pragma unroll 8
+#pragma unroll
                   for (int c = 0; c < kBwdQ; ++c)
                     if (q0 + c < a.Sq) dp[(int64_t)c * a.Skv] = __float2bfloat16_rn(x[c]);
                 } else {
                   float* dp = a.dbias_acc + (bias_base + q0) * a.Skv + kj;
-#pragma unroll 8
+#pragma unroll
                   for (int c = 0; c < kBwdQ; ++c)
                     if (q0 + c < a.Sq) dp[(int64_t)c * a.Skv] += x[c];
                 }
@@ -563,7 +626,11 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t st = 0, gc = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
+          idx < 0)
+        break;
       const DkdvItem w = dkdv_item(a, idx);
       const int kj = w.t * kTile + j;
       const bool row_ok = kj < a.Skv;
@@ -590,6 +657,7 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               for (int s = 0; s < nq; ++s, ++st) {
                 const uint32_t buf = st & 1;
                 if (!(ok = mbar_wait_warp(&bars->dq_full[buf], (st >> 1) & 1))) break;
+                if (j == 0) ATTN_TL(30, st);
                 tc_fence_after();
                 uint32_t u0[32], u1[32];
                 tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + buf * 64, u0);
@@ -609,6 +677,7 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
                   for (int c = 0; c < 32; ++c)
                     if (32 + c < nv) red_add_f32(base + (32 + c) * rs, __uint_as_float(u1[c]) * a.scale);
                 }
+                if (j == 0) ATTN_TL(31, st);
               }
             }
             if (!ok) break;
@@ -687,7 +756,7 @@ struct DqLayout {
   static constexpr int kKOff = kSOff + kSBytes;
   static constexpr int kVOff = kKOff + kKStages * kKBytes;
   static constexpr int kBarOff = kVOff + kVStages * kVBytes;
-  static constexpr int kBytes = kBarOff + 256;
+  static constexpr int kBytes = kBarOff + 512;  // barriers, then the item ring at +256
   static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
 };
@@ -708,6 +777,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
   DqBars* bars = reinterpret_cast<DqBars*>(sm + L::kBarOff);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(DqBars));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  ItemRing* ring = reinterpret_cast<ItemRing*>(sm + L::kBarOff + 256);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = a.B * a.n_qt * a.Hq;
 
@@ -729,6 +799,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
+    ring_init(ring, 1 + 128);  // MMA issuer + softmax warpgroup
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -761,7 +832,11 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
       prefetch_tensormap(&a.tm_do);
       uint32_t kt = 0, it = 0, k_loads = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[2], n_items, idx)) ||
+            idx < 0)
+          break;
         int b, t, h, kv_lo, n;
         item_of(idx, b, t, h, kv_lo, n);
         if (n == 0) continue;
@@ -812,8 +887,13 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
       constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, false, true);
-      const uint32_t q_addr = smem_u32(sm + L::kQOff), o_addr = smem_u32(sm + L::kOOff);
-      const uint32_t s_addr = smem_u32(sm + L::kSOff);
+      // operand descriptors are built once; each MMA only adds a constant offset
+      const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+      const uint64_t o_km = sdesc_sw128(smem_u32(sm + L::kOOff), 16, 1024);
+      const uint64_t s_km = sdesc_sw128(smem_u32(sm + L::kSOff), 16, 1024);
+      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);
+      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
       uint32_t kt = 0, it = 0;
       bool ok = true;
       auto issue_s = [&](uint32_t k) -> bool {  // S = Q K^T
@@ -821,12 +901,11 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
         if (!mbar_wait(&bars->k_full[ks_], (k / KS) & 1)) return false;
         if (k > 0 && !mbar_wait(&bars->s_free, (k - 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(sm + L::kKOff + ks_ * L::kKBytes);
+        const uint64_t kd = k_km + static_cast<uint32_t>((ks_ * L::kKBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < DQK / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(tmem + L::kColS, sdesc_sw128(q_addr + off, 16, 1024),
-                 sdesc_sw128(k_addr + off, 16, 1024), id_s, ks > 0);
+          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + L::kColS, q_km + off16, kd + off16, id_s, ks > 0);
         }
         mma_commit(&bars->s_full);
         return true;
@@ -836,18 +915,19 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
         if (!mbar_wait(&bars->v_full[vs], (k / VS) & 1)) return false;
         if (k > 0 && !mbar_wait(&bars->dp_free, (k - 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(sm + L::kVOff + vs * L::kVBytes);
+        const uint64_t vd = v_km + static_cast<uint32_t>((vs * L::kVBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < DV / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(tmem + L::kColDP, sdesc_sw128(o_addr + off, 16, 1024),
-                 sdesc_sw128(v_addr + off, 16, 1024), id_s, ks > 0);
+          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + L::kColDP, o_km + off16, vd + off16, id_s, ks > 0);
         }
         mma_commit(&bars->dp_full);
         mma_commit(&bars->v_empty[vs]);
         return true;
       };
-      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
         int b, t, h, kv_lo, n;
         item_of(idx, b, t, h, kv_lo, n);
         if (n == 0) continue;
@@ -863,12 +943,11 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
           if (!(ok = mbar_wait(&bars->ds_ready, k & 1))) break;
           if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->acc_empty, (it - 1) & 1))) break;
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(sm + L::kKOff + (k % KS) * L::kKBytes);
+          const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)  // dQ += dS K
-            mma_ss(tmem + L::kColDQ,
-                   sdesc_sw128(s_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                   sdesc_sw128(k_addr + ks * 2048, 16384, 1024), id_dq, (j > 0 || ks > 0));
+            mma_ss(tmem + L::kColDQ, s_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                   kd + ((ks * 2048) >> 4), id_dq, (j > 0 || ks > 0));
           mma_commit(&bars->ds_free);
           mma_commit(&bars->k_empty[k % KS]);
           if (KS == 1 && more) {
@@ -893,7 +972,11 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
     const uint32_t s_addr = smem_u32(sm + L::kSOff);
     uint32_t kt = 0, it = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
+          idx < 0)
+        break;
       int b, t, h, kv_lo, n;
       item_of(idx, b, t, h, kv_lo, n);
       const int i = t * kTile + r;
@@ -947,39 +1030,17 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
         if (HAS_BIAS && row_ok) {
           const bf16* bp = bias_row + k0;
           const int nv = min(kTile, a.Skv - k0);
-#pragma unroll 8
+#pragma unroll
           for (int c = 0; c < kTile; ++c)
             if (c < nv) x[c] += __bfloat162float(bp[c]) * kLog2e;
         }
-        bool full;
-        if (!general) {
-          full = (k0 >= rlo) && (k0 + kTile <= rhi);
-        } else {
-          full = false;
-          if (k0 + kTile <= a.Skv && my_id != 0) {
-            const int nkc = (a.Skv + kChunk - 1) / kChunk;
-            const ChunkInfo c0 = a.kv_chunk[b * nkc + k0 / kChunk];
-            const ChunkInfo c1 = a.kv_chunk[b * nkc + k0 / kChunk + 1];
-            full = c0.uniform && c1.uniform && c0.min_id == my_id && c1.min_id == my_id &&
-                   (!a.causal || max(c0.max_pos, c1.max_pos) <= my_pos);
-          }
-        }
-        if (!full) {
-          const int32_t* kid = a.kv_id + (int64_t)b * a.Skv + k0;
-          const int32_t* kpos = a.kv_pos + (int64_t)b * a.Skv + k0;
-          const int nv = min(kTile, a.Skv - k0);
+        uint64_t vb[2];
+        kv_valid_bits(a, general, b, k0, rlo, rhi, my_id, my_pos, vb);
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) {
-            bool v;
-            if (!general) v = (k0 + c >= rlo) && (k0 + c < rhi);
-            else
-              v = c < nv && __ldg(kid + c) == my_id && my_id != 0 &&
-                  (!a.causal || __ldg(kpos + c) <= my_pos);
-            if (!v) x[c] = -INFINITY;
-          }
+        for (int c = 0; c < kTile; ++c) {
+          const float p = ex2_approx(x[c] - lse2);
+          x[c] = ((vb[c >> 6] >> (c & 63)) & 1ull) ? p : 0.f;
         }
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) x[c] = ex2_approx(x[c] - lse2);
         if (!(ok = mbar_wait_warp(&bars->dp_full, k & 1))) break;
         tc_fence_after();
 #pragma unroll
@@ -1156,3 +1217,15 @@ cudaError_t launch_dbias_convert(const KernelArgs& a, cudaStream_t st) {
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TIMELINE
+// Debug builds only: copies the timeline records out and resets the counter.
+extern "C" int attn_debug_timeline(unsigned long long* out, int cap) {
+  cudaDeviceSynchronize();
+  const int n = cap < attn::kTimelineCap ? cap : attn::kTimelineCap;
+  cudaMemcpyFromSymbol(out, attn::g_timeline, sizeof(unsigned long long) * n);
+  static unsigned long long zeros[attn::kTimelineCap];
+  cudaMemcpyToSymbol(attn::g_timeline, zeros, sizeof(zeros));
+  return n;
+}
+#endif

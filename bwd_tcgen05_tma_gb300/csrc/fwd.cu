@@ -45,7 +45,7 @@ struct FwdLayout {
   static constexpr int kVOff = kKOff + kKStages * kKBytes;
   static constexpr int kPOff = kVOff + kVStages * kVBytes;
   static constexpr int kBarOff = kPOff + kPBytes;
-  static constexpr int kBytes = kBarOff + 256;
+  static constexpr int kBytes = kBarOff + 512;  // barriers, then the item ring at +256
   // at least ~116 KB so two CTAs never share an SM (each allocates all of TMEM)
   static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
   Bars* bars = reinterpret_cast<Bars*>(sm + L::kBarOff);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(Bars));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  ItemRing* ring = reinterpret_cast<ItemRing*>(sm + L::kBarOff + 256);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = a.B * a.n_qt * a.Hq;
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->s_empty[s], 128);
     }
+    ring_init(ring, 1 + 128);  // MMA issuer + softmax warpgroup
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -147,7 +149,11 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
       prefetch_tensormap(&a.tm_v);
       uint32_t kt = 0, it = 0, q_loads = 0, k_loads = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[0], n_items, idx)) ||
+            idx < 0)
+          break;
         const FwdItem w = fwd_item(a, idx);
         if (w.n == 0) continue;
         if (it > 0 && !(ok = mbar_wait(&bars->q_empty, (it - 1) & 1))) break;
@@ -200,8 +206,11 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, DV, false, true);
-      const uint32_t q_addr = smem_u32(sm + L::kQOff);
-      const uint32_t p_addr = smem_u32(sm + L::kPOff);
+      // operand descriptors are built once; each MMA only adds a constant offset
+      const uint64_t q_desc = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+      const uint64_t p_desc = sdesc_sw128(smem_u32(sm + L::kPOff), 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm + L::kVOff), 16384, 1024);
       uint32_t kt = 0, it = 0;
       bool ok = true;
       auto issue_s = [&](uint32_t k) -> bool {
@@ -209,18 +218,20 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         if (!mbar_wait(&bars->k_full[s], (k / L::kKStages) & 1)) return false;
         if (k >= 2 && !mbar_wait(&bars->s_empty[sb], ((k >> 1) - 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(sm + L::kKOff + s * L::kKBytes);
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>((s * L::kKBytes) >> 4);
+        const uint32_t dt = tmem + L::kColS + sb * kTile;
 #pragma unroll
         for (int ks = 0; ks < DQK / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(tmem + L::kColS + sb * kTile, sdesc_sw128(q_addr + off, 16, 1024),
-                 sdesc_sw128(k_addr + off, 16, 1024), idesc_s, ks > 0);
+          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+          mma_ss(dt, q_desc + off16, kd + off16, idesc_s, ks > 0);
         }
         mma_commit(&bars->s_full[sb]);
         mma_commit(&bars->k_empty[s]);
         return true;
       };
-      for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
         const FwdItem w = fwd_item(a, idx);
         if (w.n == 0) continue;
         if (!(ok = mbar_wait(&bars->q_full, it & 1))) break;
@@ -237,12 +248,12 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
           const int s = k % L::kVStages;
           if (!(ok = mbar_wait(&bars->v_full[s], (k / L::kVStages) & 1))) break;
           tc_fence_after();
-          const uint32_t v_addr = smem_u32(sm + L::kVOff + s * L::kVBytes);
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>((s * L::kVBytes) >> 4);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks) {
-            const uint32_t poff = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + L::kColO, sdesc_sw128(p_addr + poff, 16, 1024),
-                   sdesc_sw128(v_addr + ks * 2048, 16384, 1024), idesc_o, (j > 0 || ks > 0));
+            const uint32_t poff16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            mma_ss(tmem + L::kColO, p_desc + poff16, vd + static_cast<uint32_t>(ks * (2048 >> 4)),
+                   idesc_o, (j > 0 || ks > 0));
           }
           mma_commit(&bars->pv_done);
           mma_commit(&bars->v_empty[s]);
@@ -265,7 +276,11 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
     const uint32_t p_addr = smem_u32(sm + L::kPOff);
     uint32_t kt = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok && !*abort_flag; idx += gridDim.x) {
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
+          idx < 0)
+        break;
       const FwdItem w = fwd_item(a, idx);
       const int i = w.t * kTile + r;
       const bool row_ok = i < a.Sq;
@@ -316,52 +331,12 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         tc_fence_before();
         mbar_arrive(&bars->s_empty[sb]);
         if (HAS_BIAS && row_ok) add_bias_row(x, bias_row + k0, min(kTile, a.Skv - k0));
-        // mask
-        bool full;
-        if (!general) {
-          full = (k0 >= rlo) && (k0 + kTile <= rhi);
-        } else {
-          full = false;
-          if (k0 + kTile <= a.Skv && my_id != 0) {
-            const int nkc = (a.Skv + kChunk - 1) / kChunk;
-            const ChunkInfo c0 = a.kv_chunk[w.b * nkc + k0 / kChunk];
-            const ChunkInfo c1 = a.kv_chunk[w.b * nkc + k0 / kChunk + 1];
-            full = c0.uniform && c1.uniform && c0.min_id == my_id && c1.min_id == my_id &&
-                   (!a.causal || max(c0.max_pos, c1.max_pos) <= my_pos);
-          }
-        }
-        if (!full) {
-          if (!general) {
+        // mask (branch-free: a validity bitmask per row and tile)
+        uint64_t vb[2];
+        kv_valid_bits(a, general, w.b, k0, rlo, rhi, my_id, my_pos, vb);
 #pragma unroll
-            for (int c = 0; c < kTile; ++c)
-              if (k0 + c < rlo || k0 + c >= rhi) x[c] = -INFINITY;
-          } else {
-            const int32_t* kid = a.kv_id + (int64_t)w.b * a.Skv + k0;
-            const int32_t* kpos = a.kv_pos + (int64_t)w.b * a.Skv + k0;
-            const int nv = min(kTile, a.Skv - k0);
-#pragma unroll
-            for (int c = 0; c < kTile; c += 4) {
-              int ids4[4], pos4[4];
-              if (c + 4 <= nv && ((reinterpret_cast<uintptr_t>(kid + c) & 15u) == 0)) {
-                const int4 t1 = __ldg(reinterpret_cast<const int4*>(kid + c));
-                const int4 t2 = __ldg(reinterpret_cast<const int4*>(kpos + c));
-                ids4[0] = t1.x; ids4[1] = t1.y; ids4[2] = t1.z; ids4[3] = t1.w;
-                pos4[0] = t2.x; pos4[1] = t2.y; pos4[2] = t2.z; pos4[3] = t2.w;
-              } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  ids4[e] = (c + e < nv) ? __ldg(kid + c + e) : -1;
-                  pos4[e] = (c + e < nv) ? __ldg(kpos + c + e) : 0;
-                }
-              }
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const bool v = ids4[e] == my_id && my_id != 0 && (!a.causal || pos4[e] <= my_pos);
-                if (!v) x[c + e] = -INFINITY;
-              }
-            }
-          }
-        }
+        for (int c = 0; c < kTile; ++c)
+          x[c] = ((vb[c >> 6] >> (c & 63)) & 1ull) ? x[c] : -INFINITY;
         float mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, x[c]);
