@@ -198,6 +198,19 @@ bool make_map(CUtensorMap* m, const void* base, int D, int H, int64_t T, int64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the fp32 dQ accumulator [T, H, D]: box {32, 1, 64}, no swizzle.
+bool make_map_f32(CUtensorMap* m, const void* base, int D, int H, int64_t T) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+  cuuint32_t box[3] = {32, 1, (cuuint32_t)kBwdQ};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -418,6 +431,8 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
       !make_map(&a.tm_v, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
       !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
                 kBwdQ))
+    return ATTN_ERR_CUDA;
+  if (atomic && !make_map_f32(&a.tm_dqacc, a.dq_acc, p->d_qk, p->Hq, (int64_t)p->B * p->Sq))
     return ATTN_ERR_CUDA;
   const int nsm = sm_count();
   trace(ATTN_TRACE_DKDV, false, st);

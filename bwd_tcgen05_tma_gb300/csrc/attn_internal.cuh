@@ -94,6 +94,7 @@ struct KernelArgs {
   CUtensorMap tm_k;    // dims {d_qk, Hkv, B*Skv}, box {64, 1, 128}
   CUtensorMap tm_v;    // dims {d_v, Hkv, B*Skv},  box {64, 1, 128}
   CUtensorMap tm_do;   // dims {d_v, Hq, B*Sq},    box {64, 1, 128 or 64}
+  CUtensorMap tm_dqacc;  // fp32 dQ accumulator: dims {d_qk, Hq, B*Sq}, box {32, 1, 64}
 
   int B, Sq, Skv, Hq, Hkv, d_qk, d_v;
   int causal;
@@ -231,9 +232,10 @@ __device__ __forceinline__ bool path_general(const KernelArgs& a) {
   return *reinterpret_cast<const volatile int32_t*>(&a.hdr->path) != 0;
 }
 
+// Records a timed-out wait; the first one (by arrival) keeps its location.
 __device__ __forceinline__ void report_timeout(const KernelArgs& a, int where) {
   atomicExch(&a.hdr->status, 6 /* ATTN_ERR_DEVICE_TIMEOUT */);
-  atomicExch(&a.hdr->where, where);
+  atomicCAS(&a.hdr->where, 0, where);
 }
 
 // Kernel launchers (defined in the kernel translation units).

@@ -104,37 +104,43 @@ __global__ void dbias_convert_kernel(const KernelArgs a) {
 }
 
 // =========================================================== dK / dV pass
-template <int DQK, int DV>
+template <int DQK, int DV, bool ATOMIC>
 struct DkdvLayout {
   static constexpr int kKBytes = kTile * DQK * 2;
   static constexpr int kVBytes = kTile * DV * 2;
   static constexpr int kQBytes = kBwdQ * DQK * 2;  // one 64-row query tile
   static constexpr int kOBytes = kBwdQ * DV * 2;
-  static constexpr int kPBytes = kTile * kBwdQ * 2;
+  static constexpr int kDSBytes = kTile * kBwdQ * 2;
+  static constexpr int kDQStageBytes = ATOMIC ? kBwdQ * DQK * 4 : 0;  // fp32 dQ tile for TMA reduce
   static constexpr int kStageBytes = kQBytes + kOBytes;
-  static constexpr int kFixed = kKBytes + kVBytes + 2 * kPBytes;
-  static constexpr int kStages = (kFixed + 3 * kStageBytes <= 200 * 1024) ? 3 : 2;
+  static constexpr int kFixed = kKBytes + kVBytes + kDSBytes + kDQStageBytes;
+  static constexpr int kStages = (kFixed + 4 * kStageBytes + 4 * 1024 <= 216 * 1024) ? 4
+                                 : (kFixed + 3 * kStageBytes + 3 * 1024 <= 216 * 1024) ? 3 : 2;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKBytes;
-  static constexpr int kPOff = kKBytes + kVBytes;
-  static constexpr int kDSOff = kPOff + kPBytes;
-  static constexpr int kStageOff = kDSOff + kPBytes;
+  static constexpr int kDSOff = kKBytes + kVBytes;
+  static constexpr int kDQOff = kDSOff + kDSBytes;
+  static constexpr int kStageOff = kDQOff + kDQStageBytes;
   static constexpr int kVecOff = kStageOff + kStages * kStageBytes;  // 1 KB per stage
   static constexpr int kBarOff = kVecOff + kStages * 1024;
   static constexpr int kBytes = kBarOff + 512;
   static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
+  // tensor memory: dV, dK accumulators; two S^T buffers (P^T is written back
+  // over its own S^T as packed bf16); dP^T; dQ^T (atomic mode, d_qk <= 128)
   static constexpr uint32_t kColDV = 0;
   static constexpr uint32_t kColDK = 128;
-  static constexpr uint32_t kColS = (DQK > 128) ? 320 : 256;
-  static constexpr uint32_t kColDP = kColS + 64;
-  static constexpr uint32_t kColDQ = 384;  // two 64-column buffers (d_qk <= 128 only)
+  static constexpr uint32_t kColS = (DQK > 128) ? 320 : 256;  // + 64 * (step & 1)
+  static constexpr uint32_t kColDP = kColS + 128;
+  static constexpr uint32_t kColDQ = kColDP + 64;
 };
 
+// Every barrier below can run at most one phase ahead of its waiters (parity
+// waits rely on that): per-S-buffer barriers for the S^T / P^T double buffer.
 struct DkdvBars {
-  uint64_t kv_full, kv_empty, s_full, s_free, dp_full, dp_free, p_ready, p_free, ds_ready,
-      ds_free, acc_full, acc_empty, drain;
-  uint64_t dq_full[2], dq_free[2];
-  uint64_t qd_full[3], qd_empty[3];
+  uint64_t kv_full, kv_empty, dp_full, dp_free, ds_ready, ds_free, acc_full, acc_empty, drain,
+      dq_full, dq_free, stg_full, stg_free;
+  uint64_t s_full[2], p_ready[2], p_free[2];
+  uint64_t qd_full[4], qd_empty[4];
 };
 
 struct StageVec {  // per query tile: log2-LSE, D, and (general path) ids / positions
@@ -180,7 +186,7 @@ __device__ __forceinline__ int dkdv_q_tiles(const KernelArgs& a, int b, int t, i
 
 template <int DQK, int DV, bool ATOMIC, bool HAS_BIAS, int DBIAS>
 __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ KernelArgs a) {
-  using L = DkdvLayout<DQK, DV>;
+  using L = DkdvLayout<DQK, DV, ATOMIC>;
   constexpr int NS = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -198,22 +204,23 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->kv_empty, 1);
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 128);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(&bars->s_full[b2], 1);
+      mbar_init(&bars->p_ready[b2], 128);
+      mbar_init(&bars->p_free[b2], 1);
+    }
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->dp_free, 128);
-    mbar_init(&bars->p_ready, 128);
-    mbar_init(&bars->p_free, 1);
     mbar_init(&bars->ds_ready, 128);
     mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 128);
     mbar_init(&bars->drain, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->dq_full[s], 1);
-      mbar_init(&bars->dq_free[s], 128);
-    }
-    for (int s = 0; s < 3; ++s) {
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->stg_full, 128);
+    mbar_init(&bars->stg_free, 1);
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->qd_full[s], 1 + 64);
       mbar_init(&bars->qd_empty[s], 1 + 128);
     }
@@ -347,7 +354,6 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
       const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);      // K, K-major
       const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);   // K^T, MN-major
       const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
-      const uint64_t p_km = sdesc_sw128(smem_u32(sm + L::kPOff), 16, 1024);
       const uint64_t ds_km = sdesc_sw128(smem_u32(sm + L::kDSOff), 16, 1024);
       const uint64_t ds_mn = sdesc_sw128(smem_u32(sm + L::kDSOff), 8192, 1024);
       const uint64_t st_km = sdesc_sw128(smem_u32(sm + L::kStageOff), 16, 1024);   // Q / dO tiles
@@ -357,16 +363,18 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
       auto stage_off16 = [&](uint32_t x) -> uint32_t {
         return static_cast<uint32_t>(((x % NS) * L::kStageBytes) >> 4);
       };
-      auto issue_s = [&](uint32_t x) -> bool {  // S^T = K Q^T
+      auto issue_s = [&](uint32_t x) -> bool {  // S^T = K Q^T into buffer x & 1
         if (!mbar_wait(&bars->qd_full[x % NS], (x / NS) & 1)) return false;
-        if (x > 0 && !mbar_wait(&bars->s_free, (x - 1) & 1)) return false;
+        // buffer x & 1 still holds P^T(x - 2) until dV(x - 2) has read it
+        if (x >= 2 && !mbar_wait(&bars->p_free[x & 1], ((x >> 1) - 1) & 1)) return false;
         tc_fence_after();
         const uint64_t qd = st_km + stage_off16(x);
+        const uint32_t dt = tmem + L::kColS + 64 * (x & 1);
 #pragma unroll
         for (int ks = 0; ks < DQK / 16; ++ks)
-          mma_ss(tmem + L::kColS, k_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+          mma_ss(dt, k_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                  qd + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id_s, ks > 0);
-        mma_commit(&bars->s_full);
+        mma_commit(&bars->s_full[x & 1]);
         ATTN_TL(10, x);
         return true;
       };
@@ -399,17 +407,18 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
             for (uint32_t u = 0; u < nsteps; ++u) {
               const uint32_t cur = st + u;
               if (u + 1 < nsteps && !(ok = issue_s(cur + 1))) break;
-              if (!(ok = mbar_wait(&bars->p_ready, cur & 1))) break;
+              if (!(ok = mbar_wait(&bars->p_ready[cur & 1], (cur >> 1) & 1))) break;
               ATTN_TL(12, cur);
               if (u == 0 && gc > 0 && !(ok = mbar_wait(&bars->acc_empty, (gc - 1) & 1))) break;
               tc_fence_after();
               const uint64_t q_mn = st_mn + stage_off16(cur);
               const uint64_t o_mn = q_mn + (L::kQBytes >> 4);
+              const uint32_t p_tm = tmem + L::kColS + 64 * (cur & 1);  // P^T, packed bf16
 #pragma unroll
-              for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dV += P^T dO
-                mma_ss(tmem + L::kColDV, p_km + ((ks * 32) >> 4), o_mn + ((ks * 2048) >> 4), id_dv,
+              for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dV += P^T dO  (A from tensor memory)
+                mma_ts(tmem + L::kColDV, p_tm + ks * 8, o_mn + ((ks * 2048) >> 4), id_dv,
                        (u > 0 || ks > 0));
-              mma_commit(&bars->p_free);
+              mma_commit(&bars->p_free[cur & 1]);
               if (u + 1 < nsteps && !(ok = issue_dp(cur + 1))) break;
               if (!(ok = mbar_wait(&bars->ds_ready, cur & 1))) break;
               ATTN_TL(14, cur);
@@ -419,14 +428,13 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
                 mma_ss(tmem + L::kColDK, ds_km + ((ks * 32) >> 4), q_mn + ((ks * 2048) >> 4), id_dk,
                        (u > 0 || ks > 0));
               if constexpr (ATOMIC) {  // dQ^T = K^T dS^T
-                const uint32_t buf = cur & 1;
-                if (cur >= 2 && !(ok = mbar_wait(&bars->dq_free[buf], ((cur >> 1) - 1) & 1))) break;
+                if (cur >= 1 && !(ok = mbar_wait(&bars->dq_free, (cur - 1) & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kTile / 16; ++ks)
-                  mma_ss(tmem + L::kColDQ + buf * 64, k_mn + ((ks * 2048) >> 4),
-                         ds_mn + ((ks * 2048) >> 4), id_dq, ks > 0);
-                mma_commit(&bars->dq_full[buf]);
+                  mma_ss(tmem + L::kColDQ, k_mn + ((ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4),
+                         id_dq, ks > 0);
+                mma_commit(&bars->dq_full);
               }
               mma_commit(&bars->ds_free);
               mma_commit(&bars->qd_empty[cur % NS]);
@@ -451,7 +459,7 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
     // ------------------------------------------------------------ P / dS warps
     const int j = tid - 128;  // KV row of the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t p_addr = smem_u32(sm + L::kPOff), ds_addr = smem_u32(sm + L::kDSOff);
+    const uint32_t ds_addr = smem_u32(sm + L::kDSOff);
     const int nqc = (a.Sq + kChunk - 1) / kChunk;
     uint32_t st = 0;
     bool ok = true;
@@ -492,19 +500,18 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               if (j == 0) ATTN_TL(20, cur);
               if (!(ok = mbar_wait_warp(&bars->qd_full[stage], (cur / NS) & 1))) break;
               if (j == 0) ATTN_TL(26, cur);
-              if (!(ok = mbar_wait_warp(&bars->s_full, cur & 1))) break;
+              if (!(ok = mbar_wait_warp(&bars->s_full[cur & 1], (cur >> 1) & 1))) break;
               if (j == 0) ATTN_TL(21, cur);
               tc_fence_after();
+              const uint32_t s_tm = tmem + lane_base + L::kColS + 64 * (cur & 1);
 #pragma unroll
               for (int q = 0; q < kBwdQ / 32; ++q) {
                 uint32_t u[32];
-                tmem_ld32x32b_x32(tmem + lane_base + L::kColS + q * 32, u);
+                tmem_ld32x32b_x32(s_tm + q * 32, u);
                 tmem_ld_wait();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
               }
-              tc_fence_before();
-              mbar_arrive(&bars->s_free);
               if (j == 0) ATTN_TL(40, cur);
               const StageVec& V = vec[stage];
               if (HAS_BIAS && row_ok) {
@@ -552,18 +559,17 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
                 }
               }
               if (j == 0) ATTN_TL(41, cur);
-              // P^T row j -> shared memory (K-major, 128-byte swizzle)
-              if (cur > 0 && !(ok = mbar_wait_warp(&bars->p_free, (cur - 1) & 1))) break;
-              if (j == 0) ATTN_TL(42, cur);
+              // P^T row j -> tensor memory over its own S^T, packed bf16 pairs
+              {
+                uint32_t pk[32];
 #pragma unroll
-              for (int u8 = 0; u8 < 8; ++u8) {
-                const float* p8 = x + u8 * 8;
-                st_shared_v4(p_addr + j * 128 + ((u8 ^ (j & 7)) << 4), pack_bf16x2(p8[0], p8[1]),
-                             pack_bf16x2(p8[2], p8[3]), pack_bf16x2(p8[4], p8[5]),
-                             pack_bf16x2(p8[6], p8[7]));
+                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                tmem_st32x32b_x32(s_tm, pk);
+                tmem_st_wait();
               }
-              fence_proxy_async_smem();
-              mbar_arrive(&bars->p_ready);
+              tc_fence_before();
+              mbar_arrive(&bars->p_ready[cur & 1]);
+              if (j == 0) ATTN_TL(42, cur);
               if (j == 0) ATTN_TL(22, cur);
               // dS^T = P^T (dP^T - D)
               if (!(ok = mbar_wait_warp(&bars->dp_full, cur & 1))) break;
@@ -652,31 +658,46 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
             continue;
           }
           if constexpr (ATOMIC) {
+            // dQ^T tile -> fp32 staging [d box of 32][64 q][32 d] -> one bulk
+            // tensor reduce-add per box into the fp32 dQ accumulator
+            float* stg = reinterpret_cast<float*>(sm + L::kDQOff);
             for (int hh = 0; hh < G && ok; ++hh) {
               const int h = g * G + hh;
               for (int s = 0; s < nq; ++s, ++st) {
-                const uint32_t buf = st & 1;
-                if (!(ok = mbar_wait_warp(&bars->dq_full[buf], (st >> 1) & 1))) break;
+                if (!(ok = mbar_wait_warp(&bars->dq_full, st & 1))) break;
                 if (j == 0) ATTN_TL(30, st);
                 tc_fence_after();
                 uint32_t u0[32], u1[32];
-                tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + buf * 64, u0);
-                tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + buf * 64 + 32, u1);
+                tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ, u0);
+                tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + 32, u1);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&bars->dq_free[buf]);
+                mbar_arrive(&bars->dq_free);
+                // the previous tile's reduce must have finished reading the staging buffer
+                if (st > 0 && !(ok = mbar_wait_warp(&bars->stg_free, (st - 1) & 1))) break;
                 if (j < DQK) {
-                  const int q0 = q_lo + s * kBwdQ;
-                  float* base = a.dq_acc + (((int64_t)b * a.Sq + q0) * a.Hq + h) * DQK + j;
-                  const int64_t rs = (int64_t)a.Hq * DQK;
-                  const int nv = min(kBwdQ, a.Sq - q0);
+                  float* col = stg + (j >> 5) * (kBwdQ * 32) + (j & 31);
+                  const float sc = a.scale;
 #pragma unroll
-                  for (int c = 0; c < 32; ++c)
-                    if (c < nv) red_add_f32(base + c * rs, __uint_as_float(u0[c]) * a.scale);
+                  for (int c = 0; c < 32; ++c) col[c * 32] = __uint_as_float(u0[c]) * sc;
 #pragma unroll
-                  for (int c = 0; c < 32; ++c)
-                    if (32 + c < nv) red_add_f32(base + (32 + c) * rs, __uint_as_float(u1[c]) * a.scale);
+                  for (int c = 0; c < 32; ++c) col[(32 + c) * 32] = __uint_as_float(u1[c]) * sc;
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->stg_full);
+                if (j == 0) {
+                  if ((ok = mbar_wait(&bars->stg_full, st & 1))) {
+                    const int q0 = q_lo + s * kBwdQ;
+#pragma unroll
+                    for (int bx = 0; bx < DQK / 32; ++bx)
+                      tma_reduce_add_3d(&a.tm_dqacc, stg + bx * (kBwdQ * 32), bx * 32, h,
+                                        b * a.Sq + q0);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                    mbar_arrive(&bars->stg_free);
+                  }
+                }
+                ok = __all_sync(0xffffffffu, ok);
                 if (j == 0) ATTN_TL(31, st);
               }
             }
@@ -724,6 +745,9 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
           ++gc;
         }
       }
+    }
+    if constexpr (ATOMIC) {
+      if (j == 0) bulk_wait_all();  // every reduce-add issued by this thread has landed
     }
     if (!ok) {
       if (lane == 0) report_timeout(a, 0x150 + (warp & 3));
@@ -1114,7 +1138,7 @@ cudaError_t set_smem(K kern, int bytes) {
 
 template <int DQK, int DV, bool AT, bool HB, int DB>
 cudaError_t dkdv_go(const KernelArgs& a, int nsm, cudaStream_t st) {
-  using L = DkdvLayout<DQK, DV>;
+  using L = DkdvLayout<DQK, DV, AT>;
   auto kern = dkdv_kernel<DQK, DV, AT, HB, DB>;
   cudaError_t e = set_smem(kern, L::kAlloc);
   if (e != cudaSuccess) return e;

@@ -97,6 +97,23 @@ SM103_DEV void tma_load_3d(void* dst, const void* map, uint64_t* bar, int x, int
       : "memory");
 }
 
+// Bulk tensor reduce-add (fp32) from shared memory into global memory, tracked
+// by the issuing thread's bulk-async group.
+SM103_DEV void tma_reduce_add_3d(const void* map, const void* src, int x, int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+SM103_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group has finished reading its shared-memory source.
+SM103_DEV void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed bulk group has completed (global writes done).
+SM103_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 SM103_DEV void prefetch_tensormap(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
