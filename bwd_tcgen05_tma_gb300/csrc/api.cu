@@ -10,6 +10,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -25,7 +26,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 struct Plan {
   size_t hdr, q_id, q_pos, seg_lo, seg_hi, kv_id, kv_pos, kv_seg_lo, kv_seg_hi;
-  size_t q_chunk, kv_chunk, q_range, kv_range;
+  size_t q_chunk, kv_chunk, q_range, kv_range, meta_scan;
   size_t fwd_total;
   size_t lse2, dvec, dq_acc, dbias_acc;
   size_t bwd_total;
@@ -58,6 +59,7 @@ Plan make_plan(const attn_params_t* p) {
   pl.kv_chunk = o; o = up(o + B * nkc * sizeof(ChunkInfo));
   pl.q_range = o; o = up(o + B * nqt * sizeof(int2));
   pl.kv_range = o; o = up(o + B * nkt * sizeof(int2));
+  pl.meta_scan = o; o = up(o + 2 * B * ((std::max(Sq, Skv) + 1023) / 1024) * sizeof(int2));
   pl.fwd_total = o;
   pl.lse2 = o; o = up(o + B * p->Hq * Sq * 4);
   pl.dvec = o; o = up(o + B * p->Hq * Sq * 4);
@@ -242,6 +244,7 @@ void fill_common(KernelArgs& a, const attn_params_t* p, char* ws, const Plan& pl
   a.kv_seg_hi = reinterpret_cast<int32_t*>(ws + pl.kv_seg_hi);
   a.q_chunk = reinterpret_cast<ChunkInfo*>(ws + pl.q_chunk);
   a.kv_chunk = reinterpret_cast<ChunkInfo*>(ws + pl.kv_chunk);
+  a.meta_scan = reinterpret_cast<int2*>(ws + pl.meta_scan);
   a.q_tile_range = reinterpret_cast<int2*>(ws + pl.q_range);
   a.kv_tile_range = reinterpret_cast<int2*>(ws + pl.kv_range);
   a.bias = static_cast<const bf16*>(p->bias);

@@ -115,6 +115,7 @@ struct KernelArgs {
   const int32_t* kv_seg_hi;
   const ChunkInfo* q_chunk;
   const ChunkInfo* kv_chunk;
+  const int2* meta_scan;      // [2][B][chunks of 1024] first/last run boundary per chunk
   const int2* q_tile_range;   // [B*n_qt]  KV token range of each 128-row query tile
   const int2* kv_tile_range;  // [B*n_kt]  query token range of each 128-row KV tile
   WsHeader* hdr;
