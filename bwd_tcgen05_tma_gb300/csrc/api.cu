@@ -428,26 +428,31 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   trace(ATTN_TRACE_BWD_PRE, false, st);
   if (launch_bwd_pre(a, atomic ? 1 : 0, st) != cudaSuccess) return ATTN_ERR_CUDA;
   trace(ATTN_TRACE_BWD_PRE, true, st);
-  // dK/dV pass: query tiles of 64 rows
-  if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kBwdQ) ||
+  // dK/dV pass: 128-row query tiles (deterministic dQ mode, head dims <= 128),
+  // otherwise 64-row query tiles
+  const bool tile128 = !atomic && p->d_qk <= 128 && p->d_v <= 128;
+  const int qrows = tile128 ? kTile : kBwdQ;
+  if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, qrows) ||
       !make_map(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
       !make_map(&a.tm_v, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
       !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
-                kBwdQ))
+                qrows))
     return ATTN_ERR_CUDA;
   if (atomic && !make_map_f32(&a.tm_dqacc, a.dq_acc, p->d_qk, p->Hq, (int64_t)p->B * p->Sq))
     return ATTN_ERR_CUDA;
   const int nsm = sm_count();
   trace(ATTN_TRACE_DKDV, false, st);
-  if (launch_bwd_dkdv(a, atomic, nsm, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  const cudaError_t ek = tile128 ? launch_bwd_dkdv128(a, nsm, st) : launch_bwd_dkdv(a, atomic, nsm, st);
+  if (ek != cudaSuccess) return ATTN_ERR_CUDA;
   trace(ATTN_TRACE_DKDV, true, st);
   trace(ATTN_TRACE_DQ, false, st);
   if (atomic) {
     if (launch_dq_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
   } else {
-    if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
-        !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
-                  kTile))
+    if (!tile128 &&
+        (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
+         !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
+                   kTile)))
       return ATTN_ERR_CUDA;
     if (launch_bwd_dq(a, nsm, st) != cudaSuccess) return ATTN_ERR_CUDA;
   }

@@ -239,6 +239,43 @@ __device__ __forceinline__ void report_timeout(const KernelArgs& a, int where) {
   atomicCAS(&a.hdr->where, 0, where);
 }
 
+// ---------------------------------------------------------------- dK/dV work items
+// Work item -> (KV tile, batch range, KV-head range).
+struct DkdvItem {
+  int t, b0, b1, g0, g1;
+};
+
+__device__ __forceinline__ int dkdv_n_items(const KernelArgs& a) {
+  const int nb = a.dkdv_batch_loop ? 1 : a.B;
+  const int ng = a.dkdv_head_loop ? 1 : a.Hkv;
+  return a.n_kt * nb * ng;
+}
+
+__device__ __forceinline__ DkdvItem dkdv_item(const KernelArgs& a, int idx) {
+  const int nb = a.dkdv_batch_loop ? 1 : a.B;
+  const int ng = a.dkdv_head_loop ? 1 : a.Hkv;
+  DkdvItem it;
+  // (batch row, KV head)-major: CTAs running at the same time work on KV tiles
+  // of the same head and re-read the same Q / dO tiles from L2
+  const int combo = idx / a.n_kt;
+  it.t = idx - combo * a.n_kt;
+  const int bi = combo / ng, gi = combo - (combo / ng) * ng;
+  it.b0 = a.dkdv_batch_loop ? 0 : bi;
+  it.b1 = a.dkdv_batch_loop ? a.B : bi + 1;
+  it.g0 = a.dkdv_head_loop ? 0 : gi;
+  it.g1 = a.dkdv_head_loop ? a.Hkv : gi + 1;
+  return it;
+}
+
+// Query range of KV tile t of row b; returns the number of BQ-row query tiles.
+template <int BQ = kBwdQ>
+__device__ __forceinline__ int dkdv_q_tiles(const KernelArgs& a, int b, int t, int& q_lo) {
+  const int2 r = a.kv_tile_range[b * a.n_kt + t];
+  q_lo = r.x;
+  return (r.y > r.x) ? (r.y - r.x + BQ - 1) / BQ : 0;
+}
+
+
 // Kernel launchers (defined in the kernel translation units).
 cudaError_t launch_meta(const KernelArgs& a, int fmt, const int32_t* q_ids, const int32_t* q_pos,
                         const int32_t* kv_ids, const int32_t* kv_pos, const int32_t* cu_q,
@@ -248,6 +285,8 @@ cudaError_t launch_fwd(const KernelArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic_dq, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_dq(const KernelArgs& a, int num_sms, cudaStream_t st);
+// dK/dV pass with 128-row query tiles (deterministic dQ mode, d_qk and d_v <= 128).
+cudaError_t launch_bwd_dkdv128(const KernelArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_dq_convert(const KernelArgs& a, cudaStream_t st);
 cudaError_t launch_dbias_convert(const KernelArgs& a, cudaStream_t st);
 

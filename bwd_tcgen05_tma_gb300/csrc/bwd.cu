@@ -150,42 +150,8 @@ struct StageVec {  // per query tile: log2-LSE, D, and (general path) ids / posi
   int32_t qpos[kBwdQ];
 };
 
-// Work item -> (KV tile, batch range, KV-head range).
-struct DkdvItem {
-  int t, b0, b1, g0, g1;
-};
-
-__device__ __forceinline__ int dkdv_n_items(const KernelArgs& a) {
-  const int nb = a.dkdv_batch_loop ? 1 : a.B;
-  const int ng = a.dkdv_head_loop ? 1 : a.Hkv;
-  return a.n_kt * nb * ng;
-}
-
-__device__ __forceinline__ DkdvItem dkdv_item(const KernelArgs& a, int idx) {
-  const int nb = a.dkdv_batch_loop ? 1 : a.B;
-  const int ng = a.dkdv_head_loop ? 1 : a.Hkv;
-  DkdvItem it;
-  // (batch row, KV head)-major: CTAs running at the same time work on KV tiles
-  // of the same head and re-read the same Q / dO tiles from L2
-  const int combo = idx / a.n_kt;
-  it.t = idx - combo * a.n_kt;
-  const int bi = combo / ng, gi = combo - (combo / ng) * ng;
-  it.b0 = a.dkdv_batch_loop ? 0 : bi;
-  it.b1 = a.dkdv_batch_loop ? a.B : bi + 1;
-  it.g0 = a.dkdv_head_loop ? 0 : gi;
-  it.g1 = a.dkdv_head_loop ? a.Hkv : gi + 1;
-  return it;
-}
-
-// Query range of KV tile t of row b; returns the number of 64-row query tiles.
-__device__ __forceinline__ int dkdv_q_tiles(const KernelArgs& a, int b, int t, int& q_lo) {
-  const int2 r = a.kv_tile_range[b * a.n_kt + t];
-  q_lo = r.x;
-  return (r.y > r.x) ? (r.y - r.x + kBwdQ - 1) / kBwdQ : 0;
-}
-
 template <int DQK, int DV, bool ATOMIC, bool HAS_BIAS, int DBIAS>
-__global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ KernelArgs a) {
+__global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ KernelArgs a) {
   using L = DkdvLayout<DQK, DV, ATOMIC>;
   constexpr int NS = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -206,12 +172,12 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
     mbar_init(&bars->kv_empty, 1);
     for (int b2 = 0; b2 < 2; ++b2) {
       mbar_init(&bars->s_full[b2], 1);
-      mbar_init(&bars->p_ready[b2], 128);
+      mbar_init(&bars->p_ready[b2], 256);
       mbar_init(&bars->p_free[b2], 1);
     }
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->dp_free, 128);
-    mbar_init(&bars->ds_ready, 128);
+    mbar_init(&bars->dp_free, 256);
+    mbar_init(&bars->ds_ready, 256);
     mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 128);
@@ -222,9 +188,9 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
     mbar_init(&bars->stg_free, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->qd_full[s], 1 + 64);
-      mbar_init(&bars->qd_empty[s], 1 + 128);
+      mbar_init(&bars->qd_empty[s], 1 + 256);
     }
-    ring_init(ring, 1 + 64 + 128 + 128);  // MMA, vector loader, P/dS warps, epilogue
+    ring_init(ring, 1 + 64 + 256 + 128);  // MMA, vector loader, P/dS warps, epilogue
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -413,11 +379,12 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               tc_fence_after();
               const uint64_t q_mn = st_mn + stage_off16(cur);
               const uint64_t o_mn = q_mn + (L::kQBytes >> 4);
-              const uint32_t p_tm = tmem + L::kColS + 64 * (cur & 1);  // P^T, packed bf16
+              // P^T, packed bf16: query columns [0,32) at S^T columns [0,16), [32,64) at [32,48)
+              const uint32_t p_tm = tmem + L::kColS + 64 * (cur & 1);
 #pragma unroll
               for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dV += P^T dO  (A from tensor memory)
-                mma_ts(tmem + L::kColDV, p_tm + ks * 8, o_mn + ((ks * 2048) >> 4), id_dv,
-                       (u > 0 || ks > 0));
+                mma_ts(tmem + L::kColDV, p_tm + ks * 8 + (ks >> 1) * 16, o_mn + ((ks * 2048) >> 4),
+                       id_dv, (u > 0 || ks > 0));
               mma_commit(&bars->p_free[cur & 1]);
               if (u + 1 < nsteps && !(ok = issue_dp(cur + 1))) break;
               if (!(ok = mbar_wait(&bars->ds_ready, cur & 1))) break;
@@ -455,9 +422,13 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, 200000000ull);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P / dS warps
-    const int j = tid - 128;  // KV row of the tile == TMEM lane
+    // two warpgroups: each thread owns KV row j (TMEM lane j) and one half of
+    // the 64 query columns of every step
+    const int j = (tid - 128) & 127;
+    const int half = (tid - 128) >> 7;
+    const int c0h = half * 32;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t ds_addr = smem_u32(sm + L::kDSOff);
     const int nqc = (a.Sq + kChunk - 1) / kChunk;
@@ -496,124 +467,122 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
               const uint32_t cur = st;
               const int stage = cur % NS;
               const int q0 = q_lo + s * kBwdQ;
-              float x[kBwdQ];
-              if (j == 0) ATTN_TL(20, cur);
+              float x[32];
+              if (j == 0 && half == 0) ATTN_TL(20, cur);
               if (!(ok = mbar_wait_warp(&bars->qd_full[stage], (cur / NS) & 1))) break;
-              if (j == 0) ATTN_TL(26, cur);
+              if (j == 0 && half == 0) ATTN_TL(26, cur);
               if (!(ok = mbar_wait_warp(&bars->s_full[cur & 1], (cur >> 1) & 1))) break;
-              if (j == 0) ATTN_TL(21, cur);
+              if (j == 0 && half == 0) ATTN_TL(21, cur);
               tc_fence_after();
               const uint32_t s_tm = tmem + lane_base + L::kColS + 64 * (cur & 1);
-#pragma unroll
-              for (int q = 0; q < kBwdQ / 32; ++q) {
+              {
                 uint32_t u[32];
-                tmem_ld32x32b_x32(s_tm + q * 32, u);
+                tmem_ld32x32b_x32(s_tm + c0h, u);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
+                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(u[e]) * a.scale_log2;
               }
-              if (j == 0) ATTN_TL(40, cur);
+              if (j == 0 && half == 0) ATTN_TL(40, cur);
               const StageVec& V = vec[stage];
               if (HAS_BIAS && row_ok) {
-                const bf16* bp = a.bias + (bias_base + q0) * a.Skv + kj;
+                const bf16* bp = a.bias + (bias_base + q0 + c0h) * a.Skv + kj;
 #pragma unroll
-                for (int c = 0; c < kBwdQ; ++c)
-                  if (q0 + c < a.Sq) x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
+                for (int c = 0; c < 32; ++c)
+                  if (q0 + c0h + c < a.Sq) x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
               }
-              // validity of the 64 query columns for this key row, as a bitmask
-              uint64_t vbits;
+              // validity of this thread's 32 query columns, as a bitmask
+              uint32_t vbits;
               if (!general) {
-                vbits = row_ok ? range_bits64(qlo - q0, qhi - q0) : 0ull;
+                vbits = row_ok ? (uint32_t)(range_bits64(qlo - q0 - c0h, qhi - q0 - c0h)) : 0u;
               } else {
-                vbits = 0ull;
+                vbits = 0u;
                 bool full = false;
                 if (row_ok && my_id != 0 && q0 + kBwdQ <= a.Sq) {
                   const ChunkInfo ci = a.q_chunk[b * nqc + q0 / kChunk];
                   full = ci.uniform && ci.min_id == my_id && (!a.causal || ci.min_pos >= my_pos);
                 }
                 if (full) {
-                  vbits = ~0ull;
+                  vbits = ~0u;
                 } else if (row_ok && my_id != 0) {
 #pragma unroll
-                  for (int c = 0; c < kBwdQ; c += 4) {
-                    const int4 id4 = *reinterpret_cast<const int4*>(&V.qid[c]);
-                    const int4 ps4 = *reinterpret_cast<const int4*>(&V.qpos[c]);
+                  for (int c = 0; c < 32; c += 4) {
+                    const int4 id4 = *reinterpret_cast<const int4*>(&V.qid[c0h + c]);
+                    const int4 ps4 = *reinterpret_cast<const int4*>(&V.qpos[c0h + c]);
                     const int ids[4] = {id4.x, id4.y, id4.z, id4.w};
                     const int pss[4] = {ps4.x, ps4.y, ps4.z, ps4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                       const bool v = (ids[e] == my_id) & (!a.causal | (my_pos <= pss[e]));
-                      vbits |= static_cast<uint64_t>(v) << (c + e);
+                      vbits |= static_cast<uint32_t>(v) << (c + e);
                     }
                   }
                 }
               }
 #pragma unroll
-              for (int c = 0; c < kBwdQ; c += 4) {
-                const float4 l4 = *reinterpret_cast<const float4*>(&V.lse2[c]);
+              for (int c = 0; c < 32; c += 4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(&V.lse2[c0h + c]);
                 const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  const float p = ex2_approx(x[c + e] - ls[e]);
-                  x[c + e] = ((vbits >> (c + e)) & 1ull) ? p : 0.f;
+                  const float pv = ex2_approx(x[c + e] - ls[e]);
+                  x[c + e] = ((vbits >> (c + e)) & 1u) ? pv : 0.f;
                 }
               }
-              if (j == 0) ATTN_TL(41, cur);
-              // P^T row j -> tensor memory over its own S^T, packed bf16 pairs
+              if (j == 0 && half == 0) ATTN_TL(41, cur);
+              // P^T -> tensor memory, packed bf16 pairs, inside this half's own S^T
+              // columns [c0h, c0h + 32) (the other half may still be reading its S^T)
               {
-                uint32_t pk[32];
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-                tmem_st32x32b_x32(s_tm, pk);
+                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                tmem_st32x32b_x16(s_tm + c0h, pk);
                 tmem_st_wait();
               }
               tc_fence_before();
               mbar_arrive(&bars->p_ready[cur & 1]);
-              if (j == 0) ATTN_TL(42, cur);
-              if (j == 0) ATTN_TL(22, cur);
+              if (j == 0 && half == 0) ATTN_TL(22, cur);
               // dS^T = P^T (dP^T - D)
               if (!(ok = mbar_wait_warp(&bars->dp_full, cur & 1))) break;
-              if (j == 0) ATTN_TL(23, cur);
+              if (j == 0 && half == 0) ATTN_TL(23, cur);
               tc_fence_after();
-#pragma unroll
-              for (int q = 0; q < kBwdQ / 32; ++q) {
+              {
                 uint32_t u[32];
-                tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + q * 32, u);
+                tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + c0h, u);
                 tmem_ld_wait();
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
-                  const int c = q * 32 + e;
-                  const float4 d4 = *reinterpret_cast<const float4*>(&V.D[c]);
-                  x[c] = x[c] * (__uint_as_float(u[e]) - d4.x);
-                  x[c + 1] = x[c + 1] * (__uint_as_float(u[e + 1]) - d4.y);
-                  x[c + 2] = x[c + 2] * (__uint_as_float(u[e + 2]) - d4.z);
-                  x[c + 3] = x[c + 3] * (__uint_as_float(u[e + 3]) - d4.w);
+                  const float4 d4 = *reinterpret_cast<const float4*>(&V.D[c0h + e]);
+                  x[e] = x[e] * (__uint_as_float(u[e]) - d4.x);
+                  x[e + 1] = x[e + 1] * (__uint_as_float(u[e + 1]) - d4.y);
+                  x[e + 2] = x[e + 2] * (__uint_as_float(u[e + 2]) - d4.z);
+                  x[e + 3] = x[e + 3] * (__uint_as_float(u[e + 3]) - d4.w);
                 }
               }
               tc_fence_before();
               mbar_arrive(&bars->dp_free);
               if (cur > 0 && !(ok = mbar_wait_warp(&bars->ds_free, (cur - 1) & 1))) break;
 #pragma unroll
-              for (int u8 = 0; u8 < 8; ++u8) {
-                const float* p8 = x + u8 * 8;
-                st_shared_v4(ds_addr + j * 128 + ((u8 ^ (j & 7)) << 4), pack_bf16x2(p8[0], p8[1]),
+              for (int u4 = 0; u4 < 4; ++u4) {  // 16-byte units half*4 .. half*4+3 of row j
+                const float* p8 = x + u4 * 8;
+                const int un = half * 4 + u4;
+                st_shared_v4(ds_addr + j * 128 + ((un ^ (j & 7)) << 4), pack_bf16x2(p8[0], p8[1]),
                              pack_bf16x2(p8[2], p8[3]), pack_bf16x2(p8[4], p8[5]),
                              pack_bf16x2(p8[6], p8[7]));
               }
               fence_proxy_async_smem();
               mbar_arrive(&bars->ds_ready);
-              if (j == 0) ATTN_TL(24, cur);
+              if (j == 0 && half == 0) ATTN_TL(24, cur);
               if (DBIAS != 0 && row_ok) {
                 if (DBIAS == 1) {
-                  bf16* dp = a.dbias + (bias_base + q0) * a.Skv + kj;
+                  bf16* dp = a.dbias + (bias_base + q0 + c0h) * a.Skv + kj;
 #pragma unroll
-                  for (int c = 0; c < kBwdQ; ++c)
-                    if (q0 + c < a.Sq) dp[(int64_t)c * a.Skv] = __float2bfloat16_rn(x[c]);
+                  for (int c = 0; c < 32; ++c)
+                    if (q0 + c0h + c < a.Sq) dp[(int64_t)c * a.Skv] = __float2bfloat16_rn(x[c]);
                 } else {
-                  float* dp = a.dbias_acc + (bias_base + q0) * a.Skv + kj;
+                  float* dp = a.dbias_acc + (bias_base + q0 + c0h) * a.Skv + kj;
 #pragma unroll
-                  for (int c = 0; c < kBwdQ; ++c)
-                    if (q0 + c < a.Sq) dp[(int64_t)c * a.Skv] += x[c];
+                  for (int c = 0; c < 32; ++c)
+                    if (q0 + c0h + c < a.Sq) dp[(int64_t)c * a.Skv] += x[c];
                 }
               }
               mbar_arrive(&bars->qd_empty[stage]);
@@ -626,9 +595,9 @@ __global__ void __launch_bounds__(384, 1) dkdv_kernel(const __grid_constant__ Ke
       if (lane == 0) report_timeout(a, 0x140 + (warp & 3));
       *abort_flag = 1;
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-    const int j = tid - 256;  // TMEM lane: KV row for dK/dV, head-dim index for dQ^T
+    const int j = tid - 384;  // TMEM lane: KV row for dK/dV, head-dim index for dQ^T
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t st = 0, gc = 0;
     bool ok = true;
@@ -1145,7 +1114,7 @@ cudaError_t dkdv_go(const KernelArgs& a, int nsm, cudaStream_t st) {
   const int nb = a.dkdv_batch_loop ? 1 : a.B, ng = a.dkdv_head_loop ? 1 : a.Hkv;
   const int items = a.n_kt * nb * ng;
   const int grid = items < nsm ? items : nsm;
-  kern<<<grid, 384, L::kAlloc, st>>>(a);
+  kern<<<grid, 512, L::kAlloc, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,619 @@
+// dK / dV pass with 128-row query tiles, for the deterministic-dQ mode
+// (d_qk, d_v <= 128).  dQ is produced by the separate query-tile pass.
+//
+// Per 128-row KV tile of one KV head (a work item, as in the 64-row pass) the
+// CTA loops sequentially over the query heads of the group and every
+// 128-row query tile that can see the KV tile (maxdiffusion PR #485, Summary:
+// dK/dV held across Q blocks and GQA heads, accumulation order fixed inside
+// the CTA).  Per query tile c:
+//
+//   S^T(c)  = K Q(c)^T                     smem x smem -> TMEM   (M=128, N=128)
+//   P^T(c)  = exp2(S^T - LSE)              softmax warps, written back to TMEM
+//                                          as packed bf16 over S^T
+//   dP^T(c) = V dO(c)^T                    smem x smem -> TMEM
+//   dS^T(c) = P^T (dP^T - D)               written back over dP^T, packed bf16
+//   dV     += P^T(c) dO(c)                 A from TMEM
+//   dK     += dS^T(c) Q(c)                 A from TMEM, issued one step later
+//
+// Every MMA has N = 128, half of the operand traffic comes from tensor memory,
+// and the tensor core issues S(c), dK(c-1), dP(c) while the softmax warps
+// exponentiate P(c).  MMAs that overwrite a TMEM region another MMA reads
+// (S(c) over P(c-1), dP(c) over dS(c-1)) are issued after the reader by the
+// same thread, so the in-order MMA pipeline orders them.
+#include <cmath>
+
+#include "attn_internal.cuh"
+
+namespace attn {
+namespace {
+using namespace sm103;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kQ = 128;  // query tile
+
+template <int DQK, int DV>
+struct D128Layout {
+  static constexpr int kKBytes = kTile * DQK * 2;
+  static constexpr int kVBytes = kTile * DV * 2;
+  static constexpr int kQBytes = kQ * DQK * 2;
+  static constexpr int kOBytes = kQ * DV * 2;
+  static constexpr int kStageBytes = kQBytes + kOBytes;
+  static constexpr int kStages = 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKBytes;
+  static constexpr int kStageOff = kKBytes + kVBytes;
+  static constexpr int kVecOff = kStageOff + kStages * kStageBytes;  // 2 KB per stage
+  static constexpr int kBarOff = kVecOff + kStages * 2048;
+  static constexpr int kBytes = kBarOff + 512;
+  static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
+  static constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
+};
+
+struct D128Bars {
+  uint64_t kv_full, kv_empty, s_full, dp_full, p_ready, ds_ready, acc_full, acc_empty, drain;
+  uint64_t qd_full[2], qd_empty[2];
+};
+
+struct Vec128 {  // per query tile: log2-LSE, D, and (general path) ids / positions
+  float lse2[kQ];
+  float D[kQ];
+  int32_t qid[kQ];
+  int32_t qpos[kQ];
+};
+
+template <int DQK, int DV, bool HAS_BIAS, int DBIAS>
+__global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__ KernelArgs a) {
+  using L = D128Layout<DQK, DV>;
+  constexpr int NS = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  D128Bars* bars = reinterpret_cast<D128Bars*>(sm + L::kBarOff);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(D128Bars));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  Vec128* vec = reinterpret_cast<Vec128*>(sm + L::kVecOff);
+  ItemRing* ring = reinterpret_cast<ItemRing*>(sm + L::kBarOff + 256);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_items = dkdv_n_items(a);
+  const int G = a.Hq / a.Hkv;
+
+  if (tid == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, 256);
+    mbar_init(&bars->ds_ready, 256);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_empty, 128);
+    mbar_init(&bars->drain, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars->qd_full[s], 1 + 64);
+      mbar_init(&bars->qd_empty[s], 1 + 256);
+    }
+    ring_init(ring, 1 + 64 + 256 + 128);  // MMA, vector loader, softmax, epilogue
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const bool general = path_general(a);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&a.tm_q);
+      prefetch_tensormap(&a.tm_k);
+      prefetch_tensormap(&a.tm_v);
+      prefetch_tensormap(&a.tm_do);
+      uint32_t st = 0, kvc = 0;
+      bool ok = true;
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[1], n_items, idx)) ||
+            idx < 0)
+          break;
+        const DkdvItem w = dkdv_item(a, idx);
+        for (int b = w.b0; b < w.b1 && ok; ++b) {
+          for (int g = w.g0; g < w.g1 && ok; ++g) {
+            int q_lo;
+            const int nq = dkdv_q_tiles<kQ>(a, b, w.t, q_lo);
+            if (nq == 0) continue;
+            if (kvc > 0 && !(ok = mbar_wait(&bars->kv_empty, (kvc - 1) & 1))) break;
+            const int krow = b * a.Skv + w.t * kTile;
+            mbar_arrive_expect_tx(&bars->kv_full, L::kKBytes + L::kVBytes);
+#pragma unroll
+            for (int c = 0; c < DQK / 64; ++c)
+              tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
+#pragma unroll
+            for (int c = 0; c < DV / 64; ++c)
+              tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
+            ++kvc;
+            for (int hh = 0; hh < G && ok; ++hh) {
+              const int h = g * G + hh;
+              for (int s = 0; s < nq; ++s, ++st) {
+                const int stage = st % NS;
+                if (st >= (uint32_t)NS &&
+                    !(ok = mbar_wait(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
+                  break;
+                const int qrow = b * a.Sq + q_lo + s * kQ;
+                uint8_t* qs = sm + L::kStageOff + stage * L::kStageBytes;
+                mbar_arrive_expect_tx(&bars->qd_full[stage], L::kStageBytes);
+#pragma unroll
+                for (int c = 0; c < DQK / 64; ++c)
+                  tma_load_3d(qs + c * 16384, &a.tm_q, &bars->qd_full[stage], c * 64, h, qrow);
+#pragma unroll
+                for (int c = 0; c < DV / 64; ++c)
+                  tma_load_3d(qs + L::kQBytes + c * 16384, &a.tm_do, &bars->qd_full[stage],
+                              c * 64, h, qrow);
+                ATTN_TL(1, st);
+              }
+            }
+          }
+        }
+      }
+      if (!ok) {
+        report_timeout(a, 0x310);
+        *abort_flag = 1;
+      }
+      if (*abort_flag) {
+        if (kvc > 0) mbar_wait(&bars->kv_full, (kvc - 1) & 1, 100000000ull);
+        for (uint32_t u = (st > (uint32_t)NS ? st - NS : 0u); u < st; ++u)
+          mbar_wait(&bars->qd_full[u % NS], (u / NS) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ vector loader
+    const int t = tid - 64;
+    uint32_t st = 0;
+    bool ok = true;
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
+          idx < 0)
+        break;
+      const DkdvItem w = dkdv_item(a, idx);
+      for (int b = w.b0; b < w.b1 && ok; ++b) {
+        for (int g = w.g0; g < w.g1 && ok; ++g) {
+          int q_lo;
+          const int nq = dkdv_q_tiles<kQ>(a, b, w.t, q_lo);
+          for (int hh = 0; hh < G && ok && nq > 0; ++hh) {
+            const int h = g * G + hh;
+            for (int s = 0; s < nq; ++s, ++st) {
+              const int stage = st % NS;
+              if (st >= (uint32_t)NS &&
+                  !(ok = mbar_wait_warp(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
+                break;
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const int e = t + 64 * r;
+                const int i = q_lo + s * kQ + e;
+                const bool in = i < a.Sq;
+                const int64_t vi = ((int64_t)b * a.Hq + h) * a.Sq + i;
+                vec[stage].lse2[e] = in ? a.lse2[vi] : INFINITY;
+                vec[stage].D[e] = in ? a.Dvec[vi] : 0.f;
+                if (general) {
+                  vec[stage].qid[e] = in ? a.q_id[(int64_t)b * a.Sq + i] : -1;
+                  vec[stage].qpos[e] = in ? a.q_pos[(int64_t)b * a.Sq + i] : 0;
+                }
+              }
+              mbar_arrive(&bars->qd_full[stage]);
+            }
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(a, 0x320 + warp);
+      *abort_flag = 1;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, kQ, false, false);   // S^T, N = query
+      constexpr uint32_t id_p = idesc_bf16_f32(128, kQ, false, false);   // dP^T
+      constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, false, true);   // dV, B = dO (MN)
+      constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, false, true);  // dK, B = Q (MN)
+      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
+      const uint64_t st_km = sdesc_sw128(smem_u32(sm + L::kStageOff), 16, 1024);
+      const uint64_t st_mn = sdesc_sw128(smem_u32(sm + L::kStageOff), 16384, 1024);
+      uint32_t st = 0, kvc = 0, gc = 0;
+      bool ok = true;
+      auto soff16 = [&](uint32_t x) -> uint32_t {
+        return static_cast<uint32_t>(((x % NS) * L::kStageBytes) >> 4);
+      };
+      // dK += dS^T(x) Q(x): A = packed dS^T (query columns [0,64) at dP^T columns
+      // [0,32), [64,128) at [64,96)), B = Q(x) MN-major; K = 128 query rows
+      auto issue_dk = [&](uint32_t x, bool first) {
+        const uint64_t qd = st_mn + soff16(x);
+#pragma unroll
+        for (int ks = 0; ks < kQ / 16; ++ks)
+          mma_ts(tmem + L::kColDK, tmem + L::kColDP + ks * 8 + (ks >> 2) * 32,
+                 qd + ((ks * 2048) >> 4), id_dk, (!first || ks > 0));
+        mma_commit(&bars->qd_empty[x % NS]);
+      };
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
+        const DkdvItem w = dkdv_item(a, idx);
+        for (int b = w.b0; b < w.b1 && ok; ++b) {
+          for (int g = w.g0; g < w.g1 && ok; ++g) {
+            int q_lo;
+            const int nq = dkdv_q_tiles<kQ>(a, b, w.t, q_lo);
+            if (nq == 0) continue;
+            const uint32_t nsteps = (uint32_t)nq * G;
+            if (!(ok = mbar_wait(&bars->kv_full, kvc & 1))) break;
+            ++kvc;
+            for (uint32_t u = 0; u < nsteps; ++u) {
+              const uint32_t cur = st + u;
+              if (!(ok = mbar_wait(&bars->qd_full[cur % NS], (cur / NS) & 1))) break;
+              tc_fence_after();
+              {  // S^T(cur) = K Q^T  (over P^T(cur-1), read by dV(cur-1) issued earlier)
+                const uint64_t qd = st_km + soff16(cur);
+#pragma unroll
+                for (int ks = 0; ks < DQK / 16; ++ks)
+                  mma_ss(tmem + L::kColS, k_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                         qd + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), id_s, ks > 0);
+                mma_commit(&bars->s_full);
+                ATTN_TL(10, cur);
+              }
+              if (u > 0) {  // dK(cur-1), once its dS^T is in tensor memory
+                if (!(ok = mbar_wait(&bars->ds_ready, (cur - 1) & 1))) break;
+                tc_fence_after();
+                issue_dk(cur - 1, u == 1);
+                ATTN_TL(15, cur - 1);
+              }
+              {  // dP^T(cur) = V dO^T  (over dS^T(cur-1), read by dK(cur-1) just issued)
+                const uint64_t od = st_km + soff16(cur) + (L::kQBytes >> 4);
+#pragma unroll
+                for (int ks = 0; ks < DV / 16; ++ks)
+                  mma_ss(tmem + L::kColDP, v_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                         od + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), id_p, ks > 0);
+                mma_commit(&bars->dp_full);
+                ATTN_TL(11, cur);
+              }
+              // dV += P^T(cur) dO(cur)
+              if (!(ok = mbar_wait(&bars->p_ready, cur & 1))) break;
+              ATTN_TL(12, cur);
+              if (u == 0 && gc > 0 && !(ok = mbar_wait(&bars->acc_empty, (gc - 1) & 1))) break;
+              tc_fence_after();
+              {
+                const uint64_t od = st_mn + soff16(cur) + (L::kQBytes >> 4);
+#pragma unroll
+                for (int ks = 0; ks < kQ / 16; ++ks)
+                  mma_ts(tmem + L::kColDV, tmem + L::kColS + ks * 8 + (ks >> 2) * 32,
+                         od + ((ks * 2048) >> 4), id_dv, (u > 0 || ks > 0));
+              }
+            }
+            if (!ok) break;
+            // the group's last dK
+            const uint32_t last = st + nsteps - 1;
+            if (!(ok = mbar_wait(&bars->ds_ready, last & 1))) break;
+            tc_fence_after();
+            issue_dk(last, nsteps == 1);
+            mma_commit(&bars->acc_full);
+            mma_commit(&bars->kv_empty);
+            ++gc;
+            st += nsteps;
+          }
+        }
+      }
+      if (!ok) {
+        report_timeout(a, 0x330);
+        *abort_flag = 1;
+      }
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, 200000000ull);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ P / dS warps
+    // two warpgroups: thread (j, half) owns KV row j (TMEM lane j) and query
+    // columns [64 half, 64 half + 64) of every step
+    const int j = (tid - 128) & 127;
+    const int half = (tid - 128) >> 7;
+    const int c0h = half * 64;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int nqc = (a.Sq + kChunk - 1) / kChunk;
+    uint32_t st = 0;
+    bool ok = true;
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
+          idx < 0)
+        break;
+      const DkdvItem w = dkdv_item(a, idx);
+      const int kj = w.t * kTile + j;
+      const bool row_ok = kj < a.Skv;
+      for (int b = w.b0; b < w.b1 && ok; ++b) {
+        for (int g = w.g0; g < w.g1 && ok; ++g) {
+          int q_lo;
+          const int nq = dkdv_q_tiles<kQ>(a, b, w.t, q_lo);
+          if (nq == 0) continue;
+          const int64_t gk = (int64_t)b * a.Skv + kj;
+          int qlo = 0, qhi = 0, my_id = 0, my_pos = 0;
+          if (row_ok) {
+            if (!general) {
+              const int sl = a.kv_seg_lo[gk], sh = a.kv_seg_hi[gk];
+              qlo = a.causal ? max(kj, sl) : sl;
+              qhi = sh;
+            } else {
+              my_id = a.kv_id[gk];
+              my_pos = a.kv_pos[gk];
+            }
+          }
+          for (int hh = 0; hh < G && ok; ++hh) {
+            const int h = g * G + hh;
+            const int bb = a.bias_b > 1 ? b : 0, bh = a.bias_h > 1 ? h : 0;
+            const int64_t bias_base = ((int64_t)bb * a.bias_h + bh) * a.Sq;
+            for (int s = 0; s < nq; ++s, ++st) {
+              const uint32_t cur = st;
+              const int stage = cur % NS;
+              const int q0 = q_lo + s * kQ;
+              const int qh = q0 + c0h;  // first query row of this thread's columns
+              if (j == 0 && half == 0) ATTN_TL(20, cur);
+              if (!(ok = mbar_wait_warp(&bars->qd_full[stage], (cur / NS) & 1))) break;
+              const Vec128& V = vec[stage];
+              uint64_t vbits;
+              if (!general) {
+                vbits = row_ok ? range_bits64(qlo - qh, qhi - qh) : 0ull;
+              } else {
+                vbits = 0ull;
+                bool full = false;
+                if (row_ok && my_id != 0 && qh + 64 <= a.Sq && (qh % kChunk) == 0) {
+                  const ChunkInfo ci = a.q_chunk[b * nqc + qh / kChunk];
+                  full = ci.uniform && ci.min_id == my_id && (!a.causal || ci.min_pos >= my_pos);
+                }
+                if (full) {
+                  vbits = ~0ull;
+                } else if (row_ok && my_id != 0) {
+#pragma unroll
+                  for (int c = 0; c < 64; c += 4) {
+                    const int4 id4 = *reinterpret_cast<const int4*>(&V.qid[c0h + c]);
+                    const int4 ps4 = *reinterpret_cast<const int4*>(&V.qpos[c0h + c]);
+                    const int ids[4] = {id4.x, id4.y, id4.z, id4.w};
+                    const int pss[4] = {ps4.x, ps4.y, ps4.z, ps4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const bool v = (ids[e] == my_id) & (!a.causal | (my_pos <= pss[e]));
+                      vbits |= static_cast<uint64_t>(v) << (c + e);
+                    }
+                  }
+                }
+              }
+              if (!(ok = mbar_wait_warp(&bars->s_full, cur & 1))) break;
+              if (j == 0 && half == 0) ATTN_TL(21, cur);
+              tc_fence_after();
+              const uint32_t s_tm = tmem + lane_base + L::kColS + c0h;
+              // P^T in two 32-column chunks; packed bf16 pairs go back over this
+              // thread's own S^T columns (chunk q at packed columns [16 q, 16 q + 16))
+              uint32_t pp[32];  // packed P of all 64 columns, kept for dS
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                uint32_t u[32];
+                tmem_ld32x32b_x32(s_tm + q * 32, u);
+                tmem_ld_wait();
+                float x[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(u[e]) * a.scale_log2;
+                if (HAS_BIAS && row_ok) {
+                  const bf16* bp = a.bias + (bias_base + qh + q * 32) * a.Skv + kj;
+#pragma unroll
+                  for (int c = 0; c < 32; ++c)
+                    if (qh + q * 32 + c < a.Sq)
+                      x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
+                }
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                  const float4 l4 = *reinterpret_cast<const float4*>(&V.lse2[c0h + q * 32 + c]);
+                  const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const float pv = ex2_approx(x[c + e] - ls[e]);
+                    x[c + e] = ((vbits >> (q * 32 + c + e)) & 1ull) ? pv : 0.f;
+                  }
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                  pp[q * 16 + e] = pk[e];
+                }
+                tmem_st32x32b_x16(s_tm + q * 16, pk);
+              }
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(&bars->p_ready);
+              if (j == 0 && half == 0) ATTN_TL(22, cur);
+              // dS^T = P^T (dP^T - D), packed bf16 back over this thread's dP^T columns
+              if (!(ok = mbar_wait_warp(&bars->dp_full, cur & 1))) break;
+              if (j == 0 && half == 0) ATTN_TL(23, cur);
+              tc_fence_after();
+              const uint32_t dp_tm = tmem + lane_base + L::kColDP + c0h;
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                uint32_t u[32];
+                tmem_ld32x32b_x32(dp_tm + q * 32, u);
+                tmem_ld_wait();
+                float ds[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                  const float4 d4 = *reinterpret_cast<const float4*>(&V.D[c0h + q * 32 + e]);
+                  const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    const uint32_t w2 = pp[q * 16 + (e + k) / 2];
+                    const float pv = __uint_as_float(((e + k) & 1) ? (w2 & 0xFFFF0000u) : (w2 << 16));
+                    ds[e + k] = pv * (__uint_as_float(u[e + k]) - dd[k]);
+                  }
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
+                tmem_st32x32b_x16(dp_tm + q * 16, pk);
+                if (DBIAS != 0 && row_ok) {
+                  if (DBIAS == 1) {
+                    bf16* dpb = a.dbias + (bias_base + qh + q * 32) * a.Skv + kj;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                      if (qh + q * 32 + c < a.Sq) dpb[(int64_t)c * a.Skv] = __float2bfloat16_rn(ds[c]);
+                  } else {
+                    float* dpb = a.dbias_acc + (bias_base + qh + q * 32) * a.Skv + kj;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                      if (qh + q * 32 + c < a.Sq) dpb[(int64_t)c * a.Skv] += ds[c];
+                  }
+                }
+              }
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(&bars->ds_ready);
+              if (j == 0 && half == 0) ATTN_TL(24, cur);
+              mbar_arrive(&bars->qd_empty[stage]);
+            }
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(a, 0x340 + (warp & 7));
+      *abort_flag = 1;
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dK/dV epilogue
+    const int j = tid - 384;  // TMEM lane = KV row
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t gc = 0;
+    bool ok = true;
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
+          idx < 0)
+        break;
+      const DkdvItem w = dkdv_item(a, idx);
+      const int kj = w.t * kTile + j;
+      const bool row_ok = kj < a.Skv;
+      for (int b = w.b0; b < w.b1 && ok; ++b) {
+        for (int g = w.g0; g < w.g1 && ok; ++g) {
+          int q_lo;
+          const int nq = dkdv_q_tiles<kQ>(a, b, w.t, q_lo);
+          bf16* dv_row = a.dv + ((int64_t)b * a.Skv + kj) * a.dv_stride + (int64_t)g * DV;
+          bf16* dk_row = a.dk + ((int64_t)b * a.Skv + kj) * a.dk_stride + (int64_t)g * DQK;
+          if (nq == 0) {
+            if (row_ok) {
+#pragma unroll
+              for (int c = 0; c < DV; c += 8)
+                *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+              for (int c = 0; c < DQK; c += 8)
+                *reinterpret_cast<uint4*>(dk_row + c) = make_uint4(0, 0, 0, 0);
+            }
+            continue;
+          }
+          if (!(ok = mbar_wait_warp(&bars->acc_full, gc & 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < DV / 32; ++q) {
+            uint32_t u[32];
+            tmem_ld32x32b_x32(tmem + lane_base + L::kColDV + q * 32, u);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+                v.y = pack_bf16x2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
+                v.z = pack_bf16x2(__uint_as_float(u[c + 4]), __uint_as_float(u[c + 5]));
+                v.w = pack_bf16x2(__uint_as_float(u[c + 6]), __uint_as_float(u[c + 7]));
+                *reinterpret_cast<uint4*>(dv_row + q * 32 + c) = v;
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < DQK / 32; ++q) {
+            uint32_t u[32];
+            tmem_ld32x32b_x32(tmem + lane_base + L::kColDK + q * 32, u);
+            tmem_ld_wait();
+            if (row_ok) {
+              const float sc = a.scale;
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(u[c]) * sc, __uint_as_float(u[c + 1]) * sc);
+                v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * sc, __uint_as_float(u[c + 3]) * sc);
+                v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * sc, __uint_as_float(u[c + 5]) * sc);
+                v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * sc, __uint_as_float(u[c + 7]) * sc);
+                *reinterpret_cast<uint4*>(dk_row + q * 32 + c) = v;
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&bars->acc_empty);
+          ++gc;
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) report_timeout(a, 0x350 + (warp & 3));
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV, bool HB, int DB>
+cudaError_t go(const KernelArgs& a, int nsm, cudaStream_t st) {
+  using L = D128Layout<DQK, DV>;
+  auto kern = dkdv128_kernel<DQK, DV, HB, DB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int nb = a.dkdv_batch_loop ? 1 : a.B, ng = a.dkdv_head_loop ? 1 : a.Hkv;
+  const int items = a.n_kt * nb * ng;
+  const int grid = items < nsm ? items : nsm;
+  kern<<<grid, 512, L::kAlloc, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DQK, int DV>
+cudaError_t go_bias(const KernelArgs& a, int nsm, cudaStream_t st) {
+  if (!a.bias) return go<DQK, DV, false, 0>(a, nsm, st);
+  if (a.dbias_mode == 0) return go<DQK, DV, true, 0>(a, nsm, st);
+  if (a.dbias_mode == 1) return go<DQK, DV, true, 1>(a, nsm, st);
+  return go<DQK, DV, true, 2>(a, nsm, st);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dkdv128(const KernelArgs& a, int nsm, cudaStream_t st) {
+  if (a.d_qk == 64 && a.d_v == 64) return go_bias<64, 64>(a, nsm, st);
+  if (a.d_qk == 64 && a.d_v == 128) return go_bias<64, 128>(a, nsm, st);
+  if (a.d_qk == 128 && a.d_v == 64) return go_bias<128, 64>(a, nsm, st);
+  if (a.d_qk == 128 && a.d_v == 128) return go_bias<128, 128>(a, nsm, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn
+
+#ifdef ATTN_TIMELINE
+// Debug builds only: timeline of this translation unit's kernels.
+extern "C" int attn_debug_timeline128(unsigned long long* out, int cap) {
+  cudaDeviceSynchronize();
+  const int n = cap < attn::kTimelineCap ? cap : attn::kTimelineCap;
+  cudaMemcpyFromSymbol(out, attn::g_timeline, sizeof(unsigned long long) * n);
+  static unsigned long long zeros[attn::kTimelineCap];
+  cudaMemcpyToSymbol(attn::g_timeline, zeros, sizeof(zeros));
+  return n;
+}
+#endif
