@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="thd_gqa")
-    ap.add_argument("--dq-mode", default="atomic", choices=["atomic", "deterministic"])
+    ap.add_argument("--dq-mode", default="deterministic", choices=["atomic", "deterministic"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
@@ -344,6 +344,52 @@ def run_reference(args, case):
     print(json.dumps(line), flush=True)
 
 
+class Ranks:
+    """Replica bookkeeping for N > 1 (one process per GPU, launched by torchrun):
+    a barrier around the timed region and the maximum of a timing over ranks.
+    The workload itself needs no exchange; nothing else is communicated."""
+
+    def __init__(self, backend=None):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = None
+        self.device = "cpu"
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+
+            if backend is None:
+                backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend)
+            self.dist = dist
+            self.device = "cuda" if backend == "nccl" else "cpu"
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x):
+        if self.dist is None:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
+def aggregate_tflops(world, flops_per_replica, ms_max):
+    """Whole-job throughput: every rank processed flops_per_replica in at most
+    ms_max milliseconds."""
+    return world * flops_per_replica / (ms_max * 1e-3) / 1e12
+
+
 def timed(fn, steps, stream, barrier):
     import torch
 
@@ -371,28 +417,10 @@ def main():
 
     import torch
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rk = Ranks()
+    rank, world, local = rk.rank, rk.world, rk.local
     torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-
-        def barrier():
-            dist.barrier()
-
-        def max_over_ranks(x):
-            t = torch.tensor([x], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-    else:
-        def barrier():
-            pass
-
-        def max_over_ranks(x):
-            return x
+    barrier, max_over_ranks = rk.barrier, rk.max
 
     from bwd_tcgen05_tma_gb300 import build
     from bwd_tcgen05_tma_gb300 import flops as F
@@ -435,7 +463,7 @@ def main():
         if vals:
             kern_ms[name] = statistics.mean(vals)
     # the metadata slot is recorded twice per step (fwd and bwd); events hold the last
-    value = world * total_flops / (ms * 1e-3) / 1e12
+    value = aggregate_tflops(world, total_flops, ms)
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
@@ -476,17 +504,17 @@ def main():
     if not args.no_extras:
         t_f = max_over_ranks(timed(prob.fwd, max(20, args.steps // 4), stream, barrier))
         t_b = max_over_ranks(timed(prob.bwd, max(20, args.steps // 4), stream, barrier))
-        line["fwd_tflops"] = world * fwd_flops / (t_f * 1e-3) / 1e12
-        line["bwd_tflops"] = world * bwd_flops / (t_b * 1e-3) / 1e12
-        if args.dq_mode == "atomic":
-            det = Problem(case, "deterministic")
-            for _ in range(3):
-                det.step()
-            t_d = max_over_ranks(timed(det.step, max(20, args.steps // 4), stream, barrier))
-            det.check_status()
-            line["deterministic"] = {"value": world * total_flops / (t_d * 1e-3) / 1e12,
-                                     "unit": "TFLOP/s", "ms_per_step": t_d}
-            del det
+        line["fwd_tflops"] = aggregate_tflops(world, fwd_flops, t_f)
+        line["bwd_tflops"] = aggregate_tflops(world, bwd_flops, t_b)
+        other = "atomic" if args.dq_mode == "deterministic" else "deterministic"
+        alt = Problem(case, other)
+        for _ in range(3):
+            alt.step()
+        t_d = max_over_ranks(timed(alt.step, max(20, args.steps // 4), stream, barrier))
+        alt.check_status()
+        line["other_dq_mode"] = {"dq_mode": other, "value": aggregate_tflops(world, total_flops, t_d),
+                                 "unit": "TFLOP/s", "ms_per_step": t_d}
+        del alt
 
     if not args.no_e2e:
         host_out = prob.host_outputs()
@@ -497,7 +525,7 @@ def main():
         prob.check_status()
         h2d = sum(v.numel() * v.element_size() for v in prob.host_in.values())
         d2h = sum(v.numel() * v.element_size() for v in host_out.values())
-        line["e2e"] = {"value": world * total_flops / (t_e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        line["e2e"] = {"value": aggregate_tflops(world, total_flops, t_e), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": t_e}
 
@@ -508,10 +536,7 @@ def main():
                                 "seconds": dt}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.destroy_process_group()
+    rk.close()
 
 
 if __name__ == "__main__":
