@@ -252,7 +252,6 @@ __device__ __forceinline__ int dkdv_n_items(const KernelArgs& a) {
 }
 
 __device__ __forceinline__ DkdvItem dkdv_item(const KernelArgs& a, int idx) {
-  const int nb = a.dkdv_batch_loop ? 1 : a.B;
   const int ng = a.dkdv_head_loop ? 1 : a.Hkv;
   DkdvItem it;
   // (batch row, KV head)-major: CTAs running at the same time work on KV tiles

@@ -37,37 +37,46 @@ struct D128Layout {
   static constexpr int kVBytes = kTile * DV * 2;
   static constexpr int kQBytes = kQ * DQK * 2;
   static constexpr int kOBytes = kQ * DV * 2;
-  static constexpr int kStageBytes = kQBytes + kOBytes;
-  static constexpr int kStages = 2;
+  // Q(c) is read by S(c) and by dK(c), which is issued one step later, so Q
+  // gets one stage more than dO (read by dP(c) and dV(c) within step c).
+  static constexpr int kQStages = 3;
+  static constexpr int kOStages = 2;
+  static constexpr int kVecStages = 2;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKBytes;
-  static constexpr int kStageOff = kKBytes + kVBytes;
-  static constexpr int kVecOff = kStageOff + kStages * kStageBytes;  // 2 KB per stage
-  static constexpr int kBarOff = kVecOff + kStages * 2048;
+  static constexpr int kQOff = kKBytes + kVBytes;
+  static constexpr int kOOff = kQOff + kQStages * kQBytes;
+  static constexpr int kVecOff = kOOff + kOStages * kOBytes;  // 1 KB per stage
+  static constexpr int kBarOff = kVecOff + kVecStages * 1024;
   static constexpr int kBytes = kBarOff + 512;
-  static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
+  // the dynamic window starts 1 KB-aligned (checked at kernel entry), so no slack
+  static constexpr int kAlloc = kBytes;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 };
 
 struct D128Bars {
   uint64_t kv_full, kv_empty, s_full, dp_full, p_ready, ds_ready, acc_full, acc_empty, drain;
-  uint64_t qd_full[2], qd_empty[2];
+  uint64_t q_full[3], q_empty[3], o_full[2], o_empty[2], vec_full[2], vec_empty[2];
 };
 
-struct Vec128 {  // per query tile: log2-LSE, D, and (general path) ids / positions
+struct Vec128 {  // per query tile: log2-LSE and D
   float lse2[kQ];
   float D[kQ];
-  int32_t qid[kQ];
-  int32_t qpos[kQ];
 };
 
 template <int DQK, int DV, bool HAS_BIAS, int DBIAS>
 __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__ KernelArgs a) {
   using L = D128Layout<DQK, DV>;
-  constexpr int NS = L::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  constexpr int NQ = L::kQStages, NO = L::kOStages, NV = L::kVecStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  // 128-byte swizzled operand tiles need 1 KB alignment; the allocation has no
+  // slack to realign, so a misaligned window is reported instead of used
+  if (smem_u32(sm) & 1023u) {
+    if (threadIdx.x == 0) report_timeout(a, 0x3ff);
+    return;
+  }
   D128Bars* bars = reinterpret_cast<D128Bars*>(sm + L::kBarOff);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(D128Bars));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -88,9 +97,17 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 128);
     mbar_init(&bars->drain, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&bars->qd_full[s], 1 + 64);
-      mbar_init(&bars->qd_empty[s], 1 + 256);
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+    }
+    for (int s = 0; s < NO; ++s) {
+      mbar_init(&bars->o_full[s], 1);
+      mbar_init(&bars->o_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&bars->vec_full[s], 64);
+      mbar_init(&bars->vec_empty[s], 256);
     }
     ring_init(ring, 1 + 64 + 256 + 128);  // MMA, vector loader, softmax, epilogue
     *abort_flag = 0;
@@ -113,7 +130,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
       prefetch_tensormap(&a.tm_k);
       prefetch_tensormap(&a.tm_v);
       prefetch_tensormap(&a.tm_do);
-      uint32_t st = 0, kvc = 0;
+      uint32_t st = 0, kvc = 0, q_issued = 0, o_issued = 0;
       bool ok = true;
       for (uint32_t rn = 0;; ++rn) {
         int32_t idx;
@@ -126,34 +143,45 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
             int q_lo;
             const int nq = dkdv_q_tiles<kQ>(a, b, w.t, q_lo);
             if (nq == 0) continue;
-            if (kvc > 0 && !(ok = mbar_wait(&bars->kv_empty, (kvc - 1) & 1))) break;
-            const int krow = b * a.Skv + w.t * kTile;
-            mbar_arrive_expect_tx(&bars->kv_full, L::kKBytes + L::kVBytes);
-#pragma unroll
-            for (int c = 0; c < DQK / 64; ++c)
-              tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
-#pragma unroll
-            for (int c = 0; c < DV / 64; ++c)
-              tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
-            ++kvc;
             for (int hh = 0; hh < G && ok; ++hh) {
               const int h = g * G + hh;
               for (int s = 0; s < nq; ++s, ++st) {
-                const int stage = st % NS;
-                if (st >= (uint32_t)NS &&
-                    !(ok = mbar_wait(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
-                  break;
                 const int qrow = b * a.Sq + q_lo + s * kQ;
-                uint8_t* qs = sm + L::kStageOff + stage * L::kStageBytes;
-                mbar_arrive_expect_tx(&bars->qd_full[stage], L::kStageBytes);
+                const int sq = st % NQ, so = st % NO;
+                if (st >= (uint32_t)NQ &&
+                    !(ok = mbar_wait(&bars->q_empty[sq], ((st / NQ) - 1) & 1)))
+                  break;
+                uint8_t* qs = sm + L::kQOff + sq * L::kQBytes;
+                mbar_arrive_expect_tx(&bars->q_full[sq], L::kQBytes);
 #pragma unroll
                 for (int c = 0; c < DQK / 64; ++c)
-                  tma_load_3d(qs + c * 16384, &a.tm_q, &bars->qd_full[stage], c * 64, h, qrow);
+                  tma_load_3d(qs + c * 16384, &a.tm_q, &bars->q_full[sq], c * 64, h, qrow);
+                ++q_issued;
+                ATTN_TL(1, st);
+                if (hh == 0 && s == 0) {
+                  // the group's K / V, after its first Q tile so that Q keeps
+                  // streaming while the previous group drains
+                  if (kvc > 0 && !(ok = mbar_wait(&bars->kv_empty, (kvc - 1) & 1))) break;
+                  const int krow = b * a.Skv + w.t * kTile;
+                  mbar_arrive_expect_tx(&bars->kv_full, L::kKBytes + L::kVBytes);
+#pragma unroll
+                  for (int c = 0; c < DQK / 64; ++c)
+                    tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
+#pragma unroll
+                  for (int c = 0; c < DV / 64; ++c)
+                    tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
+                  ++kvc;
+                }
+                if (st >= (uint32_t)NO &&
+                    !(ok = mbar_wait(&bars->o_empty[so], ((st / NO) - 1) & 1)))
+                  break;
+                uint8_t* os = sm + L::kOOff + so * L::kOBytes;
+                mbar_arrive_expect_tx(&bars->o_full[so], L::kOBytes);
 #pragma unroll
                 for (int c = 0; c < DV / 64; ++c)
-                  tma_load_3d(qs + L::kQBytes + c * 16384, &a.tm_do, &bars->qd_full[stage],
-                              c * 64, h, qrow);
-                ATTN_TL(1, st);
+                  tma_load_3d(os + c * 16384, &a.tm_do, &bars->o_full[so], c * 64, h, qrow);
+                ++o_issued;
+                ATTN_TL(2, st);
               }
             }
           }
@@ -165,8 +193,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
       }
       if (*abort_flag) {
         if (kvc > 0) mbar_wait(&bars->kv_full, (kvc - 1) & 1, 100000000ull);
-        for (uint32_t u = (st > (uint32_t)NS ? st - NS : 0u); u < st; ++u)
-          mbar_wait(&bars->qd_full[u % NS], (u / NS) & 1, 100000000ull);
+        for (uint32_t u = (q_issued > (uint32_t)NQ ? q_issued - NQ : 0u); u < q_issued; ++u)
+          mbar_wait(&bars->q_full[u % NQ], (u / NQ) & 1, 100000000ull);
+        for (uint32_t u = (o_issued > (uint32_t)NO ? o_issued - NO : 0u); u < o_issued; ++u)
+          mbar_wait(&bars->o_full[u % NO], (u / NO) & 1, 100000000ull);
       }
     }
   } else if (warp == 2 || warp == 3) {
@@ -187,24 +217,26 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
           for (int hh = 0; hh < G && ok && nq > 0; ++hh) {
             const int h = g * G + hh;
             for (int s = 0; s < nq; ++s, ++st) {
-              const int stage = st % NS;
-              if (st >= (uint32_t)NS &&
-                  !(ok = mbar_wait_warp(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
+              const int stage = st % NV;
+              float l2[2], dd[2];
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {  // global loads ahead of the slot wait
+                const int i = q_lo + s * kQ + t + 64 * r;
+                const bool in = i < a.Sq;
+                const int64_t vi = ((int64_t)b * a.Hq + h) * a.Sq + i;
+                l2[r] = in ? a.lse2[vi] : INFINITY;
+                dd[r] = in ? a.Dvec[vi] : 0.f;
+              }
+              if (st >= (uint32_t)NV &&
+                  !(ok = mbar_wait_warp(&bars->vec_empty[stage], ((st / NV) - 1) & 1)))
                 break;
 #pragma unroll
               for (int r = 0; r < 2; ++r) {
-                const int e = t + 64 * r;
-                const int i = q_lo + s * kQ + e;
-                const bool in = i < a.Sq;
-                const int64_t vi = ((int64_t)b * a.Hq + h) * a.Sq + i;
-                vec[stage].lse2[e] = in ? a.lse2[vi] : INFINITY;
-                vec[stage].D[e] = in ? a.Dvec[vi] : 0.f;
-                if (general) {
-                  vec[stage].qid[e] = in ? a.q_id[(int64_t)b * a.Sq + i] : -1;
-                  vec[stage].qpos[e] = in ? a.q_pos[(int64_t)b * a.Sq + i] : 0;
-                }
+                vec[stage].lse2[t + 64 * r] = l2[r];
+                vec[stage].D[t + 64 * r] = dd[r];
               }
-              mbar_arrive(&bars->qd_full[stage]);
+              mbar_arrive(&bars->vec_full[stage]);
+              if (lane == 0 && warp == 2) ATTN_TL(3, st);
             }
           }
         }
@@ -223,22 +255,27 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
       constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, false, true);  // dK, B = Q (MN)
       const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
       const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
-      const uint64_t st_km = sdesc_sw128(smem_u32(sm + L::kStageOff), 16, 1024);
-      const uint64_t st_mn = sdesc_sw128(smem_u32(sm + L::kStageOff), 16384, 1024);
+      const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+      const uint64_t q_mn = sdesc_sw128(smem_u32(sm + L::kQOff), 16384, 1024);
+      const uint64_t o_km = sdesc_sw128(smem_u32(sm + L::kOOff), 16, 1024);
+      const uint64_t o_mn = sdesc_sw128(smem_u32(sm + L::kOOff), 16384, 1024);
       uint32_t st = 0, kvc = 0, gc = 0;
       bool ok = true;
-      auto soff16 = [&](uint32_t x) -> uint32_t {
-        return static_cast<uint32_t>(((x % NS) * L::kStageBytes) >> 4);
+      auto qoff16 = [&](uint32_t x) -> uint32_t {
+        return static_cast<uint32_t>(((x % NQ) * L::kQBytes) >> 4);
+      };
+      auto ooff16 = [&](uint32_t x) -> uint32_t {
+        return static_cast<uint32_t>(((x % NO) * L::kOBytes) >> 4);
       };
       // dK += dS^T(x) Q(x): A = packed dS^T (query columns [0,64) at dP^T columns
       // [0,32), [64,128) at [64,96)), B = Q(x) MN-major; K = 128 query rows
       auto issue_dk = [&](uint32_t x, bool first) {
-        const uint64_t qd = st_mn + soff16(x);
+        const uint64_t qd = q_mn + qoff16(x);
 #pragma unroll
         for (int ks = 0; ks < kQ / 16; ++ks)
           mma_ts(tmem + L::kColDK, tmem + L::kColDP + ks * 8 + (ks >> 2) * 32,
                  qd + ((ks * 2048) >> 4), id_dk, (!first || ks > 0));
-        mma_commit(&bars->qd_empty[x % NS]);
+        mma_commit(&bars->q_empty[x % NQ]);
       };
       for (uint32_t rn = 0;; ++rn) {
         int32_t idx;
@@ -254,10 +291,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
             ++kvc;
             for (uint32_t u = 0; u < nsteps; ++u) {
               const uint32_t cur = st + u;
-              if (!(ok = mbar_wait(&bars->qd_full[cur % NS], (cur / NS) & 1))) break;
+              if (!(ok = mbar_wait(&bars->q_full[cur % NQ], (cur / NQ) & 1))) break;
               tc_fence_after();
               {  // S^T(cur) = K Q^T  (over P^T(cur-1), read by dV(cur-1) issued earlier)
-                const uint64_t qd = st_km + soff16(cur);
+                const uint64_t qd = q_km + qoff16(cur);
 #pragma unroll
                 for (int ks = 0; ks < DQK / 16; ++ks)
                   mma_ss(tmem + L::kColS, k_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
@@ -271,8 +308,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 issue_dk(cur - 1, u == 1);
                 ATTN_TL(15, cur - 1);
               }
+              if (!(ok = mbar_wait(&bars->o_full[cur % NO], (cur / NO) & 1))) break;
+              tc_fence_after();
               {  // dP^T(cur) = V dO^T  (over dS^T(cur-1), read by dK(cur-1) just issued)
-                const uint64_t od = st_km + soff16(cur) + (L::kQBytes >> 4);
+                const uint64_t od = o_km + ooff16(cur);
 #pragma unroll
                 for (int ks = 0; ks < DV / 16; ++ks)
                   mma_ss(tmem + L::kColDP, v_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
@@ -286,11 +325,13 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
               if (u == 0 && gc > 0 && !(ok = mbar_wait(&bars->acc_empty, (gc - 1) & 1))) break;
               tc_fence_after();
               {
-                const uint64_t od = st_mn + soff16(cur) + (L::kQBytes >> 4);
+                const uint64_t od = o_mn + ooff16(cur);
 #pragma unroll
                 for (int ks = 0; ks < kQ / 16; ++ks)
                   mma_ts(tmem + L::kColDV, tmem + L::kColS + ks * 8 + (ks >> 2) * 32,
                          od + ((ks * 2048) >> 4), id_dv, (u > 0 || ks > 0));
+                mma_commit(&bars->o_empty[cur % NO]);
+                ATTN_TL(13, cur);
               }
             }
             if (!ok) break;
@@ -355,12 +396,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
             const int64_t bias_base = ((int64_t)bb * a.bias_h + bh) * a.Sq;
             for (int s = 0; s < nq; ++s, ++st) {
               const uint32_t cur = st;
-              const int stage = cur % NS;
+              const int stage = cur % NV;
               const int q0 = q_lo + s * kQ;
               const int qh = q0 + c0h;  // first query row of this thread's columns
               if (j == 0 && half == 0) ATTN_TL(20, cur);
-              if (!(ok = mbar_wait_warp(&bars->qd_full[stage], (cur / NS) & 1))) break;
-              const Vec128& V = vec[stage];
               uint64_t vbits;
               if (!general) {
                 vbits = row_ok ? range_bits64(qlo - qh, qhi - qh) : 0ull;
@@ -374,20 +413,19 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 if (full) {
                   vbits = ~0ull;
                 } else if (row_ok && my_id != 0) {
-#pragma unroll
-                  for (int c = 0; c < 64; c += 4) {
-                    const int4 id4 = *reinterpret_cast<const int4*>(&V.qid[c0h + c]);
-                    const int4 ps4 = *reinterpret_cast<const int4*>(&V.qpos[c0h + c]);
-                    const int ids[4] = {id4.x, id4.y, id4.z, id4.w};
-                    const int pss[4] = {ps4.x, ps4.y, ps4.z, ps4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                      const bool v = (ids[e] == my_id) & (!a.causal | (my_pos <= pss[e]));
-                      vbits |= static_cast<uint64_t>(v) << (c + e);
-                    }
+                  // per-token compare; every lane of the warp reads the same query row
+                  const int32_t* qid = a.q_id + (int64_t)b * a.Sq;
+                  const int32_t* qps = a.q_pos + (int64_t)b * a.Sq;
+                  const int n = min(64, a.Sq - qh);
+                  for (int c = 0; c < n; ++c) {
+                    const bool v = (__ldg(qid + qh + c) == my_id) &
+                                   (!a.causal | (my_pos <= __ldg(qps + qh + c)));
+                    vbits |= static_cast<uint64_t>(v) << c;
                   }
                 }
               }
+              if (!(ok = mbar_wait_warp(&bars->vec_full[stage], (cur / NV) & 1))) break;
+              const Vec128& V = vec[stage];
               if (!(ok = mbar_wait_warp(&bars->s_full, cur & 1))) break;
               if (j == 0 && half == 0) ATTN_TL(21, cur);
               tc_fence_after();
@@ -395,37 +433,50 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
               // P^T in two 32-column chunks; packed bf16 pairs go back over this
               // thread's own S^T columns (chunk q at packed columns [16 q, 16 q + 16))
               uint32_t pp[32];  // packed P of all 64 columns, kept for dS
+              bool none[2];     // warp-uniform: no valid pair in the 32-column chunk
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
-                uint32_t u[32];
-                tmem_ld32x32b_x32(s_tm + q * 32, u);
-                tmem_ld_wait();
-                float x[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(u[e]) * a.scale_log2;
-                if (HAS_BIAS && row_ok) {
-                  const bf16* bp = a.bias + (bias_base + qh + q * 32) * a.Skv + kj;
-#pragma unroll
-                  for (int c = 0; c < 32; ++c)
-                    if (qh + q * 32 + c < a.Sq)
-                      x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
-                }
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                  const float4 l4 = *reinterpret_cast<const float4*>(&V.lse2[c0h + q * 32 + c]);
-                  const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const float pv = ex2_approx(x[c + e] - ls[e]);
-                    x[c + e] = ((vbits >> (q * 32 + c + e)) & 1ull) ? pv : 0.f;
-                  }
-                }
+                const uint32_t m32 = static_cast<uint32_t>(vbits >> (q * 32));
+                none[q] = __all_sync(0xffffffffu, m32 == 0u);
+                const bool all = __all_sync(0xffffffffu, m32 == 0xffffffffu);
                 uint32_t pk[16];
+                if (none[q]) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-                  pp[q * 16 + e] = pk[e];
+                  for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                } else {
+                  uint32_t u[32];
+                  tmem_ld32x32b_x32(s_tm + q * 32, u);
+                  tmem_ld_wait();
+                  float x[32];
+                  if (HAS_BIAS) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(u[e]) * a.scale_log2;
+                    if (row_ok) {
+                      const bf16* bp = a.bias + (bias_base + qh + q * 32) * a.Skv + kj;
+#pragma unroll
+                      for (int c = 0; c < 32; ++c)
+                        if (qh + q * 32 + c < a.Sq)
+                          x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
+                    }
+                  }
+#pragma unroll
+                  for (int c = 0; c < 32; c += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(&V.lse2[c0h + q * 32 + c]);
+                    const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                      x[c + e] = HAS_BIAS ? ex2_approx(x[c + e] - ls[e])
+                                          : ex2_approx(fmaf(__uint_as_float(u[c + e]), a.scale_log2, -ls[e]));
+                  }
+                  if (!all) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = (m32 & (1u << e)) ? x[e] : 0.f;
+                  }
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
                 }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pp[q * 16 + e] = pk[e];
                 tmem_st32x32b_x16(s_tm + q * 16, pk);
               }
               tmem_st_wait();
@@ -439,6 +490,13 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
               const uint32_t dp_tm = tmem + lane_base + L::kColDP + c0h;
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
+                if (none[q]) {  // P = 0, so dS = 0 (dBias already holds zeros)
+                  uint32_t pk[16];
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                  tmem_st32x32b_x16(dp_tm + q * 16, pk);
+                  continue;
+                }
                 uint32_t u[32];
                 tmem_ld32x32b_x32(dp_tm + q * 32, u);
                 tmem_ld_wait();
@@ -476,7 +534,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
               tc_fence_before();
               mbar_arrive(&bars->ds_ready);
               if (j == 0 && half == 0) ATTN_TL(24, cur);
-              mbar_arrive(&bars->qd_empty[stage]);
+              mbar_arrive(&bars->vec_empty[stage]);
             }
           }
         }
