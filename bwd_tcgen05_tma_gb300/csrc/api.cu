@@ -454,7 +454,8 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
          !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
                    kTile)))
       return ATTN_ERR_CUDA;
-    if (launch_bwd_dq(a, nsm, st) != cudaSuccess) return ATTN_ERR_CUDA;
+    if ((tile128 ? launch_bwd_dq128(a, nsm, st) : launch_bwd_dq(a, nsm, st)) != cudaSuccess)
+      return ATTN_ERR_CUDA;
   }
   trace(ATTN_TRACE_DQ, true, st);
   if (a.dbias_mode == 2) {

@@ -286,6 +286,8 @@ cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic_dq, int num_sms, cu
 cudaError_t launch_bwd_dq(const KernelArgs& a, int num_sms, cudaStream_t st);
 // dK/dV pass with 128-row query tiles (deterministic dQ mode, d_qk and d_v <= 128).
 cudaError_t launch_bwd_dkdv128(const KernelArgs& a, int num_sms, cudaStream_t st);
+// Deterministic dQ pass with Q, dO and dS as tensor-memory operands (d_qk, d_v <= 128).
+cudaError_t launch_bwd_dq128(const KernelArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_dq_convert(const KernelArgs& a, cudaStream_t st);
 cudaError_t launch_dbias_convert(const KernelArgs& a, cudaStream_t st);
 
