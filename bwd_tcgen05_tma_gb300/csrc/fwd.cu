@@ -334,42 +334,55 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         // mask (branch-free: a validity bitmask per row and tile)
         uint64_t vb[2];
         kv_valid_bits(a, general, w.b, k0, rlo, rhi, my_id, my_pos, vb);
+        // 32-column chunks valid for every row of the warp skip the selects
+        // (a separate loop per case keeps both free of per-element branches)
 #pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          x[c] = ((vb[c >> 6] >> (c & 63)) & 1ull) ? x[c] : -INFINITY;
-        float mx = -INFINITY;
+        for (int q = 0; q < kTile / 32; ++q) {
+          const uint32_t m32 = static_cast<uint32_t>(vb[q >> 1] >> ((q & 1) * 32));
+          if (!__all_sync(0xffffffffu, m32 == 0xffffffffu)) {
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) mx = fmaxf(mx, x[c]);
+            for (int e = 0; e < 32; ++e) x[q * 32 + e] = (m32 & (1u << e)) ? x[q * 32 + e] : -INFINITY;
+          }
+        }
+        float mx8[8];  // independent max chains
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+#pragma unroll
+        for (int c = 8; c < kTile; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_ref, mx);
         // P(j-1) V(j-1) must be finished before O is touched or P is overwritten
         if (j > 0 && !(ok = mbar_wait_warp(&bars->pv_done, (k - 1) & 1))) break;
         tc_fence_after();
-        if (m_new > m_ref + kRescaleThreshold) {
-          if (j > 0 && m_ref > -INFINITY) {
-            const float f = ex2_approx(m_ref - m_new);
-            l *= f;
+        const bool grow_max = m_new > m_ref + kRescaleThreshold;
+        const bool rescale = grow_max && j > 0 && m_ref > -INFINITY;
+        // tensor-memory loads/stores are warp-wide: every lane takes part and
+        // the rows that keep their max scale by 1
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? ex2_approx(m_ref - m_new) : 1.f;
+          l *= f;
 #pragma unroll
-            for (int q = 0; q < DV / 32; ++q) {
-              uint32_t u[32];
-              const uint32_t ta = tmem + lane_base + L::kColO + q * 32;
-              tmem_ld32x32b_x32(ta, u);
-              tmem_ld_wait();
+          for (int q = 0; q < DV / 32; ++q) {
+            uint32_t u[32];
+            const uint32_t ta = tmem + lane_base + L::kColO + q * 32;
+            tmem_ld32x32b_x32(ta, u);
+            tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
-              tmem_st32x32b_x32(ta, u);
-            }
-            tmem_st_wait();
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
+            tmem_st32x32b_x32(ta, u);
           }
-          m_ref = m_new;
+          tmem_st_wait();
         }
+        if (grow_max) m_ref = m_new;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs = 0.f;
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // independent sum chains
 #pragma unroll
         for (int c = 0; c < kTile; ++c) {
           x[c] = ex2_approx(x[c] - m_use);
-          rs += x[c];
+          rs4[c & 3] += x[c];
         }
-        l += rs;
+        l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         // P row r -> shared memory, K-major with the 128-byte swizzle
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
