@@ -500,6 +500,23 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 uint32_t u[32];
                 tmem_ld32x32b_x32(dp_tm + q * 32, u);
                 tmem_ld_wait();
+                uint32_t pk[16];
+                if (DBIAS == 0) {
+                  // dP - D in fp32, then one packed bf16 product with P (already
+                  // bf16): the product's rounding is the one dS gets anyway
+#pragma unroll
+                  for (int e = 0; e < 32; e += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4*>(&V.D[c0h + q * 32 + e]);
+                    pk[e / 2] = mul_bf16x2(pp[q * 16 + e / 2],
+                                           pack_bf16x2(__uint_as_float(u[e]) - d4.x,
+                                                       __uint_as_float(u[e + 1]) - d4.y));
+                    pk[e / 2 + 1] = mul_bf16x2(pp[q * 16 + e / 2 + 1],
+                                               pack_bf16x2(__uint_as_float(u[e + 2]) - d4.z,
+                                                           __uint_as_float(u[e + 3]) - d4.w));
+                  }
+                  tmem_st32x32b_x16(dp_tm + q * 16, pk);
+                  continue;
+                }
                 float ds[32];
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
@@ -512,7 +529,6 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                     ds[e + k] = pv * (__uint_as_float(u[e + k]) - dd[k]);
                   }
                 }
-                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
                 tmem_st32x32b_x16(dp_tm + q * 16, pk);

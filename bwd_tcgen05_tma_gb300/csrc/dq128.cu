@@ -414,13 +414,11 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
             uint32_t u[32];
             tmem_ld32x32b_x32(dp_tm + q * 32, u);
             tmem_ld_wait();
+            // dP - D in fp32, then one packed bf16 product with P (already bf16)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const uint32_t w2 = pp[q * 16 + e];
-              const float p0 = __uint_as_float(w2 << 16), p1 = __uint_as_float(w2 & 0xFFFF0000u);
-              pk[e] = pack_bf16x2(p0 * (__uint_as_float(u[2 * e]) - Di),
-                                  p1 * (__uint_as_float(u[2 * e + 1]) - Di));
-            }
+            for (int e = 0; e < 16; ++e)
+              pk[e] = mul_bf16x2(pp[q * 16 + e], pack_bf16x2(__uint_as_float(u[2 * e]) - Di,
+                                                             __uint_as_float(u[2 * e + 1]) - Di));
           }
           tmem_st32x32b_x16(dp_tm + q * 16, pk);
         }
