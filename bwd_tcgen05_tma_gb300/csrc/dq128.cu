@@ -47,7 +47,7 @@ struct Dq128Layout {
 
 struct Dq128Bars {
   uint64_t qo_full, qo_empty, qo_ready, s_full, s_free, dp_full, ds_ready, acc_full, acc_empty,
-      drain;
+      drain, drain2;
   uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
 };
 
@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->acc_empty, 128);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain2, 1);
     for (int s = 0; s < KS; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    ring_init(ring, 1 + 256 + 128);  // MMA issuer, softmax warps, epilogue
+    ring_init(ring, 1 + 1 + 256 + 128);  // two MMA issuers, softmax warps, epilogue
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -198,9 +199,14 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
           mbar_wait(&bars->v_full[u % VS], (u / VS) & 1, 100000000ull);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads on different schedulers, one per tensor-memory
+    // region: warp 1 issues S (S region), warp 2 issues dP and dQ (dP / dS
+    // region and the dQ accumulator).  Each region's writer and readers are in
+    // one thread, which orders them.
     if (lane == 0) {
+      const bool s_side = (warp == 1);
       constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
       constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, false, true);
       const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
@@ -243,40 +249,46 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
         // after the previous item's last S / dP had been read)
         if (!(ok = mbar_wait(&bars->qo_ready, it & 1))) break;
         tc_fence_after();
-        if (!(ok = issue_s(kt)) || !(ok = issue_dp(kt))) break;
-        for (int j = 0; j < n && ok; ++j) {
-          const uint32_t k = kt + j;
-          const bool more = j + 1 < n;
-          if (more) {  // S(k+1) over S(k), once the softmax warps hold P(k)
+        if (s_side) {
+          if (!(ok = issue_s(kt))) break;
+          for (int j = 0; j + 1 < n && ok; ++j) {  // S(k+1) over S(k) once P(k) is held
+            const uint32_t k = kt + j;
             if (!(ok = mbar_wait(&bars->s_free, k & 1))) break;
-            if (!(ok = issue_s(k + 1))) break;
+            ok = issue_s(k + 1);
           }
-          if (!(ok = mbar_wait(&bars->ds_ready, k & 1))) break;
-          if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->acc_empty, (it - 1) & 1))) break;
-          tc_fence_after();
-          {  // dQ += dS K: A = packed dS (key columns [0,64) at dP columns [0,32),
-             // [64,128) at [64,96)), B = K(k) MN-major, K = 128 keys
-            const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
+        } else {
+          if (!(ok = issue_dp(kt))) break;
+          for (int j = 0; j < n && ok; ++j) {
+            const uint32_t k = kt + j;
+            if (!(ok = mbar_wait(&bars->ds_ready, k & 1))) break;
+            if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->acc_empty, (it - 1) & 1))) break;
+            tc_fence_after();
+            {  // dQ += dS K: A = packed dS (key columns [0,64) at dP columns [0,32),
+               // [64,128) at [64,96)), B = K(k) MN-major, K = 128 keys
+              const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks)
-              mma_ts(tmem + L::kColDQ, tmem + L::kColDP + (ks >> 2) * 64 + (ks & 3) * 8,
-                     kd + ((ks * 2048) >> 4), id_dq, (j > 0 || ks > 0));
-            mma_commit(&bars->k_empty[k % KS]);
+              for (int ks = 0; ks < kTile / 16; ++ks)
+                mma_ts(tmem + L::kColDQ, tmem + L::kColDP + (ks >> 2) * 64 + (ks & 3) * 8,
+                       kd + ((ks * 2048) >> 4), id_dq, (j > 0 || ks > 0));
+              // S(k) was complete before dS(k) existed: K(k) is free after this
+              mma_commit(&bars->k_empty[k % KS]);
+            }
+            // dP(k+1) over dS(k), after dQ(k) that reads it (same issuing thread)
+            if (j + 1 < n) ok = issue_dp(k + 1);
           }
-          // dP(k+1) over dS(k), after dQ(k) that reads it (same issuing thread)
-          if (more && !(ok = issue_dp(k + 1))) break;
+          if (ok) mma_commit(&bars->acc_full);
         }
         if (!ok) break;
-        mma_commit(&bars->acc_full);
         kt += n;
         ++it;
       }
       if (!ok) {
-        report_timeout(a, 0x430);
+        report_timeout(a, s_side ? 0x430 : 0x431);
         *abort_flag = 1;
       }
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 200000000ull);
+      uint64_t* dr = s_side ? &bars->drain : &bars->drain2;
+      mma_commit(dr);
+      mbar_wait(dr, 0, 200000000ull);
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / dS warps
