@@ -82,6 +82,7 @@ attn_status_t validate(const attn_params_t* p) {
   if ((int64_t)p->B * p->Sq >= (1ll << 31) || (int64_t)p->B * p->Skv >= (1ll << 31))
     return ATTN_ERR_UNSUPPORTED;
   if (p->Hq % p->Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (p->Hq > 256) return ATTN_ERR_UNSUPPORTED;
   if (!(p->scale > 0.f) || p->scale != p->scale) return ATTN_ERR_INVALID_ARG;
   if (p->d_qk != 64 && p->d_qk != 128 && p->d_qk != 192) return ATTN_ERR_UNSUPPORTED;
   if (p->d_v != 64 && p->d_v != 128) return ATTN_ERR_UNSUPPORTED;

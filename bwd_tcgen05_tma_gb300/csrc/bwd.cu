@@ -39,53 +39,65 @@ using namespace sm103;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // =========================================================== preprocess
+// One warp per token: all Hq head rows of a token are Hq * DV * 2 contiguous
+// bytes of O and of dO, read front to back.  Eight consecutive tokens per
+// block; their D and LSE values go out through shared memory so each head's
+// eight values are written as one 32-byte run of the [B, Hq, Sq] arrays.
+constexpr int kPreTok = 8;
+constexpr int kPreMaxH = 256;
+
 template <int DV>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const KernelArgs a, int dq_mode_used) {
-  // Rows are walked in (b, h, i) order, the order of D and LSE, so each warp's
-  // D / LSE accesses are contiguous; each O / dO row is DV * 2 contiguous bytes.
-  constexpr int LPR = DV / 8;    // lanes per row, 16 bytes each
-  constexpr int RPW = 32 / LPR;  // rows per warp and unrolled step
-  constexpr int U = 4;           // unrolled steps: 2 * U loads in flight per lane
-  const int64_t nrows = (int64_t)a.B * a.Hq * a.Sq;
-  const int lane = threadIdx.x & 31;
+  constexpr int LPR = DV / 8;    // lanes per head row, 16 bytes each
+  constexpr int HPI = 32 / LPR;  // head rows per warp-wide load
+  __shared__ float dsm[kPreTok][kPreMaxH];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane / LPR, l = lane % LPR;
-  const int64_t wg = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t r0 = wg * (RPW * U); r0 < nrows; r0 += nw * (RPW * U)) {
-    uint4 o[U], d[U];
+  const int64_t ntok = (int64_t)a.B * a.Sq;
+  const int64_t t0 = (int64_t)blockIdx.x * kPreTok;
+  const int64_t tok = t0 + warp;
+  if (tok < ntok) {
+    const bf16* orow = a.o_in + tok * a.Hq * DV;
+    const bf16* drow = a.d_o + tok * a.Hq * DV;
+    for (int h0 = 0; h0 < a.Hq; h0 += 2 * HPI) {  // two loads of each array in flight
+      uint4 o[2], d[2];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t row = r0 + u * RPW + sub;  // (b * Hq + h) * Sq + i
-      if (row < nrows) {
-        const int64_t bh = row / a.Sq;
-        const int i = static_cast<int>(row - bh * a.Sq);
-        const int b = static_cast<int>(bh / a.Hq), h = static_cast<int>(bh - (int64_t)b * a.Hq);
-        const int64_t off = (((int64_t)b * a.Sq + i) * a.Hq + h) * DV + l * 8;
-        o[u] = ld_nc_v4(a.o_in + off);
-        d[u] = ld_nc_v4(a.d_o + off);
-      } else {
-        o[u] = d[u] = make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < 2; ++u) {
+        const int h = h0 + u * HPI + sub;
+        if (h < a.Hq) {
+          o[u] = ld_nc_v4(orow + h * DV + l * 8);
+          d[u] = ld_nc_v4(drow + h * DV + l * 8);
+        } else {
+          o[u] = d[u] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t ow[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
+        const uint32_t dw[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), acc);
+          acc = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(dw[e] & 0xFFFF0000u), acc);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const int h = h0 + u * HPI + sub;
+        if (l == 0 && h < a.Hq) dsm[warp][h] = acc;
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t ow[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
-      const uint32_t dw[4] = {d[u].x, d[u].y, d[u].z, d[u].w};
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), acc);
-        acc = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(dw[e] & 0xFFFF0000u), acc);
-      }
-#pragma unroll
-      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      const int64_t row = r0 + u * RPW + sub;
-      if (l == 0 && row < nrows) {
-        a.Dvec[row] = acc;
-        const float lse = a.lse_in[row];
-        a.lse2[row] = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
-      }
-    }
+  }
+  __syncthreads();
+  for (int v = threadIdx.x; v < a.Hq * kPreTok; v += blockDim.x) {
+    const int h = v / kPreTok, j = v - h * kPreTok;
+    const int64_t t = t0 + j;
+    if (t >= ntok) continue;
+    const int b = static_cast<int>(t / a.Sq), i = static_cast<int>(t - (int64_t)b * a.Sq);
+    const int64_t idx = ((int64_t)b * a.Hq + h) * a.Sq + i;
+    a.Dvec[idx] = dsm[j][h];
+    const float lse = a.lse_in[idx];
+    a.lse2[idx] = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) a.hdr->dq_mode = dq_mode_used;
 }
@@ -1172,12 +1184,14 @@ cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st
     e = cudaMemsetAsync(a.dbias_acc, 0, nb * sizeof(float), st);
     if (e != cudaSuccess) return e;
   }
-  const int64_t rows = (int64_t)a.B * a.Sq * a.Hq;
   const int mode = zero_dq_acc ? 0 : 1;
+  if (a.Hq > kPreMaxH) return cudaErrorInvalidValue;  // rejected on the host before launch
+  const int64_t ntok = (int64_t)a.B * a.Sq;
+  const unsigned blocks = static_cast<unsigned>((ntok + kPreTok - 1) / kPreTok);
   if (a.d_v == 64)
-    bwd_pre_kernel<64><<<blocks_for(rows, 8 * 4 * 4), 256, 0, st>>>(a, mode);
+    bwd_pre_kernel<64><<<blocks, 256, 0, st>>>(a, mode);
   else
-    bwd_pre_kernel<128><<<blocks_for(rows, 8 * 2 * 4), 256, 0, st>>>(a, mode);
+    bwd_pre_kernel<128><<<blocks, 256, 0, st>>>(a, mode);
   return cudaGetLastError();
 }
 

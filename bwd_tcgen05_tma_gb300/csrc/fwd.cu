@@ -43,8 +43,11 @@ struct FwdLayout {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + kKStages * kKBytes;
+  // two P buffers where they fit: P(j) is written while P(j-1) V(j-1) runs
+  static constexpr int kPStages =
+      (kQBytes + kKStages * kKBytes + kVStages * kVBytes + 2 * kPBytes <= 224 * 1024) ? 2 : 1;
   static constexpr int kPOff = kVOff + kVStages * kVBytes;
-  static constexpr int kBarOff = kPOff + kPBytes;
+  static constexpr int kBarOff = kPOff + kPStages * kPBytes;
   static constexpr int kBytes = kBarOff + 512;  // barriers, then the item ring at +256
   // at least ~116 KB so two CTAs never share an SM (each allocates all of TMEM)
   static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
@@ -54,7 +57,10 @@ struct FwdLayout {
 };
 
 struct Bars {
-  uint64_t q_full, q_empty, p_full, pv_done, o_empty, drain;
+  uint64_t q_full, q_empty, pv_done, o_full, o_empty, drain;
+  // per P buffer: with two, warps that finish step j+1 early must not count
+  // toward step j
+  uint64_t p_full[2];
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], s_empty[2];
 };
@@ -115,8 +121,10 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->p_full[0], 128);
+    mbar_init(&bars->p_full[1], 128);
     mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, 128);
     mbar_init(&bars->drain, 1);
     for (int s = 0; s < 2; ++s) {
@@ -243,22 +251,24 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
           } else {
             mma_commit(&bars->q_empty);  // every S MMA of this item has been issued
           }
-          if (!(ok = mbar_wait(&bars->p_full, k & 1))) break;
+          if (!(ok = mbar_wait(&bars->p_full[k & 1], (k >> 1) & 1))) break;
           if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->o_empty, (it - 1) & 1))) break;
           const int s = k % L::kVStages;
           if (!(ok = mbar_wait(&bars->v_full[s], (k / L::kVStages) & 1))) break;
           tc_fence_after();
           const uint64_t vd = v_desc0 + static_cast<uint64_t>((s * L::kVBytes) >> 4);
+          const uint64_t pd = p_desc + static_cast<uint32_t>(((k % L::kPStages) * L::kPBytes) >> 4);
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks) {
             const uint32_t poff16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-            mma_ss(tmem + L::kColO, p_desc + poff16, vd + static_cast<uint32_t>(ks * (2048 >> 4)),
+            mma_ss(tmem + L::kColO, pd + poff16, vd + static_cast<uint32_t>(ks * (2048 >> 4)),
                    idesc_o, (j > 0 || ks > 0));
           }
           mma_commit(&bars->pv_done);
           mma_commit(&bars->v_empty[s]);
         }
         if (!ok) break;
+        mma_commit(&bars->o_full);  // O of this item complete once these land
         kt += w.n;
         ++it;
       }
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
     const int r = tid - 128;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t p_addr = smem_u32(sm + L::kPOff);
-    uint32_t kt = 0;
+    uint32_t kt = 0, it_sm = 0;  // it_sm: items with work, as the MMA issuer counts them
     bool ok = true;
     for (uint32_t rn = 0;; ++rn) {
       int32_t idx;
@@ -352,11 +362,15 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_ref, mx);
-        // P(j-1) V(j-1) must be finished before O is touched or P is overwritten
-        if (j > 0 && !(ok = mbar_wait_warp(&bars->pv_done, (k - 1) & 1))) break;
-        tc_fence_after();
         const bool grow_max = m_new > m_ref + kRescaleThreshold;
         const bool rescale = grow_max && j > 0 && m_ref > -INFINITY;
+        // P(j-1) V(j-1) must be finished before O is rescaled or, with one P
+        // buffer, before P(j) overwrites P(j-1).  (With two buffers P(j-2) V is
+        // already done: S(j) was issued after it.)
+        if (j > 0 && (L::kPStages == 1 || __any_sync(0xffffffffu, rescale))) {
+          if (!(ok = mbar_wait_warp(&bars->pv_done, (k - 1) & 1))) break;
+          tc_fence_after();
+        }
         // tensor-memory loads/stores are warp-wide: every lane takes part and
         // the rows that keep their max scale by 1
         if (__any_sync(0xffffffffu, rescale)) {
@@ -389,18 +403,18 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const float* p8 = x + cc * 64 + u * 8;
-            st_shared_v4(p_addr + cc * 16384 + r * 128 + ((u ^ (r & 7)) << 4),
+            st_shared_v4(p_addr + (k % L::kPStages) * L::kPBytes + cc * 16384 + r * 128 + ((u ^ (r & 7)) << 4),
                          pack_bf16x2(p8[0], p8[1]), pack_bf16x2(p8[2], p8[3]),
                          pack_bf16x2(p8[4], p8[5]), pack_bf16x2(p8[6], p8[7]));
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bars->p_full);
+        mbar_arrive(&bars->p_full[k & 1]);
       }
       if (!ok) break;
       // epilogue: O / l and LSE
-      if (!(ok = mbar_wait_warp(&bars->pv_done, (kt + w.n - 1) & 1))) break;
+      if (!(ok = mbar_wait_warp(&bars->o_full, it_sm & 1))) break;
       tc_fence_after();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
@@ -424,6 +438,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
       kt += w.n;
+      ++it_sm;
     }
     if (!ok) {
       if (lane == 0) report_timeout(a, 0x30 + (warp & 3));

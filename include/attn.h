@@ -106,7 +106,7 @@ typedef struct {
   int32_t dq_mode;        /* attn_dq_mode_t (backward only) */
   int32_t B, Sq, Skv, Hq, Hkv, d_qk, d_v;
   /* Supported head dims: d_qk in {64, 128, 192}, d_v in {64, 128};
-   * Hq a multiple of Hkv. */
+   * Hq a multiple of Hkv and at most 256 (ATTN_ERR_UNSUPPORTED beyond). */
   float scale;  /* softmax scale, applied to Q.K before the bias is added */
   const void* q;
   const void* k;

@@ -86,6 +86,7 @@ def test_resolve_kv_packed_uses_v_head_dim(lib):
     (dict(layout="HD_2HD", d_qk=192, d_v=128), 3),     # KV-packed needs equal head dims
     (dict(d_qk=96), 2),                                 # unsupported head dim
     (dict(Hq=6, Hkv=4), 1),                             # Hq not a multiple of Hkv
+    (dict(Hq=512, Hkv=8), 2),                           # more query heads than supported
     (dict(B=0), 1),
     (dict(scale=0.0), 1),
 ])
