@@ -281,6 +281,8 @@ cudaError_t launch_meta(const KernelArgs& a, int fmt, const int32_t* q_ids, cons
                         const int32_t* cu_kv, int num_segments, int force_general,
                         cudaStream_t st);
 cudaError_t launch_fwd(const KernelArgs& a, int num_sms, cudaStream_t st);
+// Forward over pairs of query heads of one KV group (even group size, d <= 128).
+cudaError_t launch_fwd2t(const KernelArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic_dq, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_dq(const KernelArgs& a, int num_sms, cudaStream_t st);

@@ -475,6 +475,9 @@ cudaError_t launch_fwd_b(const KernelArgs& a, int num_sms, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_fwd(const KernelArgs& a, int num_sms, cudaStream_t st) {
+  // query heads in pairs sharing a KV head: two tiles per CTA, one softmax
+  // warpgroup each, P in tensor memory
+  if ((a.Hq / a.Hkv) % 2 == 0 && a.d_qk <= 128 && a.d_v <= 128) return launch_fwd2t(a, num_sms, st);
   if (a.d_v == 64) {
     if (a.d_qk == 64) return launch_fwd_b<64, 64>(a, num_sms, st);
     if (a.d_qk == 128) return launch_fwd_b<128, 64>(a, num_sms, st);
