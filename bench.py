@@ -172,7 +172,8 @@ class Problem:
             layout=c.layout, fmt=c.fmt, mask=c.mask, B=c.B, Sq=c.Sq, Skv=c.Skv, Hq=c.Hq,
             Hkv=c.Hkv, d_qk=c.d_qk, d_v=c.d_v, scale=c.scale, q=q, k=k, v=v,
             q_seg_ids=d.get("q_ids"), q_seg_pos=d.get("q_pos"), kv_seg_ids=d.get("kv_ids"),
-            kv_seg_pos=d.get("kv_pos"), bias=d.get("bias"), dq_mode=dq_mode)
+            kv_seg_pos=d.get("kv_pos"), bias=d.get("bias"), dq_mode=dq_mode,
+            metadata_from_forward=True)  # one workspace: the backward reuses the metadata
         ws = max(A.attn_fwd_workspace_size(self.params), A.attn_bwd_workspace_size(self.params))
         self.ws = torch.empty(ws, dtype=torch.uint8, device="cuda")
         self.o = torch.empty((c.B * c.Sq, c.Hq, c.d_v), dtype=torch.bfloat16, device="cuda")
@@ -274,12 +275,13 @@ class E2EPipeline:
 
 
 def launches_per_step(case):
-    """Kernels of this library launched per step (memsets excluded): metadata
-    (3, plus the Q/KV match check when Sq == Skv) before the forward and again
-    before the backward; the forward; preprocess, dK/dV pass and dQ pass or
-    conversion; the broadcast dBias conversion when one is needed."""
-    meta = 4 if case.Sq == case.Skv else 3
-    bwd = meta + 3
+    """Kernels of this library launched per step (memsets excluded): the
+    metadata pass before the forward (ids, positions, chunk summaries, tile
+    ranges, plus the Q/KV match check when Sq == Skv; the backward reuses it);
+    the forward; preprocess, dK/dV pass and dQ pass or conversion; the
+    broadcast dBias conversion when one is needed."""
+    meta = 5 if case.Sq == case.Skv else 4
+    bwd = 3
     if case.bias is not None and ((case.bias.shape[0] == 1 and case.B > 1) or
                                   (case.bias.shape[1] == 1 and case.Hq > 1)):
         bwd += 1

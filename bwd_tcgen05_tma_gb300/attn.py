@@ -13,7 +13,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_sm103.so")
 
-ATTN_PARAMS_VERSION = 1
+ATTN_PARAMS_VERSION = 2
 
 LAYOUTS = {"3HD": 0, "HD_2HD": 1, "HD_HD_HD": 2}
 FORMATS = {"BSHD": 0, "THD_SEGMENTS": 1, "THD_CU_SEQLENS": 2}
@@ -47,6 +47,7 @@ class attn_params_t(ctypes.Structure):
         ("cu_seqlens_q", c_vp), ("cu_seqlens_kv", c_vp), ("num_segments", c_i32),
         ("bias", c_vp), ("bias_b", c_i32), ("bias_h", c_i32),
         ("force_general_path", c_i32),
+        ("metadata_from_forward", c_i32),
     ]
 
 
@@ -128,7 +129,7 @@ def _stream(stream):
 def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, k=None, v=None,
                 q_seg_ids=None, q_seg_pos=None, kv_seg_ids=None, kv_seg_pos=None,
                 cu_seqlens_q=None, cu_seqlens_kv=None, bias=None, dq_mode="deterministic",
-                force_general_path=False):
+                force_general_path=False, metadata_from_forward=False):
     """Fill an ``attn_params_t`` from tensors (any object with data_ptr/shape)."""
     p = attn_params_t()
     p.struct_version = ATTN_PARAMS_VERSION
@@ -159,6 +160,7 @@ def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, 
     if bias is not None:
         p.bias_b, p.bias_h = int(bias.shape[0]), int(bias.shape[1])
     p.force_general_path = 1 if force_general_path else 0
+    p.metadata_from_forward = 1 if metadata_from_forward else 0
     return p
 
 

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define ATTN_PARAMS_VERSION 1
+#define ATTN_PARAMS_VERSION 2
 
 typedef enum {
   ATTN_OK = 0,
@@ -129,6 +129,13 @@ typedef struct {
   const void* bias;
   int32_t bias_b, bias_h;
   int32_t force_general_path; /* testing knob: skip the fast metadata path */
+  /* Backward only.  Nonzero: the workspace given to attn_bwd already holds the
+   * segment metadata that an attn_fwd call wrote into that same buffer for
+   * these same parameters and segment arrays, nothing has written its
+   * metadata region since, and attn_bwd reuses it instead of recomputing it
+   * (one metadata pass per training step instead of two).  Zero: attn_bwd
+   * recomputes it.  attn_fwd ignores the field. */
+  int32_t metadata_from_forward;
 } attn_params_t;
 
 /* Which metadata path the device chose (read back by attn_read_status). */

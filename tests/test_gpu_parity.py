@@ -228,3 +228,33 @@ def test_padding_garbage_isolation():
         assert torch.all(g2[k][padt] == 0)
         assert torch.equal(g1[k].view(torch.int16), g2[k].view(torch.int16))
     assert torch.equal(g1["dq"].view(torch.int16), g2["dq"].view(torch.int16))
+
+
+@pytest.mark.parametrize("name,force_general", [("thd_gqa_3hd", False), ("thd_gqa_3hd", True),
+                                                ("bshd_causal_ragged", False)])
+def test_backward_reusing_forward_metadata(name, force_general):
+    """With metadata_from_forward set, attn_bwd on the forward's workspace skips
+    the metadata pass; the gradients are bit-identical to a backward that
+    recomputes it, and the reported path is the forward's."""
+    from gpu_util import DevCase
+
+    from bwd_tcgen05_tma_gb300 import attn as A
+
+    case = CASES[name]()
+    d = DevCase(case, dq_mode="deterministic", force_general=force_general)
+    d.forward()
+    g_ref, _ = d.backward()
+    g_ref = {k: v.clone() for k, v in g_ref.items()}
+    path_ref = (d.bwd_stats.path, d.bwd_stats.reason)
+
+    d.params.metadata_from_forward = 1
+    ws = d.ws_bwd  # one buffer for both calls
+    A.attn_fwd(d.params, d.o, d.lse, ws)
+    g, (dq, dk, dv) = d.grad_buffers()
+    for _ in range(2):  # the work counters restart on every call
+        A.attn_bwd(d.params, d.o, d.do, d.lse, dq, dk, dv, None, ws)
+        st, stats = A.attn_read_status(ws)
+        assert st == 0
+        assert (stats.path, stats.reason) == path_ref
+        for k in g_ref:
+            assert torch.equal(g[k].view(torch.int16), g_ref[k].view(torch.int16)), k
