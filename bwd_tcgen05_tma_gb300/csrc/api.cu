@@ -263,6 +263,50 @@ void trace(int slot, bool end, cudaStream_t st) {
   if (e) cudaEventRecord(e, st);
 }
 
+// Second stream for the deterministic 128-row dQ pass, one per host thread
+// and device, made on first use outside stream capture.  The dQ pass reads
+// what the preprocess wrote and nothing the dK/dV pass writes, so the two run
+// side by side: the dK/dV grid (the larger work items) stays on the caller's
+// stream right behind the preprocess and takes the SMs first, while the dQ
+// grid, released by an event, takes each SM that a dK/dV CTA leaves once the
+// dK/dV work queue has run dry, instead of waiting for the slowest dK/dV CTA.
+// (A dK/dV grid on the second stream, even at a higher priority, loses the
+// SMs to a dQ grid queued directly behind the preprocess, and running CTAs
+// are not displaced.)  The fork and join events keep the pair capturable into
+// a CUDA graph.
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool failed = false;
+};
+constexpr int kMaxDevices = 64;
+thread_local AuxStream g_aux[kMaxDevices];
+
+// The auxiliary stream of this thread on the current device, or nullptr when
+// none can be had (then both passes run one after the other on `st`).
+AuxStream* aux_stream(cudaStream_t st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  AuxStream& x = g_aux[dev];
+  if (x.s) return &x;
+  if (x.failed) return nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return nullptr;  // not made while capturing; a later uncaptured call makes it
+  if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (x.s) cudaStreamDestroy(x.s);
+    if (x.fork) cudaEventDestroy(x.fork);
+    x.s = nullptr;
+    x.fork = nullptr;
+    x.failed = true;
+    return nullptr;
+  }
+  return &x;
+}
+
 attn_status_t run_meta(const KernelArgs& a, const attn_params_t* p, cudaStream_t st) {
   const bool seg = p->fmt != ATTN_FMT_THD_CU_SEQLENS && p->q_seg_ids != nullptr;
   trace(ATTN_TRACE_META, false, st);
@@ -449,11 +493,21 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   if (atomic && !make_map_f32(&a.tm_dqacc, a.dq_acc, p->d_qk, p->Hq, (int64_t)p->B * p->Sq))
     return ATTN_ERR_CUDA;
   const int nsm = sm_count();
+  // 128-row passes: the dQ pass goes on the auxiliary stream, forked here
+  // after the preprocess
+  AuxStream* ax = tile128 ? aux_stream(st) : nullptr;
+  cudaStream_t sq = st;
+  if (ax) {
+    if (cudaEventRecord(ax->fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(ax->s, ax->fork, 0) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    sq = ax->s;
+  }
   trace(ATTN_TRACE_DKDV, false, st);
   const cudaError_t ek = tile128 ? launch_bwd_dkdv128(a, nsm, st) : launch_bwd_dkdv(a, atomic, nsm, st);
   if (ek != cudaSuccess) return ATTN_ERR_CUDA;
   trace(ATTN_TRACE_DKDV, true, st);
-  trace(ATTN_TRACE_DQ, false, st);
+  trace(ATTN_TRACE_DQ, false, sq);
   if (atomic) {
     if (launch_dq_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
   } else {
@@ -462,10 +516,15 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
          !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
                    kTile)))
       return ATTN_ERR_CUDA;
-    if ((tile128 ? launch_bwd_dq128(a, nsm, st) : launch_bwd_dq(a, nsm, st)) != cudaSuccess)
+    if ((tile128 ? launch_bwd_dq128(a, nsm, sq) : launch_bwd_dq(a, nsm, st)) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
-  trace(ATTN_TRACE_DQ, true, st);
+  trace(ATTN_TRACE_DQ, true, sq);
+  if (ax) {
+    if (cudaEventRecord(ax->join, sq) != cudaSuccess ||
+        cudaStreamWaitEvent(st, ax->join, 0) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
   if (a.dbias_mode == 2) {
     trace(ATTN_TRACE_DBIAS, false, st);
     if (launch_dbias_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -181,7 +181,15 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
  *   HD_2HD:   dq [T_q,Hq,d_qk]; dk -> packed dKV [T_kv,2,Hkv,d_v] (dv ignored);
  *   HD_HD_HD: dq, dk, dv separate.
  * dbias: bf16 like the bias (NULL: not computed; must be NULL without bias).
- * Every element of every gradient is written (padding rows get exact 0). */
+ * Every element of every gradient is written (padding rows get exact 0).
+ * Streams: in deterministic mode with d_qk, d_v <= 128 the dQ pass runs on a
+ * second stream that the library owns (one per host thread and device, made
+ * by the first such call that is not under stream capture), forked from
+ * `stream` after the preprocess and joined back before the call returns; the
+ * dK/dV pass runs beside it on `stream`.  Everything later on `stream` sees
+ * all gradients.  The fork and join are events, so the call can be captured
+ * into a CUDA graph.  Under capture before that stream exists, or if it
+ * cannot be made, both passes run one after the other on `stream`. */
 attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, const float* lse,
                        void* dq, void* dk, void* dv, void* dbias, void* ws, size_t ws_bytes,
                        void* stream);
@@ -211,7 +219,8 @@ attn_status_t attn_resolve_layout(const attn_params_t* p, void* dq, void* dk, vo
  * cudaEvent_t handles created by the caller (start, end of each slot), or is
  * NULL to switch tracing off.  While set (per host thread), every attn_fwd /
  * attn_bwd call records each slot's start event before the first launch of
- * that stage and its end event after the last one, on the call's stream.  A
+ * that stage and its end event after the last one, on the stream the stage
+ * runs on (the call's stream, or the dQ pass's second stream).  A
  * slot whose handles are NULL is skipped.  The handles are copied; the caller
  * keeps ownership. */
 #define ATTN_TRACE_SLOTS 6
@@ -220,7 +229,10 @@ typedef enum {
   ATTN_TRACE_FWD = 1,      /* forward kernel */
   ATTN_TRACE_BWD_PRE = 2,  /* D = rowsum(dO*O), accumulator zeroing */
   ATTN_TRACE_DKDV = 3,     /* dK/dV pass (with atomic dQ) */
-  ATTN_TRACE_DQ = 4,       /* deterministic dQ pass or dQ conversion */
+  ATTN_TRACE_DQ = 4,       /* deterministic dQ pass or dQ conversion; on the
+                              second stream (see attn_bwd) its events span
+                              from the end of the preprocess to the end of
+                              the dQ pass, overlapping the dK/dV pass */
   ATTN_TRACE_DBIAS = 5     /* broadcast dBias conversion */
 } attn_trace_slot_t;
 attn_status_t attn_set_trace_events(void* const* events);
