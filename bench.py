@@ -276,11 +276,10 @@ class E2EPipeline:
 
 def launches_per_step(case):
     """Kernels of this library launched per step (memsets excluded): the
-    metadata pass before the forward (ids, positions, chunk summaries, tile
-    ranges, plus the Q/KV match check when Sq == Skv; the backward reuses it);
-    the forward; preprocess, dK/dV pass and dQ pass or conversion; the
-    broadcast dBias conversion when one is needed."""
-    meta = 5 if case.Sq == case.Skv else 4
+    metadata kernel before the forward (one cooperative launch; the backward
+    reuses its results); the forward; preprocess, dK/dV pass and dQ pass or
+    conversion; the broadcast dBias conversion when one is needed."""
+    meta = 1
     bwd = 3
     if case.bias is not None and ((case.bias.shape[0] == 1 and case.B > 1) or
                                   (case.bias.shape[1] == 1 and case.Hq > 1)):

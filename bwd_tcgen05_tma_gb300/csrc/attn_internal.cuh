@@ -26,6 +26,7 @@ struct WsHeader {
   int32_t mismatch;    // bit0 ids differ, bit1 pos differ, bit2 nonstandard pos
   int32_t where;       // debug: which wait timed out (role * 16 + barrier)
   int32_t next_item[4];  // work-item counters of the persistent kernels (zeroed per call)
+  uint32_t meta_barrier;  // arrivals at the metadata kernel's grid barriers (zeroed per call)
 };
 
 // Dynamic work distribution inside a persistent CTA: one thread claims items

@@ -11,6 +11,7 @@
 // cross-attention with independent metadata takes the general path).  When
 // segment positions are absent they are derived from the ids as the offset
 // inside each run of equal ids (PR #2692, Description: from_segment_ids_and_pos).
+#include <algorithm>
 #include <climits>
 
 #include "attn_internal.cuh"
@@ -93,80 +94,135 @@ __device__ __forceinline__ int id_at(const int32_t* id_row, int t) {
   return t >= 0 ? id_row[t] : INT_MIN;
 }
 
-// Pass 1, grid (chunks, B, 2 sides), one thread per token of a 1024-token
-// chunk: normalised ids, plus the chunk's first and last run boundary (a
-// boundary is a token whose id differs from its predecessor's, or token 0).
-__global__ void __launch_bounds__(kMetaThreads) meta_ids_kernel(
-    const KernelArgs a, int fmt, const int32_t* q_ids, const int32_t* kv_ids, const int32_t* cu_q,
-    const int32_t* cu_kv, int nseg, int2* bounds, int nblk) {
-  __shared__ int sh[32];
-  const int blk = blockIdx.x, b = blockIdx.y;
-  const bool kvside = blockIdx.z == 1;
+// All passes run in one cooperative kernel of 1024-thread blocks, separated
+// by grid-wide barriers; every pass strides over its work units, so the grid
+// only has to fit on the GPU at once (which the cooperative launch checks).
+//
+//   pass 1  per 1024-token block of each row and side: normalised ids, and
+//           the block's first and last run boundary (a boundary is a token
+//           whose id differs from its predecessor's, or token 0);
+//   pass 2  same blocks: run starts / ends from block scans plus the
+//           boundaries of the other blocks; positions (given, or derived as
+//           the offset inside the run); fast-path segment bounds; flags
+//           positions that do not restart at 0 and count up in a segment;
+//   pass 3  Q/KV equality per token (Sq == Skv only) and the 64-token chunk
+//           summaries of both sides;
+//   pass 4  per 128-row tile the token range of the other side it may meet,
+//           and the path decision.
+
+// Grid-wide barrier number k (1, 2, ...) over the header's arrival counter,
+// which is zero when the kernel starts.  Thread 0 of each block publishes the
+// block's writes (the fence after the block barrier is cumulative), arrives,
+// and waits with acquire loads until every block has arrived k times.  The
+// wait is bounded: after 2 s it records a timeout and every thread of the
+// block gets false, so the kernel returns instead of hanging.
+__device__ bool grid_barrier(const KernelArgs& a, unsigned k, int* flag_sh) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&a.hdr->meta_barrier, 1u);
+    const unsigned target = k * gridDim.x;
+    int ok = 1;
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&a.hdr->meta_barrier) : "memory");
+    if (v < target) {
+      const uint64_t t0 = sm103::globaltimer_ns();
+      for (uint32_t it = 1;; ++it) {
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&a.hdr->meta_barrier) : "memory");
+        if (v >= target) break;
+        if ((it & 63u) == 0u && sm103::globaltimer_ns() - t0 > 2000000000ull) {
+          report_timeout(a, 0x300 + static_cast<int>(k));
+          ok = 0;
+          break;
+        }
+      }
+    }
+    *flag_sh = ok;
+  }
+  __syncthreads();
+  return *flag_sh != 0;
+}
+
+struct MetaIn {
+  int fmt;  // 0 dense rows or per-token ids, 1 per-token ids, 2 ragged offsets
+  const int32_t* q_ids;
+  const int32_t* q_pos;
+  const int32_t* kv_ids;
+  const int32_t* kv_pos;
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+  int nseg;
+  int force_general;
+  int fast_reason;
+  int nblk;  // 1024-token blocks of the longer side
+};
+
+struct MetaShared {
+  int sh[32];
+  int shl[32];
+  int carry_start, carry_end;
+  int flag;
+};
+
+// Pass 1 for one (block, row, side) unit.
+__device__ void meta_ids_unit(const KernelArgs& a, const MetaIn& in, int blk, int b, bool kvside,
+                              int2* bounds, MetaShared& sm) {
   const int S = kvside ? a.Skv : a.Sq;
   const int c0 = blk * kMetaThreads;
-  if (c0 >= S) return;
-  const int32_t* ids = kvside ? kv_ids : q_ids;
-  const int32_t* cu = kvside ? cu_kv : cu_q;
+  if (c0 >= S) return;  // uniform over the block
+  const int32_t* ids = kvside ? in.kv_ids : in.q_ids;
+  const int32_t* cu = kvside ? in.cu_kv : in.cu_q;
   int32_t* id_out = const_cast<int32_t*>(kvside ? a.kv_id : a.q_id) + (int64_t)b * S;
   const int t = c0 + threadIdx.x;
   int first = INT_MAX, last = -1;
   if (t < S) {
-    const int id = token_id(fmt, ids, cu, nseg, b, S, t);
+    const int id = token_id(in.fmt, ids, cu, in.nseg, b, S, t);
     id_out[t] = id;
-    const bool bnd = (t == 0) || (token_id(fmt, ids, cu, nseg, b, S, t - 1) != id);
+    const bool bnd = (t == 0) || (token_id(in.fmt, ids, cu, in.nseg, b, S, t - 1) != id);
     if (bnd) first = last = t;
   }
-  // block min / max of the boundary positions
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int o = 16; o > 0; o >>= 1) {
     first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
     last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
   }
-  __shared__ int shl[32];
-  if (lane == 0) { sh[w] = first; shl[w] = last; }
+  if (lane == 0) { sm.sh[w] = first; sm.shl[w] = last; }
   __syncthreads();
   if (w == 0) {
-    first = sh[lane];
-    last = shl[lane];
+    first = sm.sh[lane];
+    last = sm.shl[lane];
     for (int o = 16; o > 0; o >>= 1) {
       first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
       last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
     }
-    if (lane == 0) bounds[((int)kvside * a.B + b) * nblk + blk] = make_int2(first, last);
+    if (lane == 0) bounds[((int)kvside * a.B + b) * in.nblk + blk] = make_int2(first, last);
   }
+  __syncthreads();  // sm.sh is reused by the next unit
 }
 
-// Pass 2, same grid: run starts / ends from block scans plus the boundaries of
-// the other chunks; positions (given, or derived as the offset inside the run);
-// fast-path segment bounds; flags positions that do not restart at 0 and count
-// up inside every segment.
-__global__ void __launch_bounds__(kMetaThreads) meta_pos_kernel(
-    const KernelArgs a, int fmt, const int32_t* q_ids, const int32_t* q_pos_in,
-    const int32_t* kv_ids, const int32_t* kv_pos_in, const int2* bounds, int nblk) {
-  __shared__ int sh[32];
-  __shared__ int carry_start, carry_end;
-  const int blk = blockIdx.x, b = blockIdx.y;
-  const bool kvside = blockIdx.z == 1;
+// Pass 2 for one (block, row, side) unit.
+__device__ void meta_pos_unit(const KernelArgs& a, const MetaIn& in, int blk, int b, bool kvside,
+                              const int2* bounds, MetaShared& sm) {
   const int S = kvside ? a.Skv : a.Sq;
   const int c0 = blk * kMetaThreads;
-  if (c0 >= S) return;
-  const int32_t* ids = kvside ? kv_ids : q_ids;
-  const int32_t* pos_in = kvside ? kv_pos_in : q_pos_in;
+  if (c0 >= S) return;  // uniform over the block
+  const int32_t* ids = kvside ? in.kv_ids : in.q_ids;
+  const int32_t* pos_in = kvside ? in.kv_pos : in.q_pos;
   const int32_t* id_row = (kvside ? a.kv_id : a.q_id) + (int64_t)b * S;
   int32_t* pos_out = const_cast<int32_t*>(kvside ? a.kv_pos : a.q_pos) + (int64_t)b * S;
   int32_t* lo_out = const_cast<int32_t*>(kvside ? a.kv_seg_lo : a.seg_lo) + (int64_t)b * S;
   int32_t* hi_out = const_cast<int32_t*>(kvside ? a.kv_seg_hi : a.seg_hi) + (int64_t)b * S;
-  const int2* bd = bounds + ((int)kvside * a.B + b) * nblk;
+  const int2* bd = bounds + ((int)kvside * a.B + b) * in.nblk;
   if (threadIdx.x == 0) {
-    int cs = 0;  // last boundary before this chunk (token 0 always is one)
+    int cs = 0;  // last boundary before this block (token 0 always is one)
     for (int k = blk - 1; k >= 0; --k)
       if (bd[k].y >= 0) { cs = bd[k].y; break; }
-    int ce = S;  // first boundary after this chunk
+    int ce = S;  // first boundary after this block
     const int nb = (S + kMetaThreads - 1) / kMetaThreads;
     for (int k = blk + 1; k < nb; ++k)
       if (bd[k].x != INT_MAX) { ce = bd[k].x; break; }
-    carry_start = cs;
-    carry_end = ce;
+    sm.carry_start = cs;
+    sm.carry_end = ce;
   }
   const int t = c0 + threadIdx.x;
   int id = 0, start_c = -1, end_c = INT_MAX;
@@ -175,36 +231,25 @@ __global__ void __launch_bounds__(kMetaThreads) meta_pos_kernel(
     if (t == 0 || id_at(id_row, t - 1) != id) start_c = t;
     if (t + 1 < S && id_row[t + 1] != id) end_c = t + 1;
   }
-  int start = block_prefix_max(start_c, sh);
-  int end = block_suffix_min(end_c, sh);
+  int start = block_prefix_max(start_c, sm.sh);
+  int end = block_suffix_min(end_c, sm.sh);
   if (t < S) {
-    if (start < 0) start = carry_start;
-    if (end == INT_MAX) end = (t + 1 >= S) ? S : carry_end;
+    if (start < 0) start = sm.carry_start;
+    if (end == INT_MAX) end = (t + 1 >= S) ? S : sm.carry_end;
   }
   int nonstd = 0;
   if (t < S) {
     int pos;
-    if (fmt == 2 || pos_in == nullptr) pos = (ids == nullptr && fmt != 2) ? t : t - start;
+    if (in.fmt == 2 || pos_in == nullptr) pos = (ids == nullptr && in.fmt != 2) ? t : t - start;
     else pos = __ldg(pos_in + (int64_t)b * S + t);
     pos_out[t] = pos;
     if (id != 0 && pos != t - start) nonstd = 1;
     lo_out[t] = id != 0 ? start : 0;
     hi_out[t] = id != 0 ? end : 0;
   }
+  // also orders this unit's reads of carry_start/end before the next unit's
+  // thread 0 rewrites them
   if (__syncthreads_or(nonstd) && threadIdx.x == 0) atomicOr(&a.hdr->mismatch, 4);
-}
-
-// Q/KV equality per token (only launched when Sq == Skv).
-__global__ void meta_match_kernel(const KernelArgs a) {
-  const int64_t n = (int64_t)a.B * a.Sq;
-  int bits = 0;
-  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    if (a.q_id[t] != a.kv_id[t]) bits |= 1;
-    if (a.q_pos[t] != a.kv_pos[t]) bits |= 2;
-  }
-  bits = __reduce_or_sync(0xffffffffu, bits);
-  if ((threadIdx.x & 31) == 0 && bits) atomicOr(&a.hdr->mismatch, bits);
 }
 
 // Summary of one 64-token chunk computed by a warp (two tokens per lane).
@@ -245,7 +290,20 @@ __device__ ChunkInfo chunk_info_warp(const int32_t* id, const int32_t* pos, int 
   return ci;
 }
 
-__global__ void meta_chunks_kernel(const KernelArgs a) {
+// Pass 3: Q/KV equality per token (grid-stride over tokens) and the chunk
+// summaries (one warp per chunk).
+__device__ void meta_match_chunks(const KernelArgs& a) {
+  if (a.Sq == a.Skv) {
+    const int64_t n = (int64_t)a.B * a.Sq;
+    int bits = 0;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n;
+         t += (int64_t)gridDim.x * blockDim.x) {
+      if (a.q_id[t] != a.kv_id[t]) bits |= 1;
+      if (a.q_pos[t] != a.kv_pos[t]) bits |= 2;
+    }
+    bits = __reduce_or_sync(0xffffffffu, bits);
+    if ((threadIdx.x & 31) == 0 && bits) atomicOr(&a.hdr->mismatch, bits);
+  }
   const int nqc = (a.Sq + kChunk - 1) / kChunk, nkc = (a.Skv + kChunk - 1) / kChunk;
   const int total = a.B * (nqc + nkc);
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -280,24 +338,24 @@ __device__ __forceinline__ int warp_max(int v) {
   return v;
 }
 
-// Per 128-row query tile: the KV token range it may attend to; per 128-row KV
-// tile: the query token range that may attend to it.  One warp per tile.
-__global__ void meta_ranges_kernel(const KernelArgs a, int force_general, int fmt_cu,
-                                   int fast_reason) {
-  const int mism = a.hdr->mismatch;
-  const bool general = force_general || a.Sq != a.Skv || (mism & 7) != 0;
+// Pass 4: per 128-row query tile the KV token range it may attend to; per
+// 128-row KV tile the query token range that may attend to it.  One warp per
+// tile.
+__device__ void meta_ranges(const KernelArgs& a, const MetaIn& in) {
+  const int mism = *reinterpret_cast<const volatile int32_t*>(&a.hdr->mismatch);
+  const bool general = in.force_general || a.Sq != a.Skv || (mism & 7) != 0;
   const int nqc = (a.Sq + kChunk - 1) / kChunk, nkc = (a.Skv + kChunk - 1) / kChunk;
   const int totq = a.B * a.n_qt, totk = a.B * a.n_kt;
   const int lane = threadIdx.x & 31;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     a.hdr->path = general ? 1 : 0;
     int reason;
-    if (force_general) reason = 2;
+    if (in.force_general) reason = 2;
     else if (a.Sq != a.Skv) reason = 3;
-    else if (mism & 1) reason = fmt_cu ? 7 : 4;
-    else if (mism & 2) reason = fmt_cu ? 7 : 5;
+    else if (mism & 1) reason = in.fmt == 2 ? 7 : 4;
+    else if (mism & 2) reason = in.fmt == 2 ? 7 : 5;
     else if (mism & 4) reason = 6;
-    else reason = fast_reason;  // dense rows or matching metadata
+    else reason = in.fast_reason;  // dense rows or matching metadata
     a.hdr->reason = reason;
   }
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -364,38 +422,82 @@ __global__ void meta_ranges_kernel(const KernelArgs a, int force_general, int fm
   }
 }
 
+__global__ void __launch_bounds__(kMetaThreads) meta_kernel(const KernelArgs a, const MetaIn in) {
+  __shared__ MetaShared sm;
+  int2* bounds = const_cast<int2*>(a.meta_scan);
+  const int units = in.nblk * a.B * 2;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int blk = u % in.nblk, rest = u / in.nblk;
+    meta_ids_unit(a, in, blk, rest % a.B, rest >= a.B, bounds, sm);
+  }
+  if (!grid_barrier(a, 1, &sm.flag)) return;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int blk = u % in.nblk, rest = u / in.nblk;
+    meta_pos_unit(a, in, blk, rest % a.B, rest >= a.B, bounds, sm);
+  }
+  if (!grid_barrier(a, 2, &sm.flag)) return;
+  meta_match_chunks(a);
+  if (!grid_barrier(a, 3, &sm.flag)) return;
+  meta_ranges(a, in);
+}
+
+int meta_max_blocks() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int per_sm = 0, nsm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, meta_kernel, kMetaThreads, 0) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  const int n = per_sm * nsm;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_meta(const KernelArgs& a, int fmt, const int32_t* q_ids, const int32_t* q_pos,
                         const int32_t* kv_ids, const int32_t* kv_pos, const int32_t* cu_q,
                         const int32_t* cu_kv, int num_segments, int force_general,
                         cudaStream_t st) {
-  const int fast_reason = (fmt == 0 && q_ids == nullptr) ? 0 /* dense */ : 1 /* match */;
+  MetaIn in;
+  in.fmt = fmt;
+  in.q_ids = q_ids;
+  in.q_pos = q_pos;
+  in.kv_ids = kv_ids;
+  in.kv_pos = kv_pos;
+  in.cu_q = cu_q;
+  in.cu_kv = cu_kv;
+  in.nseg = num_segments;
+  in.force_general = force_general;
+  in.fast_reason = (fmt == 0 && q_ids == nullptr) ? 0 /* dense */ : 1 /* match */;
+  const int smax = a.Sq > a.Skv ? a.Sq : a.Skv;
+  in.nblk = (smax + kMetaThreads - 1) / kMetaThreads;
   cudaError_t e = cudaMemsetAsync(a.hdr, 0, sizeof(WsHeader), st);
   if (e != cudaSuccess) return e;
-  const int smax = a.Sq > a.Skv ? a.Sq : a.Skv;
-  const int nblk = (smax + kMetaThreads - 1) / kMetaThreads;
-  int2* bounds = const_cast<int2*>(a.meta_scan);
-  const dim3 grid(nblk, a.B, 2);
-  meta_ids_kernel<<<grid, kMetaThreads, 0, st>>>(a, fmt, q_ids, kv_ids, cu_q, cu_kv, num_segments,
-                                                 bounds, nblk);
-  meta_pos_kernel<<<grid, kMetaThreads, 0, st>>>(a, fmt, q_ids, q_pos, kv_ids, kv_pos, bounds,
-                                                 nblk);
-  if (a.Sq == a.Skv) {
-    const int64_t n = (int64_t)a.B * a.Sq;
-    const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
-    meta_match_kernel<<<blocks, 256, 0, st>>>(a);
-  }
-  {
-    const int nqc = (a.Sq + kChunk - 1) / kChunk, nkc = (a.Skv + kChunk - 1) / kChunk;
-    const int warps = a.B * (nqc + nkc);
-    meta_chunks_kernel<<<(warps + 7) / 8, 256, 0, st>>>(a);
-  }
-  {
-    const int warps = a.B * (a.n_qt + a.n_kt);
-    meta_ranges_kernel<<<(warps + 7) / 8, 256, 0, st>>>(a, force_general, fmt == 2, fast_reason);
-  }
-  return cudaGetLastError();
+  // enough blocks for the widest pass, at most what fits on the GPU at once
+  const int64_t units = (int64_t)in.nblk * a.B * 2;
+  const int64_t nqc = (a.Sq + kChunk - 1) / kChunk, nkc = (a.Skv + kChunk - 1) / kChunk;
+  const int64_t wpb = kMetaThreads / 32;
+  const int64_t chunk_blocks = ((int64_t)a.B * (nqc + nkc) + wpb - 1) / wpb;
+  const int64_t range_blocks = ((int64_t)a.B * (a.n_qt + a.n_kt) + wpb - 1) / wpb;
+  const int cap = meta_max_blocks();
+  if (cap <= 0) return cudaErrorInvalidConfiguration;
+  const int64_t want = std::max<int64_t>(1, std::max(units, std::max(chunk_blocks, range_blocks)));
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, cap));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMetaThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, meta_kernel, a, in);
 }
 
 }  // namespace attn

@@ -258,3 +258,38 @@ def test_backward_reusing_forward_metadata(name, force_general):
         assert (stats.path, stats.reason) == path_ref
         for k in g_ref:
             assert torch.equal(g[k].view(torch.int16), g_ref[k].view(torch.int16)), k
+
+
+@pytest.mark.parametrize("force_general", [False, True])
+def test_many_rows_match_single_row_calls(force_general):
+    """160 rows of 2100 tokens: more 1024-token metadata blocks than the
+    metadata kernel's grid holds, so every pass strides over its units, and
+    segment bounds carry across blocks.  Rows are independent: each row's
+    outputs and gradients equal, bit for bit, those of a call on that row
+    alone (whose parity with the oracle the other tests cover)."""
+    import copy
+
+    from gpu_util import DevCase
+
+    big = I.synth("rows", B=160, Sq=2100, Skv=2100, Hq=1, Hkv=1, d_qk=64, d_v=64,
+                  layout="HD_HD_HD", fmt="THD_SEGMENTS", causal=True, seed=51, seg=(64, 2048),
+                  pad_frac=0.05)
+    d = DevCase(big, force_general=force_general)
+    o, lse = d.forward()
+    g, _ = d.backward()
+    assert d.fwd_stats.path == (1 if force_general else 0)
+    for b in (0, 77, 159):
+        one = copy.copy(big)
+        one.B = 1
+        one.buffers = {k: v[b:b + 1] for k, v in big.buffers.items()}
+        one.do = big.do[b:b + 1]
+        for f in ("q_ids", "q_pos", "kv_ids", "kv_pos"):
+            setattr(one, f, getattr(big, f)[b:b + 1])
+        s = DevCase(one, force_general=force_general)
+        o1, l1 = s.forward()
+        g1, _ = s.backward()
+        assert torch.equal(o.view(160, 2100, -1)[b].view(torch.int16),
+                           o1.view(2100, -1).view(torch.int16)), b
+        assert torch.equal(lse[b], l1[0]), b
+        for k in g1:
+            assert torch.equal(g[k][b].view(torch.int16), g1[k][0].view(torch.int16)), (k, b)
