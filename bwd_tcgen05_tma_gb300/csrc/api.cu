@@ -469,14 +469,9 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   a.dbias_acc = (a.dbias_mode == 2) ? reinterpret_cast<float*>(w + pl.dbias_acc) : nullptr;
   a.dkdv_batch_loop = (a.dbias_mode == 2 && p->bias_b == 1 && p->B > 1) ? 1 : 0;
   a.dkdv_head_loop = (a.dbias_mode == 2 && p->bias_h == 1 && p->Hkv > 1) ? 1 : 0;
-  if (p->metadata_from_forward) {
-    // the forward's metadata stays; only the work counters of the backward
-    // passes start again from zero
-    if (cudaMemsetAsync(&a.hdr->next_item[1], 0, 3 * sizeof(int32_t), st) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-  } else if ((s = run_meta(a, p, st)) != ATTN_OK) {
-    return s;
-  }
+  // With metadata_from_forward the forward's metadata stays; the preprocess
+  // kernel restarts the work counters of the backward passes either way.
+  if (!p->metadata_from_forward && (s = run_meta(a, p, st)) != ATTN_OK) return s;
   trace(ATTN_TRACE_BWD_PRE, false, st);
   if (launch_bwd_pre(a, atomic ? 1 : 0, st) != cudaSuccess) return ATTN_ERR_CUDA;
   trace(ATTN_TRACE_BWD_PRE, true, st);

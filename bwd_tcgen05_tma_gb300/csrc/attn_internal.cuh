@@ -276,6 +276,26 @@ __device__ __forceinline__ int dkdv_q_tiles(const KernelArgs& a, int b, int t, i
 }
 
 
+// Launches `kern` with programmatic stream serialisation: the grid may be
+// scheduled while the kernel before it on the stream still runs, and waits
+// in grid_dep_wait() (which every such kernel calls before it touches data
+// that kernel writes) until that kernel has completed.
+template <typename... P, typename... Act>
+inline cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Act&&>(args)...);
+}
+
 // Kernel launchers (defined in the kernel translation units).
 cudaError_t launch_meta(const KernelArgs& a, int fmt, const int32_t* q_ids, const int32_t* q_pos,
                         const int32_t* kv_ids, const int32_t* kv_pos, const int32_t* cu_q,

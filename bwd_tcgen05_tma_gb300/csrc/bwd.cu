@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const KernelArgs a, int dq
   const int sub = lane / LPR, l = lane % LPR;
   const int64_t ntok = (int64_t)a.B * a.Sq;
   const int64_t t0 = (int64_t)blockIdx.x * kPreTok;
+  grid_dep_wait();  // O and LSE come from the forward
+  grid_dep_launch();
   const int64_t tok = t0 + warp;
   if (tok < ntok) {
     const bf16* orow = a.o_in + tok * a.Hq * DV;
@@ -99,7 +101,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const KernelArgs a, int dq
     const float lse = a.lse_in[idx];
     a.lse2[idx] = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) a.hdr->dq_mode = dq_mode_used;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    a.hdr->dq_mode = dq_mode_used;
+    // work counters of the dK/dV and dQ passes, which start after this kernel
+    a.hdr->next_item[1] = a.hdr->next_item[2] = a.hdr->next_item[3] = 0;
+  }
 }
 
 // =========================================================== converts
@@ -227,6 +233,8 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dep_wait();  // the previous kernel on the stream has finished
+  grid_dep_launch();
   const bool general = path_general(a);
 
   if (warp == 0) {
@@ -829,6 +837,8 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dep_wait();  // the previous kernel on the stream has finished
+  grid_dep_launch();
   const bool general = path_general(a);
 
   auto item_of = [&](int idx, int& b, int& t, int& h, int& kv_lo, int& n) {
@@ -1188,11 +1198,8 @@ cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st
   if (a.Hq > kPreMaxH) return cudaErrorInvalidValue;  // rejected on the host before launch
   const int64_t ntok = (int64_t)a.B * a.Sq;
   const unsigned blocks = static_cast<unsigned>((ntok + kPreTok - 1) / kPreTok);
-  if (a.d_v == 64)
-    bwd_pre_kernel<64><<<blocks, 256, 0, st>>>(a, mode);
-  else
-    bwd_pre_kernel<128><<<blocks, 256, 0, st>>>(a, mode);
-  return cudaGetLastError();
+  return launch_pdl(a.d_v == 64 ? bwd_pre_kernel<64> : bwd_pre_kernel<128>, dim3(blocks), dim3(256),
+                    0, st, a, mode);
 }
 
 cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic, int nsm, cudaStream_t st) {

@@ -60,8 +60,8 @@ struct D128Bars {
   uint64_t q_full[3], q_empty[3], o_full[2], o_empty[2], vec_full[2], vec_empty[2];
 };
 
-struct Vec128 {  // per query tile: log2-LSE and D
-  float lse2[kQ];
+struct Vec128 {  // per query tile: negated log2-LSE and D
+  float nlse2[kQ];
   float D[kQ];
 };
 
@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dep_wait();  // the previous kernel on the stream has finished
+  grid_dep_launch();
   const bool general = path_general(a);
 
   if (warp == 0) {
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 break;
 #pragma unroll
               for (int r = 0; r < 2; ++r) {
-                vec[stage].lse2[t + 64 * r] = l2[r];
+                vec[stage].nlse2[t + 64 * r] = -l2[r];
                 vec[stage].D[t + 64 * r] = dd[r];
               }
               mbar_arrive(&bars->vec_full[stage]);
@@ -461,12 +463,25 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                   }
 #pragma unroll
                   for (int c = 0; c < 32; c += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(&V.lse2[c0h + q * 32 + c]);
-                    const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float4 l4 = *reinterpret_cast<const float4*>(&V.nlse2[c0h + q * 32 + c]);
+                    if (HAS_BIAS) {
+                      const float nl[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                      x[c + e] = HAS_BIAS ? ex2_approx(x[c + e] - ls[e])
-                                          : ex2_approx(fmaf(__uint_as_float(u[c + e]), a.scale_log2, -ls[e]));
+                      for (int e = 0; e < 4; ++e) x[c + e] = ex2_approx(x[c + e] + nl[e]);
+                    } else {
+                      // x * scale - lse, two columns per instruction
+                      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+                      const float2 y0 = fma_f32x2(
+                          make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sc2,
+                          make_float2(l4.x, l4.y));
+                      const float2 y1 = fma_f32x2(
+                          make_float2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sc2,
+                          make_float2(l4.z, l4.w));
+                      x[c] = ex2_approx(y0.x);
+                      x[c + 1] = ex2_approx(y0.y);
+                      x[c + 2] = ex2_approx(y1.x);
+                      x[c + 3] = ex2_approx(y1.y);
+                    }
                   }
                   if (!all) {
 #pragma unroll
@@ -507,12 +522,14 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
 #pragma unroll
                   for (int e = 0; e < 32; e += 4) {
                     const float4 d4 = *reinterpret_cast<const float4*>(&V.D[c0h + q * 32 + e]);
-                    pk[e / 2] = mul_bf16x2(pp[q * 16 + e / 2],
-                                           pack_bf16x2(__uint_as_float(u[e]) - d4.x,
-                                                       __uint_as_float(u[e + 1]) - d4.y));
-                    pk[e / 2 + 1] = mul_bf16x2(pp[q * 16 + e / 2 + 1],
-                                               pack_bf16x2(__uint_as_float(u[e + 2]) - d4.z,
-                                                           __uint_as_float(u[e + 3]) - d4.w));
+                    const float2 g0 = sub_f32x2(
+                        make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])),
+                        make_float2(d4.x, d4.y));
+                    const float2 g1 = sub_f32x2(
+                        make_float2(__uint_as_float(u[e + 2]), __uint_as_float(u[e + 3])),
+                        make_float2(d4.z, d4.w));
+                    pk[e / 2] = mul_bf16x2(pp[q * 16 + e / 2], pack_bf16x2(g0.x, g0.y));
+                    pk[e / 2 + 1] = mul_bf16x2(pp[q * 16 + e / 2 + 1], pack_bf16x2(g1.x, g1.y));
                   }
                   tmem_st32x32b_x16(dp_tm + q * 16, pk);
                   continue;

@@ -124,6 +124,8 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dep_wait();  // the previous kernel on the stream has finished
+  grid_dep_launch();
   const bool general = path_general(a);
 
   // causal work is heaviest in the last query tiles: hand those out first
@@ -400,9 +402,16 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[e] = ex2_approx(x[e] - lse2);
           } else {
+            // x * scale - lse, two columns per instruction
+            const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+            const float2 nl2 = make_float2(-lse2, -lse2);
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              x[e] = ex2_approx(fmaf(__uint_as_float(u[e]), a.scale_log2, -lse2));
+            for (int e = 0; e < 32; e += 2) {
+              const float2 y = fma_f32x2(
+                  make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), sc2, nl2);
+              x[e] = ex2_approx(y.x);
+              x[e + 1] = ex2_approx(y.y);
+            }
           }
           if (!all) {
 #pragma unroll
@@ -427,10 +436,13 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
             tmem_ld32x32b_x32(dp_tm + q * 32, u);
             tmem_ld_wait();
             // dP - D in fp32, then one packed bf16 product with P (already bf16)
+            const float2 d2 = make_float2(Di, Di);
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = mul_bf16x2(pp[q * 16 + e], pack_bf16x2(__uint_as_float(u[2 * e]) - Di,
-                                                             __uint_as_float(u[2 * e + 1]) - Di));
+            for (int e = 0; e < 16; ++e) {
+              const float2 g = sub_f32x2(
+                  make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1])), d2);
+              pk[e] = mul_bf16x2(pp[q * 16 + e], pack_bf16x2(g.x, g.y));
+            }
           }
           tmem_st32x32b_x16(dp_tm + q * 16, pk);
         }

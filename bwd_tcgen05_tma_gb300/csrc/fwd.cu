@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dep_wait();  // the previous kernel on the stream has finished
+  grid_dep_launch();
   const bool general = path_general(a);
 
   if (warp == 0) {
@@ -462,8 +464,7 @@ cudaError_t launch_fwd_t(const KernelArgs& a, int num_sms, cudaStream_t st) {
   const int n_items = a.B * a.n_qt * a.Hq;
   const int grid = n_items < num_sms ? n_items : num_sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, 256, L::kAlloc, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(256), L::kAlloc, st, a);
 }
 
 template <int DQK, int DV>

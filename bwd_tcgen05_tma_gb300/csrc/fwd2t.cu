@@ -79,14 +79,18 @@ __device__ __forceinline__ void chunk_max2(const uint32_t (&u)[32], uint32_t m32
                                            const bf16* bias_row, int kc0, int Skv, bool row_ok,
                                            float (&mx8)[8]) {
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    float x = __uint_as_float(u[e]);
-    if (HAS_BIAS) {
-      x *= scale_log2;
-      if (row_ok && kc0 + e < Skv) x += __bfloat162float(bias_row[kc0 + e]) * kLog2e;
+  for (int e = 0; e < 32; e += 2) {
+    float x[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      x[t] = __uint_as_float(u[e + t]);
+      if (HAS_BIAS) {
+        x[t] *= scale_log2;
+        if (row_ok && kc0 + e + t < Skv) x[t] += __bfloat162float(bias_row[kc0 + e + t]) * kLog2e;
+      }
+      if (MASKED) x[t] = (m32 & (1u << (e + t))) ? x[t] : -INFINITY;
     }
-    if (MASKED) x = (m32 & (1u << e)) ? x : -INFINITY;
-    mx8[e & 7] = fmaxf(mx8[e & 7], x);
+    mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], x[0], x[1]);
   }
 }
 
@@ -96,22 +100,33 @@ __device__ __forceinline__ void chunk_exp2(const uint32_t (&u)[32], uint32_t m32
                                            bool row_ok, float (&rs4)[4], uint32_t (&pk)[16]) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
+    float y[2];
+    if (HAS_BIAS) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int c = 2 * e + t;
+        y[t] = __uint_as_float(u[c]) * scale_log2;
+        if (row_ok && kc0 + c < Skv) y[t] += __bfloat162float(bias_row[kc0 + c]) * kLog2e;
+        y[t] -= m_use;
+      }
+    } else {
+      // both lanes of the pair in one instruction: x * scale - m
+      const float2 y2 = fma_f32x2(make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1])),
+                                  make_float2(scale_log2, scale_log2), make_float2(-m_use, -m_use));
+      y[0] = y2.x;
+      y[1] = y2.y;
+    }
     float p2[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const int c = 2 * e + t;
-      float y;
-      if (HAS_BIAS) {
-        y = __uint_as_float(u[c]) * scale_log2;
-        if (row_ok && kc0 + c < Skv) y += __bfloat162float(bias_row[kc0 + c]) * kLog2e;
-        y -= m_use;
-      } else {
-        y = fmaf(__uint_as_float(u[c]), scale_log2, -m_use);
-      }
-      const float pv = ex2_approx(y);
-      p2[t] = MASKED ? ((m32 & (1u << c)) ? pv : 0.f) : pv;
+      const float pv = ex2_approx(y[t]);
+      p2[t] = MASKED ? ((m32 & (1u << (2 * e + t))) ? pv : 0.f) : pv;
     }
-    rs4[e & 3] += p2[0] + p2[1];
+    // two running pairs of partial row sums, (rs4[0], rs4[1]) and (rs4[2], rs4[3])
+    const int r = (e & 1) * 2;
+    const float2 acc = add_f32x2(make_float2(rs4[r], rs4[r + 1]), make_float2(p2[0], p2[1]));
+    rs4[r] = acc.x;
+    rs4[r + 1] = acc.y;
     pk[e] = pack_bf16x2(p2[0], p2[1]);
   }
 }
@@ -159,6 +174,8 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  grid_dep_wait();  // the previous kernel on the stream has finished
+  grid_dep_launch();
   const bool general = path_general(a);
 
   if (warp == 0) {
@@ -487,8 +504,7 @@ cudaError_t go(const KernelArgs& a, int nsm, cudaStream_t st) {
   const int items = a.B * a.n_qt * (a.Hq / 2);
   const int grid = items < nsm ? items : nsm;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, 384, L::kAlloc, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(384), L::kAlloc, st, a);
 }
 
 }  // namespace

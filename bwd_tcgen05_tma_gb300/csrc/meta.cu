@@ -424,6 +424,7 @@ __device__ void meta_ranges(const KernelArgs& a, const MetaIn& in) {
 
 __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const KernelArgs a, const MetaIn in) {
   __shared__ MetaShared sm;
+  sm103::grid_dep_launch();  // the forward may be scheduled now; it waits for this grid to finish
   int2* bounds = const_cast<int2*>(a.meta_scan);
   const int units = in.nblk * a.B * 2;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
