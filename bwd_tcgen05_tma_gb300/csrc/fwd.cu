@@ -338,7 +338,12 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
           tmem_ld32x32b_x32(tmem + lane_base + L::kColS + sb * kTile + q * 32, u);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
+          for (int e = 0; e < 32; e += 2) {
+            const float2 y = mul_f32x2(make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])),
+                                       make_float2(a.scale_log2, a.scale_log2));
+            x[q * 32 + e] = y.x;
+            x[q * 32 + e + 1] = y.y;
+          }
         }
         tc_fence_before();
         mbar_arrive(&bars->s_empty[sb]);
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = x[e];
 #pragma unroll
-        for (int c = 8; c < kTile; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+        for (int c = 8; c < kTile; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], x[c], x[c + 1]);
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_ref, mx);
@@ -392,13 +397,16 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         }
         if (grow_max) m_ref = m_new;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // independent sum chains
+        // two columns per instruction: x - m, and two pairs of running sums
+        float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          x[c] = ex2_approx(x[c] - m_use);
-          rs4[c & 3] += x[c];
+        for (int c = 0; c < kTile; c += 2) {
+          const float2 y = sub_f32x2(make_float2(x[c], x[c + 1]), make_float2(m_use, m_use));
+          x[c] = ex2_approx(y.x);
+          x[c + 1] = ex2_approx(y.y);
+          rs[(c >> 1) & 1] = add_f32x2(rs[(c >> 1) & 1], make_float2(x[c], x[c + 1]));
         }
-        l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
         // P row r -> shared memory, K-major with the 128-byte swizzle
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {

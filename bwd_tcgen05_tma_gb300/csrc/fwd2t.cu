@@ -286,6 +286,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           if (!(ok = mbar_wait(&bars->kv_full[vc % NKV], (vc / NKV) & 1))) break;
           for (int x = 0; x < 2 && ok; ++x) {
             if (!(ok = mbar_wait(&bars->p_full[x], k & 1))) break;
+            ATTN_TL(30 + x, k);
             if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->o_empty[x], (it - 1) & 1))) break;
             tc_fence_after();
             issue_pv(x, vc, j == 0);
@@ -298,6 +299,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
               break;
             tc_fence_after();
             issue_s(x, qs, vc + 1);
+            ATTN_TL(32 + x, k + 1);
           }
           if (!ok) break;
           mma_commit(&bars->kv_empty[vc % NKV]);  // V(j) read by both P V
@@ -377,6 +379,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           all[q] = __all_sync(0xffffffffu, m32s[q] == 0xffffffffu);
         }
         if (!(ok = mbar_wait_warp(&bars->s_full[x], k & 1))) break;
+        if (lane == 0 && (warp & 3) == 0) ATTN_TL(34 + x, k);
         tc_fence_after();
         // pass 1: the row max over valid keys (log2 units), two chunks per load round
         float mx8[8];
@@ -403,6 +406,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                          fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         if (!HAS_BIAS) mx *= a.scale_log2;  // scale > 0 keeps the order
+        if (lane == 0 && (warp & 3) == 0) ATTN_TL(36 + x, k);
         const float m_new = fmaxf(m_ref, mx);
         const bool grow_max = m_new > m_ref + kRescaleThreshold;
         const bool rescale = grow_max && j > 0 && m_ref > -INFINITY;
@@ -452,6 +456,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         tmem_st_wait();
         tc_fence_before();
+        if (lane == 0 && (warp & 3) == 0) ATTN_TL(38 + x, k);
         mbar_arrive(&bars->p_full[x]);
       }
       if (!ok) break;
@@ -518,3 +523,15 @@ cudaError_t launch_fwd2t(const KernelArgs& a, int nsm, cudaStream_t st) {
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TIMELINE
+// Debug builds only: timeline of this translation unit's kernels.
+extern "C" int attn_debug_timeline_f2(unsigned long long* out, int cap) {
+  cudaDeviceSynchronize();
+  const int n = cap < attn::kTimelineCap ? cap : attn::kTimelineCap;
+  cudaMemcpyFromSymbol(out, attn::g_timeline, sizeof(unsigned long long) * n);
+  static unsigned long long zeros[attn::kTimelineCap];
+  cudaMemcpyToSymbol(attn::g_timeline, zeros, sizeof(zeros));
+  return n;
+}
+#endif
