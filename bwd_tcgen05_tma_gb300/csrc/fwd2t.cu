@@ -178,7 +178,13 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
   grid_dep_launch();
   const bool general = path_general(a);
 
-  if (warp == 0) {
+  // Registers: 384 threads x 168 at launch = 64,512 per CTA.  Warpgroup 0
+  // (producer, MMA issuer, two idle warps) drops to 104 and the two softmax
+  // warpgroups rise to 200, room for a whole S row per thread:
+  // 128 x 104 + 256 x 200 = 64,512.
+  if (warp < 4) {
+    regs_lower<104>();  // once for the whole warpgroup
+    if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&a.tm_q);
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           mbar_wait(&bars->kv_full[u % NKV], (u / NKV) & 1, 100000000ull);
       }
     }
-  } else if (warp == 1) {
+    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
@@ -318,7 +324,9 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, 200000000ull);
     }
-  } else if (warp >= 4) {
+    }  // warps 2 and 3 have no role
+  } else {
+    regs_raise<200>();
     // ------------------------------------------------------------ softmax + epilogue
     const int x = (warp - 4) >> 2;  // head of the pair
     const int r = (tid - 128) & 127;  // TMEM lane = query row
@@ -381,27 +389,24 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         if (!(ok = mbar_wait_warp(&bars->s_full[x], k & 1))) break;
         if (lane == 0 && (warp & 3) == 0) ATTN_TL(34 + x, k);
         tc_fence_after();
-        // pass 1: the row max over valid keys (log2 units), two chunks per load round
+        // the whole S row of this thread in registers: four loads, one wait
+        uint32_t u[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32x32b_x32(s_tm + q * 32, u[q]);
+        tmem_ld_wait();
+        // pass 1: the row max over valid keys (log2 units)
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t u[2][32];
-#pragma unroll
-          for (int qq = 0; qq < 2; ++qq) tmem_ld32x32b_x32(s_tm + (2 * h2 + qq) * 32, u[qq]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int qq = 0; qq < 2; ++qq) {
-            const int q = 2 * h2 + qq;
-            if (none[q]) continue;
-            if (all[q])
-              chunk_max2<false, HAS_BIAS>(u[qq], m32s[q], a.scale_log2, bias_row, k0 + q * 32,
-                                          a.Skv, row_ok, mx8);
-            else
-              chunk_max2<true, HAS_BIAS>(u[qq], m32s[q], a.scale_log2, bias_row, k0 + q * 32,
-                                         a.Skv, row_ok, mx8);
-          }
+        for (int q = 0; q < 4; ++q) {
+          if (none[q]) continue;
+          if (all[q])
+            chunk_max2<false, HAS_BIAS>(u[q], m32s[q], a.scale_log2, bias_row, k0 + q * 32, a.Skv,
+                                        row_ok, mx8);
+          else
+            chunk_max2<true, HAS_BIAS>(u[q], m32s[q], a.scale_log2, bias_row, k0 + q * 32, a.Skv,
+                                       row_ok, mx8);
         }
         float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                          fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -410,50 +415,41 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         const float m_new = fmaxf(m_ref, mx);
         const bool grow_max = m_new > m_ref + kRescaleThreshold;
         const bool rescale = grow_max && j > 0 && m_ref > -INFINITY;
-        // P_X(j-1) V is complete (S_X(j) was issued after it): O_X may be rescaled.
-        // Tensor-memory loads/stores are warp-wide, so every lane takes part.
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float f = rescale ? ex2_approx(m_ref - m_new) : 1.f;
-          l *= f;
-#pragma unroll
-          for (int q = 0; q < DV / 32; ++q) {
-            uint32_t u[32];
-            tmem_ld32x32b_x32(o_tm + q * 32, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
-            tmem_st32x32b_x32(o_tm + q * 32, u);
-          }
-          tmem_st_wait();
-        }
+        const float f = rescale ? ex2_approx(m_ref - m_new) : 1.f;
         if (grow_max) m_ref = m_new;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         // pass 2: P = exp2(x - m), packed over S_X (chunk q -> columns [16 q, 16 q + 16))
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t u[2][32];
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+          if (none[q]) {
 #pragma unroll
-          for (int qq = 0; qq < 2; ++qq) tmem_ld32x32b_x32(s_tm + (2 * h2 + qq) * 32, u[qq]);
-          tmem_ld_wait();
+            for (int e = 0; e < 16; ++e) pk[e] = 0u;
+          } else if (all[q]) {
+            chunk_exp2<false, HAS_BIAS>(u[q], m32s[q], a.scale_log2, m_use, bias_row, k0 + q * 32,
+                                        a.Skv, row_ok, rs4, pk);
+          } else {
+            chunk_exp2<true, HAS_BIAS>(u[q], m32s[q], a.scale_log2, m_use, bias_row, k0 + q * 32,
+                                       a.Skv, row_ok, rs4, pk);
+          }
+          tmem_st32x32b_x16(s_tm + q * 16, pk);
+        }
+        l = l * f + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+        // P_X(j-1) V is complete (S_X(j) was issued after it) and P_X(j) V waits
+        // for this warpgroup's arrival below: O_X may be rescaled here.
+        // Tensor-memory loads/stores are warp-wide, so every lane takes part.
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-          for (int qq = 0; qq < 2; ++qq) {
-            const int q = 2 * h2 + qq;
-            uint32_t pk[16];
-            if (none[q]) {
+          for (int q = 0; q < DV / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32x32b_x32(o_tm + q * 32, o);
+            tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) pk[e] = 0u;
-            } else if (all[q]) {
-              chunk_exp2<false, HAS_BIAS>(u[qq], m32s[q], a.scale_log2, m_use, bias_row,
-                                          k0 + q * 32, a.Skv, row_ok, rs4, pk);
-            } else {
-              chunk_exp2<true, HAS_BIAS>(u[qq], m32s[q], a.scale_log2, m_use, bias_row,
-                                         k0 + q * 32, a.Skv, row_ok, rs4, pk);
-            }
-            tmem_st32x32b_x16(s_tm + q * 16, pk);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32x32b_x32(o_tm + q * 32, o);
           }
         }
-        l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         tmem_st_wait();
         tc_fence_before();
         if (lane == 0 && (warp & 3) == 0) ATTN_TL(38 + x, k);

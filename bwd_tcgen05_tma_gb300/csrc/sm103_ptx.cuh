@@ -270,6 +270,19 @@ SM103_DEV uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// Per-warpgroup register budgets.  Every warp of a warpgroup executes the
+// same call, at the top of its role's code.  A raise waits until lowered
+// budgets elsewhere in the CTA have returned enough registers, so callers keep
+// the sum of all budgets within the launch's registers per CTA.
+template <uint32_t N>
+SM103_DEV void regs_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+SM103_DEV void regs_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Programmatic dependent launch.  grid_dep_wait holds the calling thread until
 // every grid this one was launched behind has completed and its memory writes
 // are visible (a no-op for a grid launched without the attribute);
