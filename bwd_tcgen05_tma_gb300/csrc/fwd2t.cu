@@ -111,8 +111,9 @@ __device__ __forceinline__ void chunk_exp2(const uint32_t (&u)[32], uint32_t m32
       }
     } else {
       // both lanes of the pair in one instruction: x * scale - m
-      const float2 y2 = fma_f32x2(make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1])),
-                                  make_float2(scale_log2, scale_log2), make_float2(-m_use, -m_use));
+      const float2 x2 = make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1]));
+      const float2 y2 =
+          fma_f32x2(x2, make_float2(scale_log2, scale_log2), make_float2(-m_use, -m_use));
       y[0] = y2.x;
       y[1] = y2.y;
     }
@@ -185,145 +186,146 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
   if (warp < 4) {
     regs_lower<104>();  // once for the whole warpgroup
     if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tensormap(&a.tm_q);
-      prefetch_tensormap(&a.tm_k);
-      prefetch_tensormap(&a.tm_v);
-      uint32_t it = 0, kvc = 0;  // kvc: K / V stage loads issued, in ring order
-      bool ok = true;
-      auto load_kv = [&](const CUtensorMap* m, int ncols, int g, int krow) -> bool {
-        const int s = kvc % NKV;
-        if (kvc >= (uint32_t)NKV && !mbar_wait(&bars->kv_empty[s], ((kvc / NKV) - 1) & 1))
-          return false;
-        uint8_t* dst = sm + L::kKVOff + s * L::kKVBytes;
-        mbar_arrive_expect_tx(&bars->kv_full[s], kTile * ncols * 2);
-        for (int c = 0; c < ncols / 64; ++c)
-          tma_load_3d(dst + c * 16384, m, &bars->kv_full[s], c * 64, g, krow);
-        ++kvc;
-        return true;
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[0], n_items, idx)) ||
-            idx < 0)
-          break;
-        const F2Item w = f2_item(a, idx);
-        if (w.n == 0) continue;
-        const int qs = it & 1;
-        if (it >= 2 && !(ok = mbar_wait(&bars->q_empty[qs], ((it >> 1) - 1) & 1))) break;
-        const int qrow = w.b * a.Sq + w.t * kTile;
-        mbar_arrive_expect_tx(&bars->q_full[qs], 2 * L::kQBytes);
-        for (int x = 0; x < 2; ++x) {
-          uint8_t* dst = sm + L::kQOff + (qs * 2 + x) * L::kQBytes;
-#pragma unroll
-          for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(dst + c * 16384, &a.tm_q, &bars->q_full[qs], c * 64, w.h0 + x, qrow);
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        prefetch_tensormap(&a.tm_q);
+        prefetch_tensormap(&a.tm_k);
+        prefetch_tensormap(&a.tm_v);
+        uint32_t it = 0, kvc = 0;  // kvc: K / V stage loads issued, in ring order
+        bool ok = true;
+        auto load_kv = [&](const CUtensorMap* m, int ncols, int g, int krow) -> bool {
+          const int s = kvc % NKV;
+          if (kvc >= (uint32_t)NKV && !mbar_wait(&bars->kv_empty[s], ((kvc / NKV) - 1) & 1))
+            return false;
+          uint8_t* dst = sm + L::kKVOff + s * L::kKVBytes;
+          mbar_arrive_expect_tx(&bars->kv_full[s], kTile * ncols * 2);
+          for (int c = 0; c < ncols / 64; ++c)
+            tma_load_3d(dst + c * 16384, m, &bars->kv_full[s], c * 64, g, krow);
+          ++kvc;
+          return true;
+        };
+        for (uint32_t rn = 0;; ++rn) {
+          int32_t idx;
+          if (!ok || *abort_flag ||
+              !(ok = ring_push(ring, rn, &a.hdr->next_item[0], n_items, idx)) ||
+              idx < 0)
+            break;
+          const F2Item w = f2_item(a, idx);
+          if (w.n == 0) continue;
+          const int qs = it & 1;
+          if (it >= 2 && !(ok = mbar_wait(&bars->q_empty[qs], ((it >> 1) - 1) & 1))) break;
+          const int qrow = w.b * a.Sq + w.t * kTile;
+          mbar_arrive_expect_tx(&bars->q_full[qs], 2 * L::kQBytes);
+          for (int x = 0; x < 2; ++x) {
+            uint8_t* dst = sm + L::kQOff + (qs * 2 + x) * L::kQBytes;
+  #pragma unroll
+            for (int c = 0; c < DQK / 64; ++c)
+              tma_load_3d(dst + c * 16384, &a.tm_q, &bars->q_full[qs], c * 64, w.h0 + x, qrow);
+          }
+          ++it;
+          const int g = w.h0 / (a.Hq / a.Hkv);
+          for (int j = 0; j < w.n && ok; ++j) {
+            const int krow = w.b * a.Skv + w.kv_lo + j * kTile;
+            ok = load_kv(&a.tm_k, DQK, g, krow) && load_kv(&a.tm_v, DV, g, krow);
+          }
         }
-        ++it;
-        const int g = w.h0 / (a.Hq / a.Hkv);
-        for (int j = 0; j < w.n && ok; ++j) {
-          const int krow = w.b * a.Skv + w.kv_lo + j * kTile;
-          ok = load_kv(&a.tm_k, DQK, g, krow) && load_kv(&a.tm_v, DV, g, krow);
+        if (!ok) {
+          report_timeout(a, 0x610);
+          *abort_flag = 1;
+        }
+        if (*abort_flag) {  // let copies in flight land before the CTA exits
+          for (uint32_t u = (it > 2u ? it - 2u : 0u); u < it; ++u)
+            mbar_wait(&bars->q_full[u & 1], (u >> 1) & 1, 100000000ull);
+          for (uint32_t u = (kvc > (uint32_t)NKV ? kvc - NKV : 0u); u < kvc; ++u)
+            mbar_wait(&bars->kv_full[u % NKV], (u / NKV) & 1, 100000000ull);
         }
       }
-      if (!ok) {
-        report_timeout(a, 0x610);
-        *abort_flag = 1;
-      }
-      if (*abort_flag) {  // let copies in flight land before the CTA exits
-        for (uint32_t u = (it > 2u ? it - 2u : 0u); u < it; ++u)
-          mbar_wait(&bars->q_full[u & 1], (u >> 1) & 1, 100000000ull);
-        for (uint32_t u = (kvc > (uint32_t)NKV ? kvc - NKV : 0u); u < kvc; ++u)
-          mbar_wait(&bars->kv_full[u % NKV], (u / NKV) & 1, 100000000ull);
-      }
-    }
     } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
-      constexpr uint32_t id_o = idesc_bf16_f32(128, DV, false, true);
-      const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
-      const uint64_t kv_km = sdesc_sw128(smem_u32(sm + L::kKVOff), 16, 1024);
-      const uint64_t kv_mn = sdesc_sw128(smem_u32(sm + L::kKVOff), 16384, 1024);
-      uint32_t it = 0, kvc = 0, st = 0;  // st: steps (key tiles) so far
-      bool ok = true;
-      auto stage_off = [&](uint32_t c) -> uint32_t {
-        return static_cast<uint32_t>(((c % NKV) * L::kKVBytes) >> 4);
-      };
-      // S_X(step) = Q_X K^T; K at ring position kc
-      auto issue_s = [&](int x, uint32_t qs, uint32_t kc) {
-        const uint64_t qd = q_km + static_cast<uint32_t>(((qs * 2 + x) * L::kQBytes) >> 4);
-        const uint64_t kd = kv_km + stage_off(kc);
-#pragma unroll
-        for (int ks = 0; ks < DQK / 16; ++ks) {
-          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + L::kColS + x * kTile, qd + off16, kd + off16, id_s, ks > 0);
-        }
-        mma_commit(&bars->s_full[x]);
-      };
-      // O_X += P_X V; V at ring position vc; P_X packed over S_X
-      auto issue_pv = [&](int x, uint32_t vc, bool first) {
-        const uint64_t vd = kv_mn + stage_off(vc);
-        const uint32_t pa = tmem + L::kColS + x * kTile;
-#pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ts(tmem + L::kColO + x * kTile, pa + ks * 8, vd + ((ks * 2048) >> 4), id_o,
-                 (!first || ks > 0));
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-        const F2Item w = f2_item(a, idx);
-        if (w.n == 0) continue;
-        const uint32_t qs = it & 1;
-        if (!(ok = mbar_wait(&bars->q_full[qs], (it >> 1) & 1))) break;
-        // K(0): both S of the first step
-        if (!(ok = mbar_wait(&bars->kv_full[kvc % NKV], (kvc / NKV) & 1))) break;
-        tc_fence_after();
-        issue_s(0, qs, kvc);
-        issue_s(1, qs, kvc);
-        mma_commit(&bars->kv_empty[kvc % NKV]);
-        ++kvc;
-        for (int j = 0; j < w.n && ok; ++j) {
-          const uint32_t k = st + j;
-          const uint32_t vc = kvc;  // V(j)
-          const bool more = j + 1 < w.n;
-          if (!(ok = mbar_wait(&bars->kv_full[vc % NKV], (vc / NKV) & 1))) break;
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (!(ok = mbar_wait(&bars->p_full[x], k & 1))) break;
-            ATTN_TL(30 + x, k);
-            if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->o_empty[x], (it - 1) & 1))) break;
-            tc_fence_after();
-            issue_pv(x, vc, j == 0);
-            if (!more) {
-              mma_commit(&bars->o_full[x]);
-              continue;
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
+        constexpr uint32_t id_o = idesc_bf16_f32(128, DV, false, true);
+        const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+        const uint64_t kv_km = sdesc_sw128(smem_u32(sm + L::kKVOff), 16, 1024);
+        const uint64_t kv_mn = sdesc_sw128(smem_u32(sm + L::kKVOff), 16384, 1024);
+        uint32_t it = 0, kvc = 0, st = 0;  // st: steps (key tiles) so far
+        bool ok = true;
+        auto stage_off = [&](uint32_t c) -> uint32_t {
+          return static_cast<uint32_t>(((c % NKV) * L::kKVBytes) >> 4);
+        };
+        // S_X(step) = Q_X K^T; K at ring position kc
+        auto issue_s = [&](int x, uint32_t qs, uint32_t kc) {
+          const uint64_t qd = q_km + static_cast<uint32_t>(((qs * 2 + x) * L::kQBytes) >> 4);
+          const uint64_t kd = kv_km + stage_off(kc);
+  #pragma unroll
+          for (int ks = 0; ks < DQK / 16; ++ks) {
+            const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            mma_ss(tmem + L::kColS + x * kTile, qd + off16, kd + off16, id_s, ks > 0);
+          }
+          mma_commit(&bars->s_full[x]);
+        };
+        // O_X += P_X V; V at ring position vc; P_X packed over S_X
+        auto issue_pv = [&](int x, uint32_t vc, bool first) {
+          const uint64_t vd = kv_mn + stage_off(vc);
+          const uint32_t pa = tmem + L::kColS + x * kTile;
+  #pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_ts(tmem + L::kColO + x * kTile, pa + ks * 8, vd + ((ks * 2048) >> 4), id_o,
+                   (!first || ks > 0));
+        };
+        for (uint32_t rn = 0;; ++rn) {
+          int32_t idx;
+          if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
+          const F2Item w = f2_item(a, idx);
+          if (w.n == 0) continue;
+          const uint32_t qs = it & 1;
+          if (!(ok = mbar_wait(&bars->q_full[qs], (it >> 1) & 1))) break;
+          // K(0): both S of the first step
+          if (!(ok = mbar_wait(&bars->kv_full[kvc % NKV], (kvc / NKV) & 1))) break;
+          tc_fence_after();
+          issue_s(0, qs, kvc);
+          issue_s(1, qs, kvc);
+          mma_commit(&bars->kv_empty[kvc % NKV]);
+          ++kvc;
+          for (int j = 0; j < w.n && ok; ++j) {
+            const uint32_t k = st + j;
+            const uint32_t vc = kvc;  // V(j)
+            const bool more = j + 1 < w.n;
+            if (!(ok = mbar_wait(&bars->kv_full[vc % NKV], (vc / NKV) & 1))) break;
+            for (int x = 0; x < 2 && ok; ++x) {
+              if (!(ok = mbar_wait(&bars->p_full[x], k & 1))) break;
+              ATTN_TL(30 + x, k);
+              if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->o_empty[x], (it - 1) & 1))) break;
+              tc_fence_after();
+              issue_pv(x, vc, j == 0);
+              if (!more) {
+                mma_commit(&bars->o_full[x]);
+                continue;
+              }
+              // S_X(j+1) over P_X(j), after P_X(j) V (same thread, in-order pipe)
+              if (x == 0 && !(ok = mbar_wait(&bars->kv_full[(vc + 1) % NKV], ((vc + 1) / NKV) & 1)))
+                break;
+              tc_fence_after();
+              issue_s(x, qs, vc + 1);
+              ATTN_TL(32 + x, k + 1);
             }
-            // S_X(j+1) over P_X(j), after P_X(j) V (same thread, in-order pipe)
-            if (x == 0 && !(ok = mbar_wait(&bars->kv_full[(vc + 1) % NKV], ((vc + 1) / NKV) & 1)))
-              break;
-            tc_fence_after();
-            issue_s(x, qs, vc + 1);
-            ATTN_TL(32 + x, k + 1);
+            if (!ok) break;
+            mma_commit(&bars->kv_empty[vc % NKV]);  // V(j) read by both P V
+            if (more) mma_commit(&bars->kv_empty[(vc + 1) % NKV]);  // K(j+1) by both S
+            kvc += more ? 2 : 1;
           }
           if (!ok) break;
-          mma_commit(&bars->kv_empty[vc % NKV]);  // V(j) read by both P V
-          if (more) mma_commit(&bars->kv_empty[(vc + 1) % NKV]);  // K(j+1) by both S
-          kvc += more ? 2 : 1;
+          mma_commit(&bars->q_empty[qs]);  // every S of this item done once these land
+          st += w.n;
+          ++it;
         }
-        if (!ok) break;
-        mma_commit(&bars->q_empty[qs]);  // every S of this item done once these land
-        st += w.n;
-        ++it;
+        if (!ok) {
+          report_timeout(a, 0x620);
+          *abort_flag = 1;
+        }
+        mma_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, 200000000ull);
       }
-      if (!ok) {
-        report_timeout(a, 0x620);
-        *abort_flag = 1;
-      }
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 200000000ull);
-    }
     }  // warps 2 and 3 have no role
   } else {
     regs_raise<200>();
