@@ -42,6 +42,8 @@ What it computes (all in float64 on bf16-valued inputs):
   Changes 3-4); gradients of a KV head sum over the query heads that share it
   (maxdiffusion PR #485, Summary: dK/dV held across Q blocks and GQA heads);
   the bias gradient is reduced over its broadcast axes (PR #3516, Change 6).
+* Optionally the max-logit output: per batch row and query head, the largest
+  S_ij over valid pairs (``max_logit``; reading stated there).
 
 Rows are processed one block of queries at a time and each block only touches
 the keys that are valid for at least one of its rows; since every softmax row is
@@ -237,6 +239,37 @@ def attention_forward(q, k, v, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=N
                 fin = np.isfinite(m)
                 lse[b, h, r0:r1][fin] = m[fin] + np.log(l[fin])
     return o, lse
+
+
+def max_logit(q, k, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=None, row_block=256):
+    """[B, Hq]: for each batch row and query head the largest S_ij over valid
+    (i, j) pairs, in natural units (-inf where no pair is valid).
+
+    TransformerEngine PR #3516 ("[JAX] Align fused attn backward output
+    gradient sharding and other test strengthening", Description, item 5.1)
+    names max-logit runner cases without defining the output; the reading
+    here is the plainest one: the maximum of the same post-scale, post-bias
+    logits S_ij that the softmax normalises, taken per (batch row, query
+    head) over the pairs the mask keeps."""
+    B, Sq, Hq, _ = q.shape
+    Hkv = k.shape[2]
+    group = Hq // Hkv
+    out = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        mask = valid_pairs(id_q[b], pos_q[b], id_kv[b], pos_kv[b], causal)
+        for h in range(Hq):
+            g = h // group
+            for r0 in range(0, Sq, row_block):
+                r1 = min(Sq, r0 + row_block)
+                br = None
+                if bias is not None:
+                    bi, hi = _bias_index(bias.shape, b, h)
+                    br = bias[bi, hi, r0:r1]
+                cols, _, _, m, _ = _rows_softmax(q[b, r0:r1, h], k[b, :, g], mask[r0:r1],
+                                                 scale, br)
+                if cols.size:
+                    out[b, h] = max(out[b, h], float(m.max()))
+    return out
 
 
 def attention_backward(q, k, v, do, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=None,

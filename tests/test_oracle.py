@@ -465,6 +465,78 @@ def test_layout_checks():
                         2, 2, 4, 2)
 
 
+# ----------------------------------------------------------------- max-logit
+
+
+def brute_max_logit(q, k, idq, posq, idk, posk, causal, scale, bias=None):
+    """Pure-Python loops: largest valid S_ij per (b, h)."""
+    B, Sq, Hq, Dk = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    out = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            bb = b if (bias is not None and bias.shape[0] > 1) else 0
+            bh = h if (bias is not None and bias.shape[1] > 1) else 0
+            for i in range(Sq):
+                for j in range(Skv):
+                    ok = idq[b, i] == idk[b, j] and idq[b, i] != 0
+                    if causal:
+                        ok = ok and posk[b, j] <= posq[b, i]
+                    if not ok:
+                        continue
+                    acc = sum(q[b, i, h, c] * k[b, j, g, c] for c in range(Dk)) * scale
+                    if bias is not None:
+                        acc += bias[bb, bh, i, j]
+                    out[b, h] = max(out[b, h], acc)
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("cross", [False, True])
+def test_max_logit_brute_force(rng, causal, cross):
+    q, k, v, do, idq, posq, idk, posk, causal, scale, bias = small_problem(
+        rng, causal=causal, cross=cross, S=9, Skv=12 if cross else None,
+        bias_shape=(2, 1, 9, 12 if cross else 9))
+    got = R.max_logit(q, k, idq, posq, idk, posk, causal, scale, bias, row_block=4)
+    ref = brute_max_logit(q, k, idq, posq, idk, posk, causal, scale, bias)
+    assert_same(got, ref, tol=1e-12)
+
+
+def test_max_logit_single_key_rows_and_lse_bounds(rng):
+    """With one valid key per row, LSE_i is that key's logit, so the max-logit
+    is the largest LSE; in general max_i (LSE_i - ln n_i) <= max-logit <=
+    max_i LSE_i, n_i the row's number of valid keys (the forward's LSE)."""
+    B, S, Hq, Hkv, D = 2, 7, 4, 2, 5
+    q, k = rand(rng, B, S, Hq, D), rand(rng, B, S, Hkv, D)
+    v = rand(rng, B, S, Hkv, 3)
+    ids, pos = seg_meta([[1] * 6, [1] * 4], S)  # segments of one token, then padding
+    ml = R.max_logit(q, k, ids, pos, ids, pos, True, 0.8)
+    _, lse = R.attention_forward(q, k, v, ids, pos, ids, pos, True, 0.8)
+    np.testing.assert_allclose(ml, lse.max(axis=2), rtol=0, atol=1e-12)
+    q, k, v, do, idq, posq, idk, posk, causal, scale, bias = small_problem(rng, cross=True,
+                                                                           Skv=13)
+    ml = R.max_logit(q, k, idq, posq, idk, posk, causal, scale, bias)
+    _, lse = R.attention_forward(q, k, v, idq, posq, idk, posk, causal, scale, bias)
+    for b in range(q.shape[0]):
+        n = R.valid_pairs(idq[b], posq[b], idk[b], posk[b], causal).sum(axis=1)
+        has = n > 0
+        for h in range(q.shape[2]):
+            lo = np.max(lse[b, h, has] - np.log(n[has]))
+            hi = np.max(lse[b, h, has])
+            assert lo - 1e-12 <= ml[b, h] <= hi + 1e-12
+
+
+def test_max_logit_planted_mistake_caught(rng):
+    """Keeping only the last row block's maximum disagrees with the loops."""
+    prob = small_problem(rng, S=11, bias_shape=(1, 4, 11, 11))
+    q, k, v, do, idq, posq, idk, posk, causal, scale, bias = prob
+    ref = brute_max_logit(q, k, idq, posq, idk, posk, causal, scale, bias)
+    bad = _mutant("out[b, h] = max(out[b, h], float(m.max()))", "out[b, h] = float(m.max())")
+    got = bad.max_logit(q, k, idq, posq, idk, posk, causal, scale, bias, row_block=4)
+    assert not np.allclose(got, ref)
+
+
 # ----------------------------------------------------------------- planted mistakes
 
 MUTATIONS = [
