@@ -13,7 +13,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_sm103.so")
 
-ATTN_PARAMS_VERSION = 2
+ATTN_PARAMS_VERSION = 3
 
 LAYOUTS = {"3HD": 0, "HD_2HD": 1, "HD_HD_HD": 2}
 FORMATS = {"BSHD": 0, "THD_SEGMENTS": 1, "THD_CU_SEQLENS": 2}
@@ -48,6 +48,7 @@ class attn_params_t(ctypes.Structure):
         ("bias", c_vp), ("bias_b", c_i32), ("bias_h", c_i32),
         ("force_general_path", c_i32),
         ("metadata_from_forward", c_i32),
+        ("max_logit", c_vp),
     ]
 
 
@@ -129,8 +130,9 @@ def _stream(stream):
 def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, k=None, v=None,
                 q_seg_ids=None, q_seg_pos=None, kv_seg_ids=None, kv_seg_pos=None,
                 cu_seqlens_q=None, cu_seqlens_kv=None, bias=None, dq_mode="deterministic",
-                force_general_path=False, metadata_from_forward=False):
-    """Fill an ``attn_params_t`` from tensors (any object with data_ptr/shape)."""
+                force_general_path=False, metadata_from_forward=False, max_logit=None):
+    """Fill an ``attn_params_t`` from tensors (any object with data_ptr/shape).
+    max_logit: optional fp32 [B, Hq] tensor the forward fills (see attn.h)."""
     p = attn_params_t()
     p.struct_version = ATTN_PARAMS_VERSION
     p.fmt = FORMATS[fmt]
@@ -161,6 +163,7 @@ def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, 
         p.bias_b, p.bias_h = int(bias.shape[0]), int(bias.shape[1])
     p.force_general_path = 1 if force_general_path else 0
     p.metadata_from_forward = 1 if metadata_from_forward else 0
+    p.max_logit = _ptr(max_logit)
     return p
 
 

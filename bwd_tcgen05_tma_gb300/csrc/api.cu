@@ -402,6 +402,7 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
   if (s != ATTN_OK) return s;
   if (!o || !lse || !ws || !aligned16(o) || (reinterpret_cast<uintptr_t>(ws) % kAlign))
     return ATTN_ERR_INVALID_ARG;
+  if (p->max_logit && (reinterpret_cast<uintptr_t>(p->max_logit) & 3u)) return ATTN_ERR_INVALID_ARG;
   const Plan pl = make_plan(p);
   if (ws_bytes < pl.fwd_total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   attn_resolved_t r;
@@ -419,6 +420,7 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
     return ATTN_ERR_CUDA;
   a.o = static_cast<bf16*>(o);
   a.lse = lse;
+  a.max_logit = p->max_logit;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
   trace(ATTN_TRACE_FWD, false, st);
   if (launch_fwd(a, sm_count(), st) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -119,6 +119,7 @@ struct KernelArgs {
   const int2* meta_scan;      // [2][B][chunks of 1024] first/last run boundary per chunk
   const int2* q_tile_range;   // [B*n_qt]  KV token range of each 128-row query tile
   const int2* kv_tile_range;  // [B*n_kt]  query token range of each 128-row KV tile
+  float* max_logit;  // forward only: fp32 [B, Hq] or null
   WsHeader* hdr;
 
   // bias
@@ -232,6 +233,25 @@ __device__ __forceinline__ void kv_valid_bits(const KernelArgs& a, bool general,
 
 __device__ __forceinline__ bool path_general(const KernelArgs& a) {
   return *reinterpret_cast<const volatile int32_t*>(&a.hdr->path) != 0;
+}
+
+// Largest of the value held at p and v, for any fp32 values including -inf
+// (non-negative values order like signed integers, negative ones reversed
+// like unsigned integers).
+__device__ __forceinline__ void atomic_max_f32(float* p, float v) {
+  if (v >= 0.f)
+    atomicMax(reinterpret_cast<int*>(p), __float_as_int(v));
+  else
+    atomicMin(reinterpret_cast<unsigned int*>(p), __float_as_uint(v));
+}
+
+// Max-logit of one warp's rows (row_max in log2 units of scaled logits,
+// -inf for rows without a valid key) folded into out[b * Hq + h].
+__device__ __forceinline__ void warp_max_logit(float* out, float row_max_log2) {
+  float v = row_max_log2;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0 && v > -INFINITY) atomic_max_f32(out, v * 0.6931471805599453f);
 }
 
 // Records a timed-out wait; the first one (by arrival) keeps its location.

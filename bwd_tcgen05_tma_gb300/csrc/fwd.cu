@@ -325,6 +325,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         bias_row = a.bias + (((int64_t)bb * a.bias_h + bh) * a.Sq + i) * a.Skv;
       }
       float m_ref = -INFINITY, l = 0.f;
+      float row_max = -INFINITY;  // exact row max of the scaled logits (log2 units)
       for (int j = 0; j < w.n; ++j) {
         const uint32_t k = kt + j;
         const int sb = k & 1;
@@ -368,6 +369,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         for (int c = 8; c < kTile; c += 2) mx8[(c >> 1) & 7] = fmax3(mx8[(c >> 1) & 7], x[c], x[c + 1]);
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        row_max = fmaxf(row_max, mx);
         const float m_new = fmaxf(m_ref, mx);
         const bool grow_max = m_new > m_ref + kRescaleThreshold;
         const bool rescale = grow_max && j > 0 && m_ref > -INFINITY;
@@ -445,6 +447,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         }
       }
       if (row_ok) *lse_out = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      if (a.max_logit) warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + w.h, row_max);
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
       kt += w.n;

@@ -374,6 +374,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         bias_row = a.bias + (((int64_t)bb * a.bias_h + bh) * a.Sq + i) * a.Skv;
       }
       float m_ref = -INFINITY, l = 0.f;
+      float row_max = -INFINITY;  // exact row max of the scaled logits (log2 units)
       for (int j = 0; j < w.n; ++j) {
         const uint32_t k = st + j;
         const int k0 = w.kv_lo + j * kTile;
@@ -414,6 +415,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
                          fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         if (!HAS_BIAS) mx *= a.scale_log2;  // scale > 0 keeps the order
         if (lane == 0 && (warp & 3) == 0) ATTN_TL(36 + x, k);
+        row_max = fmaxf(row_max, mx);
         const float m_new = fmaxf(m_ref, mx);
         const bool grow_max = m_new > m_ref + kRescaleThreshold;
         const bool rescale = grow_max && j > 0 && m_ref > -INFINITY;
@@ -480,6 +482,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         }
       }
       if (row_ok) *lse_out = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      if (a.max_logit) warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + h, row_max);
       tc_fence_before();
       mbar_arrive(&bars->o_empty[x]);
       st += w.n;

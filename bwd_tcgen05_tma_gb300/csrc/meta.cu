@@ -425,6 +425,11 @@ __device__ void meta_ranges(const KernelArgs& a, const MetaIn& in) {
 __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const KernelArgs a, const MetaIn in) {
   __shared__ MetaShared sm;
   sm103::grid_dep_launch();  // the forward may be scheduled now; it waits for this grid to finish
+  if (a.max_logit) {  // the forward folds its row maxima into these
+    const int n = a.B * a.Hq;
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < n; t += gridDim.x * blockDim.x)
+      a.max_logit[t] = -INFINITY;
+  }
   int2* bounds = const_cast<int2*>(a.meta_scan);
   const int units = in.nblk * a.B * 2;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define ATTN_PARAMS_VERSION 2
+#define ATTN_PARAMS_VERSION 3
 
 typedef enum {
   ATTN_OK = 0,
@@ -136,6 +136,14 @@ typedef struct {
    * (one metadata pass per training step instead of two).  Zero: attn_bwd
    * recomputes it.  attn_fwd ignores the field. */
   int32_t metadata_from_forward;
+  /* Forward only, optional (NULL: not computed).  fp32 [B, Hq], written by
+   * attn_fwd: for each batch row and query head the largest logit
+   * S_ij = scale * Q_i.K_j + bias_ij over the (i, j) pairs the mask keeps, in
+   * natural units; -inf where no pair is kept.  4-byte aligned.  (Max-logit
+   * cases of TransformerEngine PR #3516, Description item 5.1; the page does
+   * not define the output, this is the plainest reading.)  attn_bwd ignores
+   * the field. */
+  float* max_logit;
 } attn_params_t;
 
 /* Which metadata path the device chose (read back by attn_read_status). */

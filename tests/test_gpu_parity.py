@@ -293,3 +293,32 @@ def test_many_rows_match_single_row_calls(force_general):
         assert torch.equal(lse[b], l1[0]), b
         for k in g1:
             assert torch.equal(g[k][b].view(torch.int16), g1[k][0].view(torch.int16)), (k, b)
+
+
+@pytest.mark.parametrize("name", ["tiny", "thd_gqa_3hd", "cross_bias_192", "bshd_causal_ragged",
+                                  "qk192_v64"])
+def test_max_logit_matches_oracle(name):
+    """The optional max-logit output of the forward against the oracle's; the
+    forward's other outputs are unchanged by requesting it."""
+    from conftest import oracle_metadata, oracle_qkv
+    from gpu_util import DevCase
+    from oracle import attn_ref as R
+
+    case = CASES[name]()
+    d = DevCase(case)
+    o0, l0 = d.forward()
+    o0, l0 = o0.clone(), l0.clone()
+    ml = torch.full((case.B, case.Hq), 123.0, dtype=torch.float32, device="cuda")
+    d.params.max_logit = ml.data_ptr()
+    o1, l1 = d.forward()
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
+    assert torch.equal(l0, l1)
+    q, k, _ = oracle_qkv(case)
+    qi, qp, ki, kp = oracle_metadata(case)
+    bias = None if case.bias is None else case.bias.astype(np.float64)
+    ref = R.max_logit(q, k, qi, qp, ki, kp, case.causal, case.scale, bias)
+    got = ml.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isfinite(got), np.isfinite(ref))
+    fin = np.isfinite(ref)
+    np.testing.assert_allclose(got[fin], ref[fin], rtol=1e-4, atol=1e-4)
+    assert np.all(got[~fin] == -np.inf)
