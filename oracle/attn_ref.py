@@ -44,6 +44,9 @@ What it computes (all in float64 on bf16-valued inputs):
   the bias gradient is reduced over its broadcast axes (PR #3516, Change 6).
 * Optionally the max-logit output: per batch row and query head, the largest
   S_ij over valid pairs (``max_logit``; reading stated there).
+* Optionally per-head sink logits that join every softmax row as a column
+  without a value vector, and their gradient (``attention_forward``,
+  ``sink_gradient``; reading stated there).
 
 Rows are processed one block of queries at a time and each block only touches
 the keys that are valid for at least one of its rows; since every softmax row is
@@ -192,30 +195,45 @@ def _bias_index(bias_shape, b, h):
     return (b if bb > 1 else 0), (h if bh > 1 else 0)
 
 
-def _rows_softmax(q_rows, k_b, mask_rows, scale, bias_rows):
+def _rows_softmax(q_rows, k_b, mask_rows, scale, bias_rows, sink=None):
     """Scores and probabilities of a block of query rows over the keys valid
-    for at least one of them.  Returns (cols, S, P, m, l)."""
+    for at least one of them.  Returns (cols, S, P, m, l).  With a sink logit
+    (a float), every row's softmax runs over its valid logits and the sink:
+    m and l include the sink, whose own probability is exp(sink - m) / l."""
     cols = np.nonzero(mask_rows.any(axis=0))[0]
     R = q_rows.shape[0]
     if cols.size == 0:
+        if sink is not None and np.isfinite(sink):
+            return cols, np.zeros((R, 0)), np.zeros((R, 0)), np.full(R, float(sink)), np.ones(R)
         return cols, np.zeros((R, 0)), np.zeros((R, 0)), np.full(R, -np.inf), np.zeros(R)
     s = scale * (q_rows @ k_b[cols].T)
     if bias_rows is not None:
         s = s + bias_rows[:, cols]
     s = np.where(mask_rows[:, cols], s, -np.inf)
     m = s.max(axis=1)
+    if sink is not None:
+        m = np.maximum(m, sink)
     finite = np.isfinite(m)
     e = np.zeros_like(s)
     e[finite] = np.exp(s[finite] - m[finite, None])
     l = e.sum(axis=1)
+    if sink is not None:
+        l[finite] += np.exp(sink - m[finite])
     p = np.zeros_like(e)
     p[finite] = e[finite] / l[finite, None]
     return cols, s, p, m, l
 
 
 def attention_forward(q, k, v, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=None,
-                      row_block=256):
-    """O [B,Sq,Hq,d_v] and LSE [B,Hq,Sq] (natural log) by the definition above."""
+                      row_block=256, sink=None):
+    """O [B,Sq,Hq,d_v] and LSE [B,Hq,Sq] (natural log) by the definition above.
+
+    sink: optional [Hq] per-head logits that join every row's softmax as one
+    more column with no value vector (the sink attention of TransformerEngine
+    PR #2225, which PR #2358 "[JAX] Make all jax attention calls use
+    non-packed common calls" links without defining it; the reading is the
+    usual one: the sink only enlarges the normaliser).  A row without valid
+    keys then has O = 0 and LSE = sink."""
     B, Sq, Hq, _ = q.shape
     _, Skv, Hkv, d_v = v.shape
     group = Hq // Hkv
@@ -231,13 +249,14 @@ def attention_forward(q, k, v, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=N
                 if bias is not None:
                     bi, hi = _bias_index(bias.shape, b, h)
                     br = bias[bi, hi, r0:r1]
+                sk = None if sink is None else float(sink[h])
                 cols, _, p, m, l = _rows_softmax(q[b, r0:r1, h], k[b, :, g], mask[r0:r1],
-                                                 scale, br)
+                                                 scale, br, sk)
+                fin = np.isfinite(m)
+                lse[b, h, r0:r1][fin] = m[fin] + np.log(l[fin])
                 if cols.size == 0:
                     continue
                 o[b, r0:r1, h] = p @ v[b, cols, g]
-                fin = np.isfinite(m)
-                lse[b, h, r0:r1][fin] = m[fin] + np.log(l[fin])
     return o, lse
 
 
@@ -273,8 +292,10 @@ def max_logit(q, k, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=None, row_bl
 
 
 def attention_backward(q, k, v, do, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=None,
-                       row_block=256):
+                       row_block=256, sink=None):
     """Closed-form gradients (dQ, dK, dV, dBias or None) for the incoming dO.
+    With sink logits the probabilities include the sink column (see
+    attention_forward); its gradient is sink_gradient().
 
     The probabilities are recomputed here from Q, K, V (and bias), so the
     backward depends on nothing but the definition.  dBias has the shape of the
@@ -296,8 +317,9 @@ def attention_backward(q, k, v, do, id_q, pos_q, id_kv, pos_kv, causal, scale, b
                 if bias is not None:
                     bi, hi = _bias_index(bias.shape, b, h)
                     br = bias[bi, hi, r0:r1]
+                sk = None if sink is None else float(sink[h])
                 cols, _, p, _, _ = _rows_softmax(q[b, r0:r1, h], k[b, :, g], mask[r0:r1],
-                                                 scale, br)
+                                                 scale, br, sk)
                 if cols.size == 0:
                     continue
                 do_r = do[b, r0:r1, h]
@@ -310,6 +332,39 @@ def attention_backward(q, k, v, do, id_q, pos_q, id_kv, pos_kv, causal, scale, b
                 if dbias is not None:
                     dbias[bi, hi, r0:r1][:, cols] += ds
     return dq, dk, dv, dbias
+
+
+def sink_gradient(q, k, v, do, id_q, pos_q, id_kv, pos_kv, causal, scale, sink, bias=None,
+                  row_block=256):
+    """[Hq]: derivative of sum(dO * O) with respect to each head's sink logit.
+    The sink column has no value vector, so dP there is 0 and its dS is
+    -P_sink,i D_i with D_i = sum_j P_ij dP_ij; summed over batch rows and query
+    rows: dsink_h = -sum_{b,i} P_sink,i D_i."""
+    B, Sq, Hq, _ = q.shape
+    Hkv = v.shape[2]
+    group = Hq // Hkv
+    out = np.zeros(Hq)
+    for b in range(B):
+        mask = valid_pairs(id_q[b], pos_q[b], id_kv[b], pos_kv[b], causal)
+        for h in range(Hq):
+            g = h // group
+            for r0 in range(0, Sq, row_block):
+                r1 = min(Sq, r0 + row_block)
+                br = None
+                if bias is not None:
+                    bi, hi = _bias_index(bias.shape, b, h)
+                    br = bias[bi, hi, r0:r1]
+                cols, _, p, m, l = _rows_softmax(q[b, r0:r1, h], k[b, :, g], mask[r0:r1],
+                                                 scale, br, float(sink[h]))
+                if cols.size == 0:
+                    continue
+                dp = do[b, r0:r1, h] @ v[b, cols, g].T
+                D = (p * dp).sum(axis=1)
+                fin = np.isfinite(m)
+                p_sink = np.zeros(r1 - r0)
+                p_sink[fin] = np.exp(sink[h] - m[fin]) / l[fin]
+                out[h] -= float((p_sink * D).sum())
+    return out
 
 
 # --------------------------------------------------------------------------

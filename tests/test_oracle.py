@@ -37,9 +37,10 @@ def seg_meta(lens_per_row, S):
     return ids, pos
 
 
-def brute_force(q, k, v, do, idq, posq, idk, posk, causal, scale, bias=None):
+def brute_force(q, k, v, do, idq, posq, idk, posk, causal, scale, bias=None, sink=None):
     """Pure-Python scalar loops (no BLAS).  D is taken as the row sum of
-    dO * O, the other form of the identity the oracle's D uses."""
+    dO * O, the other form of the identity the oracle's D uses.  With sink
+    logits each row's normaliser also holds exp(sink_h - m)."""
     B, Sq, Hq, Dk = q.shape
     _, Skv, Hkv, Dv = v.shape
     grp = Hq // Hkv
@@ -71,10 +72,12 @@ def brute_force(q, k, v, do, idq, posq, idk, posk, causal, scale, bias=None):
                         valid.append(j)
                         s.append(acc)
                 if not valid:
+                    if sink is not None:
+                        lse[b, h, i] = sink[h]
                     continue
-                m = max(s)
+                m = max(s) if sink is None else max(max(s), sink[h])
                 e = [math.exp(x - m) for x in s]
-                l = sum(e)
+                l = sum(e) + (0.0 if sink is None else math.exp(sink[h] - m))
                 p = [x / l for x in e]
                 lse[b, h, i] = m + math.log(l)
                 for c in range(Dv):
@@ -465,6 +468,66 @@ def test_layout_checks():
                         2, 2, 4, 2)
 
 
+# ----------------------------------------------------------------- sink attention
+
+
+@pytest.mark.parametrize("cross", [False, True])
+def test_sink_brute_force(rng, cross):
+    prob = small_problem(rng, S=9, Skv=12 if cross else None, cross=cross,
+                         bias_shape=(1, 4, 9, 12 if cross else 9))
+    q, k, v, do, idq, posq, idk, posk, causal, scale, bias = prob
+    sink = rng.standard_normal(q.shape[2]) * 2.0
+    o, lse = R.attention_forward(q, k, v, idq, posq, idk, posk, causal, scale, bias,
+                                 row_block=4, sink=sink)
+    dq, dk, dv, db = R.attention_backward(q, k, v, do, idq, posq, idk, posk, causal, scale,
+                                          bias, row_block=4, sink=sink)
+    ref = brute_force(q, k, v, do, idq, posq, idk, posk, causal, scale, bias, sink=sink)
+    for a, b in zip((o, lse, dq, dk, dv, db), ref):
+        assert_same(a, b, tol=1e-10)
+    # rows without valid keys: O = 0 and LSE = the sink
+    assert np.all(np.isfinite(lse))
+
+
+def test_sink_minus_infinity_is_no_sink(rng):
+    prob = small_problem(rng, S=9)
+    q, k, v, do, idq, posq, idk, posk, causal, scale, bias = prob
+    none = run_oracle(R, prob)
+    sink = np.full(q.shape[2], -np.inf)
+    o, lse = R.attention_forward(q, k, v, idq, posq, idk, posk, causal, scale, bias, sink=sink)
+    g = R.attention_backward(q, k, v, do, idq, posq, idk, posk, causal, scale, bias, sink=sink)
+    for a, b in zip((o, lse) + tuple(g), none):
+        assert_same(a, b, tol=1e-13)
+
+
+def test_sink_gradient_finite_differences_and_row_sums(rng):
+    """dsink against central differences of L = sum(dO * O); each row's key
+    probabilities plus the sink's sum to 1."""
+    prob = small_problem(rng, S=11, bias_shape=(1, 4, 11, 11))
+    q, k, v, do, idq, posq, idk, posk, causal, scale, bias = prob
+    sink = rng.standard_normal(q.shape[2])
+    ds = R.sink_gradient(q, k, v, do, idq, posq, idk, posk, causal, scale, sink, bias,
+                         row_block=3)
+
+    def loss(sk):
+        o, _ = R.attention_forward(q, k, v, idq, posq, idk, posk, causal, scale, bias, sink=sk)
+        return float((do * o).sum())
+
+    eps = 1e-6
+    for h in range(q.shape[2]):
+        sp, sm = sink.copy(), sink.copy()
+        sp[h] += eps
+        sm[h] -= eps
+        fd = (loss(sp) - loss(sm)) / (2 * eps)
+        assert abs(fd - ds[h]) <= 1e-6 * max(1.0, abs(fd)), (h, fd, ds[h])
+    b, h = 0, 1
+    mask = R.valid_pairs(idq[b], posq[b], idk[b], posk[b], causal)
+    cols, _, p, m, l = R._rows_softmax(q[b, :, h], k[b, :, h // 2], mask, scale,
+                                       bias[0, h], float(sink[h]))
+    has = mask.any(axis=1)
+    total = p.sum(axis=1) + np.exp(sink[h] - m) / l
+    np.testing.assert_allclose(total[has], 1.0, atol=1e-13)
+
+
 # ----------------------------------------------------------------- max-logit
 
 
@@ -577,3 +640,38 @@ def test_pins_catch_planted_mistake(old, new):
         except AssertionError:
             caught = True
     assert caught, f"mutation not caught: {new}"
+
+
+@pytest.mark.parametrize("old,new", [
+    ("out[h] -= float((p_sink * D).sum())", "out[h] += float((p_sink * D).sum())"),
+    ("l[finite] += np.exp(sink - m[finite])", "l[finite] += 0.0"),
+    ("m = np.maximum(m, sink)", "m = m"),
+])
+def test_sink_pins_catch_planted_mistake(old, new):
+    """A flipped sink-gradient sign, a normaliser without the sink, or a max
+    that ignores the sink each disagree with the loops or the differences."""
+    rng = np.random.default_rng(11)
+    prob = small_problem(rng, S=11, bias_shape=(1, 4, 11, 11))
+    q, k, v, do, idq, posq, idk, posk, causal, scale, bias = prob
+    sink = rng.standard_normal(q.shape[2]) + 3.0  # above most logits
+    bad = _mutant(old, new)
+    ref = brute_force(q, k, v, do, idq, posq, idk, posk, causal, scale, bias, sink=sink)
+    with np.errstate(all="ignore"):  # a mutant may divide by zero
+        o, lse = bad.attention_forward(q, k, v, idq, posq, idk, posk, causal, scale, bias,
+                                       sink=sink)
+        ds = bad.sink_gradient(q, k, v, do, idq, posq, idk, posk, causal, scale, sink, bias)
+    fwd_ok = np.allclose(o, ref[0], atol=1e-10) and np.allclose(lse, ref[1], atol=1e-10)
+
+    def loss(sk):
+        o2, _ = R.attention_forward(q, k, v, idq, posq, idk, posk, causal, scale, bias, sink=sk)
+        return float((do * o2).sum())
+
+    eps = 1e-6
+    fd = []
+    for h in range(q.shape[2]):
+        sp, sm = sink.copy(), sink.copy()
+        sp[h] += eps
+        sm[h] -= eps
+        fd.append((loss(sp) - loss(sm)) / (2 * eps))
+    grad_ok = np.allclose(ds, fd, atol=1e-6)
+    assert not (fwd_ok and grad_ok), f"mutation not caught: {new}"
