@@ -13,7 +13,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_sm103.so")
 
-ATTN_PARAMS_VERSION = 3
+ATTN_PARAMS_VERSION = 4
 
 LAYOUTS = {"3HD": 0, "HD_2HD": 1, "HD_HD_HD": 2}
 FORMATS = {"BSHD": 0, "THD_SEGMENTS": 1, "THD_CU_SEQLENS": 2}
@@ -49,6 +49,7 @@ class attn_params_t(ctypes.Structure):
         ("force_general_path", c_i32),
         ("metadata_from_forward", c_i32),
         ("max_logit", c_vp),
+        ("sink", c_vp), ("dsink", c_vp),
     ]
 
 
@@ -130,9 +131,12 @@ def _stream(stream):
 def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, k=None, v=None,
                 q_seg_ids=None, q_seg_pos=None, kv_seg_ids=None, kv_seg_pos=None,
                 cu_seqlens_q=None, cu_seqlens_kv=None, bias=None, dq_mode="deterministic",
-                force_general_path=False, metadata_from_forward=False, max_logit=None):
+                force_general_path=False, metadata_from_forward=False, max_logit=None,
+                sink=None, dsink=None):
     """Fill an ``attn_params_t`` from tensors (any object with data_ptr/shape).
-    max_logit: optional fp32 [B, Hq] tensor the forward fills (see attn.h)."""
+    max_logit: optional fp32 [B, Hq] tensor the forward fills; sink: optional
+    fp32 [Hq] sink logits; dsink: optional fp32 [Hq] tensor the backward fills
+    with their gradient (see attn.h)."""
     p = attn_params_t()
     p.struct_version = ATTN_PARAMS_VERSION
     p.fmt = FORMATS[fmt]
@@ -164,6 +168,8 @@ def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, 
     p.force_general_path = 1 if force_general_path else 0
     p.metadata_from_forward = 1 if metadata_from_forward else 0
     p.max_logit = _ptr(max_logit)
+    p.sink = _ptr(sink)
+    p.dsink = _ptr(dsink)
     return p
 
 

@@ -28,7 +28,7 @@ struct Plan {
   size_t hdr, q_id, q_pos, seg_lo, seg_hi, kv_id, kv_pos, kv_seg_lo, kv_seg_hi;
   size_t q_chunk, kv_chunk, q_range, kv_range, meta_scan;
   size_t fwd_total;
-  size_t lse2, dvec, dq_acc, dbias_acc;
+  size_t lse2, dvec, dq_acc, dbias_acc, sink_part;
   size_t bwd_total;
 };
 
@@ -67,6 +67,8 @@ Plan make_plan(const attn_params_t* p) {
   if (effective_atomic(p)) o = up(o + B * Sq * p->Hq * (size_t)p->d_qk * 4);
   pl.dbias_acc = o;
   if (dbias_needs_acc(p)) o = up(o + (size_t)p->bias_b * p->bias_h * Sq * Skv * 4);
+  pl.sink_part = o;  // per preprocess block and head: partial sink gradient
+  if (p->dsink) o = up(o + ((B * Sq + kPreTok - 1) / kPreTok) * (size_t)p->Hq * 4);
   pl.bwd_total = o;
   return pl;
 }
@@ -403,6 +405,7 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
   if (!o || !lse || !ws || !aligned16(o) || (reinterpret_cast<uintptr_t>(ws) % kAlign))
     return ATTN_ERR_INVALID_ARG;
   if (p->max_logit && (reinterpret_cast<uintptr_t>(p->max_logit) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (p->sink && (reinterpret_cast<uintptr_t>(p->sink) & 3u)) return ATTN_ERR_INVALID_ARG;
   const Plan pl = make_plan(p);
   if (ws_bytes < pl.fwd_total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   attn_resolved_t r;
@@ -421,6 +424,7 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
   a.o = static_cast<bf16*>(o);
   a.lse = lse;
   a.max_logit = p->max_logit;
+  a.sink = p->sink;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
   trace(ATTN_TRACE_FWD, false, st);
   if (launch_fwd(a, sm_count(), st) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -441,6 +445,10 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   if (p->layout == ATTN_LAYOUT_HD_HD_HD && (!dv || !aligned16(dv))) return ATTN_ERR_INVALID_ARG;
   if (dbias && !p->bias) return ATTN_ERR_INVALID_ARG;
   if (dbias && !aligned16(dbias)) return ATTN_ERR_INVALID_ARG;
+  if (p->dsink && !p->sink) return ATTN_ERR_INVALID_ARG;  // a gradient needs its logits
+  if ((p->sink && (reinterpret_cast<uintptr_t>(p->sink) & 3u)) ||
+      (p->dsink && (reinterpret_cast<uintptr_t>(p->dsink) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
   const Plan pl = make_plan(p);
   if (ws_bytes < pl.bwd_total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   attn_resolved_t r;
@@ -458,6 +466,9 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   a.lse_in = lse;
   a.lse2 = reinterpret_cast<float*>(w + pl.lse2);
   a.Dvec = reinterpret_cast<float*>(w + pl.dvec);
+  a.sink = p->sink;
+  a.dsink = p->dsink;
+  a.sink_part = p->dsink ? reinterpret_cast<float*>(w + pl.sink_part) : nullptr;
   const bool atomic = effective_atomic(p);
   a.dq_acc = atomic ? reinterpret_cast<float*>(w + pl.dq_acc) : nullptr;
   a.dq = static_cast<bf16*>(const_cast<void*>(r.dq));
@@ -476,6 +487,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   if (!p->metadata_from_forward && (s = run_meta(a, p, st)) != ATTN_OK) return s;
   trace(ATTN_TRACE_BWD_PRE, false, st);
   if (launch_bwd_pre(a, atomic ? 1 : 0, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (a.dsink && launch_sink_reduce(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
   trace(ATTN_TRACE_BWD_PRE, true, st);
   // dK/dV pass: 128-row query tiles (deterministic dQ mode, head dims <= 128),
   // otherwise 64-row query tiles

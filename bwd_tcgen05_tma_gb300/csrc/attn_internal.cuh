@@ -14,6 +14,7 @@ using bf16 = __nv_bfloat16;
 
 constexpr int kChunk = 64;   // granularity of the per-chunk metadata summaries
 constexpr int kTile = 128;   // query tile (forward, dQ pass) and KV tile (all kernels)
+constexpr int kPreTok = 8;   // tokens per block of the backward preprocess
 constexpr int kBwdQ = 64;    // query tile of the dK/dV pass
 
 // Workspace header (first 256 bytes of every workspace).
@@ -120,6 +121,9 @@ struct KernelArgs {
   const int2* q_tile_range;   // [B*n_qt]  KV token range of each 128-row query tile
   const int2* kv_tile_range;  // [B*n_kt]  query token range of each 128-row KV tile
   float* max_logit;  // forward only: fp32 [B, Hq] or null
+  const float* sink;  // fp32 [Hq] sink logits or null
+  float* dsink;       // backward only: fp32 [Hq] or null
+  float* sink_part;   // backward workspace: per preprocess block and head, partial dsink
   WsHeader* hdr;
 
   // bias
@@ -325,6 +329,7 @@ cudaError_t launch_fwd(const KernelArgs& a, int num_sms, cudaStream_t st);
 // Forward over pairs of query heads of one KV group (even group size, d <= 128).
 cudaError_t launch_fwd2t(const KernelArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st);
+cudaError_t launch_sink_reduce(const KernelArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic_dq, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_dq(const KernelArgs& a, int num_sms, cudaStream_t st);
 // dK/dV pass with 128-row query tiles (deterministic dQ mode, d_qk and d_v <= 128).

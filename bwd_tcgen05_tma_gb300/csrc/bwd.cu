@@ -43,7 +43,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 // bytes of O and of dO, read front to back.  Eight consecutive tokens per
 // block; their D and LSE values go out through shared memory so each head's
 // eight values are written as one 32-byte run of the [B, Hq, Sq] arrays.
-constexpr int kPreTok = 8;
 constexpr int kPreMaxH = 256;
 
 template <int DV>
@@ -91,21 +90,53 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const KernelArgs a, int dq
     }
   }
   __syncthreads();
-  for (int v = threadIdx.x; v < a.Hq * kPreTok; v += blockDim.x) {
+  // thread v handles head v / 8 and token v % 8 of this block; the eight
+  // tokens of a head are eight consecutive lanes (blockDim is a multiple of 8)
+  for (int v0 = 0; v0 < a.Hq * kPreTok; v0 += blockDim.x) {
+    const int v = v0 + threadIdx.x;
     const int h = v / kPreTok, j = v - h * kPreTok;
     const int64_t t = t0 + j;
-    if (t >= ntok) continue;
-    const int b = static_cast<int>(t / a.Sq), i = static_cast<int>(t - (int64_t)b * a.Sq);
-    const int64_t idx = ((int64_t)b * a.Hq + h) * a.Sq + i;
-    a.Dvec[idx] = dsm[j][h];
-    const float lse = a.lse_in[idx];
-    a.lse2[idx] = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+    float part = 0.f;  // this token's share of the sink gradient
+    if (v < a.Hq * kPreTok && t < ntok) {
+      const int b = static_cast<int>(t / a.Sq), i = static_cast<int>(t - (int64_t)b * a.Sq);
+      const int64_t idx = ((int64_t)b * a.Hq + h) * a.Sq + i;
+      const float D = dsm[j][h];
+      a.Dvec[idx] = D;
+      const float lse = a.lse_in[idx];
+      a.lse2[idx] = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+      // dsink_h = -sum_i P_sink,i D_i with P_sink,i = exp(sink_h - LSE_i)
+      if (a.dsink && lse > -INFINITY) part = -__expf(a.sink[h] - lse) * D;
+    }
+    if (a.dsink) {
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      part += __shfl_xor_sync(0xffffffffu, part, 4);
+      if (j == 0 && v < a.Hq * kPreTok) a.sink_part[(int64_t)blockIdx.x * a.Hq + h] = part;
+    }
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     a.hdr->dq_mode = dq_mode_used;
     // work counters of the dK/dV and dQ passes, which start after this kernel
     a.hdr->next_item[1] = a.hdr->next_item[2] = a.hdr->next_item[3] = 0;
   }
+}
+
+// =========================================================== sink gradient
+// dsink[h] = sum over the preprocess blocks of their partials, one block per
+// head, in a fixed order (strided per thread, then a fixed tree): the result
+// does not depend on scheduling.
+__global__ void __launch_bounds__(256) sink_reduce_kernel(const KernelArgs a, int nblocks) {
+  __shared__ float red[256];
+  const int h = blockIdx.x;
+  float acc = 0.f;
+  for (int k = threadIdx.x; k < nblocks; k += blockDim.x) acc += a.sink_part[(int64_t)k * a.Hq + h];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.dsink[h] = red[0];
 }
 
 // =========================================================== converts
@@ -1234,6 +1265,13 @@ cudaError_t launch_bwd_dq(const KernelArgs& a, int nsm, cudaStream_t st) {
 cudaError_t launch_dq_convert(const KernelArgs& a, cudaStream_t st) {
   const int64_t n = (int64_t)a.B * a.Sq * a.Hq * a.d_qk / 8;
   dq_convert_kernel<<<blocks_for(n, 256), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sink_reduce(const KernelArgs& a, cudaStream_t st) {
+  const int64_t ntok = (int64_t)a.B * a.Sq;
+  const int nblocks = static_cast<int>((ntok + kPreTok - 1) / kPreTok);
+  sink_reduce_kernel<<<a.Hq, 256, 0, st>>>(a, nblocks);
   return cudaGetLastError();
 }
 

@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
 #pragma unroll
           for (int c = 0; c < DV; c += 8)
             *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-          *lse_out = -INFINITY;
+          *lse_out = a.sink ? a.sink[h] : -INFINITY;  // only the sink, if any
         }
         continue;
       }
@@ -463,7 +463,17 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       // epilogue: O / l and LSE
       if (!(ok = mbar_wait_warp(&bars->o_full[x], it & 1))) break;
       tc_fence_after();
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      // the sink logit, if any, joins the normaliser (it has no value vector)
+      float l_fin = l, m_fin = m_ref, o_scale = 1.f;
+      if (a.sink) {
+        const float s2 = a.sink[h] * kLog2e;
+        if (s2 > -INFINITY) {
+          m_fin = fmaxf(m_ref, s2);
+          o_scale = ex2_approx(m_ref - m_fin);  // 0 for a row without valid keys
+          l_fin = l * o_scale + ex2_approx(s2 - m_fin);
+        }
+      }
+      const float inv_l = (l_fin > 0.f) ? o_scale / l_fin : 0.f;
 #pragma unroll
       for (int q = 0; q < DV / 32; ++q) {
         uint32_t u[32];
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           }
         }
       }
-      if (row_ok) *lse_out = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      if (row_ok) *lse_out = (l_fin > 0.f) ? (m_fin + __log2f(l_fin)) * kLn2 : -INFINITY;
       if (a.max_logit) warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + h, row_max);
       tc_fence_before();
       mbar_arrive(&bars->o_empty[x]);

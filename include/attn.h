@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define ATTN_PARAMS_VERSION 3
+#define ATTN_PARAMS_VERSION 4
 
 typedef enum {
   ATTN_OK = 0,
@@ -144,6 +144,17 @@ typedef struct {
    * not define the output, this is the plainest reading.)  attn_bwd ignores
    * the field. */
   float* max_logit;
+  /* Optional sink logits, fp32 [Hq] in natural units (NULL: none): each query
+   * head's sink joins every softmax row as one more logit that has no value
+   * vector, so it only enlarges the normaliser; a row without valid keys then
+   * gets O = 0 and LSE = its head's sink.  Read by attn_fwd and attn_bwd.
+   * (Sink attention of TransformerEngine PR #2225, linked from PR #2358
+   * without a definition; this is the usual reading.) */
+  const float* sink;
+  /* Backward only, optional (NULL: not computed; needs sink): fp32 [Hq], the
+   * gradient of the loss with respect to each sink logit, summed over batch
+   * rows and query rows in a fixed order (bit-reproducible). */
+  float* dsink;
 } attn_params_t;
 
 /* Which metadata path the device chose (read back by attn_read_status). */

@@ -322,3 +322,54 @@ def test_max_logit_matches_oracle(name):
     fin = np.isfinite(ref)
     np.testing.assert_allclose(got[fin], ref[fin], rtol=1e-4, atol=1e-4)
     assert np.all(got[~fin] == -np.inf)
+
+
+@pytest.mark.parametrize("name", ["tiny", "thd_gqa_3hd", "cross_bias_192"])
+def test_sink_attention_matches_oracle(name):
+    """Per-head sink logits: O, LSE (a row without valid keys gets its head's
+    sink), dQ/dK/dV/dBias, and the sink gradient against the oracle; the sink
+    gradient reproduces itself bit for bit."""
+    from conftest import oracle_metadata, oracle_qkv
+    from gpu_util import DevCase, check_backward, check_forward
+    from oracle import attn_ref as R
+
+    case = CASES[name]()
+    rng = np.random.default_rng(21)
+    sink_h = (rng.standard_normal(case.Hq) * 1.5 + 0.5).astype(np.float32)
+    sink = torch.from_numpy(sink_h).cuda()
+    dsink = torch.full((case.Hq,), float("nan"), dtype=torch.float32, device="cuda")
+    d = DevCase(case)
+    d.params.sink = sink.data_ptr()
+    d.params.dsink = dsink.data_ptr()
+    d.ws_bwd = torch.zeros(max(A_bwd_ws(d.params), 256), dtype=torch.uint8, device="cuda")
+
+    q, k, v = oracle_qkv(case)
+    qi, qp, ki, kp = oracle_metadata(case)
+    bias = None if case.bias is None else case.bias.astype(np.float64)
+    do = case.do.astype(np.float64)
+    s64 = sink_h.astype(np.float64)
+    o_r, lse_r = R.attention_forward(q, k, v, qi, qp, ki, kp, case.causal, case.scale, bias,
+                                     sink=s64)
+    dq_r, dk_r, dv_r, db_r = R.attention_backward(q, k, v, do, qi, qp, ki, kp, case.causal,
+                                                  case.scale, bias, sink=s64)
+    ds_r = R.sink_gradient(q, k, v, do, qi, qp, ki, kp, case.causal, case.scale, s64, bias)
+    ref = {"o": o_r, "lse": lse_r, "dq": dq_r, "dk": dk_r, "dv": dv_r, "dbias": db_r}
+
+    o, lse = d.forward()
+    check_forward(case, ref, o, lse)
+    g, db = d.backward()
+    check_backward(case, ref, g, db)
+    got = dsink.cpu().numpy().astype(np.float64)
+    # the sum of per-row terms may cancel: bound the error by their magnitudes
+    D = (do * o_r).sum(axis=3)  # [B, Sq, Hq]
+    mag = np.abs(np.exp(s64[None, :, None] - lse_r) * D.transpose(0, 2, 1)).sum(axis=(0, 2))
+    assert np.all(np.abs(got - ds_r) <= 1e-2 * mag + 1e-6), (got, ds_r, mag)
+    first = dsink.clone()
+    d.backward()
+    assert torch.equal(first, dsink)
+
+
+def A_bwd_ws(params):
+    from bwd_tcgen05_tma_gb300 import attn as A
+
+    return A.attn_bwd_workspace_size(params)
