@@ -341,7 +341,7 @@ def test_sink_attention_matches_oracle(name):
     d = DevCase(case)
     d.params.sink = sink.data_ptr()
     d.params.dsink = dsink.data_ptr()
-    d.ws_bwd = torch.zeros(max(A_bwd_ws(d.params), 256), dtype=torch.uint8, device="cuda")
+    d.ws_bwd = torch.zeros(max(_bwd_ws_size(d.params), 256), dtype=torch.uint8, device="cuda")
 
     q, k, v = oracle_qkv(case)
     qi, qp, ki, kp = oracle_metadata(case)
@@ -369,7 +369,7 @@ def test_sink_attention_matches_oracle(name):
     assert torch.equal(first, dsink)
 
 
-def A_bwd_ws(params):
+def _bwd_ws_size(params):
     from bwd_tcgen05_tma_gb300 import attn as A
 
     return A.attn_bwd_workspace_size(params)
