@@ -159,10 +159,20 @@ __global__ void dq_convert_kernel(const KernelArgs a) {
 }
 
 __global__ void dbias_convert_kernel(const KernelArgs a) {
+  // four elements per thread and step: one 16-byte load, one 8-byte store
+  // (both buffers are 16-byte aligned); the last n % 4 elements one by one
   const int64_t n = (int64_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
-  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n;
-       v += (int64_t)gridDim.x * blockDim.x)
-    a.dbias[v] = __float2bfloat16_rn(a.dbias_acc[v]);
+  const int64_t n4 = n / 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  for (int64_t v = t0; v < n4; v += stride) {
+    const float4 x = reinterpret_cast<const float4*>(a.dbias_acc)[v];
+    uint2 o;
+    o.x = pack_bf16x2(x.x, x.y);
+    o.y = pack_bf16x2(x.z, x.w);
+    reinterpret_cast<uint2*>(a.dbias)[v] = o;
+  }
+  for (int64_t v = 4 * n4 + t0; v < n; v += stride) a.dbias[v] = __float2bfloat16_rn(a.dbias_acc[v]);
 }
 
 // =========================================================== dK / dV pass
@@ -644,9 +654,18 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
                     if (q0 + c0h + c < a.Sq) dp[(int64_t)c * a.Skv] = __float2bfloat16_rn(x[c]);
                 } else {
                   float* dp = a.dbias_acc + (bias_base + q0 + c0h) * a.Skv + kj;
+                  // eight loads in flight before their stores (a store between
+                  // two loads would serialise them: the addresses may alias)
 #pragma unroll
-                  for (int c = 0; c < 32; ++c)
-                    if (q0 + c0h + c < a.Sq) dp[(int64_t)c * a.Skv] += x[c];
+                  for (int c8 = 0; c8 < 32; c8 += 8) {
+                    float acc[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                      acc[c] = (q0 + c0h + c8 + c < a.Sq) ? dp[(int64_t)(c8 + c) * a.Skv] : 0.f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                      if (q0 + c0h + c8 + c < a.Sq) dp[(int64_t)(c8 + c) * a.Skv] = acc[c] + x[c8 + c];
+                  }
                 }
               }
               mbar_arrive(&bars->qd_empty[stage]);

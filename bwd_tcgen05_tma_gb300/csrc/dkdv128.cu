@@ -557,9 +557,19 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                       if (qh + q * 32 + c < a.Sq) dpb[(int64_t)c * a.Skv] = __float2bfloat16_rn(ds[c]);
                   } else {
                     float* dpb = a.dbias_acc + (bias_base + qh + q * 32) * a.Skv + kj;
+                    // eight loads in flight before their stores (a store between
+                    // two loads would serialise them: the addresses may alias)
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                      if (qh + q * 32 + c < a.Sq) dpb[(int64_t)c * a.Skv] += ds[c];
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                      float acc[8];
+#pragma unroll
+                      for (int c = 0; c < 8; ++c)
+                        acc[c] = (qh + q * 32 + c8 + c < a.Sq) ? dpb[(int64_t)(c8 + c) * a.Skv] : 0.f;
+#pragma unroll
+                      for (int c = 0; c < 8; ++c)
+                        if (qh + q * 32 + c8 + c < a.Sq)
+                          dpb[(int64_t)(c8 + c) * a.Skv] = acc[c] + ds[c8 + c];
+                    }
                   }
                 }
               }
