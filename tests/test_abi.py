@@ -129,3 +129,54 @@ def test_fwd_rejects_before_launch(lib):
                      ctypes.c_size_t(A.attn_bwd_workspace_size(p)), None)
     assert s == 1  # dbias without a bias
     assert lib.attn_status_string(6) == b"device-side wait timed out"
+
+
+def _bwd(lib, p, dbias=None):
+    return lib.attn_bwd(ctypes.byref(p), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                        ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                        ctypes.c_void_p(FAKE), dbias, ctypes.c_void_p(FAKE * 4),
+                        ctypes.c_size_t(A.attn_bwd_workspace_size(p)), None)
+
+
+def test_params_version_checked(lib):
+    p = params()
+    p.struct_version = A.ATTN_PARAMS_VERSION - 1
+    r = A.attn_resolved_t()
+    assert lib.attn_resolve_layout(ctypes.byref(p), None, None, None, ctypes.byref(r)) == 1
+    assert lib.attn_abi_version() == A.ATTN_PARAMS_VERSION
+
+
+def test_max_logit_and_sink_arguments_checked(lib):
+    """Optional max-logit / sink / dsink pointers: misaligned ones and a sink
+    gradient without sink logits are rejected before any launch."""
+    p = params()
+    ws_need = A.attn_fwd_workspace_size(p)
+
+    def fwd():
+        return lib.attn_fwd(ctypes.byref(p), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                            ctypes.c_void_p(FAKE * 4), ctypes.c_size_t(ws_need), None)
+
+    p.max_logit = FAKE + 2
+    assert fwd() == 1
+    p.max_logit = None
+    p.sink = FAKE + 1
+    assert fwd() == 1
+    p.sink = None
+    p.dsink = FAKE
+    assert _bwd(lib, p) == 1  # a sink gradient needs sink logits
+    p.sink = FAKE + 2
+    assert _bwd(lib, p) == 1  # misaligned sink
+    p.sink = FAKE
+    p.dsink = FAKE + 6
+    assert _bwd(lib, p) == 1  # misaligned dsink
+
+
+def test_sink_gradient_workspace(lib):
+    """The sink gradient needs one partial per preprocess block (8 tokens) and
+    query head in the backward workspace."""
+    p = params()
+    base = A.attn_bwd_workspace_size(p)
+    p.sink, p.dsink = FAKE, FAKE
+    need = (2 * 256 + 7) // 8 * 8 * 4
+    assert A.attn_bwd_workspace_size(p) - base == (need + 255) // 256 * 256
+    assert A.attn_fwd_workspace_size(p) == A.attn_fwd_workspace_size(params())
