@@ -21,15 +21,20 @@
  *   dP_ij = dO_i . V_j,  D_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - D_i)
  *   dQ_i = scale sum_j dS_ij K_j;  dK_j = scale sum_{h in g} sum_i dS_ij Q_i
  *   dV_j = sum_{h in g} sum_i P_ij dO_i;  dBias = dS summed over broadcast axes
- * A query row with no valid key gets O = 0, LSE = -inf and dQ = 0; gradients
- * of keys no query attends to are exactly 0.
+ * A query row with no valid key gets O = 0, LSE = -inf (its head's sink
+ * logit when sink logits are given) and dQ = 0; gradients of keys no query
+ * attends to are exactly 0.
  *
  * Conventions.
  *  - Every tensor is caller-owned device memory (including the workspace).
- *    The library never allocates, frees or synchronises, except
- *    attn_read_status(), which synchronises the given stream.
- *  - All work is enqueued on the caller's stream (a cudaStream_t passed as
- *    void*; NULL is the legacy default stream).
+ *    The library never allocates device memory and never synchronises,
+ *    except attn_read_status(), which synchronises the given stream.  Its
+ *    only resources are one extra stream and two events per host thread and
+ *    device, made by the first deterministic backward with d_qk, d_v <= 128
+ *    outside stream capture (see attn_bwd).
+ *  - All work is ordered on the caller's stream (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream); work forked to the extra
+ *    stream is joined back before the call returns.
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call returns a status and launches nothing.  No call aborts.
  *  - Element type of Q/K/V/O/dO/bias and of all gradients: bf16.  LSE: fp32.
