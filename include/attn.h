@@ -31,7 +31,8 @@
  *    except attn_read_status(), which synchronises the given stream.  Its
  *    only resources are one extra stream and two events per host thread and
  *    device, made by the first deterministic backward with d_qk, d_v <= 128
- *    outside stream capture (see attn_bwd).
+ *    outside stream capture (see attn_bwd) and kept until the process
+ *    exits.
  *  - All work is ordered on the caller's stream (a cudaStream_t passed as
  *    void*; NULL is the legacy default stream); work forked to the extra
  *    stream is joined back before the call returns.
