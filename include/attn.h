@@ -59,7 +59,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,         /* null/misaligned pointer, bad enum, bad size */
-  ATTN_ERR_UNSUPPORTED = 2,         /* valid request this build does not implement */
+  ATTN_ERR_UNSUPPORTED = 2,         /* valid request the library does not implement */
   ATTN_ERR_SHAPE_MISMATCH = 3,      /* segment ids/pos (or Q/KV) shapes disagree */
   ATTN_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the *_workspace_size() value */
   ATTN_ERR_CUDA = 5,                /* a CUDA runtime call failed (launch, attribute) */
