@@ -293,8 +293,11 @@ AuxStream* aux_stream(cudaStream_t st) {
   if (x.s) return &x;
   if (x.failed) return nullptr;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
-    return nullptr;  // not made while capturing; a later uncaptured call makes it
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();  // leave no stale error for the launch checks that follow
+    return nullptr;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return nullptr;  // made by a later uncaptured call
   if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess) {
