@@ -44,6 +44,8 @@ What it computes (all in float64 on bf16-valued inputs):
   the bias gradient is reduced over its broadcast axes (PR #3516, Change 6).
 * Optionally the max-logit output: per batch row and query head, the largest
   S_ij over valid pairs (``max_logit``; reading stated there).
+* Optionally a band mask (``Window``: sliding windows, bottom-right causal
+  alignment) in place of the causal flag; reading stated there.
 * Optionally per-head sink logits that join every softmax row as a column
   without a value vector, and their gradient (``attention_forward``,
   ``sink_gradient``; reading stated there).
@@ -168,13 +170,43 @@ def dense_metadata(B, S):
     return np.ones((B, S), dtype=np.int64), np.tile(np.arange(S, dtype=np.int64), (B, 1))
 
 
+class Window:
+    """A band of key positions relative to each query position, usable
+    wherever a ``causal`` flag is taken: key j is kept when
+
+        -left <= pos_kv[j] - (pos_q[i] + shift) <= right
+
+    (None: unbounded on that side).  Window(None, 0) is the causal mask;
+    Window(w - 1, 0) a causal sliding window of w keys; ``shift`` = Skv - Sq
+    aligns a causal mask bottom-right for dense rows of unequal lengths.
+
+    The pages do not define windows or bottom-right alignment; this is the
+    usual reading, kept here so the "next" mask variants have a pinned
+    definition before any kernel implements them."""
+
+    def __init__(self, left=None, right=0, shift=0):
+        self.left, self.right, self.shift = left, right, shift
+
+    def keep(self, pos_q, pos_kv):
+        r = np.asarray(pos_kv)[None, :] - (np.asarray(pos_q)[:, None] + self.shift)
+        m = np.ones(r.shape, dtype=bool)
+        if self.left is not None:
+            m &= r >= -self.left
+        if self.right is not None:
+            m &= r <= self.right
+        return m
+
+
 def valid_pairs(id_q, pos_q, id_kv, pos_kv, causal):
     """Boolean [Sq, Skv] mask of one batch row: same nonzero segment and, when
-    causal, key position not after the query position."""
+    causal, key position not after the query position (``causal`` may also
+    be a Window)."""
     id_q = np.asarray(id_q)[:, None]
     id_kv = np.asarray(id_kv)[None, :]
     m = (id_q == id_kv) & (id_q != 0)
-    if causal:
+    if isinstance(causal, Window):
+        m &= causal.keep(pos_q, pos_kv)
+    elif causal:
         m &= np.asarray(pos_kv)[None, :] <= np.asarray(pos_q)[:, None]
     return m
 

@@ -60,7 +60,11 @@ def brute_force(q, k, v, do, idq, posq, idk, posk, causal, scale, bias=None, sin
                 s = []
                 for j in range(Skv):
                     ok = idq[b, i] == idk[b, j] and idq[b, i] != 0
-                    if causal:
+                    if isinstance(causal, tuple):  # (left, right, shift) band
+                        left, right, shift = causal
+                        rel = posk[b, j] - (posq[b, i] + shift)
+                        ok = ok and (left is None or rel >= -left) and (right is None or rel <= right)
+                    elif causal:
                         ok = ok and posk[b, j] <= posq[b, i]
                     if ok:
                         acc = 0.0
@@ -468,6 +472,50 @@ def test_layout_checks():
                         2, 2, 4, 2)
 
 
+# ----------------------------------------------------------------- band masks
+
+
+@pytest.mark.parametrize("band", [(3, 0, 0), (2, 1, 0), (None, 0, 2), (1, None, -1)])
+def test_window_brute_force(rng, band):
+    """Sliding windows, a two-sided band and shifted alignments against the
+    scalar loops (which test the band condition on their own)."""
+    prob = small_problem(rng, S=11, bias_shape=(1, 4, 11, 11))
+    q, k, v, do, idq, posq, idk, posk, _, scale, bias = prob
+    w = R.Window(*band)
+    o, lse = R.attention_forward(q, k, v, idq, posq, idk, posk, w, scale, bias, row_block=4)
+    g = R.attention_backward(q, k, v, do, idq, posq, idk, posk, w, scale, bias, row_block=4)
+    ref = brute_force(q, k, v, do, idq, posq, idk, posk, band, scale, bias)
+    for a, b in zip((o, lse) + tuple(g), ref):
+        assert_same(a, b, tol=1e-10)
+
+
+def test_window_limits_and_closed_forms(rng):
+    """Window(None, 0) is the causal mask and Window(None, None) no mask; a
+    zero-width window keeps only the diagonal, so O_i = V_i and LSE_i = S_ii;
+    bottom-right alignment of dense rows: the last query row sees every key."""
+    prob = small_problem(rng, S=11, with_bias=False)
+    q, k, v, do, idq, posq, idk, posk, _, scale, _ = prob
+    for w, flag in ((R.Window(None, 0), True), (R.Window(None, None), False)):
+        a = R.attention_forward(q, k, v, idq, posq, idk, posk, w, scale)
+        b = R.attention_forward(q, k, v, idq, posq, idk, posk, flag, scale)
+        for x, y in zip(a, b):
+            assert_same(x, y, tol=1e-13)
+    B, S, Hq, Hkv, D = 1, 6, 2, 2, 4
+    q, k, v = rand(rng, B, S, Hq, D), rand(rng, B, S, Hkv, D), rand(rng, B, S, Hkv, 3)
+    ids, pos = R.dense_metadata(B, S)
+    o, lse = R.attention_forward(q, k, v, ids, pos, ids, pos, R.Window(0, 0), 0.5)
+    np.testing.assert_allclose(o[0], v[0], atol=1e-13)
+    np.testing.assert_allclose(lse[0], 0.5 * np.einsum("shd,shd->hs", q[0], k[0]), atol=1e-13)
+    Sq, Skv = 3, 7
+    q, k, v = rand(rng, 1, Sq, 1, D), rand(rng, 1, Skv, 1, D), rand(rng, 1, Skv, 1, 3)
+    iq, pq = R.dense_metadata(1, Sq)
+    ik, pk = R.dense_metadata(1, Skv)
+    _, lse = R.attention_forward(q, k, v, iq, pq, ik, pk, R.Window(None, 0, Skv - Sq), 0.5)
+    s_last = 0.5 * k[0, :, 0] @ q[0, -1, 0]
+    assert abs(lse[0, 0, -1] - (s_last.max() + np.log(np.exp(s_last - s_last.max()).sum()))) < 1e-12
+    assert R.count_valid_pairs(iq, pq, ik, pk, R.Window(None, 0, Skv - Sq)) == 5 + 6 + 7
+
+
 # ----------------------------------------------------------------- sink attention
 
 
@@ -675,3 +723,25 @@ def test_sink_pins_catch_planted_mistake(old, new):
         fd.append((loss(sp) - loss(sm)) / (2 * eps))
     grad_ok = np.allclose(ds, fd, atol=1e-6)
     assert not (fwd_ok and grad_ok), f"mutation not caught: {new}"
+
+
+@pytest.mark.parametrize("old,new", [
+    ("m &= r >= -self.left", "m &= r > -self.left"),  # window one key short
+    ("r = np.asarray(pos_kv)[None, :] - (np.asarray(pos_q)[:, None] + self.shift)",
+     "r = np.asarray(pos_kv)[None, :] - (np.asarray(pos_q)[:, None] - self.shift)"),  # shift sign
+])
+def test_window_pins_catch_planted_mistake(old, new):
+    rng = np.random.default_rng(5)
+    prob = small_problem(rng, S=11, bias_shape=(1, 4, 11, 11))
+    q, k, v, do, idq, posq, idk, posk, _, scale, bias = prob
+    band = (3, 0, 1)
+    bad = _mutant(old, new)
+    o, lse = bad.attention_forward(q, k, v, idq, posq, idk, posk, bad.Window(*band), scale, bias)
+    ref = brute_force(q, k, v, do, idq, posq, idk, posk, band, scale, bias)
+    same = True
+    for a, b in zip((o, lse), ref[:2]):
+        try:
+            assert_same(a, b)
+        except AssertionError:
+            same = False
+    assert not same, f"mutation not caught: {new}"
