@@ -515,28 +515,36 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
       return ATTN_ERR_CUDA;
     sq = ax->s;
   }
+  // From here on the second stream is forked: every outcome, failed or not,
+  // leaves through the join below, so `st` always orders whatever reached
+  // the second stream and a stream capture never ends with an unjoined fork.
+  s = ATTN_OK;
   trace(ATTN_TRACE_DKDV, false, st);
   const cudaError_t ek = tile128 ? launch_bwd_dkdv128(a, nsm, st) : launch_bwd_dkdv(a, atomic, nsm, st);
-  if (ek != cudaSuccess) return ATTN_ERR_CUDA;
+  if (ek != cudaSuccess) s = ATTN_ERR_CUDA;
   trace(ATTN_TRACE_DKDV, true, st);
-  trace(ATTN_TRACE_DQ, false, sq);
-  if (atomic) {
-    if (launch_dq_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
-  } else {
-    if (!tile128 &&
-        (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
-         !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
-                   kTile)))
-      return ATTN_ERR_CUDA;
-    if ((tile128 ? launch_bwd_dq128(a, nsm, sq) : launch_bwd_dq(a, nsm, st)) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+  if (s == ATTN_OK) {
+    trace(ATTN_TRACE_DQ, false, sq);
+    if (atomic) {
+      if (launch_dq_convert(a, st) != cudaSuccess) s = ATTN_ERR_CUDA;
+    } else {
+      if (!tile128 &&
+          (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride,
+                     kTile) ||
+           !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq,
+                     (int64_t)p->Hq * p->d_v, kTile)))
+        s = ATTN_ERR_CUDA;
+      else if ((tile128 ? launch_bwd_dq128(a, nsm, sq) : launch_bwd_dq(a, nsm, st)) != cudaSuccess)
+        s = ATTN_ERR_CUDA;
+    }
+    trace(ATTN_TRACE_DQ, true, sq);
   }
-  trace(ATTN_TRACE_DQ, true, sq);
   if (ax) {
     if (cudaEventRecord(ax->join, sq) != cudaSuccess ||
         cudaStreamWaitEvent(st, ax->join, 0) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+      s = ATTN_ERR_CUDA;
   }
+  if (s != ATTN_OK) return s;
   if (a.dbias_mode == 2) {
     trace(ATTN_TRACE_DBIAS, false, st);
     if (launch_dbias_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -611,7 +619,9 @@ extern "C" attn_status_t attn_fwd_noalloc(const attn_params_t* p, void* o, float
   if (pl.fwd_total > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   if ((s = noalloc_scratch(&ws)) != ATTN_OK) return s;
-  // The header (status word, counters) is cleared by the metadata launch
-  // itself; every other scratch array is fully written before it is read.
+  // launch_meta zeroes the header (status word, work counters, grid-barrier
+  // count) with a cudaMemsetAsync on `stream` before the cooperative metadata
+  // kernel, which needs that count at zero when it starts; every other scratch
+  // array is fully written before it is read.
   return attn_fwd(p, o, lse, ws, kNoAllocScratchBytes, stream);
 }

@@ -110,26 +110,6 @@ def unpack_layout(layout, buffers, B, Sq, Skv, Hq, Hkv, d_qk, d_v):
     )
 
 
-def pack_grads(layout, dq, dk, dv):
-    """Pack gradients into the same token-major layout as the inputs
-    (the gradient of each packed slice lands where that slice was read)."""
-    B, Sq, Hq, d_qk = dq.shape
-    _, Skv, Hkv, d_v = dv.shape
-    if layout == "3HD":
-        return {
-            "dqkv": np.concatenate(
-                [dq.reshape(B * Sq, -1), dk.reshape(B * Skv, -1), dv.reshape(B * Skv, -1)],
-                axis=1,
-            )
-        }
-    if layout == "HD_2HD":
-        return {
-            "dq": dq.reshape(B * Sq, -1),
-            "dkv": np.concatenate([dk.reshape(B * Skv, -1), dv.reshape(B * Skv, -1)], axis=1),
-        }
-    return {"dq": dq, "dk": dk, "dv": dv}
-
-
 # --------------------------------------------------------------------------
 # Segment metadata
 # --------------------------------------------------------------------------
