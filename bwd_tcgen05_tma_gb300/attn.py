@@ -13,7 +13,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_sm103.so")
 
-ATTN_PARAMS_VERSION = 4
+ATTN_PARAMS_VERSION = 5
 
 LAYOUTS = {"3HD": 0, "HD_2HD": 1, "HD_HD_HD": 2}
 FORMATS = {"BSHD": 0, "THD_SEGMENTS": 1, "THD_CU_SEQLENS": 2}
@@ -50,6 +50,8 @@ class attn_params_t(ctypes.Structure):
         ("metadata_from_forward", c_i32),
         ("max_logit", c_vp),
         ("sink", c_vp), ("dsink", c_vp),
+        ("band", c_i32), ("window_left", c_i32), ("window_right", c_i32),
+        ("bottom_right", c_i32),
     ]
 
 
@@ -132,11 +134,12 @@ def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, 
                 q_seg_ids=None, q_seg_pos=None, kv_seg_ids=None, kv_seg_pos=None,
                 cu_seqlens_q=None, cu_seqlens_kv=None, bias=None, dq_mode="deterministic",
                 force_general_path=False, metadata_from_forward=False, max_logit=None,
-                sink=None, dsink=None):
+                sink=None, dsink=None, window=None, bottom_right=False):
     """Fill an ``attn_params_t`` from tensors (any object with data_ptr/shape).
     max_logit: optional fp32 [B, Hq] tensor the forward fills; sink: optional
     fp32 [Hq] sink logits; dsink: optional fp32 [Hq] tensor the backward fills
-    with their gradient (see attn.h)."""
+    with their gradient; window: optional (left, right) band, None for an
+    unbounded side; bottom_right: align positions by Skv - Sq (see attn.h)."""
     p = attn_params_t()
     p.struct_version = ATTN_PARAMS_VERSION
     p.fmt = FORMATS[fmt]
@@ -170,6 +173,12 @@ def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, 
     p.max_logit = _ptr(max_logit)
     p.sink = _ptr(sink)
     p.dsink = _ptr(dsink)
+    if window is not None:
+        left, right = window
+        p.band = 1
+        p.window_left = -1 if left is None else int(left)
+        p.window_right = -1 if right is None else int(right)
+    p.bottom_right = 1 if bottom_right else 0
     return p
 
 

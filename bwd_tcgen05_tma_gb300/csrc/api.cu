@@ -120,6 +120,8 @@ attn_status_t validate(const attn_params_t* p) {
       }
     }
   }
+  const bool causal = p->mask == ATTN_MASK_CAUSAL || p->mask == ATTN_MASK_PADDING_CAUSAL;
+  if (p->band && causal && p->window_right > 0) return ATTN_ERR_INVALID_ARG;
   if (p->bias) {
     if (!aligned16(p->bias)) return ATTN_ERR_INVALID_ARG;
     if (!(p->bias_b == 1 || p->bias_b == p->B) || !(p->bias_h == 1 || p->bias_h == p->Hq))
@@ -230,7 +232,10 @@ int sm_count() {
 void fill_common(KernelArgs& a, const attn_params_t* p, char* ws, const Plan& pl) {
   a.B = p->B; a.Sq = p->Sq; a.Skv = p->Skv; a.Hq = p->Hq; a.Hkv = p->Hkv;
   a.d_qk = p->d_qk; a.d_v = p->d_v;
-  a.causal = (p->mask == ATTN_MASK_CAUSAL || p->mask == ATTN_MASK_PADDING_CAUSAL) ? 1 : 0;
+  const bool causal = p->mask == ATTN_MASK_CAUSAL || p->mask == ATTN_MASK_PADDING_CAUSAL;
+  a.win_left = (p->band && p->window_left >= 0) ? p->window_left : -1;
+  a.win_right = causal ? 0 : ((p->band && p->window_right >= 0) ? p->window_right : -1);
+  a.shift = p->bottom_right ? p->Skv - p->Sq : 0;
   a.scale = p->scale;
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.n_qt = (p->Sq + kTile - 1) / kTile;

@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "sm103_ptx.cuh"
@@ -99,7 +100,10 @@ struct KernelArgs {
   CUtensorMap tm_dqacc;  // fp32 dQ accumulator: dims {d_qk, Hq, B*Sq}, box {32, 1, 64}
 
   int B, Sq, Skv, Hq, Hkv, d_qk, d_v;
-  int causal;
+  // Position mask: a key at position pk is kept for a query at position pq
+  // (same nonzero segment id) when -win_left <= pk - (pq + shift) <= win_right,
+  // a negative bound leaving that side open.  Causal: win_right = 0.
+  int win_left, win_right, shift;
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
   int n_qt;          // query tiles of 128 per row
@@ -185,9 +189,33 @@ __device__ __forceinline__ uint64_t range_bits64(int lo, int hi) {
 
 __device__ __forceinline__ bool path_general(const KernelArgs& a);
 
+// Key positions [x, y] (inclusive) that a query at position pq keeps.
+__device__ __forceinline__ int2 band_key_pos(const KernelArgs& a, int pq) {
+  const int c = pq + a.shift;
+  return make_int2(a.win_left < 0 ? INT_MIN : c - a.win_left,
+                   a.win_right < 0 ? INT_MAX : c + a.win_right);
+}
+// Query positions [x, y] (inclusive) that keep a key at position pk.
+__device__ __forceinline__ int2 band_query_pos(const KernelArgs& a, int pk) {
+  const int c = pk - a.shift;
+  return make_int2(a.win_right < 0 ? INT_MIN : c - a.win_right,
+                   a.win_left < 0 ? INT_MAX : c + a.win_left);
+}
+// Fast path (equal metadata on both sides, positions = offsets inside the
+// segment, shift 0, so pk - pq = j - i): the key tokens [x, y) of query token
+// i whose segment spans the tokens [sl, sh), and the query tokens of key j.
+__device__ __forceinline__ int2 band_keys_of_query(const KernelArgs& a, int i, int sl, int sh) {
+  return make_int2(a.win_left >= 0 ? max(sl, i - a.win_left) : sl,
+                   a.win_right >= 0 ? min(sh, i + a.win_right + 1) : sh);
+}
+__device__ __forceinline__ int2 band_queries_of_key(const KernelArgs& a, int j, int sl, int sh) {
+  return make_int2(a.win_right >= 0 ? max(sl, j - a.win_right) : sl,
+                   a.win_left >= 0 ? min(sh, j + a.win_left + 1) : sh);
+}
+
 // Validity of the 128 keys [k0, k0 + 128) of batch row b for one query row, as
 // two 64-bit masks.  Fast path: the row's key range [rlo, rhi).  General path:
-// same nonzero segment id and, if causal, key position <= query position.
+// same nonzero segment id and a key position inside the row's band.
 __device__ __forceinline__ void kv_valid_bits(const KernelArgs& a, bool general, int b, int k0,
                                               int rlo, int rhi, int my_id, int my_pos,
                                               uint64_t (&vb)[2]) {
@@ -198,12 +226,13 @@ __device__ __forceinline__ void kv_valid_bits(const KernelArgs& a, bool general,
   }
   vb[0] = vb[1] = 0ull;
   if (my_id == 0) return;
+  const int2 kp = band_key_pos(a, my_pos);
   const int nkc = (a.Skv + kChunk - 1) / kChunk;
   if (k0 + kTile <= a.Skv && (k0 % kChunk) == 0) {
     const ChunkInfo c0 = a.kv_chunk[b * nkc + k0 / kChunk];
     const ChunkInfo c1 = a.kv_chunk[b * nkc + k0 / kChunk + 1];
     if (c0.uniform && c1.uniform && c0.min_id == my_id && c1.min_id == my_id &&
-        (!a.causal || max(c0.max_pos, c1.max_pos) <= my_pos)) {
+        min(c0.min_pos, c1.min_pos) >= kp.x && max(c0.max_pos, c1.max_pos) <= kp.y) {
       vb[0] = vb[1] = ~0ull;
       return;
     }
@@ -229,7 +258,7 @@ __device__ __forceinline__ void kv_valid_bits(const KernelArgs& a, bool general,
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const bool v = (ids[e] == my_id) & (!a.causal | (pss[e] <= my_pos));
+      const bool v = (ids[e] == my_id) & (pss[e] >= kp.x) & (pss[e] <= kp.y);
       vb[(c + e) >> 6] |= static_cast<uint64_t>(v) << ((c + e) & 63);
     }
   }

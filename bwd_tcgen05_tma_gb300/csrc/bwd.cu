@@ -523,14 +523,16 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
           if (nq == 0) continue;
           const int64_t gk = (int64_t)b * a.Skv + kj;
           int qlo = 0, qhi = 0, my_id = 0, my_pos = 0;
+          int2 my_qp = make_int2(0, -1);  // query positions that keep this key
           if (row_ok) {
             if (!general) {
-              const int sl = a.kv_seg_lo[gk], sh = a.kv_seg_hi[gk];
-              qlo = a.causal ? max(kj, sl) : sl;
-              qhi = sh;
+              const int2 qr = band_queries_of_key(a, kj, a.kv_seg_lo[gk], a.kv_seg_hi[gk]);
+              qlo = qr.x;
+              qhi = qr.y;
             } else {
               my_id = a.kv_id[gk];
               my_pos = a.kv_pos[gk];
+              my_qp = band_query_pos(a, my_pos);
             }
           }
           for (int hh = 0; hh < G && ok; ++hh) {
@@ -573,7 +575,8 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
                 bool full = false;
                 if (row_ok && my_id != 0 && q0 + kBwdQ <= a.Sq) {
                   const ChunkInfo ci = a.q_chunk[b * nqc + q0 / kChunk];
-                  full = ci.uniform && ci.min_id == my_id && (!a.causal || ci.min_pos >= my_pos);
+                  full = ci.uniform && ci.min_id == my_id && ci.min_pos >= my_qp.x &&
+                         ci.max_pos <= my_qp.y;
                 }
                 if (full) {
                   vbits = ~0u;
@@ -586,7 +589,7 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
                     const int pss[4] = {ps4.x, ps4.y, ps4.z, ps4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                      const bool v = (ids[e] == my_id) & (!a.causal | (my_pos <= pss[e]));
+                      const bool v = (ids[e] == my_id) & (pss[e] >= my_qp.x) & (pss[e] <= my_qp.y);
                       vbits |= static_cast<uint32_t>(v) << (c + e);
                     }
                   }
@@ -1073,9 +1076,9 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
       float lse2 = INFINITY, Di = 0.f;
       if (row_ok) {
         if (!general) {
-          const int sl = a.seg_lo[grow], sh = a.seg_hi[grow];
-          rlo = sl;
-          rhi = a.causal ? min(i + 1, sh) : sh;
+          const int2 kr = band_keys_of_query(a, i, a.seg_lo[grow], a.seg_hi[grow]);
+          rlo = kr.x;
+          rhi = kr.y;
         } else {
           my_id = a.q_id[grow];
           my_pos = a.q_pos[grow];

@@ -382,14 +382,16 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
           if (nq == 0) continue;
           const int64_t gk = (int64_t)b * a.Skv + kj;
           int qlo = 0, qhi = 0, my_id = 0, my_pos = 0;
+          int2 my_qp = make_int2(0, -1);  // query positions that keep this key
           if (row_ok) {
             if (!general) {
-              const int sl = a.kv_seg_lo[gk], sh = a.kv_seg_hi[gk];
-              qlo = a.causal ? max(kj, sl) : sl;
-              qhi = sh;
+              const int2 qr = band_queries_of_key(a, kj, a.kv_seg_lo[gk], a.kv_seg_hi[gk]);
+              qlo = qr.x;
+              qhi = qr.y;
             } else {
               my_id = a.kv_id[gk];
               my_pos = a.kv_pos[gk];
+              my_qp = band_query_pos(a, my_pos);
             }
           }
           for (int hh = 0; hh < G && ok; ++hh) {
@@ -410,7 +412,8 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 bool full = false;
                 if (row_ok && my_id != 0 && qh + 64 <= a.Sq && (qh % kChunk) == 0) {
                   const ChunkInfo ci = a.q_chunk[b * nqc + qh / kChunk];
-                  full = ci.uniform && ci.min_id == my_id && (!a.causal || ci.min_pos >= my_pos);
+                  full = ci.uniform && ci.min_id == my_id && ci.min_pos >= my_qp.x &&
+                         ci.max_pos <= my_qp.y;
                 }
                 if (full) {
                   vbits = ~0ull;
@@ -420,8 +423,8 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                   const int32_t* qps = a.q_pos + (int64_t)b * a.Sq;
                   const int n = min(64, a.Sq - qh);
                   for (int c = 0; c < n; ++c) {
-                    const bool v = (__ldg(qid + qh + c) == my_id) &
-                                   (!a.causal | (my_pos <= __ldg(qps + qh + c)));
+                    const int pq = __ldg(qps + qh + c);
+                    const bool v = (__ldg(qid + qh + c) == my_id) & (pq >= my_qp.x) & (pq <= my_qp.y);
                     vbits |= static_cast<uint64_t>(v) << c;
                   }
                 }

@@ -53,15 +53,16 @@ struct Dq128Bars {
 
 // Validity of the 64 keys [kh, kh + 64) of batch row b for one query row.
 // Fast path: the row's key range [rlo, rhi).  General path: same nonzero
-// segment id and, if causal, key position <= query position.
+// segment id and a key position inside the row's band.
 __device__ __forceinline__ uint64_t kv_bits64(const KernelArgs& a, bool general, int b, int kh,
                                               int rlo, int rhi, int my_id, int my_pos) {
   if (!general) return range_bits64(rlo - kh, rhi - kh);
   if (my_id == 0 || kh >= a.Skv) return 0ull;
+  const int2 kp = band_key_pos(a, my_pos);
   if (kh + kChunk <= a.Skv && (kh % kChunk) == 0) {
     const int nkc = (a.Skv + kChunk - 1) / kChunk;
     const ChunkInfo c = a.kv_chunk[b * nkc + kh / kChunk];
-    if (c.uniform && c.min_id == my_id && (!a.causal || c.max_pos <= my_pos)) return ~0ull;
+    if (c.uniform && c.min_id == my_id && c.min_pos >= kp.x && c.max_pos <= kp.y) return ~0ull;
   }
   // every lane of the warp reads the same keys
   const int32_t* kid = a.kv_id + (int64_t)b * a.Skv + kh;
@@ -69,7 +70,8 @@ __device__ __forceinline__ uint64_t kv_bits64(const KernelArgs& a, bool general,
   const int n = min(64, a.Skv - kh);
   uint64_t v = 0ull;
   for (int c = 0; c < n; ++c) {
-    const bool ok = (__ldg(kid + c) == my_id) & (!a.causal | (__ldg(kps + c) <= my_pos));
+    const int pk = __ldg(kps + c);
+    const bool ok = (__ldg(kid + c) == my_id) & (pk >= kp.x) & (pk <= kp.y);
     v |= static_cast<uint64_t>(ok) << c;
   }
   return v;
@@ -351,8 +353,9 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
       float lse2 = INFINITY, Di = 0.f;
       if (row_ok) {
         if (!general) {
-          rlo = a.seg_lo[grow];
-          rhi = a.causal ? min(i + 1, a.seg_hi[grow]) : a.seg_hi[grow];
+          const int2 kr = band_keys_of_query(a, i, a.seg_lo[grow], a.seg_hi[grow]);
+          rlo = kr.x;
+          rhi = kr.y;
         } else {
           my_id = a.q_id[grow];
           my_pos = a.q_pos[grow];

@@ -311,9 +311,9 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
       int rlo = 0, rhi = 0, my_id = 0, my_pos = 0;
       if (row_ok) {
         if (!general) {
-          const int sl = a.seg_lo[grow], sh = a.seg_hi[grow];
-          rlo = sl;
-          rhi = a.causal ? min(i + 1, sh) : sh;
+          const int2 kr = band_keys_of_query(a, i, a.seg_lo[grow], a.seg_hi[grow]);
+          rlo = kr.x;
+          rhi = kr.y;
         } else {
           my_id = a.q_id[grow];
           my_pos = a.q_pos[grow];

@@ -361,8 +361,9 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       int rlo = 0, rhi = 0, my_id = 0, my_pos = 0;
       if (row_ok) {
         if (!general) {
-          rlo = a.seg_lo[grow];
-          rhi = a.causal ? min(i + 1, a.seg_hi[grow]) : a.seg_hi[grow];
+          const int2 kr = band_keys_of_query(a, i, a.seg_lo[grow], a.seg_hi[grow]);
+          rlo = kr.x;
+          rhi = kr.y;
         } else {
           my_id = a.q_id[grow];
           my_pos = a.q_pos[grow];

@@ -376,30 +376,37 @@ __device__ void meta_ranges(const KernelArgs& a, const MetaIn& in) {
         const int64_t g = (int64_t)b * S_own + i;
         const int sl = slo[g], sh = shi[g];
         if (sh <= sl) continue;
-        if (qside) {
-          lo = min(lo, sl);
-          hi = max(hi, a.causal ? min(i + 1, sh) : sh);
-        } else {
-          lo = min(lo, a.causal ? max(i, sl) : sl);
-          hi = max(hi, sh);
-        }
+        const int2 r = qside ? band_keys_of_query(a, i, sl, sh) : band_queries_of_key(a, i, sl, sh);
+        if (r.y <= r.x) continue;
+        lo = min(lo, r.x);
+        hi = max(hi, r.y);
       }
     } else {
       const ChunkInfo* own = qside ? a.q_chunk : a.kv_chunk;
       const ChunkInfo* oth = qside ? a.kv_chunk : a.q_chunk;
       const int nown = qside ? nqc : nkc, noth = qside ? nkc : nqc;
-      int ilo = INT_MAX, ihi = 0;
+      int ilo = INT_MAX, ihi = 0, plo = INT_MAX, phi = INT_MIN;
       for (int c = r0 / kChunk + lane; c * kChunk < r1; c += 32) {
         const ChunkInfo ci = own[b * nown + c];
         if (ci.max_id == 0) continue;
         ilo = min(ilo, ci.min_id);
         ihi = max(ihi, ci.max_id);
+        plo = min(plo, ci.min_pos);
+        phi = max(phi, ci.max_pos);
       }
       ilo = warp_min(ilo);
       ihi = warp_max(ihi);
+      plo = warp_min(plo);
+      phi = warp_max(phi);
       if (ihi != 0) {
+        // positions of the other side that the band admits for this tile's
+        // positions [plo, phi] (a chunk outside them has no valid pair here)
+        const int2 ox = qside ? band_key_pos(a, plo) : band_query_pos(a, plo);
+        const int2 oy = qside ? band_key_pos(a, phi) : band_query_pos(a, phi);
+        const int want_lo = ox.x, want_hi = oy.y;
         for (int c = lane; c < noth; c += 32) {
-          if (ids_meet(oth[b * noth + c], ilo, ihi)) {
+          const ChunkInfo co = oth[b * noth + c];
+          if (ids_meet(co, ilo, ihi) && co.max_pos >= want_lo && co.min_pos <= want_hi) {
             lo = min(lo, c * kChunk);
             hi = max(hi, min(S_oth, (c + 1) * kChunk));
           }

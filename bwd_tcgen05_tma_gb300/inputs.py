@@ -116,6 +116,8 @@ class Case:
     cu_seqlens_q: np.ndarray | None = None
     cu_seqlens_kv: np.ndarray | None = None
     bias: np.ndarray | None = None  # [bias_b, bias_h, Sq, Skv]
+    window: tuple | None = None  # band (left, right) in positions, None for an open side
+    bottom_right: bool = False  # positions aligned by Skv - Sq
 
     @property
     def mask(self):

@@ -16,6 +16,7 @@
  * Mathematics.  For batch row b, query head h, KV head g = h / (Hq / Hkv),
  * query i and key j:
  *   valid(i,j) = id_q[i] == id_kv[j] != 0 && (!causal || pos_kv[j] <= pos_q[i])
+ *                (with a band: the band's position test in place of the causal one)
  *   S_ij = scale * Q_i . K_j + bias_ij          (masked pairs: -inf)
  *   P = softmax_j(S),  O_i = sum_j P_ij V_j,  LSE_i = ln sum_j exp(S_ij)
  *   dP_ij = dO_i . V_j,  D_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - D_i)
@@ -54,7 +55,7 @@
 extern "C" {
 #endif
 
-#define ATTN_PARAMS_VERSION 4
+#define ATTN_PARAMS_VERSION 5
 
 typedef enum {
   ATTN_OK = 0,
@@ -88,9 +89,10 @@ typedef enum { ATTN_LAYOUT_3HD = 0, ATTN_LAYOUT_HD_2HD = 1, ATTN_LAYOUT_HD_HD_HD
 typedef enum { ATTN_FMT_BSHD = 0, ATTN_FMT_THD_SEGMENTS = 1, ATTN_FMT_THD_CU_SEQLENS = 2 } attn_format_t;
 
 /* Causal masking compares segment positions (pos_kv <= pos_q); without
- * segments the position is the token index (top-left alignment).  The PADDING
- * variants only document that segment metadata is present; padding (id 0) is
- * always masked. */
+ * segments the position is the token index (top-left alignment; see
+ * attn_params_t.bottom_right for the other one).  The PADDING variants only
+ * document that segment metadata is present; padding (id 0) is always
+ * masked.  Sliding windows: attn_params_t.band. */
 typedef enum {
   ATTN_MASK_NONE = 0,
   ATTN_MASK_CAUSAL = 1,
@@ -161,6 +163,21 @@ typedef struct {
    * gradient of the loss with respect to each sink logit, summed over batch
    * rows and query rows in a fixed order (bit-reproducible). */
   float* dsink;
+  /* Band mask: sliding windows and bottom-right alignment (both directions).
+   * The pages define neither; this is the usual reading.  Positions are the
+   * segment positions (token indices for dense rows), and
+   *   shift = Skv - Sq if bottom_right != 0, else 0.
+   * band == 0: no window; a causal mask keeps pos_kv[j] <= pos_q[i] + shift.
+   * band != 0: key j is kept for query i (in the same nonzero segment) when
+   *   -window_left <= pos_kv[j] - (pos_q[i] + shift) <= window_right,
+   *   a negative window_left / window_right leaving that side unbounded.  With
+   *   a causal mask window_right must be 0 or negative and is taken as 0
+   *   (window_left = w - 1 then keeps the last w keys up to the diagonal).
+   * ATTN_ERR_INVALID_ARG: a causal mask with window_right > 0. */
+  int32_t band;
+  int32_t window_left;
+  int32_t window_right;
+  int32_t bottom_right;
 } attn_params_t;
 
 /* Which metadata path the device chose (read back by attn_read_status). */

@@ -31,6 +31,21 @@ def oracle_metadata(case):
     return case.q_ids, qp, case.kv_ids, kp
 
 
+def oracle_mask(case):
+    """The oracle's mask argument for a case: the causal flag, or a Window
+    when the case has a band or bottom-right alignment (a causal mask keeps
+    the band's right side at 0)."""
+    from oracle import attn_ref as R
+
+    if case.window is None and not case.bottom_right:
+        return case.causal
+    left, right = case.window if case.window is not None else (None, None)
+    if case.causal:
+        right = 0
+    shift = case.Skv - case.Sq if case.bottom_right else 0
+    return R.Window(left, right, shift)
+
+
 def oracle_qkv(case):
     from oracle import attn_ref as R
 
@@ -45,9 +60,10 @@ def oracle_full(case):
     q, k, v = oracle_qkv(case)
     qi, qp, ki, kp = oracle_metadata(case)
     bias = None if case.bias is None else case.bias.astype(np.float64)
-    o, lse = R.attention_forward(q, k, v, qi, qp, ki, kp, case.causal, case.scale, bias)
+    mask = oracle_mask(case)
+    o, lse = R.attention_forward(q, k, v, qi, qp, ki, kp, mask, case.scale, bias)
     dq, dk, dv, dbias = R.attention_backward(q, k, v, case.do.astype(np.float64), qi, qp, ki,
-                                             kp, case.causal, case.scale, bias)
+                                             kp, mask, case.scale, bias)
     return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "dbias": dbias}
 
 

@@ -49,7 +49,8 @@ class DevCase:
             Hkv=c.Hkv, d_qk=c.d_qk, d_v=c.d_v, scale=c.scale, q=q, k=k, v=v,
             q_seg_ids=self.q_ids, q_seg_pos=self.q_pos, kv_seg_ids=self.kv_ids,
             kv_seg_pos=self.kv_pos, cu_seqlens_q=self.cu_q, cu_seqlens_kv=self.cu_kv,
-            bias=self.bias, dq_mode=dq_mode, force_general_path=force_general)
+            bias=self.bias, dq_mode=dq_mode, force_general_path=force_general,
+            window=c.window, bottom_right=c.bottom_right)
         self.ws_fwd = torch.zeros(max(A.attn_fwd_workspace_size(self.params), 256),
                                   dtype=torch.uint8, device="cuda")
         self.ws_bwd = torch.zeros(max(A.attn_bwd_workspace_size(self.params), 256),
@@ -140,11 +141,12 @@ def check_forward(case, ref, o_dev, lse_dev):
 
 def structural_masks(case):
     """Per batch row: valid-pair matrix, queries without keys, keys without queries."""
-    from conftest import oracle_metadata
+    from conftest import oracle_mask, oracle_metadata
     from oracle import attn_ref as R
 
     qi, qp, ki, kp = oracle_metadata(case)
-    valid = np.stack([R.valid_pairs(qi[b], qp[b], ki[b], kp[b], case.causal)
+    mask = oracle_mask(case)
+    valid = np.stack([R.valid_pairs(qi[b], qp[b], ki[b], kp[b], mask)
                       for b in range(case.B)])
     return valid, ~valid.any(axis=2), ~valid.any(axis=1)
 

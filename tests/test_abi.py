@@ -180,3 +180,22 @@ def test_sink_gradient_workspace(lib):
     need = (2 * 256 + 7) // 8 * 8 * 4
     assert A.attn_bwd_workspace_size(p) - base == (need + 255) // 256 * 256
     assert A.attn_fwd_workspace_size(p) == A.attn_fwd_workspace_size(params())
+
+
+def test_band_validation(lib):
+    """A causal mask keeps at most the diagonal on the right: a band that
+    reaches past it is rejected; an open or zero right side is accepted, as
+    is any band without a causal mask."""
+    p = params(mask="CAUSAL")
+    p.band, p.window_left, p.window_right = 1, 100, 5
+    assert A.attn_fwd_workspace_size(p) == 0
+    for right in (0, -1):
+        p.window_right = right
+        assert A.attn_fwd_workspace_size(p) > 0
+    q = params(mask="NONE")
+    q.band, q.window_left, q.window_right, q.bottom_right = 1, -1, 7, 1
+    assert A.attn_fwd_workspace_size(q) > 0
+    m = A.make_params(layout="HD_HD_HD", fmt="BSHD", mask="CAUSAL", B=1, Sq=8, Skv=8, Hq=1,
+                      Hkv=1, d_qk=64, d_v=64, scale=0.1, q=None, window=(None, 0),
+                      bottom_right=True)
+    assert (m.band, m.window_left, m.window_right, m.bottom_right) == (1, -1, 0, 1)
