@@ -80,6 +80,21 @@ __device__ __forceinline__ bool ring_pop1(ItemRing* r, uint32_t n, int32_t& item
   return true;
 }
 
+// Whole-warp consumer that counts as one arrival (the warp-wide MMA issuers):
+// every lane waits, lane 0 reads the entry and releases the slot, and the
+// item reaches every lane as a warp-uniform value.
+__device__ __forceinline__ bool ring_pop_warp1(ItemRing* r, uint32_t n, int32_t& item) {
+  const int s = n % kItemRing;
+  if (!sm103::mbar_wait_warp(&r->full[s], (n / kItemRing) & 1)) return false;
+  int32_t v = 0;
+  if ((threadIdx.x & 31) == 0) {
+    v = *reinterpret_cast<volatile int32_t*>(&r->item[s]);
+    sm103::mbar_arrive(&r->empty[s]);
+  }
+  item = sm103::warp_uniform(v);
+  return true;
+}
+
 // Summary of 64 consecutive tokens of one batch row.
 struct ChunkInfo {
   int32_t min_id;   // smallest nonzero id (INT32_MAX if none)

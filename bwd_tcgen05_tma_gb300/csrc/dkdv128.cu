@@ -250,112 +250,99 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, kQ, false, false);   // S^T, N = query
-      constexpr uint32_t id_p = idesc_bf16_f32(128, kQ, false, false);   // dP^T
-      constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, false, true);   // dV, B = dO (MN)
-      constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, false, true);  // dK, B = Q (MN)
-      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
-      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
-      const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
-      const uint64_t q_mn = sdesc_sw128(smem_u32(sm + L::kQOff), 16384, 1024);
-      const uint64_t o_km = sdesc_sw128(smem_u32(sm + L::kOOff), 16, 1024);
-      const uint64_t o_mn = sdesc_sw128(smem_u32(sm + L::kOOff), 16384, 1024);
-      uint32_t st = 0, kvc = 0, gc = 0;
-      bool ok = true;
-      auto qoff16 = [&](uint32_t x) -> uint32_t {
-        return static_cast<uint32_t>(((x % NQ) * L::kQBytes) >> 4);
-      };
-      auto ooff16 = [&](uint32_t x) -> uint32_t {
-        return static_cast<uint32_t>(((x % NO) * L::kOBytes) >> 4);
-      };
-      // dK += dS^T(x) Q(x): A = packed dS^T (query columns [0,64) at dP^T columns
-      // [0,32), [64,128) at [64,96)), B = Q(x) MN-major; K = 128 query rows
-      auto issue_dk = [&](uint32_t x, bool first) {
-        const uint64_t qd = q_mn + qoff16(x);
-#pragma unroll
-        for (int ks = 0; ks < kQ / 16; ++ks)
-          mma_ts(tmem + L::kColDK, tmem + L::kColDP + ks * 8 + (ks >> 2) * 32,
-                 qd + ((ks * 2048) >> 4), id_dk, (!first || ks > 0));
-        mma_commit(&bars->q_empty[x % NQ]);
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-        const DkdvItem w = dkdv_item(a, idx);
-        for (int b = w.b0; b < w.b1 && ok; ++b) {
-          for (int g = w.g0; g < w.g1 && ok; ++g) {
-            int q_lo;
-            const int nq = dkdv_q_tiles<kQ>(a, b, w.t, q_lo);
-            if (nq == 0) continue;
-            const uint32_t nsteps = (uint32_t)nq * G;
-            if (!(ok = mbar_wait(&bars->kv_full, kvc & 1))) break;
-            ++kvc;
-            for (uint32_t u = 0; u < nsteps; ++u) {
-              const uint32_t cur = st + u;
-              if (!(ok = mbar_wait(&bars->q_full[cur % NQ], (cur / NQ) & 1))) break;
-              tc_fence_after();
-              {  // S^T(cur) = K Q^T  (over P^T(cur-1), read by dV(cur-1) issued earlier)
-                const uint64_t qd = q_km + qoff16(cur);
-#pragma unroll
-                for (int ks = 0; ks < DQK / 16; ++ks)
-                  mma_ss(tmem + L::kColS, k_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                         qd + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), id_s, ks > 0);
-                mma_commit(&bars->s_full);
-                ATTN_TL(10, cur);
-              }
-              if (u > 0) {  // dK(cur-1), once its dS^T is in tensor memory
-                if (!(ok = mbar_wait(&bars->ds_ready, (cur - 1) & 1))) break;
-                tc_fence_after();
-                issue_dk(cur - 1, u == 1);
-                ATTN_TL(15, cur - 1);
-              }
-              if (!(ok = mbar_wait(&bars->o_full[cur % NO], (cur / NO) & 1))) break;
-              tc_fence_after();
-              {  // dP^T(cur) = V dO^T  (over dS^T(cur-1), read by dK(cur-1) just issued)
-                const uint64_t od = o_km + ooff16(cur);
-#pragma unroll
-                for (int ks = 0; ks < DV / 16; ++ks)
-                  mma_ss(tmem + L::kColDP, v_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                         od + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), id_p, ks > 0);
-                mma_commit(&bars->dp_full);
-                ATTN_TL(11, cur);
-              }
-              // dV += P^T(cur) dO(cur)
-              if (!(ok = mbar_wait(&bars->p_ready, cur & 1))) break;
-              ATTN_TL(12, cur);
-              if (u == 0 && gc > 0 && !(ok = mbar_wait(&bars->acc_empty, (gc - 1) & 1))) break;
-              tc_fence_after();
-              {
-                const uint64_t od = o_mn + ooff16(cur);
-#pragma unroll
-                for (int ks = 0; ks < kQ / 16; ++ks)
-                  mma_ts(tmem + L::kColDV, tmem + L::kColS + ks * 8 + (ks >> 2) * 32,
-                         od + ((ks * 2048) >> 4), id_dv, (u > 0 || ks > 0));
-                mma_commit(&bars->o_empty[cur % NO]);
-                ATTN_TL(13, cur);
-              }
-            }
-            if (!ok) break;
-            // the group's last dK
-            const uint32_t last = st + nsteps - 1;
-            if (!(ok = mbar_wait(&bars->ds_ready, last & 1))) break;
+    // The whole warp runs this loop on warp-uniform values; one elected lane
+    // issues each GEMM's MMAs from a single asm statement.
+    constexpr uint32_t id_s = idesc_bf16_f32(128, kQ, false, false);   // S^T, N = query
+    constexpr uint32_t id_p = idesc_bf16_f32(128, kQ, false, false);   // dP^T
+    constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, false, true);   // dV, B = dO (MN)
+    constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, false, true);  // dK, B = Q (MN)
+    const uint32_t tm = warp_uniform(tmem);
+    const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+    const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
+    const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+    const uint64_t q_mn = sdesc_sw128(smem_u32(sm + L::kQOff), 16384, 1024);
+    const uint64_t o_km = sdesc_sw128(smem_u32(sm + L::kOOff), 16, 1024);
+    const uint64_t o_mn = sdesc_sw128(smem_u32(sm + L::kOOff), 16384, 1024);
+    uint32_t st = 0, kvc = 0, gc = 0;
+    bool ok = true;
+    auto qoff16 = [&](uint32_t x) -> uint32_t {
+      return static_cast<uint32_t>(((x % NQ) * L::kQBytes) >> 4);
+    };
+    auto ooff16 = [&](uint32_t x) -> uint32_t {
+      return static_cast<uint32_t>(((x % NO) * L::kOBytes) >> 4);
+    };
+    // dK += dS^T(x) Q(x): A = packed dS^T (query columns [0,64) at dP^T columns
+    // [0,32), [64,128) at [64,96)), B = Q(x) MN-major; K = 128 query rows
+    auto issue_dk = [&](uint32_t x, bool first) {
+      mma_ts_warp<kQ / 16, 8, 40, 128, 128>(tm + L::kColDK, tm + L::kColDP, q_mn + qoff16(x), id_dk,
+                                            first ? 0u : 1u);
+      mma_commit_warp(&bars->q_empty[x % NQ]);
+    };
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) ||
+          !(ok = ring_pop_warp1(ring, rn, idx)) || idx < 0)
+        break;
+      const DkdvItem w = dkdv_item(a, idx);
+      for (int b = w.b0; b < w.b1 && ok; ++b) {
+        for (int g = w.g0; g < w.g1 && ok; ++g) {
+          int q_lo;
+          const int nq = warp_uniform(dkdv_q_tiles<kQ>(a, b, w.t, q_lo));
+          if (nq == 0) continue;
+          const uint32_t nsteps = (uint32_t)nq * G;
+          if (!(ok = mbar_wait_warp(&bars->kv_full, kvc & 1))) break;
+          ++kvc;
+          for (uint32_t u = 0; u < nsteps; ++u) {
+            const uint32_t cur = st + u;
+            if (!(ok = mbar_wait_warp(&bars->q_full[cur % NQ], (cur / NQ) & 1))) break;
             tc_fence_after();
-            issue_dk(last, nsteps == 1);
-            mma_commit(&bars->acc_full);
-            mma_commit(&bars->kv_empty);
-            ++gc;
-            st += nsteps;
+            // S^T(cur) = K Q^T  (over P^T(cur-1), read by dV(cur-1) issued earlier)
+            mma_ss_warp<DQK / 16, 2, 1018, 2, 1018>(tm + L::kColS, k_km, q_km + qoff16(cur), id_s,
+                                                    0u);
+            mma_commit_warp(&bars->s_full);
+            ATTN_TL(10, cur);
+            if (u > 0) {  // dK(cur-1), once its dS^T is in tensor memory
+              if (!(ok = mbar_wait_warp(&bars->ds_ready, (cur - 1) & 1))) break;
+              tc_fence_after();
+              issue_dk(cur - 1, u == 1);
+              ATTN_TL(15, cur - 1);
+            }
+            if (!(ok = mbar_wait_warp(&bars->o_full[cur % NO], (cur / NO) & 1))) break;
+            tc_fence_after();
+            // dP^T(cur) = V dO^T  (over dS^T(cur-1), read by dK(cur-1) just issued)
+            mma_ss_warp<DV / 16, 2, 1018, 2, 1018>(tm + L::kColDP, v_km, o_km + ooff16(cur), id_p,
+                                                   0u);
+            mma_commit_warp(&bars->dp_full);
+            ATTN_TL(11, cur);
+            // dV += P^T(cur) dO(cur)
+            if (!(ok = mbar_wait_warp(&bars->p_ready, cur & 1))) break;
+            ATTN_TL(12, cur);
+            if (u == 0 && gc > 0 && !(ok = mbar_wait_warp(&bars->acc_empty, (gc - 1) & 1))) break;
+            tc_fence_after();
+            mma_ts_warp<kQ / 16, 8, 40, 128, 128>(tm + L::kColDV, tm + L::kColS, o_mn + ooff16(cur),
+                                                  id_dv, u > 0 ? 1u : 0u);
+            mma_commit_warp(&bars->o_empty[cur % NO]);
+            ATTN_TL(13, cur);
           }
+          if (!ok) break;
+          // the group's last dK
+          const uint32_t last = st + nsteps - 1;
+          if (!(ok = mbar_wait_warp(&bars->ds_ready, last & 1))) break;
+          tc_fence_after();
+          issue_dk(last, nsteps == 1);
+          mma_commit_warp(&bars->acc_full);
+          mma_commit_warp(&bars->kv_empty);
+          ++gc;
+          st += nsteps;
         }
       }
-      if (!ok) {
-        report_timeout(a, 0x330);
-        *abort_flag = 1;
-      }
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 200000000ull);
     }
+    if (!ok && lane == 0) {
+      report_timeout(a, 0x330);
+      *abort_flag = 1;
+    }
+    mma_commit_warp(&bars->drain);
+    mbar_wait(&bars->drain, 0, 200000000ull);
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P / dS warps
     // two warpgroups: thread (j, half) owns KV row j (TMEM lane j) and query

@@ -205,95 +205,91 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
-    // Two issuing threads on different schedulers, one per tensor-memory
+    // Two issuing warps on different schedulers, one per tensor-memory
     // region: warp 1 issues S (S region), warp 2 issues dP and dQ (dP / dS
     // region and the dQ accumulator).  Each region's writer and readers are in
-    // one thread, which orders them.
-    if (lane == 0) {
-      const bool s_side = (warp == 1);
-      constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
-      constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, false, true);
-      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
-      const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);
-      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
-      uint32_t kt = 0, it = 0;
-      bool ok = true;
-      auto issue_s = [&](uint32_t k) -> bool {  // S = Q K^T, Q from tensor memory
-        const int s_ = k % KS;
-        if (!mbar_wait(&bars->k_full[s_], (k / KS) & 1)) return false;
-        tc_fence_after();
-        const uint64_t kd = k_km + static_cast<uint32_t>((s_ * L::kKBytes) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DQK / 16; ++ks)
-          mma_ts(tmem + L::kColS, tmem + L::kColQ + ks * 8,
-                 kd + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), id_s, ks > 0);
-        mma_commit(&bars->s_full);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t k) -> bool {  // dP = dO V^T, dO from tensor memory
-        const int s_ = k % VS;
-        if (!mbar_wait(&bars->v_full[s_], (k / VS) & 1)) return false;
-        tc_fence_after();
-        const uint64_t vd = v_km + static_cast<uint32_t>((s_ * L::kVBytes) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DV / 16; ++ks)
-          mma_ts(tmem + L::kColDP, tmem + L::kColO + ks * 8,
-                 vd + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), id_s, ks > 0);
-        mma_commit(&bars->dp_full);
-        mma_commit(&bars->v_empty[s_]);
-        return true;
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-        int b, t, h, kv_lo, n;
-        item_of(idx, b, t, h, kv_lo, n);
-        if (n == 0) continue;
-        // Q / dO of this item in tensor memory (the softmax warps copied them
-        // after the previous item's last S / dP had been read)
-        if (!(ok = mbar_wait(&bars->qo_ready, it & 1))) break;
-        tc_fence_after();
-        if (s_side) {
-          if (!(ok = issue_s(kt))) break;
-          for (int j = 0; j + 1 < n && ok; ++j) {  // S(k+1) over S(k) once P(k) is held
-            const uint32_t k = kt + j;
-            if (!(ok = mbar_wait(&bars->s_free, k & 1))) break;
-            ok = issue_s(k + 1);
-          }
-        } else {
-          if (!(ok = issue_dp(kt))) break;
-          for (int j = 0; j < n && ok; ++j) {
-            const uint32_t k = kt + j;
-            if (!(ok = mbar_wait(&bars->ds_ready, k & 1))) break;
-            if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->acc_empty, (it - 1) & 1))) break;
-            tc_fence_after();
-            {  // dQ += dS K: A = packed dS (key columns [0,64) at dP columns [0,32),
-               // [64,128) at [64,96)), B = K(k) MN-major, K = 128 keys
-              const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
-#pragma unroll
-              for (int ks = 0; ks < kTile / 16; ++ks)
-                mma_ts(tmem + L::kColDQ, tmem + L::kColDP + (ks >> 2) * 64 + (ks & 3) * 8,
-                       kd + ((ks * 2048) >> 4), id_dq, (j > 0 || ks > 0));
-              // S(k) was complete before dS(k) existed: K(k) is free after this
-              mma_commit(&bars->k_empty[k % KS]);
-            }
-            // dP(k+1) over dS(k), after dQ(k) that reads it (same issuing thread)
-            if (j + 1 < n) ok = issue_dp(k + 1);
-          }
-          if (ok) mma_commit(&bars->acc_full);
+    // one warp, whose MMAs the in-order pipe orders.  Each warp runs its loop
+    // on warp-uniform values; one elected lane issues each GEMM's MMAs from a
+    // single asm statement.
+    const bool s_side = (warp == 1);
+    constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
+    constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, false, true);
+    const uint32_t tm = warp_uniform(tmem);
+    const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+    const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);
+    const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
+    uint32_t kt = 0, it = 0;
+    bool ok = true;
+    auto issue_s = [&](uint32_t k) -> bool {  // S = Q K^T, Q from tensor memory
+      const int s_ = k % KS;
+      if (!mbar_wait_warp(&bars->k_full[s_], (k / KS) & 1)) return false;
+      tc_fence_after();
+      const uint64_t kd = k_km + static_cast<uint32_t>((s_ * L::kKBytes) >> 4);
+      mma_ts_warp<DQK / 16, 8, 8, 2, 1018>(tm + L::kColS, tm + L::kColQ, kd, id_s, 0u);
+      mma_commit_warp(&bars->s_full);
+      return true;
+    };
+    auto issue_dp = [&](uint32_t k) -> bool {  // dP = dO V^T, dO from tensor memory
+      const int s_ = k % VS;
+      if (!mbar_wait_warp(&bars->v_full[s_], (k / VS) & 1)) return false;
+      tc_fence_after();
+      const uint64_t vd = v_km + static_cast<uint32_t>((s_ * L::kVBytes) >> 4);
+      mma_ts_warp<DV / 16, 8, 8, 2, 1018>(tm + L::kColDP, tm + L::kColO, vd, id_s, 0u);
+      mma_commit_warp(&bars->dp_full);
+      mma_commit_warp(&bars->v_empty[s_]);
+      return true;
+    };
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) ||
+          !(ok = ring_pop_warp1(ring, rn, idx)) || idx < 0)
+        break;
+      int b, t, h, kv_lo, n;
+      item_of(idx, b, t, h, kv_lo, n);
+      n = warp_uniform(n);
+      if (n == 0) continue;
+      // Q / dO of this item in tensor memory (the softmax warps copied them
+      // after the previous item's last S / dP had been read)
+      if (!(ok = mbar_wait_warp(&bars->qo_ready, it & 1))) break;
+      tc_fence_after();
+      if (s_side) {
+        if (!(ok = issue_s(kt))) break;
+        for (int j = 0; j + 1 < n && ok; ++j) {  // S(k+1) over S(k) once P(k) is held
+          const uint32_t k = kt + j;
+          if (!(ok = mbar_wait_warp(&bars->s_free, k & 1))) break;
+          ok = issue_s(k + 1);
         }
-        if (!ok) break;
-        kt += n;
-        ++it;
+      } else {
+        if (!(ok = issue_dp(kt))) break;
+        for (int j = 0; j < n && ok; ++j) {
+          const uint32_t k = kt + j;
+          if (!(ok = mbar_wait_warp(&bars->ds_ready, k & 1))) break;
+          if (j == 0 && it > 0 && !(ok = mbar_wait_warp(&bars->acc_empty, (it - 1) & 1))) break;
+          tc_fence_after();
+          {  // dQ += dS K: A = packed dS (key columns [0,64) at dP columns [0,32),
+             // [64,128) at [64,96)), B = K(k) MN-major, K = 128 keys
+            const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
+            mma_ts_warp<kTile / 16, 8, 40, 128, 128>(tm + L::kColDQ, tm + L::kColDP, kd, id_dq,
+                                                     j > 0 ? 1u : 0u);
+            // S(k) was complete before dS(k) existed: K(k) is free after this
+            mma_commit_warp(&bars->k_empty[k % KS]);
+          }
+          // dP(k+1) over dS(k), after dQ(k) that reads it (same issuing warp)
+          if (j + 1 < n) ok = issue_dp(k + 1);
+        }
+        if (ok) mma_commit_warp(&bars->acc_full);
       }
-      if (!ok) {
-        report_timeout(a, s_side ? 0x430 : 0x431);
-        *abort_flag = 1;
-      }
-      uint64_t* dr = s_side ? &bars->drain : &bars->drain2;
-      mma_commit(dr);
-      mbar_wait(dr, 0, 200000000ull);
+      if (!ok) break;
+      kt += n;
+      ++it;
     }
+    if (!ok && lane == 0) {
+      report_timeout(a, s_side ? 0x430 : 0x431);
+      *abort_flag = 1;
+    }
+    uint64_t* dr = s_side ? &bars->drain : &bars->drain2;
+    mma_commit_warp(dr);
+    mbar_wait(dr, 0, 200000000ull);
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / dS warps
     // thread (r, half): query row r (TMEM lane r), key columns [64 half, 64 half + 64)

@@ -242,90 +242,88 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
-        constexpr uint32_t id_o = idesc_bf16_f32(128, DV, false, true);
-        const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
-        const uint64_t kv_km = sdesc_sw128(smem_u32(sm + L::kKVOff), 16, 1024);
-        const uint64_t kv_mn = sdesc_sw128(smem_u32(sm + L::kKVOff), 16384, 1024);
-        uint32_t it = 0, kvc = 0, st = 0;  // st: steps (key tiles) so far
-        bool ok = true;
-        auto stage_off = [&](uint32_t c) -> uint32_t {
-          return static_cast<uint32_t>(((c % NKV) * L::kKVBytes) >> 4);
-        };
-        // S_X(step) = Q_X K^T; K at ring position kc
-        auto issue_s = [&](int x, uint32_t qs, uint32_t kc) {
-          const uint64_t qd = q_km + static_cast<uint32_t>(((qs * 2 + x) * L::kQBytes) >> 4);
-          const uint64_t kd = kv_km + stage_off(kc);
-  #pragma unroll
-          for (int ks = 0; ks < DQK / 16; ++ks) {
-            const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-            mma_ss(tmem + L::kColS + x * kTile, qd + off16, kd + off16, id_s, ks > 0);
-          }
-          mma_commit(&bars->s_full[x]);
-        };
-        // O_X += P_X V; V at ring position vc; P_X packed over S_X
-        auto issue_pv = [&](int x, uint32_t vc, bool first) {
-          const uint64_t vd = kv_mn + stage_off(vc);
-          const uint32_t pa = tmem + L::kColS + x * kTile;
-  #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_ts(tmem + L::kColO + x * kTile, pa + ks * 8, vd + ((ks * 2048) >> 4), id_o,
-                   (!first || ks > 0));
-        };
-        for (uint32_t rn = 0;; ++rn) {
-          int32_t idx;
-          if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-          const F2Item w = f2_item(a, idx);
-          if (w.n == 0) continue;
-          const uint32_t qs = it & 1;
-          if (!(ok = mbar_wait(&bars->q_full[qs], (it >> 1) & 1))) break;
-          // K(0): both S of the first step
-          if (!(ok = mbar_wait(&bars->kv_full[kvc % NKV], (kvc / NKV) & 1))) break;
-          tc_fence_after();
-          issue_s(0, qs, kvc);
-          issue_s(1, qs, kvc);
-          mma_commit(&bars->kv_empty[kvc % NKV]);
-          ++kvc;
-          for (int j = 0; j < w.n && ok; ++j) {
-            const uint32_t k = st + j;
-            const uint32_t vc = kvc;  // V(j)
-            const bool more = j + 1 < w.n;
-            if (!(ok = mbar_wait(&bars->kv_full[vc % NKV], (vc / NKV) & 1))) break;
-            for (int x = 0; x < 2 && ok; ++x) {
-              if (!(ok = mbar_wait(&bars->p_full[x], k & 1))) break;
-              ATTN_TL(30 + x, k);
-              if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->o_empty[x], (it - 1) & 1))) break;
-              tc_fence_after();
-              issue_pv(x, vc, j == 0);
-              if (!more) {
-                mma_commit(&bars->o_full[x]);
-                continue;
-              }
-              // S_X(j+1) over P_X(j), after P_X(j) V (same thread, in-order pipe)
-              if (x == 0 && !(ok = mbar_wait(&bars->kv_full[(vc + 1) % NKV], ((vc + 1) / NKV) & 1)))
-                break;
-              tc_fence_after();
-              issue_s(x, qs, vc + 1);
-              ATTN_TL(32 + x, k + 1);
+      // The whole warp runs this loop on warp-uniform values; one elected lane
+      // issues each GEMM's MMAs from a single asm statement.
+      constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
+      constexpr uint32_t id_o = idesc_bf16_f32(128, DV, false, true);
+      const uint32_t tm = warp_uniform(tmem);
+      const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+      const uint64_t kv_km = sdesc_sw128(smem_u32(sm + L::kKVOff), 16, 1024);
+      const uint64_t kv_mn = sdesc_sw128(smem_u32(sm + L::kKVOff), 16384, 1024);
+      uint32_t it = 0, kvc = 0, st = 0;  // st: steps (key tiles) so far
+      bool ok = true;
+      auto stage_off = [&](uint32_t c) -> uint32_t {
+        return static_cast<uint32_t>(((c % NKV) * L::kKVBytes) >> 4);
+      };
+      // S_X(step) = Q_X K^T; K at ring position kc
+      auto issue_s = [&](int x, uint32_t qs, uint32_t kc) {
+        const uint64_t qd = q_km + static_cast<uint32_t>(((qs * 2 + x) * L::kQBytes) >> 4);
+        const uint64_t kd = kv_km + stage_off(kc);
+        mma_ss_warp<DQK / 16, 2, 1018, 2, 1018>(tm + L::kColS + x * kTile, qd, kd, id_s, 0u);
+        mma_commit_warp(&bars->s_full[x]);
+      };
+      // O_X += P_X V; V at ring position vc; P_X packed over S_X
+      auto issue_pv = [&](int x, uint32_t vc, bool first) {
+        const uint64_t vd = kv_mn + stage_off(vc);
+        mma_ts_warp<kTile / 16, 8, 8, 128, 128>(tm + L::kColO + x * kTile, tm + L::kColS + x * kTile,
+                                                vd, id_o, first ? 0u : 1u);
+      };
+      for (uint32_t rn = 0;; ++rn) {
+        int32_t idx;
+        if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) ||
+            !(ok = ring_pop_warp1(ring, rn, idx)) || idx < 0)
+          break;
+        F2Item w = f2_item(a, idx);
+        w.n = warp_uniform(w.n);
+        if (w.n == 0) continue;
+        const uint32_t qs = it & 1;
+        if (!(ok = mbar_wait_warp(&bars->q_full[qs], (it >> 1) & 1))) break;
+        // K(0): both S of the first step
+        if (!(ok = mbar_wait_warp(&bars->kv_full[kvc % NKV], (kvc / NKV) & 1))) break;
+        tc_fence_after();
+        issue_s(0, qs, kvc);
+        issue_s(1, qs, kvc);
+        mma_commit_warp(&bars->kv_empty[kvc % NKV]);
+        ++kvc;
+        for (int j = 0; j < w.n && ok; ++j) {
+          const uint32_t k = st + j;
+          const uint32_t vc = kvc;  // V(j)
+          const bool more = j + 1 < w.n;
+          if (!(ok = mbar_wait_warp(&bars->kv_full[vc % NKV], (vc / NKV) & 1))) break;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!(ok = mbar_wait_warp(&bars->p_full[x], k & 1))) break;
+            ATTN_TL(30 + x, k);
+            if (j == 0 && it > 0 && !(ok = mbar_wait_warp(&bars->o_empty[x], (it - 1) & 1))) break;
+            tc_fence_after();
+            issue_pv(x, vc, j == 0);
+            if (!more) {
+              mma_commit_warp(&bars->o_full[x]);
+              continue;
             }
-            if (!ok) break;
-            mma_commit(&bars->kv_empty[vc % NKV]);  // V(j) read by both P V
-            if (more) mma_commit(&bars->kv_empty[(vc + 1) % NKV]);  // K(j+1) by both S
-            kvc += more ? 2 : 1;
+            // S_X(j+1) over P_X(j), after P_X(j) V (same issuer, in-order pipe)
+            if (x == 0 &&
+                !(ok = mbar_wait_warp(&bars->kv_full[(vc + 1) % NKV], ((vc + 1) / NKV) & 1)))
+              break;
+            tc_fence_after();
+            issue_s(x, qs, vc + 1);
+            ATTN_TL(32 + x, k + 1);
           }
           if (!ok) break;
-          mma_commit(&bars->q_empty[qs]);  // every S of this item done once these land
-          st += w.n;
-          ++it;
+          mma_commit_warp(&bars->kv_empty[vc % NKV]);  // V(j) read by both P V
+          if (more) mma_commit_warp(&bars->kv_empty[(vc + 1) % NKV]);  // K(j+1) by both S
+          kvc += more ? 2 : 1;
         }
-        if (!ok) {
-          report_timeout(a, 0x620);
-          *abort_flag = 1;
-        }
-        mma_commit(&bars->drain);
-        mbar_wait(&bars->drain, 0, 200000000ull);
+        if (!ok) break;
+        mma_commit_warp(&bars->q_empty[qs]);  // every S of this item done once these land
+        st += w.n;
+        ++it;
       }
+      if (!ok && lane == 0) {
+        report_timeout(a, 0x620);
+        *abort_flag = 1;
+      }
+      mma_commit_warp(&bars->drain);
+      mbar_wait(&bars->drain, 0, 200000000ull);
     }  // warps 2 and 3 have no role
   } else {
     regs_raise<200>();

@@ -187,6 +187,107 @@ SM103_DEV void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t
       : "memory");
 }
 
+// ---------------------------------------------------------------- warp-collective MMA issue
+// The issuing warp runs its loop converged, on warp-uniform values, and one
+// elected lane issues.  All K slices of one GEMM (K = 16 * NK) go out from one
+// asm statement whose per-slice operand steps are immediates, so an MMA costs
+// a handful of instructions.  With a lone lane issuing one asm per MMA, the
+// operands are per-thread values that have to be moved into the uniform
+// registers the MMA reads, and next to arithmetic-bound warps on the same
+// scheduler that issue slowed to 150-170 clk per 128x128x16 MMA (a probe on
+// this GPU); issued this way it stays at the tensor core's 64 clk.
+//
+// Steps (16-byte units for descriptors, columns for tensor-memory addresses)
+// from slice k-1 to slice k: S for k = 1..3, 5..7 and J for k = 4.
+//   K-major 128-byte-swizzled tile, 64-column chunks 16 KB apart:  S 2,  J 1018
+//   MN-major 128-byte-swizzled tile (16 rows of 128 B per slice):  S 128, J 128
+//   packed 16-bit pairs in tensor memory, contiguous:              S 8,  J 8
+//   the same in two 32-column halves 64 columns apart:             S 8,  J 40
+#define SM103_MMA_F16 "@e tcgen05.mma.cta_group::1.kind::f16 "
+#define SM103_SS_STEP(ai, bi)                                                        \
+  "add.u32 alo, alo, %" #ai ";\n\tadd.u32 blo, blo, %" #bi ";\n\t"                \
+  "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16           \
+  "[%0], ad, bd, %3, p1;\n\t"
+#define SM103_TS_STEP(ai, bi)                                                        \
+  "add.u32 at, at, %" #ai ";\n\tadd.u32 blo, blo, %" #bi ";\n\t"                  \
+  "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+
+// D[tmem] (+)= A[smem] B[smem] over NK K-slices; the first slice accumulates
+// iff `accumulate`, the others always.
+template <int NK, int AS, int AJ, int BS, int BJ>
+SM103_DEV void mma_ss_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                           uint32_t accumulate) {
+  static_assert(NK == 4 || NK == 8, "K slices per GEMM");
+  if constexpr (NK == 8) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 alo, ahi, blo, bhi;\n\t.reg .b64 ad, bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+        "mov.b64 {alo, ahi}, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t" SM103_MMA_F16
+        "[%0], %1, %2, %3, p0;\n\t" SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8)
+            SM103_SS_STEP(7, 9) SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) "}" ::"r"(
+                d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u), "n"(AS), "n"(AJ), "n"(BS),
+        "n"(BJ)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 alo, ahi, blo, bhi;\n\t.reg .b64 ad, bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+        "mov.b64 {alo, ahi}, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t" SM103_MMA_F16
+        "[%0], %1, %2, %3, p0;\n\t" SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) "}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u), "n"(AS), "n"(AJ), "n"(BS),
+        "n"(BJ)
+        : "memory");
+  }
+}
+
+// D[tmem] (+)= A[tmem] B[smem] over NK K-slices (A: packed 16-bit pairs).
+template <int NK, int AS, int AJ, int BS, int BJ>
+SM103_DEV void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                           uint32_t accumulate) {
+  static_assert(NK == 4 || NK == 8, "K slices per GEMM");
+  if constexpr (NK == 8) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 at, blo, bhi;\n\t.reg .b64 bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+        "mov.b32 at, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t" SM103_MMA_F16
+        "[%0], [%1], %2, %3, p0;\n\t" SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8)
+            SM103_TS_STEP(7, 9) SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) "}" ::"r"(
+                d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u), "n"(AS), "n"(AJ), "n"(BS),
+        "n"(BJ)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 at, blo, bhi;\n\t.reg .b64 bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+        "mov.b32 at, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t" SM103_MMA_F16
+        "[%0], [%1], %2, %3, p0;\n\t" SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) "}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u), "n"(AS), "n"(AJ), "n"(BS),
+        "n"(BJ)
+        : "memory");
+  }
+}
+
+// The commit below, issued by the elected lane of a converged warp.
+SM103_DEV void mma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// Lane 0's value, known to the compiler to be the same in every lane.
+SM103_DEV int warp_uniform(int v) { return __shfl_sync(0xffffffffu, v, 0); }
+SM103_DEV uint32_t warp_uniform(uint32_t v) { return __shfl_sync(0xffffffffu, v, 0); }
+
 // Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
 SM103_DEV void mma_commit(uint64_t* bar) {
   asm volatile(
