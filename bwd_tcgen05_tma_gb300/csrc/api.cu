@@ -205,6 +205,22 @@ bool make_map(CUtensorMap* m, const void* base, int D, int H, int64_t T, int64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over a token-major tensor of B rows of S tokens: dims {D, H, S, B},
+// box {64, 1, rows, 1}.  Stores through it stop at each batch row's end.
+bool make_map_4d(CUtensorMap* m, const void* base, int D, int H, int64_t S, int B,
+                 int64_t tok_stride, int rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)tok_stride * 2,
+                           (cuuint64_t)(S * tok_stride * 2)};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D map over the fp32 dQ accumulator [T, H, D]: box {32, 1, 64}, no swizzle.
 bool make_map_f32(CUtensorMap* m, const void* base, int D, int H, int64_t T) {
   auto fn = encode_fn();
@@ -427,7 +443,8 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
   fill_common(a, p, static_cast<char*>(ws), pl);
   if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
       !make_map(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
-      !make_map(&a.tm_v, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile))
+      !make_map(&a.tm_v, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
+      !make_map_4d(&a.tm_o, o, p->d_v, p->Hq, p->Sq, p->B, (int64_t)p->Hq * p->d_v, kTile))
     return ATTN_ERR_CUDA;
   a.o = static_cast<bf16*>(o);
   a.lse = lse;

@@ -95,6 +95,71 @@ __device__ __forceinline__ bool ring_pop_warp1(ItemRing* r, uint32_t n, int32_t&
   return true;
 }
 
+// A ring of work items that also carries what the producer looked up once
+// per item: entry = (item index or -1 at the end, key tiles, first key, 0).
+// The producer claims and publishes items itself (it may claim one ahead of
+// what it publishes, see the forward), so consumers need no global loads to
+// start an item.
+struct ItemRing4 {
+  uint64_t full[kItemRing];
+  uint64_t empty[kItemRing];
+  int4 item[kItemRing];
+};
+
+__device__ __forceinline__ void ring4_init(ItemRing4* r, uint32_t consumers) {
+  for (int i = 0; i < kItemRing; ++i) {
+    sm103::mbar_init(&r->full[i], 1);
+    sm103::mbar_init(&r->empty[i], consumers);
+  }
+}
+
+// Producer: publish entry n once its slot is free (false: the wait timed out).
+__device__ __forceinline__ bool ring4_publish(ItemRing4* r, uint32_t n, int4 v) {
+  const int s = n % kItemRing;
+  if (n >= (uint32_t)kItemRing && !sm103::mbar_wait(&r->empty[s], ((n / kItemRing) - 1) & 1))
+    return false;
+  r->item[s] = v;
+  sm103::mbar_arrive(&r->full[s]);  // release: the entry is visible to waiters
+  return true;
+}
+
+// Single-thread consumer (the TMA producer); `ready` tests without waiting.
+__device__ __forceinline__ bool ring4_ready(ItemRing4* r, uint32_t n) {
+  return sm103::mbar_test_wait(&r->full[n % kItemRing], (n / kItemRing) & 1);
+}
+__device__ __forceinline__ bool ring4_pop1(ItemRing4* r, uint32_t n, int4& v) {
+  const int s = n % kItemRing;
+  if (!sm103::mbar_wait(&r->full[s], (n / kItemRing) & 1)) return false;
+  v = r->item[s];
+  sm103::mbar_arrive(&r->empty[s]);
+  return true;
+}
+
+// Consumer, every thread of the consuming warps (each arrives once).
+__device__ __forceinline__ bool ring4_pop(ItemRing4* r, uint32_t n, int4& v) {
+  const int s = n % kItemRing;
+  if (!sm103::mbar_wait_warp(&r->full[s], (n / kItemRing) & 1)) return false;
+  v = r->item[s];
+  sm103::mbar_arrive(&r->empty[s]);
+  return true;
+}
+
+// Consumer warp that counts as one arrival; v is warp-uniform.
+__device__ __forceinline__ bool ring4_pop_warp1(ItemRing4* r, uint32_t n, int4& v) {
+  const int s = n % kItemRing;
+  if (!sm103::mbar_wait_warp(&r->full[s], (n / kItemRing) & 1)) return false;
+  int4 t = make_int4(0, 0, 0, 0);
+  if ((threadIdx.x & 31) == 0) {
+    t = r->item[s];
+    sm103::mbar_arrive(&r->empty[s]);
+  }
+  v.x = sm103::warp_uniform(t.x);
+  v.y = sm103::warp_uniform(t.y);
+  v.z = sm103::warp_uniform(t.z);
+  v.w = sm103::warp_uniform(t.w);
+  return true;
+}
+
 // Summary of 64 consecutive tokens of one batch row.
 struct ChunkInfo {
   int32_t min_id;   // smallest nonzero id (INT32_MAX if none)
@@ -113,6 +178,7 @@ struct KernelArgs {
   CUtensorMap tm_v;    // dims {d_v, Hkv, B*Skv},  box {64, 1, 128}
   CUtensorMap tm_do;   // dims {d_v, Hq, B*Sq},    box {64, 1, 128 or 64}
   CUtensorMap tm_dqacc;  // fp32 dQ accumulator: dims {d_qk, Hq, B*Sq}, box {32, 1, 64}
+  CUtensorMap tm_o;    // forward output O: dims {d_v, Hq, Sq, B}, box {64, 1, 128, 1}
 
   int B, Sq, Skv, Hq, Hkv, d_qk, d_v;
   // Position mask: a key at position pk is kept for a query at position pq
@@ -182,7 +248,7 @@ constexpr int kTimelineCap = 64 * kTimelineSteps;
 static __device__ unsigned long long g_timeline[kTimelineCap];  // one copy per translation unit
 #define ATTN_TL(ev, step)                                                                    \
   do {                                                                                       \
-    if (blockIdx.x == 0 && (step) < kTimelineSteps)                                          \
+    if (blockIdx.x == 0 && (ev) >= 0 && (ev) < 64 && (step) >= 0 && (step) < kTimelineSteps) \
       g_timeline[(ev) * kTimelineSteps + (step)] = (unsigned long long)clock64();            \
   } while (0)
 #else

@@ -34,10 +34,13 @@ template <int DQK, int DV>
 struct F2Layout {
   static constexpr int kQBytes = kTile * DQK * 2;                  // one head's Q tile
   static constexpr int kKVBytes = kTile * (DQK > DV ? DQK : DV) * 2;  // one K or V stage
+  // one head's Q stage; once the item's S MMAs are done it stages that head's
+  // O tile for the TMA store, so it holds the larger of the two
+  static constexpr int kQStage = kKVBytes;
   static constexpr int kQStages = 2;   // Q of the next item loads during this one
   static constexpr int kKVStages = 3;  // K(j), V(j), K(j+1) in flight
   static constexpr int kQOff = 0;      // [stage][head]
-  static constexpr int kKVOff = kQStages * 2 * kQBytes;
+  static constexpr int kKVOff = kQStages * 2 * kQStage;
   static constexpr int kBarOff = kKVOff + kKVStages * kKVBytes;
   static constexpr int kBytes = kBarOff + 512;
   static constexpr int kAlloc = kBytes;  // the dynamic window is 1 KB-aligned (checked)
@@ -53,7 +56,7 @@ struct F2Bars {
 };
 
 struct F2Item {
-  int b, t, h0, kv_lo, n;
+  int b, t, h0;
 };
 
 // item = (query tile, head pair), longest causal tiles first
@@ -65,17 +68,32 @@ __device__ __forceinline__ F2Item f2_item(const KernelArgs& a, int idx) {
   it.t = a.n_qt - 1 - t_rev;
   it.b = rem / hp;
   it.h0 = 2 * (rem - it.b * hp);
-  const int2 r = a.q_tile_range[it.b * a.n_qt + it.t];
-  it.kv_lo = r.x;
-  it.n = (r.y > r.x) ? (r.y - r.x + kTile - 1) / kTile : 0;
   return it;
 }
 
+// Ring entry of item idx: (idx, key tiles, first key, 0); (-1, 0, 0, 0) past the end.
+__device__ __forceinline__ int4 f2_entry(const KernelArgs& a, int idx, int n_items) {
+  if (idx >= n_items) return make_int4(-1, 0, 0, 0);
+  const F2Item w = f2_item(a, idx);
+  const int2 r = a.q_tile_range[w.b * a.n_qt + w.t];
+  const int n = (r.y > r.x) ? (r.y - r.x + kTile - 1) / kTile : 0;
+  return make_int4(idx, n, r.x, 0);
+}
+
+// Per-row state of one softmax thread for one item.
+struct F2Row {
+  int h, i, b, rlo, rhi, my_id, my_pos;
+  bool row_ok;
+  int64_t grow;
+  const bf16* bias_row;
+};
+
 // One 32-column chunk of a score row in log2 units: bias and, for chunks not
 // valid throughout the warp, the key mask (separate instantiations keep the
-// per-element code free of branches).
+// per-element code free of branches).  The mask also writes -inf over the
+// masked scores, so the exponential pass needs no mask of its own.
 template <bool MASKED, bool HAS_BIAS>
-__device__ __forceinline__ void chunk_max2(const uint32_t (&u)[32], uint32_t m32, float scale_log2,
+__device__ __forceinline__ void chunk_max2(uint32_t (&u)[32], uint32_t m32, float scale_log2,
                                            const bf16* bias_row, int kc0, int Skv, bool row_ok,
                                            float (&mx8)[8]) {
 #pragma unroll
@@ -83,12 +101,12 @@ __device__ __forceinline__ void chunk_max2(const uint32_t (&u)[32], uint32_t m32
     float x[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
+      if (MASKED) u[e + t] = (m32 & (1u << (e + t))) ? u[e + t] : 0xff800000u;  // -inf
       x[t] = __uint_as_float(u[e + t]);
       if (HAS_BIAS) {
         x[t] *= scale_log2;
         if (row_ok && kc0 + e + t < Skv) x[t] += __bfloat162float(bias_row[kc0 + e + t]) * kLog2e;
       }
-      if (MASKED) x[t] = (m32 & (1u << (e + t))) ? x[t] : -INFINITY;
     }
     mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], x[0], x[1]);
   }
@@ -145,14 +163,14 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
   F2Bars* bars = reinterpret_cast<F2Bars*>(sm + L::kBarOff);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(F2Bars));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  ItemRing* ring = reinterpret_cast<ItemRing*>(sm + L::kBarOff + 256);
+  ItemRing4* ring = reinterpret_cast<ItemRing4*>(sm + L::kBarOff + 256);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = a.B * a.n_qt * (a.Hq / 2);
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->q_full[s], 1);
-      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->q_empty[s], 2);  // the two epilogue stores
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 128);
       mbar_init(&bars->o_full[s], 1);
@@ -163,7 +181,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       mbar_init(&bars->kv_empty[s], 1);
     }
     mbar_init(&bars->drain, 1);
-    ring_init(ring, 1 + 256);  // MMA issuer, two softmax warpgroups
+    ring4_init(ring, 1 + 1 + 256);  // TMA producer, MMA issuer, two softmax warpgroups
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -187,11 +205,16 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
     regs_lower<104>();  // once for the whole warpgroup
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer
+      // Takes the items from the ring like every other role.  While it streams
+      // the K / V tiles of the current item it already takes the next item
+      // (once the scheduler has published it) and loads that item's Q tiles
+      // as soon as their stage is free, so the next item's first S can follow
+      // this item's last one.
       if (lane == 0) {
         prefetch_tensormap(&a.tm_q);
         prefetch_tensormap(&a.tm_k);
         prefetch_tensormap(&a.tm_v);
-        uint32_t it = 0, kvc = 0;  // kvc: K / V stage loads issued, in ring order
+        uint32_t qi = 0, kvc = 0, rn = 0;  // Q tile pairs, K / V stage loads, ring entries
         bool ok = true;
         auto load_kv = [&](const CUtensorMap* m, int ncols, int g, int krow) -> bool {
           const int s = kvc % NKV;
@@ -204,37 +227,77 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           ++kvc;
           return true;
         };
-        for (uint32_t rn = 0;; ++rn) {
-          int32_t idx;
-          if (!ok || *abort_flag ||
-              !(ok = ring_push(ring, rn, &a.hdr->next_item[0], n_items, idx)) ||
-              idx < 0)
-            break;
-          const F2Item w = f2_item(a, idx);
-          if (w.n == 0) continue;
-          const int qs = it & 1;
-          if (it >= 2 && !(ok = mbar_wait(&bars->q_empty[qs], ((it >> 1) - 1) & 1))) break;
+        // both heads' Q tiles of item e into stage qi & 1 (its previous user done)
+        auto q_free = [&]() -> bool {
+          return qi < 2 || mbar_test_wait(&bars->q_empty[qi & 1], ((qi >> 1) - 1) & 1);
+        };
+        auto load_q = [&](int4 e) -> bool {
+          const int qs = qi & 1;
+          if (qi >= 2 && !mbar_wait(&bars->q_empty[qs], ((qi >> 1) - 1) & 1)) return false;
+          const F2Item w = f2_item(a, e.x);
           const int qrow = w.b * a.Sq + w.t * kTile;
           mbar_arrive_expect_tx(&bars->q_full[qs], 2 * L::kQBytes);
+          ATTN_TL(50, qi);
           for (int x = 0; x < 2; ++x) {
-            uint8_t* dst = sm + L::kQOff + (qs * 2 + x) * L::kQBytes;
+            uint8_t* dst = sm + L::kQOff + (qs * 2 + x) * L::kQStage;
   #pragma unroll
             for (int c = 0; c < DQK / 64; ++c)
               tma_load_3d(dst + c * 16384, &a.tm_q, &bars->q_full[qs], c * 64, w.h0 + x, qrow);
           }
-          ++it;
-          const int g = w.h0 / (a.Hq / a.Hkv);
-          for (int j = 0; j < w.n && ok; ++j) {
-            const int krow = w.b * a.Skv + w.kv_lo + j * kTile;
-            ok = load_kv(&a.tm_k, DQK, g, krow) && load_kv(&a.tm_v, DV, g, krow);
+          ++qi;
+          return true;
+        };
+        // the next item with key tiles (or the end marker), waiting for the
+        // scheduler if `wait`; items without key tiles need no loads.  Returns
+        // false without a result when not waiting and nothing is published yet.
+        auto next_item = [&](bool wait, int4& e) -> bool {
+          for (;;) {
+            if (!wait && !ring4_ready(ring, rn)) return false;  // e untouched
+            int4 t;
+            if (!(ok = ring4_pop1(ring, rn, t))) {
+              e = make_int4(-1, 0, 0, 0);
+              return true;
+            }
+            ++rn;
+            if (t.x < 0 || t.y > 0) {
+              e = t;
+              return true;
+            }
           }
+        };
+        int4 cur;
+        next_item(true, cur);
+        bool cur_q = false;  // cur's Q already loaded
+        while (ok && cur.x >= 0 && !*abort_flag) {
+          if (!cur_q && !(ok = load_q(cur))) break;
+          ATTN_TL(49, qi - 1);
+          const F2Item w = f2_item(a, cur.x);
+          const int g = w.h0 / (a.Hq / a.Hkv);
+          int4 held = make_int4(-2, 0, 0, 0);  // -2: next item not taken yet
+          bool held_q = false;
+          for (int j = 0; j < cur.y && ok; ++j) {
+            const int krow = w.b * a.Skv + cur.z + j * kTile;
+            if (!(ok = load_kv(&a.tm_k, DQK, g, krow))) break;
+            ATTN_TL(55, (kvc - 1) >> 1);
+            if (!(ok = load_kv(&a.tm_v, DV, g, krow))) break;
+            ATTN_TL(56, (kvc - 1) >> 1);
+            if (held.x == -2) next_item(false, held);
+            if (!held_q && held.x >= 0 && q_free()) {
+              if (!(ok = load_q(held))) break;
+              held_q = true;
+            }
+          }
+          if (!ok) break;
+          if (held.x == -2) next_item(true, held);
+          cur = held;
+          cur_q = held_q;
         }
         if (!ok) {
           report_timeout(a, 0x610);
           *abort_flag = 1;
         }
         if (*abort_flag) {  // let copies in flight land before the CTA exits
-          for (uint32_t u = (it > 2u ? it - 2u : 0u); u < it; ++u)
+          for (uint32_t u = (qi > 2u ? qi - 2u : 0u); u < qi; ++u)
             mbar_wait(&bars->q_full[u & 1], (u >> 1) & 1, 100000000ull);
           for (uint32_t u = (kvc > (uint32_t)NKV ? kvc - NKV : 0u); u < kvc; ++u)
             mbar_wait(&bars->kv_full[u % NKV], (u / NKV) & 1, 100000000ull);
@@ -257,7 +320,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       };
       // S_X(step) = Q_X K^T; K at ring position kc
       auto issue_s = [&](int x, uint32_t qs, uint32_t kc) {
-        const uint64_t qd = q_km + static_cast<uint32_t>(((qs * 2 + x) * L::kQBytes) >> 4);
+        const uint64_t qd = q_km + static_cast<uint32_t>(((qs * 2 + x) * L::kQStage) >> 4);
         const uint64_t kd = kv_km + stage_off(kc);
         mma_ss_warp<DQK / 16, 2, 1018, 2, 1018>(tm + L::kColS + x * kTile, qd, kd, id_s, 0u);
         mma_commit_warp(&bars->s_full[x]);
@@ -268,55 +331,74 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         mma_ts_warp<kTile / 16, 8, 8, 128, 128>(tm + L::kColO + x * kTile, tm + L::kColS + x * kTile,
                                                 vd, id_o, first ? 0u : 1u);
       };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) ||
-            !(ok = ring_pop_warp1(ring, rn, idx)) || idx < 0)
-          break;
-        F2Item w = f2_item(a, idx);
-        w.n = warp_uniform(w.n);
-        if (w.n == 0) continue;
+      uint32_t rn = 0;
+      // the next item with key tiles (-1: the end); items without any need
+      // no MMAs
+      auto next_item = [&](int4& e) -> bool {
+        do {
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+          if (!ring4_pop_warp1(ring, rn++, e)) return false;
+        } while (e.x >= 0 && e.y == 0);
+        return true;
+      };
+      int4 cur;
+      if (!(ok = next_item(cur))) cur.x = -1;
+      if (cur.x >= 0) {  // both S of the first item's first step
+        ATTN_TL(42, 0);
+        if ((ok = mbar_wait_warp(&bars->q_full[0], 0) &&
+                  mbar_wait_warp(&bars->kv_full[0], 0))) {
+          tc_fence_after();
+          issue_s(0, 0, 0);
+          issue_s(1, 0, 0);
+          mma_commit_warp(&bars->kv_empty[0]);
+          kvc = 1;
+        }
+      }
+      // Each step j: P_X(j) V, then the S that reuses P_X(j)'s columns: S_X(j+1)
+      // of this item or, at its last step, S_X(0) of the next item, so that the
+      // next item starts the way a step does.
+      while (ok && cur.x >= 0) {
+        const int n = cur.y;
         const uint32_t qs = it & 1;
-        if (!(ok = mbar_wait_warp(&bars->q_full[qs], (it >> 1) & 1))) break;
-        // K(0): both S of the first step
-        if (!(ok = mbar_wait_warp(&bars->kv_full[kvc % NKV], (kvc / NKV) & 1))) break;
-        tc_fence_after();
-        issue_s(0, qs, kvc);
-        issue_s(1, qs, kvc);
-        mma_commit_warp(&bars->kv_empty[kvc % NKV]);
-        ++kvc;
-        for (int j = 0; j < w.n && ok; ++j) {
+        int4 nxt = make_int4(-1, 0, 0, 0);
+        for (int j = 0; j < n && ok; ++j) {
           const uint32_t k = st + j;
-          const uint32_t vc = kvc;  // V(j)
-          const bool more = j + 1 < w.n;
+          const uint32_t vc = kvc;  // V(j); the next S reads K at vc + 1
+          const bool more = j + 1 < n;
+          if (!more && !(ok = next_item(nxt))) break;
+          const bool go_on = more || nxt.x >= 0;  // an S follows this step's P V
+          const uint32_t qs_s = more ? qs : ((it + 1) & 1);
           if (!(ok = mbar_wait_warp(&bars->kv_full[vc % NKV], (vc / NKV) & 1))) break;
+          ATTN_TL(57, k);
           for (int x = 0; x < 2 && ok; ++x) {
             if (!(ok = mbar_wait_warp(&bars->p_full[x], k & 1))) break;
             ATTN_TL(30 + x, k);
             if (j == 0 && it > 0 && !(ok = mbar_wait_warp(&bars->o_empty[x], (it - 1) & 1))) break;
             tc_fence_after();
             issue_pv(x, vc, j == 0);
-            if (!more) {
-              mma_commit_warp(&bars->o_full[x]);
-              continue;
+            ATTN_TL(40 + x, k);
+            if (!more) mma_commit_warp(&bars->o_full[x]);
+            if (!go_on) continue;
+            // the next S over P_X(j), after P_X(j) V (same issuer, in-order pipe)
+            if (x == 0) {
+              if (!more && !(ok = mbar_wait_warp(&bars->q_full[qs_s], ((it + 1) >> 1) & 1))) break;
+              if (!(ok = mbar_wait_warp(&bars->kv_full[(vc + 1) % NKV], ((vc + 1) / NKV) & 1)))
+                break;
             }
-            // S_X(j+1) over P_X(j), after P_X(j) V (same issuer, in-order pipe)
-            if (x == 0 &&
-                !(ok = mbar_wait_warp(&bars->kv_full[(vc + 1) % NKV], ((vc + 1) / NKV) & 1)))
-              break;
             tc_fence_after();
-            issue_s(x, qs, vc + 1);
+            issue_s(x, qs_s, vc + 1);
             ATTN_TL(32 + x, k + 1);
           }
           if (!ok) break;
           mma_commit_warp(&bars->kv_empty[vc % NKV]);  // V(j) read by both P V
-          if (more) mma_commit_warp(&bars->kv_empty[(vc + 1) % NKV]);  // K(j+1) by both S
-          kvc += more ? 2 : 1;
+          if (go_on) mma_commit_warp(&bars->kv_empty[(vc + 1) % NKV]);  // the next K by both S
+          kvc += go_on ? 2 : 1;
         }
         if (!ok) break;
-        mma_commit_warp(&bars->q_empty[qs]);  // every S of this item done once these land
-        st += w.n;
+        // this item's Q stage is released by the epilogue once its O store has read it
+        st += n;
         ++it;
+        cur = nxt;
       }
       if (!ok && lane == 0) {
         report_timeout(a, 0x620);
@@ -324,7 +406,24 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       }
       mma_commit_warp(&bars->drain);
       mbar_wait(&bars->drain, 0, 200000000ull);
-    }  // warps 2 and 3 have no role
+    } else if (warp == 2) {
+      // ------------------------------------------------------------ scheduler
+      // Claims work items from the global counter, looks up each one's key
+      // range and publishes them in order; every other role takes them from
+      // the ring, so the latency of the claim is off their paths.
+      if (lane == 0) {
+        for (uint32_t pub = 0;; ++pub) {
+          const int4 e = f2_entry(a, atomicAdd(&a.hdr->next_item[0], 1), n_items);
+          if (*abort_flag) break;
+          if (!ring4_publish(ring, pub, e)) {
+            report_timeout(a, 0x640);
+            *abort_flag = 1;
+            break;
+          }
+          if (e.x < 0) break;
+        }
+      }
+    }  // warp 3 has no role
   } else {
     regs_raise<200>();
     // ------------------------------------------------------------ softmax + epilogue
@@ -333,20 +432,47 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tm = tmem + lane_base + L::kColS + x * kTile;
     const uint32_t o_tm = tmem + lane_base + L::kColO + x * kTile;
-    uint32_t st = 0, it = 0;
+    uint32_t st = 0, it = 0, rn = 0;
+    int store_stage = -1;  // thread r == 0: Q stage its last O store still reads
     bool ok = true;
-    for (uint32_t rn = 0;; ++rn) {
-      int32_t idx;
-      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
-          idx < 0)
-        break;
-      const F2Item w = f2_item(a, idx);
-      const int h = w.h0 + x;
-      const int i = w.t * kTile + r;
-      const bool row_ok = i < a.Sq;
-      const int64_t grow = (int64_t)w.b * a.Sq + i;
-      bf16* orow = a.o + (grow * a.Hq + h) * DV;
-      float* lse_out = a.lse + ((int64_t)w.b * a.Hq + h) * a.Sq + i;
+    // this thread's row of item e: indices, mask range or metadata, bias row
+    // (the loads are issued here and consumed at the item's first step)
+    auto row_of = [&](const int4& e) -> F2Row {
+      F2Row R;
+      R.rlo = R.rhi = R.my_id = R.my_pos = 0;
+      R.bias_row = nullptr;
+      const F2Item w = f2_item(a, e.x >= 0 ? e.x : 0);
+      R.b = w.b;
+      R.h = w.h0 + x;
+      R.i = w.t * kTile + r;
+      R.row_ok = e.x >= 0 && R.i < a.Sq;
+      R.grow = (int64_t)w.b * a.Sq + R.i;
+      if (R.row_ok && e.y > 0) {
+        if (!general) {
+          const int2 kr = band_keys_of_query(a, R.i, a.seg_lo[R.grow], a.seg_hi[R.grow]);
+          R.rlo = kr.x;
+          R.rhi = kr.y;
+        } else {
+          R.my_id = a.q_id[R.grow];
+          R.my_pos = a.q_pos[R.grow];
+        }
+        if (HAS_BIAS) {
+          const int bb = a.bias_b > 1 ? w.b : 0, bh = a.bias_h > 1 ? R.h : 0;
+          R.bias_row = a.bias + (((int64_t)bb * a.bias_h + bh) * a.Sq + R.i) * a.Skv;
+        }
+      }
+      return R;
+    };
+    int4 e = make_int4(-1, 0, 0, 0);
+    if (!(ok = ring4_pop(ring, rn++, e))) e.x = -1;
+    F2Row R = row_of(e);
+    while (ok && e.x >= 0 && !__any_sync(0xffffffffu, *abort_flag != 0)) {
+      const int h = R.h;
+      const int i = R.i;
+      const bool row_ok = R.row_ok;
+      bf16* orow = a.o + (R.grow * a.Hq + h) * DV;
+      float* lse_out = a.lse + ((int64_t)R.b * a.Hq + h) * a.Sq + i;
+      struct { int b, n, kv_lo; } w = {R.b, e.y, e.z};
       if (w.n == 0) {
         if (row_ok) {
 #pragma unroll
@@ -354,24 +480,12 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
             *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
           *lse_out = a.sink ? a.sink[h] : -INFINITY;  // only the sink, if any
         }
+        if (!(ok = ring4_pop(ring, rn++, e))) break;
+        R = row_of(e);
         continue;
       }
-      int rlo = 0, rhi = 0, my_id = 0, my_pos = 0;
-      if (row_ok) {
-        if (!general) {
-          const int2 kr = band_keys_of_query(a, i, a.seg_lo[grow], a.seg_hi[grow]);
-          rlo = kr.x;
-          rhi = kr.y;
-        } else {
-          my_id = a.q_id[grow];
-          my_pos = a.q_pos[grow];
-        }
-      }
-      const bf16* bias_row = nullptr;
-      if (HAS_BIAS && row_ok) {
-        const int bb = a.bias_b > 1 ? w.b : 0, bh = a.bias_h > 1 ? h : 0;
-        bias_row = a.bias + (((int64_t)bb * a.bias_h + bh) * a.Sq + i) * a.Skv;
-      }
+      const int rlo = R.rlo, rhi = R.rhi, my_id = R.my_id, my_pos = R.my_pos;
+      const bf16* bias_row = R.bias_row;
       float m_ref = -INFINITY, l = 0.f;
       float row_max = -INFINITY;  // exact row max of the scaled logits (log2 units)
       for (int j = 0; j < w.n; ++j) {
@@ -390,6 +504,12 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         }
         if (!(ok = mbar_wait_warp(&bars->s_full[x], k & 1))) break;
         if (lane == 0 && (warp & 3) == 0) ATTN_TL(34 + x, k);
+        if (lane == 0 && x == 0) ATTN_TL(8 + (warp - 4), k);
+        if (r == 0 && store_stage >= 0) {  // the previous item's O store has read its stage
+          bulk_wait_read_all();
+          mbar_arrive(&bars->q_empty[store_stage]);
+          store_stage = -1;
+        }
         tc_fence_after();
         // the whole S row of this thread in registers: four loads, one wait
         uint32_t u[4][32];
@@ -429,12 +549,9 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           if (none[q]) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) pk[e] = 0u;
-          } else if (all[q]) {
+          } else {  // masked scores are -inf by now: exp2 gives 0 there
             chunk_exp2<false, HAS_BIAS>(u[q], m32s[q], a.scale_log2, m_use, bias_row, k0 + q * 32,
                                         a.Skv, row_ok, rs4, pk);
-          } else {
-            chunk_exp2<true, HAS_BIAS>(u[q], m32s[q], a.scale_log2, m_use, bias_row, k0 + q * 32,
-                                       a.Skv, row_ok, rs4, pk);
           }
           tmem_st32x32b_x16(s_tm + q * 16, pk);
         }
@@ -456,11 +573,18 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         tmem_st_wait();
         tc_fence_before();
         if (lane == 0 && (warp & 3) == 0) ATTN_TL(38 + x, k);
+        if (lane == 0) ATTN_TL(0 + (warp - 4), k);
         mbar_arrive(&bars->p_full[x]);
       }
       if (!ok) break;
+      // the next item, popped now so that its row loads overlap this epilogue
+      int4 e_next;
+      if (!(ok = ring4_pop(ring, rn++, e_next))) break;
+      if (lane == 0 && warp == 4) ATTN_TL(46, it);
+      const F2Row R_next = row_of(e_next);
       // epilogue: O / l and LSE
       if (!(ok = mbar_wait_warp(&bars->o_full[x], it & 1))) break;
+      if (lane == 0 && warp == 4) ATTN_TL(47, it);
       tc_fence_after();
       // the sink logit, if any, joins the normaliser (it has no value vector)
       float l_fin = l, m_fin = m_ref, o_scale = 1.f;
@@ -473,34 +597,56 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         }
       }
       const float inv_l = (l_fin > 0.f) ? o_scale / l_fin : 0.f;
+      // O / l in bf16 into this head's Q stage of the item (its S MMAs are
+      // done, o_full says so), laid out as the store map's 128-byte-swizzled
+      // 64-column boxes: 16-byte chunk c of row r at chunk c ^ (r % 8).  One
+      // row per thread; each group of 8 rows spreads over all banks.
+      uint8_t* stg = sm + L::kQOff + ((it & 1) * 2 + x) * L::kQStage;
 #pragma unroll
       for (int q = 0; q < DV / 32; ++q) {
         uint32_t u[32];
         tmem_ld32x32b_x32(o_tm + q * 32, u);
         tmem_ld_wait();
-        if (row_ok) {
+        const uint32_t row = smem_u32(stg + (q >> 1) * 16384 + r * 128);
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(u[c + 0]) * inv_l, __uint_as_float(u[c + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * inv_l, __uint_as_float(u[c + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * inv_l, __uint_as_float(u[c + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * inv_l, __uint_as_float(u[c + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + q * 32 + c) = v;
-          }
+        for (int c = 0; c < 4; ++c) {
+          const int e8 = c * 8;
+          const uint32_t chunk = static_cast<uint32_t>(((q & 1) * 4 + c) ^ (r & 7));
+          st_shared_v4(row + chunk * 16,
+                       pack_bf16x2(__uint_as_float(u[e8 + 0]) * inv_l, __uint_as_float(u[e8 + 1]) * inv_l),
+                       pack_bf16x2(__uint_as_float(u[e8 + 2]) * inv_l, __uint_as_float(u[e8 + 3]) * inv_l),
+                       pack_bf16x2(__uint_as_float(u[e8 + 4]) * inv_l, __uint_as_float(u[e8 + 5]) * inv_l),
+                       pack_bf16x2(__uint_as_float(u[e8 + 6]) * inv_l, __uint_as_float(u[e8 + 7]) * inv_l));
         }
+      }
+      // every row of the tile is in shared memory: one thread stores it (rows
+      // past the batch row's end are clipped by the map); the stage is
+      // released once the store has read it (checked at the next item)
+      fence_proxy_async_smem();
+      named_bar_sync(1 + x, 128);
+      if (r == 0) {
+        const F2Item wi = f2_item(a, e.x);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
+          tma_store_4d(&a.tm_o, stg + c * 16384, c * 64, h, wi.t * kTile, wi.b);
+        bulk_commit_group();
+        store_stage = static_cast<int>(it & 1);
       }
       if (row_ok) *lse_out = (l_fin > 0.f) ? (m_fin + __log2f(l_fin)) * kLn2 : -INFINITY;
       if (a.max_logit) warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + h, row_max);
       tc_fence_before();
       mbar_arrive(&bars->o_empty[x]);
+      if (lane == 0 && warp == 4) ATTN_TL(48, it);
       st += w.n;
       ++it;
+      e = e_next;
+      R = R_next;
     }
     if (!ok) {
       if (lane == 0) report_timeout(a, 0x630 + (warp & 7));
       *abort_flag = 1;
     }
+    if (r == 0) bulk_wait_all();  // the last O store has read shared memory and landed
   }
   tc_fence_before();
   __syncthreads();

@@ -55,6 +55,20 @@ SM103_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition (try_wait may suspend the thread
+// for a while when the phase is not complete; test_wait returns at once).
+SM103_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // once `limit_ns` of wall time has passed without completion (the caller then
 // records a timeout status and unwinds).  The limit is far above any
@@ -104,6 +118,16 @@ SM103_DEV void tma_reduce_add_3d(const void* map, const void* src, int x, int y,
       "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
       " [%0, {%2, %3, %4}], [%1];" ::"l"(map),
       "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// Bulk tensor store from shared memory (a box in the map's swizzled layout);
+// rows past the tensor's extent are not written.  Tracked by the issuing
+// thread's bulk-async group.
+SM103_DEV void tma_store_4d(const void* map, const void* src, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 SM103_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
