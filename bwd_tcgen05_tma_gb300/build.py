@@ -16,8 +16,9 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libattn_sm103.so")
-SOURCES = ["api.cu", "meta.cu", "fwd.cu", "bwd.cu", "dkdv128.cu", "dq128.cu", "fwd2t.cu"]
-HEADERS = ["attn_internal.cuh", "sm103_ptx.cuh", os.path.join("..", "..", "include", "attn.h")]
+SOURCES = ["api.cu", "meta.cu", "fwd.cu", "bwd.cu", "bwd_bf16.cu", "bwd_f16.cu", "dkdv128.cu",
+           "dq128.cu", "fwd2t.cu"]
+HEADERS = ["attn_internal.cuh", "sm103_ptx.cuh", "bwd_passes.cuh", os.path.join("..", "..", "include", "attn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -122,6 +122,7 @@ attn_status_t validate(const attn_params_t* p) {
   }
   const bool causal = p->mask == ATTN_MASK_CAUSAL || p->mask == ATTN_MASK_PADDING_CAUSAL;
   if (p->band && causal && p->window_right > 0) return ATTN_ERR_INVALID_ARG;
+  if (p->dtype != ATTN_DTYPE_BF16 && p->dtype != ATTN_DTYPE_FP16) return ATTN_ERR_INVALID_ARG;
   if (p->bias) {
     if (!aligned16(p->bias)) return ATTN_ERR_INVALID_ARG;
     if (!(p->bias_b == 1 || p->bias_b == p->B) || !(p->bias_h == 1 || p->bias_h == p->Hq))
@@ -192,23 +193,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map over a token-major tensor: dims {D, H, T}, box {64, 1, rows}.
-bool make_map(CUtensorMap* m, const void* base, int D, int H, int64_t T, int64_t tok_stride,
-              int rows) {
+bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int D, int H, int64_t T,
+              int64_t tok_stride, int rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)tok_stride * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
   cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+  return fn(m, type, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 4-D map over a token-major tensor of B rows of S tokens: dims {D, H, S, B},
 // box {64, 1, rows, 1}.  Stores through it stop at each batch row's end.
-bool make_map_4d(CUtensorMap* m, const void* base, int D, int H, int64_t S, int B,
-                 int64_t tok_stride, int rows) {
+bool make_map_4d(CUtensorMap* m, CUtensorMapDataType type, const void* base, int D, int H,
+                 int64_t S, int B, int64_t tok_stride, int rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
@@ -216,7 +217,7 @@ bool make_map_4d(CUtensorMap* m, const void* base, int D, int H, int64_t S, int 
                            (cuuint64_t)(S * tok_stride * 2)};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+  return fn(m, type, 4, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -245,7 +246,14 @@ int sm_count() {
   return n;
 }
 
+// Tensor-map element type of the call's 16-bit tensors.
+CUtensorMapDataType map_type(const attn_params_t* p) {
+  return p->dtype == ATTN_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
 void fill_common(KernelArgs& a, const attn_params_t* p, char* ws, const Plan& pl) {
+  a.elem_f16 = p->dtype == ATTN_DTYPE_FP16 ? 1 : 0;
   a.B = p->B; a.Sq = p->Sq; a.Skv = p->Skv; a.Hq = p->Hq; a.Hkv = p->Hkv;
   a.d_qk = p->d_qk; a.d_v = p->d_v;
   const bool causal = p->mask == ATTN_MASK_CAUSAL || p->mask == ATTN_MASK_PADDING_CAUSAL;
@@ -441,10 +449,11 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
   KernelArgs a;
   std::memset(&a, 0, sizeof(a));
   fill_common(a, p, static_cast<char*>(ws), pl);
-  if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
-      !make_map(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
-      !make_map(&a.tm_v, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
-      !make_map_4d(&a.tm_o, o, p->d_v, p->Hq, p->Sq, p->B, (int64_t)p->Hq * p->d_v, kTile))
+  const CUtensorMapDataType mt = map_type(p);
+  if (!make_map(&a.tm_q, mt, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
+      !make_map(&a.tm_k, mt, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
+      !make_map(&a.tm_v, mt, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
+      !make_map_4d(&a.tm_o, mt, o, p->d_v, p->Hq, p->Sq, p->B, (int64_t)p->Hq * p->d_v, kTile))
     return ATTN_ERR_CUDA;
   a.o = static_cast<bf16*>(o);
   a.lse = lse;
@@ -486,6 +495,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   KernelArgs a;
   std::memset(&a, 0, sizeof(a));
   fill_common(a, p, w, pl);
+  const CUtensorMapDataType mt = map_type(p);
   a.o_in = static_cast<const bf16*>(o);
   a.d_o = static_cast<const bf16*>(d_o);
   a.lse_in = lse;
@@ -502,6 +512,13 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   a.dq_stride = r.q_token_stride;
   a.dk_stride = r.k_token_stride;
   a.dv_stride = r.v_token_stride;
+  {
+    // every row start is the base plus a multiple of 64 elements (head dims
+    // and token strides are), so the bases decide 32-byte alignment
+    const uintptr_t bases = reinterpret_cast<uintptr_t>(r.dq) | reinterpret_cast<uintptr_t>(r.dk) |
+                            reinterpret_cast<uintptr_t>(r.dv);
+    a.grad_st32 = (bases & 31u) == 0 ? 1 : 0;
+  }
   a.dbias = static_cast<bf16*>(dbias);
   a.dbias_mode = dbias ? (dbias_needs_acc(p) ? 2 : 1) : 0;
   a.dbias_acc = (a.dbias_mode == 2) ? reinterpret_cast<float*>(w + pl.dbias_acc) : nullptr;
@@ -518,10 +535,10 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   // otherwise 64-row query tiles
   const bool tile128 = !atomic && p->d_qk <= 128 && p->d_v <= 128;
   const int qrows = tile128 ? kTile : kBwdQ;
-  if (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, qrows) ||
-      !make_map(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
-      !make_map(&a.tm_v, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
-      !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
+  if (!make_map(&a.tm_q, mt, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, qrows) ||
+      !make_map(&a.tm_k, mt, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
+      !make_map(&a.tm_v, mt, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
+      !make_map(&a.tm_do, mt, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq, (int64_t)p->Hq * p->d_v,
                 qrows))
     return ATTN_ERR_CUDA;
   if (atomic && !make_map_f32(&a.tm_dqacc, a.dq_acc, p->d_qk, p->Hq, (int64_t)p->B * p->Sq))
@@ -551,9 +568,9 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
       if (launch_dq_convert(a, st) != cudaSuccess) s = ATTN_ERR_CUDA;
     } else {
       if (!tile128 &&
-          (!make_map(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride,
+          (!make_map(&a.tm_q, mt, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride,
                      kTile) ||
-           !make_map(&a.tm_do, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq,
+           !make_map(&a.tm_do, mt, d_o, p->d_v, p->Hq, (int64_t)p->B * p->Sq,
                      (int64_t)p->Hq * p->d_v, kTile)))
         s = ATTN_ERR_CUDA;
       else if ((tile128 ? launch_bwd_dq128(a, nsm, sq) : launch_bwd_dq(a, nsm, st)) != cudaSuccess)

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -11,7 +12,46 @@
 
 namespace attn {
 
-using bf16 = __nv_bfloat16;
+using bf16 = __nv_bfloat16;  // storage of every 16-bit element (bf16 or fp16 bits)
+
+// The 16-bit floating-point element of Q/K/V/O/dO/bias and of the gradients,
+// and of the MMA operands built from them (P, dS): bf16 or fp16.  Packing and
+// products round to nearest even.  Pointers to such elements are typed bf16*
+// and hold either format's bits.
+struct ElemBf16 {
+  static constexpr uint32_t kMmaFmt = 1;  // kind::f16 operand format
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    return sm103::pack_bf16x2(lo, hi);
+  }
+  static __device__ __forceinline__ uint32_t mul(uint32_t a, uint32_t b) {
+    return sm103::mul_bf16x2(a, b);
+  }
+  static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+  static __device__ __forceinline__ float ld(const bf16* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ void st(bf16* p, float x) { *p = __float2bfloat16_rn(x); }
+};
+struct ElemF16 {
+  static constexpr uint32_t kMmaFmt = 0;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    return sm103::pack_f16x2(lo, hi);
+  }
+  static __device__ __forceinline__ uint32_t mul(uint32_t a, uint32_t b) {
+    return sm103::mul_f16x2(a, b);
+  }
+  static __device__ __forceinline__ float lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+  }
+  static __device__ __forceinline__ float hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+  }
+  static __device__ __forceinline__ float ld(const bf16* p) {
+    return __half2float(*reinterpret_cast<const __half*>(p));
+  }
+  static __device__ __forceinline__ void st(bf16* p, float x) {
+    *reinterpret_cast<__half*>(p) = __float2half_rn(x);
+  }
+};
 
 constexpr int kChunk = 64;   // granularity of the per-chunk metadata summaries
 constexpr int kTile = 128;   // query tile (forward, dQ pass) and KV tile (all kernels)
@@ -235,6 +275,8 @@ struct KernelArgs {
   bf16* dbias;
   float* dbias_acc;   // fp32 like the bias (bias broadcast along batch or heads)
   int dbias_mode;     // 0 none, 1 write bf16 directly, 2 accumulate in fp32
+  int elem_f16;        // element type: 0 bf16, 1 fp16
+  int grad_st32;       // 1: dQ/dK/dV rows start 32-byte aligned (256-bit stores)
   int dkdv_batch_loop;  // 1: one dK/dV work item loops over every batch row
   int dkdv_head_loop;   // 1: one dK/dV work item loops over every KV head
 };
@@ -256,6 +298,19 @@ static __device__ unsigned long long g_timeline[kTimelineCap];  // one copy per 
   do {                    \
   } while (0)
 #endif
+
+// Eight packed 16-bit pairs (16 consecutive elements) to global memory: one
+// 32-byte store when the row is 32-byte aligned (`st32`), else two 16-byte
+// stores.  Row-per-thread epilogues touch one line per lane and store, so
+// wider stores halve the store transactions that occupy the load/store path.
+__device__ __forceinline__ void store16_elems(bf16* dst, const uint32_t (&w)[8], bool st32) {
+  if (st32) {
+    sm103::st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+  } else {
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
 
 // Bit c set for lo <= c < hi, c in [0, 64).  Masks are applied with selects on
 // these bits so the element loops stay branch-free.
@@ -442,6 +497,11 @@ cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st
 cudaError_t launch_sink_reduce(const KernelArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic_dq, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_dq(const KernelArgs& a, int num_sms, cudaStream_t st);
+// The same two passes for one element type (bwd_bf16.cu, bwd_f16.cu).
+template <class E>
+cudaError_t launch_bwd_dkdv_t(const KernelArgs& a, bool atomic_dq, int num_sms, cudaStream_t st);
+template <class E>
+cudaError_t launch_bwd_dq_t(const KernelArgs& a, int num_sms, cudaStream_t st);
 // dK/dV pass with 128-row query tiles (deterministic dQ mode, d_qk and d_v <= 128).
 cudaError_t launch_bwd_dkdv128(const KernelArgs& a, int num_sms, cudaStream_t st);
 // Deterministic dQ pass with Q, dO and dS as tensor-memory operands (d_qk, d_v <= 128).

@@ -2,6 +2,7 @@
 //
 //   bwd_pre      D = rowsum(dO * O) per (batch row, head, query) and LSE in
 //                log2 units; zeroes the fp32 accumulators it is asked to.
+//   dkdv, dq     (bwd_passes.cuh, one translation unit per element type)
 //   dkdv         one persistent CTA per SM; a work item is one 128-row KV tile
 //                of one KV head (and, when a broadcast bias gradient has to be
 //                reduced, of every batch row / head sharing that bias slice).
@@ -21,8 +22,8 @@
 //   dq           deterministic dQ: one 128-row query tile per work item, KV
 //                tiles visited in a fixed order, dQ accumulated in tensor
 //                memory (recomputes S and dP: two more GEMMs than atomic mode).
-//   dq_convert   fp32 dQ accumulator -> bf16 in the caller's layout.
-//   dbias_convert fp32 broadcast-bias gradient -> bf16.
+//   dq_convert   fp32 dQ accumulator -> bf16 / fp16 in the caller's layout.
+//   dbias_convert fp32 broadcast-bias gradient -> bf16 / fp16.
 //
 // Gradient formulas: TransformerEngine PR #3516 (fused-attention backward:
 // Q/K/V and optional bias gradients from the saved output and dO); dK/dV of a
@@ -45,7 +46,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // eight values are written as one 32-byte run of the [B, Hq, Sq] arrays.
 constexpr int kPreMaxH = 256;
 
-template <int DV>
+template <class E, int DV>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const KernelArgs a, int dq_mode_used) {
   constexpr int LPR = DV / 8;    // lanes per head row, 16 bytes each
   constexpr int HPI = 32 / LPR;  // head rows per warp-wide load
@@ -79,8 +80,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const KernelArgs a, int dq
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(dw[e] << 16), acc);
-          acc = fmaf(__uint_as_float(ow[e] & 0xFFFF0000u), __uint_as_float(dw[e] & 0xFFFF0000u), acc);
+          acc = fmaf(E::lo(ow[e]), E::lo(dw[e]), acc);
+          acc = fmaf(E::hi(ow[e]), E::hi(dw[e]), acc);
         }
 #pragma unroll
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(256) sink_reduce_kernel(const KernelArgs a, in
 }
 
 // =========================================================== converts
+template <class E>
 __global__ void dq_convert_kernel(const KernelArgs a) {
   const int64_t per_tok = (int64_t)a.Hq * a.d_qk / 8;  // groups of 8 elements
   const int64_t n = (int64_t)a.B * a.Sq * per_tok;
@@ -150,14 +152,15 @@ __global__ void dq_convert_kernel(const KernelArgs a) {
     const float4 x0 = *reinterpret_cast<const float4*>(a.dq_acc + tok * a.Hq * a.d_qk + e);
     const float4 x1 = *reinterpret_cast<const float4*>(a.dq_acc + tok * a.Hq * a.d_qk + e + 4);
     uint4 o;
-    o.x = pack_bf16x2(x0.x, x0.y);
-    o.y = pack_bf16x2(x0.z, x0.w);
-    o.z = pack_bf16x2(x1.x, x1.y);
-    o.w = pack_bf16x2(x1.z, x1.w);
+    o.x = E::pack(x0.x, x0.y);
+    o.y = E::pack(x0.z, x0.w);
+    o.z = E::pack(x1.x, x1.y);
+    o.w = E::pack(x1.z, x1.w);
     *reinterpret_cast<uint4*>(a.dq + tok * a.dq_stride + e) = o;
   }
 }
 
+template <class E>
 __global__ void dbias_convert_kernel(const KernelArgs a) {
   // four elements per thread and step: one 16-byte load, one 8-byte store
   // (both buffers are 16-byte aligned); the last n % 4 elements one by one
@@ -168,1062 +171,11 @@ __global__ void dbias_convert_kernel(const KernelArgs a) {
   for (int64_t v = t0; v < n4; v += stride) {
     const float4 x = reinterpret_cast<const float4*>(a.dbias_acc)[v];
     uint2 o;
-    o.x = pack_bf16x2(x.x, x.y);
-    o.y = pack_bf16x2(x.z, x.w);
+    o.x = E::pack(x.x, x.y);
+    o.y = E::pack(x.z, x.w);
     reinterpret_cast<uint2*>(a.dbias)[v] = o;
   }
-  for (int64_t v = 4 * n4 + t0; v < n; v += stride) a.dbias[v] = __float2bfloat16_rn(a.dbias_acc[v]);
-}
-
-// =========================================================== dK / dV pass
-template <int DQK, int DV, bool ATOMIC>
-struct DkdvLayout {
-  static constexpr int kKBytes = kTile * DQK * 2;
-  static constexpr int kVBytes = kTile * DV * 2;
-  static constexpr int kQBytes = kBwdQ * DQK * 2;  // one 64-row query tile
-  static constexpr int kOBytes = kBwdQ * DV * 2;
-  static constexpr int kDSBytes = kTile * kBwdQ * 2;
-  static constexpr int kDQStageBytes = ATOMIC ? kBwdQ * DQK * 4 : 0;  // fp32 dQ tile for TMA reduce
-  static constexpr int kStageBytes = kQBytes + kOBytes;
-  static constexpr int kFixed = kKBytes + kVBytes + kDSBytes + kDQStageBytes;
-  static constexpr int kStages = (kFixed + 4 * kStageBytes + 4 * 1024 <= 216 * 1024) ? 4
-                                 : (kFixed + 3 * kStageBytes + 3 * 1024 <= 216 * 1024) ? 3 : 2;
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKBytes;
-  static constexpr int kDSOff = kKBytes + kVBytes;
-  static constexpr int kDQOff = kDSOff + kDSBytes;
-  static constexpr int kStageOff = kDQOff + kDQStageBytes;
-  static constexpr int kVecOff = kStageOff + kStages * kStageBytes;  // 1 KB per stage
-  static constexpr int kBarOff = kVecOff + kStages * 1024;
-  static constexpr int kBytes = kBarOff + 512;
-  static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
-  // tensor memory: dV, dK accumulators; two S^T buffers (P^T is written back
-  // over its own S^T as packed bf16); dP^T; dQ^T (atomic mode, d_qk <= 128)
-  static constexpr uint32_t kColDV = 0;
-  static constexpr uint32_t kColDK = 128;
-  static constexpr uint32_t kColS = (DQK > 128) ? 320 : 256;  // + 64 * (step & 1)
-  static constexpr uint32_t kColDP = kColS + 128;
-  static constexpr uint32_t kColDQ = kColDP + 64;
-};
-
-// Every barrier below can run at most one phase ahead of its waiters (parity
-// waits rely on that): per-S-buffer barriers for the S^T / P^T double buffer.
-struct DkdvBars {
-  uint64_t kv_full, kv_empty, dp_full, dp_free, ds_ready, ds_free, acc_full, acc_empty, drain,
-      dq_full, dq_free, stg_full, stg_free;
-  uint64_t s_full[2], p_ready[2], p_free[2];
-  uint64_t qd_full[4], qd_empty[4];
-};
-
-struct StageVec {  // per query tile: log2-LSE, D, and (general path) ids / positions
-  float lse2[kBwdQ];
-  float D[kBwdQ];
-  int32_t qid[kBwdQ];
-  int32_t qpos[kBwdQ];
-};
-
-template <int DQK, int DV, bool ATOMIC, bool HAS_BIAS, int DBIAS>
-__global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ KernelArgs a) {
-  using L = DkdvLayout<DQK, DV, ATOMIC>;
-  constexpr int NS = L::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  DkdvBars* bars = reinterpret_cast<DkdvBars*>(sm + L::kBarOff);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(DkdvBars));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  StageVec* vec = reinterpret_cast<StageVec*>(sm + L::kVecOff);
-  ItemRing* ring = reinterpret_cast<ItemRing*>(sm + L::kBarOff + 256);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = dkdv_n_items(a);
-  const int G = a.Hq / a.Hkv;
-
-  if (tid == 0) {
-    mbar_init(&bars->kv_full, 1);
-    mbar_init(&bars->kv_empty, 1);
-    for (int b2 = 0; b2 < 2; ++b2) {
-      mbar_init(&bars->s_full[b2], 1);
-      mbar_init(&bars->p_ready[b2], 256);
-      mbar_init(&bars->p_free[b2], 1);
-    }
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->dp_free, 256);
-    mbar_init(&bars->ds_ready, 256);
-    mbar_init(&bars->ds_free, 1);
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, 128);
-    mbar_init(&bars->drain, 1);
-    mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 128);
-    mbar_init(&bars->stg_full, 128);
-    mbar_init(&bars->stg_free, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&bars->qd_full[s], 1 + 64);
-      mbar_init(&bars->qd_empty[s], 1 + 256);
-    }
-    ring_init(ring, 1 + 64 + 256 + 128);  // MMA, vector loader, P/dS warps, epilogue
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_holder, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-  grid_dep_wait();  // the previous kernel on the stream has finished
-  grid_dep_launch();
-  const bool general = path_general(a);
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tensormap(&a.tm_q);
-      prefetch_tensormap(&a.tm_k);
-      prefetch_tensormap(&a.tm_v);
-      prefetch_tensormap(&a.tm_do);
-      uint32_t st = 0, kvc = 0;
-      bool ok = true;
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[1], n_items, idx)) ||
-            idx < 0)
-          break;
-        const DkdvItem w = dkdv_item(a, idx);
-        for (int b = w.b0; b < w.b1 && ok; ++b) {
-          for (int g = w.g0; g < w.g1 && ok; ++g) {
-            int q_lo;
-            const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
-            if (nq == 0) continue;
-            if (kvc > 0 && !(ok = mbar_wait(&bars->kv_empty, (kvc - 1) & 1))) break;
-            const int krow = b * a.Skv + w.t * kTile;
-            mbar_arrive_expect_tx(&bars->kv_full, L::kKBytes + L::kVBytes);
-#pragma unroll
-            for (int c = 0; c < DQK / 64; ++c)
-              tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
-#pragma unroll
-            for (int c = 0; c < DV / 64; ++c)
-              tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
-            ++kvc;
-            for (int hh = 0; hh < G && ok; ++hh) {
-              const int h = g * G + hh;
-              for (int s = 0; s < nq; ++s, ++st) {
-                const int stage = st % NS;
-                if (st >= (uint32_t)NS &&
-                    !(ok = mbar_wait(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
-                  break;
-                const int qrow = b * a.Sq + q_lo + s * kBwdQ;
-                uint8_t* qs = sm + L::kStageOff + stage * L::kStageBytes;
-                mbar_arrive_expect_tx(&bars->qd_full[stage], L::kStageBytes);
-#pragma unroll
-                for (int c = 0; c < DQK / 64; ++c)
-                  tma_load_3d(qs + c * 8192, &a.tm_q, &bars->qd_full[stage], c * 64, h, qrow);
-#pragma unroll
-                for (int c = 0; c < DV / 64; ++c)
-                  tma_load_3d(qs + L::kQBytes + c * 8192, &a.tm_do, &bars->qd_full[stage], c * 64,
-                              h, qrow);
-                ATTN_TL(1, st);
-              }
-            }
-          }
-        }
-      }
-      if (!ok) {
-        report_timeout(a, 0x110);
-        *abort_flag = 1;
-      }
-      if (*abort_flag) {
-        if (kvc > 0) mbar_wait(&bars->kv_full, (kvc - 1) & 1, 100000000ull);
-        for (uint32_t u = (st > (uint32_t)NS ? st - NS : 0u); u < st; ++u)
-          mbar_wait(&bars->qd_full[u % NS], (u / NS) & 1, 100000000ull);
-      }
-    }
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------------------------ vector loader
-    const int t = tid - 64;
-    uint32_t st = 0;
-    bool ok = true;
-    for (uint32_t rn = 0;; ++rn) {
-      int32_t idx;
-      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
-          idx < 0)
-        break;
-      const DkdvItem w = dkdv_item(a, idx);
-      for (int b = w.b0; b < w.b1 && ok; ++b) {
-        for (int g = w.g0; g < w.g1 && ok; ++g) {
-          int q_lo;
-          const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
-          for (int hh = 0; hh < G && ok && nq > 0; ++hh) {
-            const int h = g * G + hh;
-            for (int s = 0; s < nq; ++s, ++st) {
-              const int stage = st % NS;
-              if (st >= (uint32_t)NS &&
-                  !(ok = mbar_wait_warp(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
-                break;
-              const int i = q_lo + s * kBwdQ + t;
-              const bool in = i < a.Sq;
-              const int64_t vi = ((int64_t)b * a.Hq + h) * a.Sq + i;
-              vec[stage].lse2[t] = in ? a.lse2[vi] : INFINITY;
-              vec[stage].D[t] = in ? a.Dvec[vi] : 0.f;
-              if (general) {
-                vec[stage].qid[t] = in ? a.q_id[(int64_t)b * a.Sq + i] : -1;
-                vec[stage].qpos[t] = in ? a.q_pos[(int64_t)b * a.Sq + i] : 0;
-              }
-              mbar_arrive(&bars->qd_full[stage]);
-              if (t == 0) ATTN_TL(3, st);
-            }
-          }
-        }
-      }
-    }
-    if (!ok) {
-      if (lane == 0) report_timeout(a, 0x120 + warp);
-      *abort_flag = 1;
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, kBwdQ, false, false);
-      constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, false, true);
-      constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, false, true);
-      constexpr uint32_t id_dq = idesc_bf16_f32(128, kBwdQ, true, true);
-      // operand descriptors are built once; each MMA only adds a constant offset
-      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);      // K, K-major
-      const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);   // K^T, MN-major
-      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
-      const uint64_t ds_km = sdesc_sw128(smem_u32(sm + L::kDSOff), 16, 1024);
-      const uint64_t ds_mn = sdesc_sw128(smem_u32(sm + L::kDSOff), 8192, 1024);
-      const uint64_t st_km = sdesc_sw128(smem_u32(sm + L::kStageOff), 16, 1024);   // Q / dO tiles
-      const uint64_t st_mn = sdesc_sw128(smem_u32(sm + L::kStageOff), 8192, 1024);
-      uint32_t st = 0, kvc = 0, gc = 0;
-      bool ok = true;
-      auto stage_off16 = [&](uint32_t x) -> uint32_t {
-        return static_cast<uint32_t>(((x % NS) * L::kStageBytes) >> 4);
-      };
-      auto issue_s = [&](uint32_t x) -> bool {  // S^T = K Q^T into buffer x & 1
-        if (!mbar_wait(&bars->qd_full[x % NS], (x / NS) & 1)) return false;
-        // buffer x & 1 still holds P^T(x - 2) until dV(x - 2) has read it
-        if (x >= 2 && !mbar_wait(&bars->p_free[x & 1], ((x >> 1) - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t qd = st_km + stage_off16(x);
-        const uint32_t dt = tmem + L::kColS + 64 * (x & 1);
-#pragma unroll
-        for (int ks = 0; ks < DQK / 16; ++ks)
-          mma_ss(dt, k_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                 qd + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id_s, ks > 0);
-        mma_commit(&bars->s_full[x & 1]);
-        ATTN_TL(10, x);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t x) -> bool {  // dP^T = V dO^T
-        if (x > 0 && !mbar_wait(&bars->dp_free, (x - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t od = st_km + stage_off16(x) + (L::kQBytes >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DV / 16; ++ks)
-          mma_ss(tmem + L::kColDP, v_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                 od + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id_s, ks > 0);
-        mma_commit(&bars->dp_full);
-        ATTN_TL(11, x);
-        return true;
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-        const DkdvItem w = dkdv_item(a, idx);
-        for (int b = w.b0; b < w.b1 && ok; ++b) {
-          for (int g = w.g0; g < w.g1 && ok; ++g) {
-            int q_lo;
-            const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
-            if (nq == 0) continue;
-            const uint32_t nsteps = (uint32_t)nq * G;
-            if (!(ok = mbar_wait(&bars->kv_full, kvc & 1))) break;
-            ++kvc;
-            if (!(ok = issue_s(st))) break;
-            if (!(ok = issue_dp(st))) break;
-            for (uint32_t u = 0; u < nsteps; ++u) {
-              const uint32_t cur = st + u;
-              if (u + 1 < nsteps && !(ok = issue_s(cur + 1))) break;
-              if (!(ok = mbar_wait(&bars->p_ready[cur & 1], (cur >> 1) & 1))) break;
-              ATTN_TL(12, cur);
-              if (u == 0 && gc > 0 && !(ok = mbar_wait(&bars->acc_empty, (gc - 1) & 1))) break;
-              tc_fence_after();
-              const uint64_t q_mn = st_mn + stage_off16(cur);
-              const uint64_t o_mn = q_mn + (L::kQBytes >> 4);
-              // P^T, packed bf16: query columns [0,32) at S^T columns [0,16), [32,64) at [32,48)
-              const uint32_t p_tm = tmem + L::kColS + 64 * (cur & 1);
-#pragma unroll
-              for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dV += P^T dO  (A from tensor memory)
-                mma_ts(tmem + L::kColDV, p_tm + ks * 8 + (ks >> 1) * 16, o_mn + ((ks * 2048) >> 4),
-                       id_dv, (u > 0 || ks > 0));
-              mma_commit(&bars->p_free[cur & 1]);
-              if (u + 1 < nsteps && !(ok = issue_dp(cur + 1))) break;
-              if (!(ok = mbar_wait(&bars->ds_ready, cur & 1))) break;
-              ATTN_TL(14, cur);
-              tc_fence_after();
-#pragma unroll
-              for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dK += dS^T Q
-                mma_ss(tmem + L::kColDK, ds_km + ((ks * 32) >> 4), q_mn + ((ks * 2048) >> 4), id_dk,
-                       (u > 0 || ks > 0));
-              if constexpr (ATOMIC) {  // dQ^T = K^T dS^T
-                if (cur >= 1 && !(ok = mbar_wait(&bars->dq_free, (cur - 1) & 1))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks)
-                  mma_ss(tmem + L::kColDQ, k_mn + ((ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4),
-                         id_dq, ks > 0);
-                mma_commit(&bars->dq_full);
-              }
-              mma_commit(&bars->ds_free);
-              mma_commit(&bars->qd_empty[cur % NS]);
-              ATTN_TL(15, cur);
-            }
-            if (!ok) break;
-            mma_commit(&bars->acc_full);
-            mma_commit(&bars->kv_empty);
-            ++gc;
-            st += nsteps;
-          }
-        }
-      }
-      if (!ok) {
-        report_timeout(a, 0x130);
-        *abort_flag = 1;
-      }
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 200000000ull);
-    }
-  } else if (warp >= 4 && warp < 12) {
-    // ------------------------------------------------------------ P / dS warps
-    // two warpgroups: each thread owns KV row j (TMEM lane j) and one half of
-    // the 64 query columns of every step
-    const int j = (tid - 128) & 127;
-    const int half = (tid - 128) >> 7;
-    const int c0h = half * 32;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t ds_addr = smem_u32(sm + L::kDSOff);
-    const int nqc = (a.Sq + kChunk - 1) / kChunk;
-    uint32_t st = 0;
-    bool ok = true;
-    for (uint32_t rn = 0;; ++rn) {
-      int32_t idx;
-      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
-          idx < 0)
-        break;
-      const DkdvItem w = dkdv_item(a, idx);
-      const int kj = w.t * kTile + j;
-      const bool row_ok = kj < a.Skv;
-      for (int b = w.b0; b < w.b1 && ok; ++b) {
-        for (int g = w.g0; g < w.g1 && ok; ++g) {
-          int q_lo;
-          const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
-          if (nq == 0) continue;
-          const int64_t gk = (int64_t)b * a.Skv + kj;
-          int qlo = 0, qhi = 0, my_id = 0, my_pos = 0;
-          int2 my_qp = make_int2(0, -1);  // query positions that keep this key
-          if (row_ok) {
-            if (!general) {
-              const int2 qr = band_queries_of_key(a, kj, a.kv_seg_lo[gk], a.kv_seg_hi[gk]);
-              qlo = qr.x;
-              qhi = qr.y;
-            } else {
-              my_id = a.kv_id[gk];
-              my_pos = a.kv_pos[gk];
-              my_qp = band_query_pos(a, my_pos);
-            }
-          }
-          for (int hh = 0; hh < G && ok; ++hh) {
-            const int h = g * G + hh;
-            const int bb = a.bias_b > 1 ? b : 0, bh = a.bias_h > 1 ? h : 0;
-            const int64_t bias_base = ((int64_t)bb * a.bias_h + bh) * a.Sq;
-            for (int s = 0; s < nq; ++s, ++st) {
-              const uint32_t cur = st;
-              const int stage = cur % NS;
-              const int q0 = q_lo + s * kBwdQ;
-              float x[32];
-              if (j == 0 && half == 0) ATTN_TL(20, cur);
-              if (!(ok = mbar_wait_warp(&bars->qd_full[stage], (cur / NS) & 1))) break;
-              if (j == 0 && half == 0) ATTN_TL(26, cur);
-              if (!(ok = mbar_wait_warp(&bars->s_full[cur & 1], (cur >> 1) & 1))) break;
-              if (j == 0 && half == 0) ATTN_TL(21, cur);
-              tc_fence_after();
-              const uint32_t s_tm = tmem + lane_base + L::kColS + 64 * (cur & 1);
-              {
-                uint32_t u[32];
-                tmem_ld32x32b_x32(s_tm + c0h, u);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(u[e]) * a.scale_log2;
-              }
-              if (j == 0 && half == 0) ATTN_TL(40, cur);
-              const StageVec& V = vec[stage];
-              if (HAS_BIAS && row_ok) {
-                const bf16* bp = a.bias + (bias_base + q0 + c0h) * a.Skv + kj;
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                  if (q0 + c0h + c < a.Sq) x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
-              }
-              // validity of this thread's 32 query columns, as a bitmask
-              uint32_t vbits;
-              if (!general) {
-                vbits = row_ok ? (uint32_t)(range_bits64(qlo - q0 - c0h, qhi - q0 - c0h)) : 0u;
-              } else {
-                vbits = 0u;
-                bool full = false;
-                if (row_ok && my_id != 0 && q0 + kBwdQ <= a.Sq) {
-                  const ChunkInfo ci = a.q_chunk[b * nqc + q0 / kChunk];
-                  full = ci.uniform && ci.min_id == my_id && ci.min_pos >= my_qp.x &&
-                         ci.max_pos <= my_qp.y;
-                }
-                if (full) {
-                  vbits = ~0u;
-                } else if (row_ok && my_id != 0) {
-#pragma unroll
-                  for (int c = 0; c < 32; c += 4) {
-                    const int4 id4 = *reinterpret_cast<const int4*>(&V.qid[c0h + c]);
-                    const int4 ps4 = *reinterpret_cast<const int4*>(&V.qpos[c0h + c]);
-                    const int ids[4] = {id4.x, id4.y, id4.z, id4.w};
-                    const int pss[4] = {ps4.x, ps4.y, ps4.z, ps4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                      const bool v = (ids[e] == my_id) & (pss[e] >= my_qp.x) & (pss[e] <= my_qp.y);
-                      vbits |= static_cast<uint32_t>(v) << (c + e);
-                    }
-                  }
-                }
-              }
-#pragma unroll
-              for (int c = 0; c < 32; c += 4) {
-                const float4 l4 = *reinterpret_cast<const float4*>(&V.lse2[c0h + c]);
-                const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float pv = ex2_approx(x[c + e] - ls[e]);
-                  x[c + e] = ((vbits >> (c + e)) & 1u) ? pv : 0.f;
-                }
-              }
-              if (j == 0 && half == 0) ATTN_TL(41, cur);
-              // P^T -> tensor memory, packed bf16 pairs, inside this half's own S^T
-              // columns [c0h, c0h + 32) (the other half may still be reading its S^T)
-              {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-                tmem_st32x32b_x16(s_tm + c0h, pk);
-                tmem_st_wait();
-              }
-              tc_fence_before();
-              mbar_arrive(&bars->p_ready[cur & 1]);
-              if (j == 0 && half == 0) ATTN_TL(22, cur);
-              // dS^T = P^T (dP^T - D)
-              if (!(ok = mbar_wait_warp(&bars->dp_full, cur & 1))) break;
-              if (j == 0 && half == 0) ATTN_TL(23, cur);
-              tc_fence_after();
-              {
-                uint32_t u[32];
-                tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + c0h, u);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                  const float4 d4 = *reinterpret_cast<const float4*>(&V.D[c0h + e]);
-                  x[e] = x[e] * (__uint_as_float(u[e]) - d4.x);
-                  x[e + 1] = x[e + 1] * (__uint_as_float(u[e + 1]) - d4.y);
-                  x[e + 2] = x[e + 2] * (__uint_as_float(u[e + 2]) - d4.z);
-                  x[e + 3] = x[e + 3] * (__uint_as_float(u[e + 3]) - d4.w);
-                }
-              }
-              tc_fence_before();
-              mbar_arrive(&bars->dp_free);
-              if (cur > 0 && !(ok = mbar_wait_warp(&bars->ds_free, (cur - 1) & 1))) break;
-#pragma unroll
-              for (int u4 = 0; u4 < 4; ++u4) {  // 16-byte units half*4 .. half*4+3 of row j
-                const float* p8 = x + u4 * 8;
-                const int un = half * 4 + u4;
-                st_shared_v4(ds_addr + j * 128 + ((un ^ (j & 7)) << 4), pack_bf16x2(p8[0], p8[1]),
-                             pack_bf16x2(p8[2], p8[3]), pack_bf16x2(p8[4], p8[5]),
-                             pack_bf16x2(p8[6], p8[7]));
-              }
-              fence_proxy_async_smem();
-              mbar_arrive(&bars->ds_ready);
-              if (j == 0 && half == 0) ATTN_TL(24, cur);
-              if (DBIAS != 0 && row_ok) {
-                if (DBIAS == 1) {
-                  bf16* dp = a.dbias + (bias_base + q0 + c0h) * a.Skv + kj;
-#pragma unroll
-                  for (int c = 0; c < 32; ++c)
-                    if (q0 + c0h + c < a.Sq) dp[(int64_t)c * a.Skv] = __float2bfloat16_rn(x[c]);
-                } else {
-                  float* dp = a.dbias_acc + (bias_base + q0 + c0h) * a.Skv + kj;
-                  // eight loads in flight before their stores (a store between
-                  // two loads would serialise them: the addresses may alias)
-#pragma unroll
-                  for (int c8 = 0; c8 < 32; c8 += 8) {
-                    float acc[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                      acc[c] = (q0 + c0h + c8 + c < a.Sq) ? dp[(int64_t)(c8 + c) * a.Skv] : 0.f;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                      if (q0 + c0h + c8 + c < a.Sq) dp[(int64_t)(c8 + c) * a.Skv] = acc[c] + x[c8 + c];
-                  }
-                }
-              }
-              mbar_arrive(&bars->qd_empty[stage]);
-            }
-          }
-        }
-      }
-    }
-    if (!ok) {
-      if (lane == 0) report_timeout(a, 0x140 + (warp & 3));
-      *abort_flag = 1;
-    }
-  } else if (warp >= 12) {
-    // ------------------------------------------------------------ dQ drain + dK/dV epilogue
-    const int j = tid - 384;  // TMEM lane: KV row for dK/dV, head-dim index for dQ^T
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t st = 0, gc = 0;
-    bool ok = true;
-    for (uint32_t rn = 0;; ++rn) {
-      int32_t idx;
-      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
-          idx < 0)
-        break;
-      const DkdvItem w = dkdv_item(a, idx);
-      const int kj = w.t * kTile + j;
-      const bool row_ok = kj < a.Skv;
-      for (int b = w.b0; b < w.b1 && ok; ++b) {
-        for (int g = w.g0; g < w.g1 && ok; ++g) {
-          int q_lo;
-          const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
-          bf16* dv_row = a.dv + ((int64_t)b * a.Skv + kj) * a.dv_stride + (int64_t)g * DV;
-          bf16* dk_row = a.dk + ((int64_t)b * a.Skv + kj) * a.dk_stride + (int64_t)g * DQK;
-          if (nq == 0) {
-            if (row_ok) {
-#pragma unroll
-              for (int c = 0; c < DV; c += 8)
-                *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0, 0, 0, 0);
-#pragma unroll
-              for (int c = 0; c < DQK; c += 8)
-                *reinterpret_cast<uint4*>(dk_row + c) = make_uint4(0, 0, 0, 0);
-            }
-            continue;
-          }
-          if constexpr (ATOMIC) {
-            // dQ^T tile -> fp32 staging [d box of 32][64 q][32 d] -> one bulk
-            // tensor reduce-add per box into the fp32 dQ accumulator
-            float* stg = reinterpret_cast<float*>(sm + L::kDQOff);
-            for (int hh = 0; hh < G && ok; ++hh) {
-              const int h = g * G + hh;
-              for (int s = 0; s < nq; ++s, ++st) {
-                if (!(ok = mbar_wait_warp(&bars->dq_full, st & 1))) break;
-                if (j == 0) ATTN_TL(30, st);
-                tc_fence_after();
-                uint32_t u0[32], u1[32];
-                tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ, u0);
-                tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + 32, u1);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&bars->dq_free);
-                // the previous tile's reduce must have finished reading the staging buffer
-                if (st > 0 && !(ok = mbar_wait_warp(&bars->stg_free, (st - 1) & 1))) break;
-                if (j < DQK) {
-                  float* col = stg + (j >> 5) * (kBwdQ * 32) + (j & 31);
-                  const float sc = a.scale;
-#pragma unroll
-                  for (int c = 0; c < 32; ++c) col[c * 32] = __uint_as_float(u0[c]) * sc;
-#pragma unroll
-                  for (int c = 0; c < 32; ++c) col[(32 + c) * 32] = __uint_as_float(u1[c]) * sc;
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&bars->stg_full);
-                if (j == 0) {
-                  if ((ok = mbar_wait(&bars->stg_full, st & 1))) {
-                    const int q0 = q_lo + s * kBwdQ;
-#pragma unroll
-                    for (int bx = 0; bx < DQK / 32; ++bx)
-                      tma_reduce_add_3d(&a.tm_dqacc, stg + bx * (kBwdQ * 32), bx * 32, h,
-                                        b * a.Sq + q0);
-                    bulk_commit_group();
-                    bulk_wait_read_all();
-                    mbar_arrive(&bars->stg_free);
-                  }
-                }
-                ok = __all_sync(0xffffffffu, ok);
-                if (j == 0) ATTN_TL(31, st);
-              }
-            }
-            if (!ok) break;
-          }
-          if (!(ok = mbar_wait_warp(&bars->acc_full, gc & 1))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int q = 0; q < DV / 32; ++q) {
-            uint32_t u[32];
-            tmem_ld32x32b_x32(tmem + lane_base + L::kColDV + q * 32, u);
-            tmem_ld_wait();
-            if (row_ok) {
-#pragma unroll
-              for (int c = 0; c < 32; c += 8) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(u[c]), __uint_as_float(u[c + 1]));
-                v.y = pack_bf16x2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
-                v.z = pack_bf16x2(__uint_as_float(u[c + 4]), __uint_as_float(u[c + 5]));
-                v.w = pack_bf16x2(__uint_as_float(u[c + 6]), __uint_as_float(u[c + 7]));
-                *reinterpret_cast<uint4*>(dv_row + q * 32 + c) = v;
-              }
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < DQK / 32; ++q) {
-            uint32_t u[32];
-            tmem_ld32x32b_x32(tmem + lane_base + L::kColDK + q * 32, u);
-            tmem_ld_wait();
-            if (row_ok) {
-              const float sc = a.scale;
-#pragma unroll
-              for (int c = 0; c < 32; c += 8) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(u[c]) * sc, __uint_as_float(u[c + 1]) * sc);
-                v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * sc, __uint_as_float(u[c + 3]) * sc);
-                v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * sc, __uint_as_float(u[c + 5]) * sc);
-                v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * sc, __uint_as_float(u[c + 7]) * sc);
-                *reinterpret_cast<uint4*>(dk_row + q * 32 + c) = v;
-              }
-            }
-          }
-          tc_fence_before();
-          mbar_arrive(&bars->acc_empty);
-          ++gc;
-        }
-      }
-    }
-    if constexpr (ATOMIC) {
-      if (j == 0) bulk_wait_all();  // every reduce-add issued by this thread has landed
-    }
-    if (!ok) {
-      if (lane == 0) report_timeout(a, 0x150 + (warp & 3));
-      *abort_flag = 1;
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// =========================================================== deterministic dQ pass
-template <int DQK, int DV>
-struct DqLayout {
-  static constexpr int kQBytes = kTile * DQK * 2;
-  static constexpr int kOBytes = kTile * DV * 2;
-  static constexpr int kKBytes = kTile * DQK * 2;
-  static constexpr int kVBytes = kTile * DV * 2;
-  static constexpr int kSBytes = kTile * kTile * 2;
-  static constexpr int kBase = kQBytes + kOBytes + kSBytes;
-  static constexpr int kLimit = 224 * 1024;
-  static constexpr int kKStages = (kBase + 2 * kKBytes + kVBytes <= kLimit) ? 2 : 1;
-  static constexpr int kVStages = (kBase + kKStages * kKBytes + 2 * kVBytes <= kLimit) ? 2 : 1;
-  static constexpr int kQOff = 0;
-  static constexpr int kOOff = kQBytes;
-  static constexpr int kSOff = kQBytes + kOBytes;
-  static constexpr int kKOff = kSOff + kSBytes;
-  static constexpr int kVOff = kKOff + kKStages * kKBytes;
-  static constexpr int kBarOff = kVOff + kVStages * kVBytes;
-  static constexpr int kBytes = kBarOff + 512;  // barriers, then the item ring at +256
-  static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
-};
-
-struct DqBars {
-  uint64_t q_full, q_empty, s_full, s_free, dp_full, dp_free, ds_ready, ds_free, acc_full,
-      acc_empty, drain;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-};
-
-template <int DQK, int DV, bool HAS_BIAS>
-__global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ KernelArgs a) {
-  using L = DqLayout<DQK, DV>;
-  constexpr int KS = L::kKStages, VS = L::kVStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  DqBars* bars = reinterpret_cast<DqBars*>(sm + L::kBarOff);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(DqBars));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  ItemRing* ring = reinterpret_cast<ItemRing*>(sm + L::kBarOff + 256);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = a.B * a.n_qt * a.Hq;
-
-  if (tid == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 128);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->dp_free, 128);
-    mbar_init(&bars->ds_ready, 128);
-    mbar_init(&bars->ds_free, 1);
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, 128);
-    mbar_init(&bars->drain, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
-    }
-    ring_init(ring, 1 + 128);  // MMA issuer + softmax warpgroup
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_holder, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-  grid_dep_wait();  // the previous kernel on the stream has finished
-  grid_dep_launch();
-  const bool general = path_general(a);
-
-  auto item_of = [&](int idx, int& b, int& t, int& h, int& kv_lo, int& n) {
-    const int per_t = a.B * a.Hq;
-    const int t_rev = idx / per_t, rem = idx - t_rev * per_t;
-    t = a.n_qt - 1 - t_rev;
-    b = rem / a.Hq;
-    h = rem - b * a.Hq;
-    const int2 r = a.q_tile_range[b * a.n_qt + t];
-    kv_lo = r.x;
-    n = (r.y > r.x) ? (r.y - r.x + kTile - 1) / kTile : 0;
-  };
-
-  if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tensormap(&a.tm_q);
-      prefetch_tensormap(&a.tm_k);
-      prefetch_tensormap(&a.tm_v);
-      prefetch_tensormap(&a.tm_do);
-      uint32_t kt = 0, it = 0, k_loads = 0;
-      bool ok = true;
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[2], n_items, idx)) ||
-            idx < 0)
-          break;
-        int b, t, h, kv_lo, n;
-        item_of(idx, b, t, h, kv_lo, n);
-        if (n == 0) continue;
-        if (it > 0 && !(ok = mbar_wait(&bars->q_empty, (it - 1) & 1))) break;
-        const int qrow = b * a.Sq + t * kTile;
-        mbar_arrive_expect_tx(&bars->q_full, L::kQBytes + L::kOBytes);
-#pragma unroll
-        for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->q_full, c * 64, h, qrow);
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sm + L::kOOff + c * 16384, &a.tm_do, &bars->q_full, c * 64, h, qrow);
-        ++it;
-        const int g = h / (a.Hq / a.Hkv);
-        for (int j = 0; j < n; ++j, ++kt) {
-          const int krow = b * a.Skv + kv_lo + j * kTile;
-          const int ks = kt % KS, vs = kt % VS;
-          if (kt >= (uint32_t)KS && !(ok = mbar_wait(&bars->k_empty[ks], ((kt / KS) - 1) & 1)))
-            break;
-          mbar_arrive_expect_tx(&bars->k_full[ks], L::kKBytes);
-#pragma unroll
-          for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(sm + L::kKOff + ks * L::kKBytes + c * 16384, &a.tm_k, &bars->k_full[ks],
-                        c * 64, g, krow);
-          ++k_loads;
-          if (kt >= (uint32_t)VS && !(ok = mbar_wait(&bars->v_empty[vs], ((kt / VS) - 1) & 1)))
-            break;
-          mbar_arrive_expect_tx(&bars->v_full[vs], L::kVBytes);
-#pragma unroll
-          for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(sm + L::kVOff + vs * L::kVBytes + c * 16384, &a.tm_v, &bars->v_full[vs],
-                        c * 64, g, krow);
-        }
-      }
-      if (!ok) {
-        report_timeout(a, 0x210);
-        *abort_flag = 1;
-      }
-      if (*abort_flag) {
-        if (it > 0) mbar_wait(&bars->q_full, (it - 1) & 1, 100000000ull);
-        for (uint32_t u = (k_loads > 2u ? k_loads - 2u : 0u); u < k_loads; ++u)
-          mbar_wait(&bars->k_full[u % KS], (u / KS) & 1, 100000000ull);
-        for (uint32_t u = (kt > 2u ? kt - 2u : 0u); u < kt; ++u)
-          mbar_wait(&bars->v_full[u % VS], (u / VS) & 1, 100000000ull);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
-      constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, false, true);
-      // operand descriptors are built once; each MMA only adds a constant offset
-      const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
-      const uint64_t o_km = sdesc_sw128(smem_u32(sm + L::kOOff), 16, 1024);
-      const uint64_t s_km = sdesc_sw128(smem_u32(sm + L::kSOff), 16, 1024);
-      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
-      const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);
-      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
-      uint32_t kt = 0, it = 0;
-      bool ok = true;
-      auto issue_s = [&](uint32_t k) -> bool {  // S = Q K^T
-        const int ks_ = k % KS;
-        if (!mbar_wait(&bars->k_full[ks_], (k / KS) & 1)) return false;
-        if (k > 0 && !mbar_wait(&bars->s_free, (k - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t kd = k_km + static_cast<uint32_t>((ks_ * L::kKBytes) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DQK / 16; ++ks) {
-          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + L::kColS, q_km + off16, kd + off16, id_s, ks > 0);
-        }
-        mma_commit(&bars->s_full);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t k) -> bool {  // dP = dO V^T
-        const int vs = k % VS;
-        if (!mbar_wait(&bars->v_full[vs], (k / VS) & 1)) return false;
-        if (k > 0 && !mbar_wait(&bars->dp_free, (k - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t vd = v_km + static_cast<uint32_t>((vs * L::kVBytes) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DV / 16; ++ks) {
-          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + L::kColDP, o_km + off16, vd + off16, id_s, ks > 0);
-        }
-        mma_commit(&bars->dp_full);
-        mma_commit(&bars->v_empty[vs]);
-        return true;
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-        int b, t, h, kv_lo, n;
-        item_of(idx, b, t, h, kv_lo, n);
-        if (n == 0) continue;
-        if (!(ok = mbar_wait(&bars->q_full, it & 1))) break;
-        if (!(ok = issue_s(kt)) || !(ok = issue_dp(kt))) break;
-        for (int j = 0; j < n; ++j) {
-          const uint32_t k = kt + j;
-          const bool more = j + 1 < n;
-          if (KS >= 2 && more) {
-            if (!(ok = issue_s(k + 1)) || !(ok = issue_dp(k + 1))) break;
-          }
-          if (!more) mma_commit(&bars->q_empty);  // last S / dP of the item issued
-          if (!(ok = mbar_wait(&bars->ds_ready, k & 1))) break;
-          if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->acc_empty, (it - 1) & 1))) break;
-          tc_fence_after();
-          const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)  // dQ += dS K
-            mma_ss(tmem + L::kColDQ, s_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                   kd + ((ks * 2048) >> 4), id_dq, (j > 0 || ks > 0));
-          mma_commit(&bars->ds_free);
-          mma_commit(&bars->k_empty[k % KS]);
-          if (KS == 1 && more) {
-            if (!(ok = issue_s(k + 1)) || !(ok = issue_dp(k + 1))) break;
-          }
-        }
-        if (!ok) break;
-        mma_commit(&bars->acc_full);
-        kt += n;
-        ++it;
-      }
-      if (!ok) {
-        report_timeout(a, 0x230);
-        *abort_flag = 1;
-      }
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 200000000ull);
-    }
-  } else if (warp >= 4) {
-    const int r = tid - 128;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_addr = smem_u32(sm + L::kSOff);
-    uint32_t kt = 0, it = 0;
-    bool ok = true;
-    for (uint32_t rn = 0;; ++rn) {
-      int32_t idx;
-      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
-          idx < 0)
-        break;
-      int b, t, h, kv_lo, n;
-      item_of(idx, b, t, h, kv_lo, n);
-      const int i = t * kTile + r;
-      const bool row_ok = i < a.Sq;
-      const int64_t grow = (int64_t)b * a.Sq + i;
-      bf16* dq_row = a.dq + grow * a.dq_stride + (int64_t)h * DQK;
-      if (n == 0) {
-        if (row_ok) {
-#pragma unroll
-          for (int c = 0; c < DQK; c += 8)
-            *reinterpret_cast<uint4*>(dq_row + c) = make_uint4(0, 0, 0, 0);
-        }
-        continue;
-      }
-      int rlo = 0, rhi = 0, my_id = 0, my_pos = 0;
-      float lse2 = INFINITY, Di = 0.f;
-      if (row_ok) {
-        if (!general) {
-          const int2 kr = band_keys_of_query(a, i, a.seg_lo[grow], a.seg_hi[grow]);
-          rlo = kr.x;
-          rhi = kr.y;
-        } else {
-          my_id = a.q_id[grow];
-          my_pos = a.q_pos[grow];
-        }
-        const int64_t vi = ((int64_t)b * a.Hq + h) * a.Sq + i;
-        lse2 = a.lse2[vi];
-        Di = a.Dvec[vi];
-      }
-      const bf16* bias_row = nullptr;
-      if (HAS_BIAS && row_ok) {
-        const int bb = a.bias_b > 1 ? b : 0, bh = a.bias_h > 1 ? h : 0;
-        bias_row = a.bias + (((int64_t)bb * a.bias_h + bh) * a.Sq + i) * a.Skv;
-      }
-      for (int j = 0; j < n; ++j) {
-        const uint32_t k = kt + j;
-        const int k0 = kv_lo + j * kTile;
-        float x[kTile];
-        if (!(ok = mbar_wait_warp(&bars->s_full, k & 1))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < kTile / 32; ++q) {
-          uint32_t u[32];
-          tmem_ld32x32b_x32(tmem + lane_base + L::kColS + q * 32, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->s_free);
-        if (HAS_BIAS && row_ok) {
-          const bf16* bp = bias_row + k0;
-          const int nv = min(kTile, a.Skv - k0);
-#pragma unroll
-          for (int c = 0; c < kTile; ++c)
-            if (c < nv) x[c] += __bfloat162float(bp[c]) * kLog2e;
-        }
-        uint64_t vb[2];
-        kv_valid_bits(a, general, b, k0, rlo, rhi, my_id, my_pos, vb);
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          const float p = ex2_approx(x[c] - lse2);
-          x[c] = ((vb[c >> 6] >> (c & 63)) & 1ull) ? p : 0.f;
-        }
-        if (!(ok = mbar_wait_warp(&bars->dp_full, k & 1))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < kTile / 32; ++q) {
-          uint32_t u[32];
-          tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + q * 32, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[q * 32 + e] *= (__uint_as_float(u[e]) - Di);
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->dp_free);
-        if (k > 0 && !(ok = mbar_wait_warp(&bars->ds_free, (k - 1) & 1))) break;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-          for (int u8 = 0; u8 < 8; ++u8) {
-            const float* p8 = x + cc * 64 + u8 * 8;
-            st_shared_v4(s_addr + cc * 16384 + r * 128 + ((u8 ^ (r & 7)) << 4),
-                         pack_bf16x2(p8[0], p8[1]), pack_bf16x2(p8[2], p8[3]),
-                         pack_bf16x2(p8[4], p8[5]), pack_bf16x2(p8[6], p8[7]));
-          }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->ds_ready);
-      }
-      if (!ok) break;
-      if (!(ok = mbar_wait_warp(&bars->acc_full, it & 1))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int q = 0; q < DQK / 32; ++q) {
-        uint32_t u[32];
-        tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + q * 32, u);
-        tmem_ld_wait();
-        if (row_ok) {
-          const float sc = a.scale;
-#pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(u[c]) * sc, __uint_as_float(u[c + 1]) * sc);
-            v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * sc, __uint_as_float(u[c + 3]) * sc);
-            v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * sc, __uint_as_float(u[c + 5]) * sc);
-            v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * sc, __uint_as_float(u[c + 7]) * sc);
-            *reinterpret_cast<uint4*>(dq_row + q * 32 + c) = v;
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->acc_empty);
-      kt += n;
-      ++it;
-    }
-    if (!ok) {
-      if (lane == 0) report_timeout(a, 0x240 + (warp & 3));
-      *abort_flag = 1;
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// =========================================================== launchers
-template <typename K>
-cudaError_t set_smem(K kern, int bytes) {
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
-
-template <int DQK, int DV, bool AT, bool HB, int DB>
-cudaError_t dkdv_go(const KernelArgs& a, int nsm, cudaStream_t st) {
-  using L = DkdvLayout<DQK, DV, AT>;
-  auto kern = dkdv_kernel<DQK, DV, AT, HB, DB>;
-  cudaError_t e = set_smem(kern, L::kAlloc);
-  if (e != cudaSuccess) return e;
-  const int nb = a.dkdv_batch_loop ? 1 : a.B, ng = a.dkdv_head_loop ? 1 : a.Hkv;
-  const int items = a.n_kt * nb * ng;
-  const int grid = items < nsm ? items : nsm;
-  kern<<<grid, 512, L::kAlloc, st>>>(a);
-  return cudaGetLastError();
-}
-
-template <int DQK, int DV, bool AT>
-cudaError_t dkdv_bias(const KernelArgs& a, int nsm, cudaStream_t st) {
-  if (!a.bias) return dkdv_go<DQK, DV, AT, false, 0>(a, nsm, st);
-  if (a.dbias_mode == 0) return dkdv_go<DQK, DV, AT, true, 0>(a, nsm, st);
-  if (a.dbias_mode == 1) return dkdv_go<DQK, DV, AT, true, 1>(a, nsm, st);
-  return dkdv_go<DQK, DV, AT, true, 2>(a, nsm, st);
-}
-
-template <int DQK, int DV>
-cudaError_t dq_go(const KernelArgs& a, int nsm, cudaStream_t st) {
-  using L = DqLayout<DQK, DV>;
-  auto kern = a.bias ? dq_kernel<DQK, DV, true> : dq_kernel<DQK, DV, false>;
-  cudaError_t e = set_smem(kern, L::kAlloc);
-  if (e != cudaSuccess) return e;
-  const int items = a.B * a.n_qt * a.Hq;
-  const int grid = items < nsm ? items : nsm;
-  kern<<<grid, 256, L::kAlloc, st>>>(a);
-  return cudaGetLastError();
+  for (int64_t v = 4 * n4 + t0; v < n; v += stride) E::st(a.dbias + v, a.dbias_acc[v]);
 }
 
 int blocks_for(int64_t n, int per_block) {
@@ -1232,7 +184,6 @@ int blocks_for(int64_t n, int per_block) {
 }
 
 }  // namespace
-
 cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st) {
   cudaError_t e;
   if (zero_dq_acc) {
@@ -1251,42 +202,26 @@ cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st
   if (a.Hq > kPreMaxH) return cudaErrorInvalidValue;  // rejected on the host before launch
   const int64_t ntok = (int64_t)a.B * a.Sq;
   const unsigned blocks = static_cast<unsigned>((ntok + kPreTok - 1) / kPreTok);
-  return launch_pdl(a.d_v == 64 ? bwd_pre_kernel<64> : bwd_pre_kernel<128>, dim3(blocks), dim3(256),
-                    0, st, a, mode);
+  auto kern = a.elem_f16 ? (a.d_v == 64 ? bwd_pre_kernel<ElemF16, 64> : bwd_pre_kernel<ElemF16, 128>)
+                         : (a.d_v == 64 ? bwd_pre_kernel<ElemBf16, 64> : bwd_pre_kernel<ElemBf16, 128>);
+  return launch_pdl(kern, dim3(blocks), dim3(256), 0, st, a, mode);
 }
 
 cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic, int nsm, cudaStream_t st) {
-#define DKDV_CASE(DQ, DVV)                                                                  \
-  if (a.d_qk == DQ && a.d_v == DVV)                                                         \
-    return atomic ? dkdv_bias<DQ, DVV, true>(a, nsm, st) : dkdv_bias<DQ, DVV, false>(a, nsm, st);
-  DKDV_CASE(64, 64)
-  DKDV_CASE(64, 128)
-  DKDV_CASE(128, 64)
-  DKDV_CASE(128, 128)
-#undef DKDV_CASE
-  if (a.d_qk == 192 && !atomic) {
-    if (a.d_v == 64) return dkdv_bias<192, 64, false>(a, nsm, st);
-    if (a.d_v == 128) return dkdv_bias<192, 128, false>(a, nsm, st);
-  }
-  return cudaErrorInvalidValue;
+  return a.elem_f16 ? launch_bwd_dkdv_t<ElemF16>(a, atomic, nsm, st)
+                    : launch_bwd_dkdv_t<ElemBf16>(a, atomic, nsm, st);
 }
 
 cudaError_t launch_bwd_dq(const KernelArgs& a, int nsm, cudaStream_t st) {
-  if (a.d_v == 64) {
-    if (a.d_qk == 64) return dq_go<64, 64>(a, nsm, st);
-    if (a.d_qk == 128) return dq_go<128, 64>(a, nsm, st);
-    if (a.d_qk == 192) return dq_go<192, 64>(a, nsm, st);
-  } else if (a.d_v == 128) {
-    if (a.d_qk == 64) return dq_go<64, 128>(a, nsm, st);
-    if (a.d_qk == 128) return dq_go<128, 128>(a, nsm, st);
-    if (a.d_qk == 192) return dq_go<192, 128>(a, nsm, st);
-  }
-  return cudaErrorInvalidValue;
+  return a.elem_f16 ? launch_bwd_dq_t<ElemF16>(a, nsm, st) : launch_bwd_dq_t<ElemBf16>(a, nsm, st);
 }
 
 cudaError_t launch_dq_convert(const KernelArgs& a, cudaStream_t st) {
   const int64_t n = (int64_t)a.B * a.Sq * a.Hq * a.d_qk / 8;
-  dq_convert_kernel<<<blocks_for(n, 256), 256, 0, st>>>(a);
+  if (a.elem_f16)
+    dq_convert_kernel<ElemF16><<<blocks_for(n, 256), 256, 0, st>>>(a);
+  else
+    dq_convert_kernel<ElemBf16><<<blocks_for(n, 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -1299,7 +234,10 @@ cudaError_t launch_sink_reduce(const KernelArgs& a, cudaStream_t st) {
 
 cudaError_t launch_dbias_convert(const KernelArgs& a, cudaStream_t st) {
   const int64_t n = (int64_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
-  dbias_convert_kernel<<<blocks_for(n, 256), 256, 0, st>>>(a);
+  if (a.elem_f16)
+    dbias_convert_kernel<ElemF16><<<blocks_for(n, 256), 256, 0, st>>>(a);
+  else
+    dbias_convert_kernel<ElemBf16><<<blocks_for(n, 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -65,7 +65,7 @@ struct Vec128 {  // per query tile: negated log2-LSE and D
   float D[kQ];
 };
 
-template <int DQK, int DV, bool HAS_BIAS, int DBIAS>
+template <class E, int DQK, int DV, bool HAS_BIAS, int DBIAS>
 __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__ KernelArgs a) {
   using L = D128Layout<DQK, DV>;
   constexpr int NQ = L::kQStages, NO = L::kOStages, NV = L::kVecStages;
@@ -252,10 +252,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop on warp-uniform values; one elected lane
     // issues each GEMM's MMAs from a single asm statement.
-    constexpr uint32_t id_s = idesc_bf16_f32(128, kQ, false, false);   // S^T, N = query
-    constexpr uint32_t id_p = idesc_bf16_f32(128, kQ, false, false);   // dP^T
-    constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, false, true);   // dV, B = dO (MN)
-    constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, false, true);  // dK, B = Q (MN)
+    constexpr uint32_t id_s = idesc_f32acc(E::kMmaFmt, 128, kQ, false, false);   // S^T, N = query
+    constexpr uint32_t id_p = idesc_f32acc(E::kMmaFmt, 128, kQ, false, false);   // dP^T
+    constexpr uint32_t id_dv = idesc_f32acc(E::kMmaFmt, 128, DV, false, true);   // dV, B = dO (MN)
+    constexpr uint32_t id_dk = idesc_f32acc(E::kMmaFmt, 128, DQK, false, true);  // dK, B = Q (MN)
     const uint32_t tm = warp_uniform(tmem);
     const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
     const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
 #pragma unroll
                       for (int c = 0; c < 32; ++c)
                         if (qh + q * 32 + c < a.Sq)
-                          x[c] += __bfloat162float(bp[(int64_t)c * a.Skv]) * kLog2e;
+                          x[c] += E::ld(bp + (int64_t)c * a.Skv) * kLog2e;
                     }
                   }
 #pragma unroll
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                     for (int e = 0; e < 32; ++e) x[e] = (m32 & (1u << e)) ? x[e] : 0.f;
                   }
 #pragma unroll
-                  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                  for (int e = 0; e < 16; ++e) pk[e] = E::pack(x[2 * e], x[2 * e + 1]);
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pp[q * 16 + e] = pk[e];
@@ -518,8 +518,8 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                     const float2 g1 = sub_f32x2(
                         make_float2(__uint_as_float(u[e + 2]), __uint_as_float(u[e + 3])),
                         make_float2(d4.z, d4.w));
-                    pk[e / 2] = mul_bf16x2(pp[q * 16 + e / 2], pack_bf16x2(g0.x, g0.y));
-                    pk[e / 2 + 1] = mul_bf16x2(pp[q * 16 + e / 2 + 1], pack_bf16x2(g1.x, g1.y));
+                    pk[e / 2] = E::mul(pp[q * 16 + e / 2], E::pack(g0.x, g0.y));
+                    pk[e / 2 + 1] = E::mul(pp[q * 16 + e / 2 + 1], E::pack(g1.x, g1.y));
                   }
                   tmem_st32x32b_x16(dp_tm + q * 16, pk);
                   continue;
@@ -532,19 +532,19 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
 #pragma unroll
                   for (int k = 0; k < 4; ++k) {
                     const uint32_t w2 = pp[q * 16 + (e + k) / 2];
-                    const float pv = __uint_as_float(((e + k) & 1) ? (w2 & 0xFFFF0000u) : (w2 << 16));
+                    const float pv = ((e + k) & 1) ? E::hi(w2) : E::lo(w2);
                     ds[e + k] = pv * (__uint_as_float(u[e + k]) - dd[k]);
                   }
                 }
 #pragma unroll
-                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
+                for (int e = 0; e < 16; ++e) pk[e] = E::pack(ds[2 * e], ds[2 * e + 1]);
                 tmem_st32x32b_x16(dp_tm + q * 16, pk);
                 if (DBIAS != 0 && row_ok) {
                   if (DBIAS == 1) {
                     bf16* dpb = a.dbias + (bias_base + qh + q * 32) * a.Skv + kj;
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
-                      if (qh + q * 32 + c < a.Sq) dpb[(int64_t)c * a.Skv] = __float2bfloat16_rn(ds[c]);
+                      if (qh + q * 32 + c < a.Sq) E::st(dpb + (int64_t)c * a.Skv, ds[c]);
                   } else {
                     float* dpb = a.dbias_acc + (bias_base + qh + q * 32) * a.Skv + kj;
                     // eight loads in flight before their stores (a store between
@@ -617,13 +617,12 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
             tmem_ld_wait();
             if (row_ok) {
 #pragma unroll
-              for (int c = 0; c < 32; c += 8) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(u[c]), __uint_as_float(u[c + 1]));
-                v.y = pack_bf16x2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3]));
-                v.z = pack_bf16x2(__uint_as_float(u[c + 4]), __uint_as_float(u[c + 5]));
-                v.w = pack_bf16x2(__uint_as_float(u[c + 6]), __uint_as_float(u[c + 7]));
-                *reinterpret_cast<uint4*>(dv_row + q * 32 + c) = v;
+              for (int c = 0; c < 32; c += 16) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  w[e] = E::pack(__uint_as_float(u[c + 2 * e]), __uint_as_float(u[c + 2 * e + 1]));
+                store16_elems(dv_row + q * 32 + c, w, a.grad_st32 != 0);
               }
             }
           }
@@ -635,13 +634,12 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
             if (row_ok) {
               const float sc = a.scale;
 #pragma unroll
-              for (int c = 0; c < 32; c += 8) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(u[c]) * sc, __uint_as_float(u[c + 1]) * sc);
-                v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * sc, __uint_as_float(u[c + 3]) * sc);
-                v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * sc, __uint_as_float(u[c + 5]) * sc);
-                v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * sc, __uint_as_float(u[c + 7]) * sc);
-                *reinterpret_cast<uint4*>(dk_row + q * 32 + c) = v;
+              for (int c = 0; c < 32; c += 16) {
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  w[e] = E::pack(__uint_as_float(u[c + 2 * e]) * sc, __uint_as_float(u[c + 2 * e + 1]) * sc);
+                store16_elems(dk_row + q * 32 + c, w, a.grad_st32 != 0);
               }
             }
           }
@@ -664,10 +662,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
   }
 }
 
-template <int DQK, int DV, bool HB, int DB>
+template <class E, int DQK, int DV, bool HB, int DB>
 cudaError_t go(const KernelArgs& a, int nsm, cudaStream_t st) {
   using L = D128Layout<DQK, DV>;
-  auto kern = dkdv128_kernel<DQK, DV, HB, DB>;
+  auto kern = dkdv128_kernel<E, DQK, DV, HB, DB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   const int nb = a.dkdv_batch_loop ? 1 : a.B, ng = a.dkdv_head_loop ? 1 : a.Hkv;
@@ -677,12 +675,18 @@ cudaError_t go(const KernelArgs& a, int nsm, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <class E, int DQK, int DV>
+cudaError_t go_bias_e(const KernelArgs& a, int nsm, cudaStream_t st) {
+  if (!a.bias) return go<E, DQK, DV, false, 0>(a, nsm, st);
+  if (a.dbias_mode == 0) return go<E, DQK, DV, true, 0>(a, nsm, st);
+  if (a.dbias_mode == 1) return go<E, DQK, DV, true, 1>(a, nsm, st);
+  return go<E, DQK, DV, true, 2>(a, nsm, st);
+}
+
 template <int DQK, int DV>
 cudaError_t go_bias(const KernelArgs& a, int nsm, cudaStream_t st) {
-  if (!a.bias) return go<DQK, DV, false, 0>(a, nsm, st);
-  if (a.dbias_mode == 0) return go<DQK, DV, true, 0>(a, nsm, st);
-  if (a.dbias_mode == 1) return go<DQK, DV, true, 1>(a, nsm, st);
-  return go<DQK, DV, true, 2>(a, nsm, st);
+  return a.elem_f16 ? go_bias_e<ElemF16, DQK, DV>(a, nsm, st)
+                    : go_bias_e<ElemBf16, DQK, DV>(a, nsm, st);
 }
 
 }  // namespace

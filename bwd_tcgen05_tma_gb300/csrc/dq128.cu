@@ -77,7 +77,7 @@ __device__ __forceinline__ uint64_t kv_bits64(const KernelArgs& a, bool general,
   return v;
 }
 
-template <int DQK, int DV, bool HAS_BIAS>
+template <class E, int DQK, int DV, bool HAS_BIAS>
 __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ KernelArgs a) {
   using L = Dq128Layout<DQK, DV>;
   constexpr int KS = L::kKStages, VS = L::kVStages;
@@ -212,8 +212,8 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
     // on warp-uniform values; one elected lane issues each GEMM's MMAs from a
     // single asm statement.
     const bool s_side = (warp == 1);
-    constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
-    constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, false, true);
+    constexpr uint32_t id_s = idesc_f32acc(E::kMmaFmt, 128, kTile, false, false);
+    constexpr uint32_t id_dq = idesc_f32acc(E::kMmaFmt, 128, DQK, false, true);
     const uint32_t tm = warp_uniform(tmem);
     const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
     const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
               const int kq = kh + q * 32;
 #pragma unroll
               for (int e = 0; e < 32; ++e)
-                if (kq + e < a.Skv) x[e] += __bfloat162float(bias_row[kq + e]) * kLog2e;
+                if (kq + e < a.Skv) x[e] += E::ld(bias_row + kq + e) * kLog2e;
             }
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[e] = ex2_approx(x[e] - lse2);
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
             for (int e = 0; e < 32; ++e) x[e] = (m32 & (1u << e)) ? x[e] : 0.f;
           }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pp[q * 16 + e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+          for (int e = 0; e < 16; ++e) pp[q * 16 + e] = E::pack(x[2 * e], x[2 * e + 1]);
         }
         tc_fence_before();
         mbar_arrive(&bars->s_free);
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
             for (int e = 0; e < 16; ++e) {
               const float2 g = sub_f32x2(
                   make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1])), d2);
-              pk[e] = mul_bf16x2(pp[q * 16 + e], pack_bf16x2(g.x, g.y));
+              pk[e] = E::mul(pp[q * 16 + e], E::pack(g.x, g.y));
             }
           }
           tmem_st32x32b_x16(dp_tm + q * 16, pk);
@@ -484,13 +484,12 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
         if (row_ok) {
           const float sc = a.scale;
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(u[c]) * sc, __uint_as_float(u[c + 1]) * sc);
-            v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * sc, __uint_as_float(u[c + 3]) * sc);
-            v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * sc, __uint_as_float(u[c + 5]) * sc);
-            v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * sc, __uint_as_float(u[c + 7]) * sc);
-            *reinterpret_cast<uint4*>(dq_row + q * 32 + c) = v;
+          for (int c = 0; c < 32; c += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = E::pack(__uint_as_float(u[c + 2 * e]) * sc, __uint_as_float(u[c + 2 * e + 1]) * sc);
+            store16_elems(dq_row + q * 32 + c, w, a.grad_st32 != 0);
           }
         }
       }
@@ -511,10 +510,10 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
   }
 }
 
-template <int DQK, int DV>
+template <class E, int DQK, int DV>
 cudaError_t go(const KernelArgs& a, int nsm, cudaStream_t st) {
   using L = Dq128Layout<DQK, DV>;
-  auto kern = a.bias ? dq128_kernel<DQK, DV, true> : dq128_kernel<DQK, DV, false>;
+  auto kern = a.bias ? dq128_kernel<E, DQK, DV, true> : dq128_kernel<E, DQK, DV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   const int items = a.B * a.n_qt * a.Hq;
@@ -525,12 +524,18 @@ cudaError_t go(const KernelArgs& a, int nsm, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_bwd_dq128(const KernelArgs& a, int nsm, cudaStream_t st) {
-  if (a.d_qk == 64 && a.d_v == 64) return go<64, 64>(a, nsm, st);
-  if (a.d_qk == 64 && a.d_v == 128) return go<64, 128>(a, nsm, st);
-  if (a.d_qk == 128 && a.d_v == 64) return go<128, 64>(a, nsm, st);
-  if (a.d_qk == 128 && a.d_v == 128) return go<128, 128>(a, nsm, st);
+template <class E>
+cudaError_t launch_bwd_dq128_e(const KernelArgs& a, int nsm, cudaStream_t st) {
+  if (a.d_qk == 64 && a.d_v == 64) return go<E, 64, 64>(a, nsm, st);
+  if (a.d_qk == 64 && a.d_v == 128) return go<E, 64, 128>(a, nsm, st);
+  if (a.d_qk == 128 && a.d_v == 64) return go<E, 128, 64>(a, nsm, st);
+  if (a.d_qk == 128 && a.d_v == 128) return go<E, 128, 128>(a, nsm, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_dq128(const KernelArgs& a, int nsm, cudaStream_t st) {
+  return a.elem_f16 ? launch_bwd_dq128_e<ElemF16>(a, nsm, st)
+                    : launch_bwd_dq128_e<ElemBf16>(a, nsm, st);
 }
 
 }  // namespace attn

@@ -84,6 +84,7 @@ __device__ __forceinline__ FwdItem fwd_item(const KernelArgs& a, int idx) {
 }
 
 // Adds bias[i, k0 + c] * log2(e) to x[c] for c < nvalid (row pointer given).
+template <class E>
 __device__ __forceinline__ void add_bias_row(float (&x)[kTile], const bf16* row, int nvalid) {
   const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
 #pragma unroll
@@ -93,18 +94,18 @@ __device__ __forceinline__ void add_bias_row(float (&x)[kTile], const bf16* row,
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        x[c + 2 * e] += __uint_as_float(w[e] << 16) * kLog2e;
-        x[c + 2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u) * kLog2e;
+        x[c + 2 * e] += E::lo(w[e]) * kLog2e;
+        x[c + 2 * e + 1] += E::hi(w[e]) * kLog2e;
       }
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        if (c + e < nvalid) x[c + e] += __bfloat162float(row[c + e]) * kLog2e;
+        if (c + e < nvalid) x[c + e] += E::ld(row + c + e) * kLog2e;
     }
   }
 }
 
-template <int DQK, int DV, bool HAS_BIAS>
+template <class E, int DQK, int DV, bool HAS_BIAS>
 __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ KernelArgs a) {
   using L = FwdLayout<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -214,8 +215,8 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTile, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, DV, false, true);
+      constexpr uint32_t idesc_s = idesc_f32acc(E::kMmaFmt, 128, kTile, false, false);
+      constexpr uint32_t idesc_o = idesc_f32acc(E::kMmaFmt, 128, DV, false, true);
       // operand descriptors are built once; each MMA only adds a constant offset
       const uint64_t q_desc = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
       const uint64_t p_desc = sdesc_sw128(smem_u32(sm + L::kPOff), 16, 1024);
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         }
         tc_fence_before();
         mbar_arrive(&bars->s_empty[sb]);
-        if (HAS_BIAS && row_ok) add_bias_row(x, bias_row + k0, min(kTile, a.Skv - k0));
+        if (HAS_BIAS && row_ok) add_bias_row<E>(x, bias_row + k0, min(kTile, a.Skv - k0));
         // mask (branch-free: a validity bitmask per row and tile)
         uint64_t vb[2];
         kv_valid_bits(a, general, w.b, k0, rlo, rhi, my_id, my_pos, vb);
@@ -416,8 +417,8 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
           for (int u = 0; u < 8; ++u) {
             const float* p8 = x + cc * 64 + u * 8;
             st_shared_v4(p_addr + (k % L::kPStages) * L::kPBytes + cc * 16384 + r * 128 + ((u ^ (r & 7)) << 4),
-                         pack_bf16x2(p8[0], p8[1]), pack_bf16x2(p8[2], p8[3]),
-                         pack_bf16x2(p8[4], p8[5]), pack_bf16x2(p8[6], p8[7]));
+                         E::pack(p8[0], p8[1]), E::pack(p8[2], p8[3]),
+                         E::pack(p8[4], p8[5]), E::pack(p8[6], p8[7]));
           }
         }
         fence_proxy_async_smem();
@@ -448,10 +449,10 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(u[c + 0]) * inv_l, __uint_as_float(u[c + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(u[c + 2]) * inv_l, __uint_as_float(u[c + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(u[c + 4]) * inv_l, __uint_as_float(u[c + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(u[c + 6]) * inv_l, __uint_as_float(u[c + 7]) * inv_l);
+            v.x = E::pack(__uint_as_float(u[c + 0]) * inv_l, __uint_as_float(u[c + 1]) * inv_l);
+            v.y = E::pack(__uint_as_float(u[c + 2]) * inv_l, __uint_as_float(u[c + 3]) * inv_l);
+            v.z = E::pack(__uint_as_float(u[c + 4]) * inv_l, __uint_as_float(u[c + 5]) * inv_l);
+            v.w = E::pack(__uint_as_float(u[c + 6]) * inv_l, __uint_as_float(u[c + 7]) * inv_l);
             *reinterpret_cast<uint4*>(orow + q * 32 + c) = v;
           }
         }
@@ -476,10 +477,10 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
   }
 }
 
-template <int DQK, int DV, bool HB>
+template <class E, int DQK, int DV, bool HB>
 cudaError_t launch_fwd_t(const KernelArgs& a, int num_sms, cudaStream_t st) {
   using L = FwdLayout<DQK, DV>;
-  auto kern = fwd_kernel<DQK, DV, HB>;
+  auto kern = fwd_kernel<E, DQK, DV, HB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_items = a.B * a.n_qt * a.Hq;
@@ -490,8 +491,11 @@ cudaError_t launch_fwd_t(const KernelArgs& a, int num_sms, cudaStream_t st) {
 
 template <int DQK, int DV>
 cudaError_t launch_fwd_b(const KernelArgs& a, int num_sms, cudaStream_t st) {
-  return a.bias ? launch_fwd_t<DQK, DV, true>(a, num_sms, st)
-                : launch_fwd_t<DQK, DV, false>(a, num_sms, st);
+  if (a.elem_f16)
+    return a.bias ? launch_fwd_t<ElemF16, DQK, DV, true>(a, num_sms, st)
+                  : launch_fwd_t<ElemF16, DQK, DV, false>(a, num_sms, st);
+  return a.bias ? launch_fwd_t<ElemBf16, DQK, DV, true>(a, num_sms, st)
+                : launch_fwd_t<ElemBf16, DQK, DV, false>(a, num_sms, st);
 }
 
 }  // namespace

@@ -92,7 +92,7 @@ struct F2Row {
 // valid throughout the warp, the key mask (separate instantiations keep the
 // per-element code free of branches).  The mask also writes -inf over the
 // masked scores, so the exponential pass needs no mask of its own.
-template <bool MASKED, bool HAS_BIAS>
+template <class E, bool MASKED, bool HAS_BIAS>
 __device__ __forceinline__ void chunk_max2(uint32_t (&u)[32], uint32_t m32, float scale_log2,
                                            const bf16* bias_row, int kc0, int Skv, bool row_ok,
                                            float (&mx8)[8]) {
@@ -105,14 +105,14 @@ __device__ __forceinline__ void chunk_max2(uint32_t (&u)[32], uint32_t m32, floa
       x[t] = __uint_as_float(u[e + t]);
       if (HAS_BIAS) {
         x[t] *= scale_log2;
-        if (row_ok && kc0 + e + t < Skv) x[t] += __bfloat162float(bias_row[kc0 + e + t]) * kLog2e;
+        if (row_ok && kc0 + e + t < Skv) x[t] += E::ld(bias_row + kc0 + e + t) * kLog2e;
       }
     }
     mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], x[0], x[1]);
   }
 }
 
-template <bool MASKED, bool HAS_BIAS>
+template <class E, bool MASKED, bool HAS_BIAS>
 __device__ __forceinline__ void chunk_exp2(const uint32_t (&u)[32], uint32_t m32, float scale_log2,
                                            float m_use, const bf16* bias_row, int kc0, int Skv,
                                            bool row_ok, float (&rs4)[4], uint32_t (&pk)[16]) {
@@ -124,7 +124,7 @@ __device__ __forceinline__ void chunk_exp2(const uint32_t (&u)[32], uint32_t m32
       for (int t = 0; t < 2; ++t) {
         const int c = 2 * e + t;
         y[t] = __uint_as_float(u[c]) * scale_log2;
-        if (row_ok && kc0 + c < Skv) y[t] += __bfloat162float(bias_row[kc0 + c]) * kLog2e;
+        if (row_ok && kc0 + c < Skv) y[t] += E::ld(bias_row + kc0 + c) * kLog2e;
         y[t] -= m_use;
       }
     } else {
@@ -146,11 +146,11 @@ __device__ __forceinline__ void chunk_exp2(const uint32_t (&u)[32], uint32_t m32
     const float2 acc = add_f32x2(make_float2(rs4[r], rs4[r + 1]), make_float2(p2[0], p2[1]));
     rs4[r] = acc.x;
     rs4[r + 1] = acc.y;
-    pk[e] = pack_bf16x2(p2[0], p2[1]);
+    pk[e] = E::pack(p2[0], p2[1]);
   }
 }
 
-template <int DQK, int DV, bool HAS_BIAS>
+template <class E, int DQK, int DV, bool HAS_BIAS>
 __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ KernelArgs a) {
   using L = F2Layout<DQK, DV>;
   constexpr int NKV = L::kKVStages;
@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       // ------------------------------------------------------------ MMA issuer
       // The whole warp runs this loop on warp-uniform values; one elected lane
       // issues each GEMM's MMAs from a single asm statement.
-      constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, false, false);
-      constexpr uint32_t id_o = idesc_bf16_f32(128, DV, false, true);
+      constexpr uint32_t id_s = idesc_f32acc(E::kMmaFmt, 128, kTile, false, false);
+      constexpr uint32_t id_o = idesc_f32acc(E::kMmaFmt, 128, DV, false, true);
       const uint32_t tm = warp_uniform(tmem);
       const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
       const uint64_t kv_km = sdesc_sw128(smem_u32(sm + L::kKVOff), 16, 1024);
@@ -524,10 +524,10 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         for (int q = 0; q < 4; ++q) {
           if (none[q]) continue;
           if (all[q])
-            chunk_max2<false, HAS_BIAS>(u[q], m32s[q], a.scale_log2, bias_row, k0 + q * 32, a.Skv,
+            chunk_max2<E, false, HAS_BIAS>(u[q], m32s[q], a.scale_log2, bias_row, k0 + q * 32, a.Skv,
                                         row_ok, mx8);
           else
-            chunk_max2<true, HAS_BIAS>(u[q], m32s[q], a.scale_log2, bias_row, k0 + q * 32, a.Skv,
+            chunk_max2<E, true, HAS_BIAS>(u[q], m32s[q], a.scale_log2, bias_row, k0 + q * 32, a.Skv,
                                        row_ok, mx8);
         }
         float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
 #pragma unroll
             for (int e = 0; e < 16; ++e) pk[e] = 0u;
           } else {  // masked scores are -inf by now: exp2 gives 0 there
-            chunk_exp2<false, HAS_BIAS>(u[q], m32s[q], a.scale_log2, m_use, bias_row, k0 + q * 32,
+            chunk_exp2<E, false, HAS_BIAS>(u[q], m32s[q], a.scale_log2, m_use, bias_row, k0 + q * 32,
                                         a.Skv, row_ok, rs4, pk);
           }
           tmem_st32x32b_x16(s_tm + q * 16, pk);
@@ -613,10 +613,10 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           const int e8 = c * 8;
           const uint32_t chunk = static_cast<uint32_t>(((q & 1) * 4 + c) ^ (r & 7));
           st_shared_v4(row + chunk * 16,
-                       pack_bf16x2(__uint_as_float(u[e8 + 0]) * inv_l, __uint_as_float(u[e8 + 1]) * inv_l),
-                       pack_bf16x2(__uint_as_float(u[e8 + 2]) * inv_l, __uint_as_float(u[e8 + 3]) * inv_l),
-                       pack_bf16x2(__uint_as_float(u[e8 + 4]) * inv_l, __uint_as_float(u[e8 + 5]) * inv_l),
-                       pack_bf16x2(__uint_as_float(u[e8 + 6]) * inv_l, __uint_as_float(u[e8 + 7]) * inv_l));
+                       E::pack(__uint_as_float(u[e8 + 0]) * inv_l, __uint_as_float(u[e8 + 1]) * inv_l),
+                       E::pack(__uint_as_float(u[e8 + 2]) * inv_l, __uint_as_float(u[e8 + 3]) * inv_l),
+                       E::pack(__uint_as_float(u[e8 + 4]) * inv_l, __uint_as_float(u[e8 + 5]) * inv_l),
+                       E::pack(__uint_as_float(u[e8 + 6]) * inv_l, __uint_as_float(u[e8 + 7]) * inv_l));
         }
       }
       // every row of the tile is in shared memory: one thread stores it (rows
@@ -656,10 +656,10 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
   }
 }
 
-template <int DQK, int DV>
+template <class E, int DQK, int DV>
 cudaError_t go(const KernelArgs& a, int nsm, cudaStream_t st) {
   using L = F2Layout<DQK, DV>;
-  auto kern = a.bias ? fwd2t_kernel<DQK, DV, true> : fwd2t_kernel<DQK, DV, false>;
+  auto kern = a.bias ? fwd2t_kernel<E, DQK, DV, true> : fwd2t_kernel<E, DQK, DV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   const int items = a.B * a.n_qt * (a.Hq / 2);
@@ -670,12 +670,17 @@ cudaError_t go(const KernelArgs& a, int nsm, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_fwd2t(const KernelArgs& a, int nsm, cudaStream_t st) {
-  if (a.d_qk == 64 && a.d_v == 64) return go<64, 64>(a, nsm, st);
-  if (a.d_qk == 64 && a.d_v == 128) return go<64, 128>(a, nsm, st);
-  if (a.d_qk == 128 && a.d_v == 64) return go<128, 64>(a, nsm, st);
-  if (a.d_qk == 128 && a.d_v == 128) return go<128, 128>(a, nsm, st);
+template <class E>
+cudaError_t launch_fwd2t_e(const KernelArgs& a, int nsm, cudaStream_t st) {
+  if (a.d_qk == 64 && a.d_v == 64) return go<E, 64, 64>(a, nsm, st);
+  if (a.d_qk == 64 && a.d_v == 128) return go<E, 64, 128>(a, nsm, st);
+  if (a.d_qk == 128 && a.d_v == 64) return go<E, 128, 64>(a, nsm, st);
+  if (a.d_qk == 128 && a.d_v == 128) return go<E, 128, 128>(a, nsm, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd2t(const KernelArgs& a, int nsm, cudaStream_t st) {
+  return a.elem_f16 ? launch_fwd2t_e<ElemF16>(a, nsm, st) : launch_fwd2t_e<ElemBf16>(a, nsm, st);
 }
 
 }  // namespace attn

@@ -179,12 +179,14 @@ SM103_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
+// Instruction descriptor for kind::f16 with fp32 accumulation; ab_fmt is the
+// format of both A and B (0 fp16, 1 bf16; the two are always the same).
 // a_mn / b_mn select MN-major (transposed) shared-memory operands.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4)     // D: f32
-         | (1u << 7)   // A: bf16
-         | (1u << 10)  // B: bf16
+__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_fmt, int M, int N, bool a_mn,
+                                                    bool b_mn) {
+  return (1u << 4)           // D: f32
+         | (ab_fmt << 7)     // A
+         | (ab_fmt << 10)    // B
          | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
@@ -388,6 +390,18 @@ SM103_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, ok);
 }
 
+// fp16 counterparts of the two above.
+SM103_DEV uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+SM103_DEV uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Elementwise product of two packed bf16 pairs, rounded to nearest even.
 SM103_DEV uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -466,6 +480,14 @@ SM103_DEV uint4 ld_nc_v4(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
+}
+
+// 32-byte global store (the address must be 32-byte aligned).
+SM103_DEV void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                            uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
 }
 
 SM103_DEV void red_add_f32(float* p, float v) {

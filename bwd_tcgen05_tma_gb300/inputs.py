@@ -3,8 +3,8 @@
 This module only draws random numbers and lays them out; it holds none of the
 attention arithmetic.  Both the CUDA path and the float64 oracle consume what
 it returns: tensors are drawn in float32 from ``numpy.random.default_rng(seed)``
-and rounded to bfloat16 (round to nearest even), so both sides see exactly the
-same bf16 values.
+and rounded to bfloat16 (or, for cases of the fp16 element type, to float16;
+round to nearest even), so both sides see exactly the same 16-bit values.
 
 Workloads (one seed each, sizes as named):
 
@@ -56,6 +56,17 @@ def bf16_to_f32(bits):
 def bf16_round(x):
     """float32 values rounded to the nearest bf16 value (kept as float32)."""
     return bf16_to_f32(bf16_bits(x))
+
+
+def f16_round(x):
+    """float32 values rounded to the nearest fp16 value (kept as float32;
+    NumPy's float16 conversion rounds to nearest even)."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
+def round_to(x, dtype):
+    """Nearest value of the element type ("bf16" or "fp16"), as float32."""
+    return bf16_round(x) if dtype == "bf16" else f16_round(x)
 
 
 # ----------------------------------------------------------------- metadata
@@ -118,6 +129,7 @@ class Case:
     bias: np.ndarray | None = None  # [bias_b, bias_h, Sq, Skv]
     window: tuple | None = None  # band (left, right) in positions, None for an open side
     bottom_right: bool = False  # positions aligned by Skv - Sq
+    dtype: str = "bf16"  # element type of the 16-bit tensors: "bf16" or "fp16"
 
     @property
     def mask(self):
@@ -127,34 +139,38 @@ class Case:
         return "CAUSAL" if self.causal else "NONE"
 
 
-def _normal_bf16(rng, shape, std=1.0):
+def _normal_bf16(rng, shape, std=1.0, dtype="bf16"):
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
-    return bf16_round(x)
+    return round_to(x, dtype)
 
 
-def make_buffers(rng, layout, B, Sq, Skv, Hq, Hkv, d_qk, d_v):
-    """Raw token-major input buffers of the layout, N(0,1) in bf16."""
+def make_buffers(rng, layout, B, Sq, Skv, Hq, Hkv, d_qk, d_v, dtype="bf16"):
+    """Raw token-major input buffers of the layout, N(0,1) rounded to the
+    element type (bf16 unless dtype is "fp16")."""
+    def nrm(shape):
+        return _normal_bf16(rng, shape, dtype=dtype)
+
     if layout == "3HD":
         assert Sq == Skv
-        return {"qkv": _normal_bf16(rng, (B * Sq, Hq * d_qk + Hkv * d_qk + Hkv * d_v))}
+        return {"qkv": nrm((B * Sq, Hq * d_qk + Hkv * d_qk + Hkv * d_v))}
     if layout == "HD_2HD":
         assert d_qk == d_v
         return {
-            "q": _normal_bf16(rng, (B * Sq, Hq * d_qk)),
-            "kv": _normal_bf16(rng, (B * Skv, 2, Hkv, d_v)),
+            "q": nrm((B * Sq, Hq * d_qk)),
+            "kv": nrm((B * Skv, 2, Hkv, d_v)),
         }
     return {
-        "q": _normal_bf16(rng, (B, Sq, Hq, d_qk)),
-        "k": _normal_bf16(rng, (B, Skv, Hkv, d_qk)),
-        "v": _normal_bf16(rng, (B, Skv, Hkv, d_v)),
+        "q": nrm((B, Sq, Hq, d_qk)),
+        "k": nrm((B, Skv, Hkv, d_qk)),
+        "v": nrm((B, Skv, Hkv, d_v)),
     }
 
 
 def synth(name, *, B, Sq, Skv, Hq, Hkv, d_qk, d_v, layout, fmt, causal, seed,
           seg=None, kv_seg=None, pad_frac=0.0, pad_range=None, two_segments=False,
-          bias_shape=None, bias_std=0.5, scale=None):
+          bias_shape=None, bias_std=0.5, scale=None, dtype="bf16"):
     """General seeded case builder.
 
     seg / kv_seg: (lo, hi) segment length ranges for Q / KV (kv_seg None means
@@ -164,7 +180,7 @@ def synth(name, *, B, Sq, Skv, Hq, Hkv, d_qk, d_v, layout, fmt, causal, seed,
     rng = np.random.default_rng(seed)
     c = Case(name=name, B=B, Sq=Sq, Skv=Skv, Hq=Hq, Hkv=Hkv, d_qk=d_qk, d_v=d_v,
              layout=layout, fmt=fmt, causal=causal, seed=seed,
-             scale=(1.0 / math.sqrt(d_qk)) if scale is None else scale)
+             scale=(1.0 / math.sqrt(d_qk)) if scale is None else scale, dtype=dtype)
     if fmt == "THD_SEGMENTS":
         qi = np.zeros((B, Sq), np.int32)
         qp = np.zeros((B, Sq), np.int32)
@@ -187,10 +203,10 @@ def synth(name, *, B, Sq, Skv, Hq, Hkv, d_qk, d_v, layout, fmt, causal, seed,
                 klens = fill_segments(rng, Skv - kpad, *kv_seg)
                 ki[b], kp[b] = ids_pos_from_lengths(klens, Skv)
         c.q_ids, c.q_pos, c.kv_ids, c.kv_pos = qi, qp, ki, kp
-    c.buffers = make_buffers(rng, layout, B, Sq, Skv, Hq, Hkv, d_qk, d_v)
-    c.do = _normal_bf16(rng, (B, Sq, Hq, d_v))
+    c.buffers = make_buffers(rng, layout, B, Sq, Skv, Hq, Hkv, d_qk, d_v, dtype)
+    c.do = _normal_bf16(rng, (B, Sq, Hq, d_v), dtype=dtype)
     if bias_shape is not None:
-        c.bias = _normal_bf16(rng, bias_shape, std=bias_std)
+        c.bias = _normal_bf16(rng, bias_shape, std=bias_std, dtype=dtype)
     return c
 
 

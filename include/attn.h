@@ -39,7 +39,9 @@
  *    stream is joined back before the call returns.
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call returns a status and launches nothing.  No call aborts.
- *  - Element type of Q/K/V/O/dO/bias and of all gradients: bf16.  LSE: fp32.
+ *  - Element type of Q/K/V/O/dO/bias and of all gradients: bf16 or fp16
+ *    (attn_params_t.dtype; the MMAs take that type, accumulate in fp32, and
+ *    P and dS are rounded to it).  LSE: fp32.
  *  - Token-major memory: a BSHD tensor [B, S, H, D] is B*S token rows; a THD
  *    tensor with B rows of S tokens uses the same addressing (row b, token t
  *    is token row b*S + t).  With cu_seqlens, B = 1 and S = total tokens.
@@ -105,6 +107,9 @@ typedef enum {
  * separate pass per query tile that visits KV tiles in a fixed order
  * (bit-reproducible).  dK, dV and dBias are bit-reproducible in both modes. */
 typedef enum { ATTN_DQ_ATOMIC = 0, ATTN_DQ_DETERMINISTIC = 1 } attn_dq_mode_t;
+
+/* 16-bit element type of Q/K/V/O/dO/bias and of all gradients. */
+typedef enum { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_FP16 = 1 } attn_dtype_t;
 
 typedef struct {
   int32_t struct_version; /* = ATTN_PARAMS_VERSION */
@@ -178,6 +183,10 @@ typedef struct {
   int32_t window_left;
   int32_t window_right;
   int32_t bottom_right;
+  /* attn_dtype_t of every 16-bit tensor (zero: bf16).  An adjacent precision
+   * of the same computation (the pages use bf16 only); ATTN_ERR_INVALID_ARG
+   * for other values. */
+  int32_t dtype;
 } attn_params_t;
 
 /* Which metadata path the device chose (read back by attn_read_status). */

@@ -15,9 +15,18 @@ TOL_GRAD = 1.5e-2
 TOL_DBIAS = 3e-2
 
 
-def bf16_dev(x):
-    bits = I.bf16_bits(np.ascontiguousarray(x, dtype=np.float32))
+def bf16_dev(x, dtype="bf16"):
+    """A float32 array holding values of the element type -> device tensor of
+    that type (exact: the values are representable)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == "fp16":
+        return torch.from_numpy(x.astype(np.float16)).cuda()
+    bits = I.bf16_bits(x)
     return torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def torch_dtype(case):
+    return torch.float16 if case.dtype == "fp16" else torch.bfloat16
 
 
 def int_dev(x):
@@ -29,9 +38,9 @@ class DevCase:
 
     def __init__(self, case, dq_mode="deterministic", force_general=False, with_pos=True):
         self.case = c = case
-        self.t = {k: bf16_dev(v) for k, v in c.buffers.items()}
-        self.do = bf16_dev(c.do.reshape(c.B * c.Sq, c.Hq, c.d_v))
-        self.bias = bf16_dev(c.bias) if c.bias is not None else None
+        self.t = {k: bf16_dev(v, c.dtype) for k, v in c.buffers.items()}
+        self.do = bf16_dev(c.do.reshape(c.B * c.Sq, c.Hq, c.d_v), c.dtype)
+        self.bias = bf16_dev(c.bias, c.dtype) if c.bias is not None else None
         self.q_ids = int_dev(c.q_ids)
         self.kv_ids = int_dev(c.kv_ids)
         self.q_pos = int_dev(c.q_pos) if with_pos else None
@@ -50,7 +59,7 @@ class DevCase:
             q_seg_ids=self.q_ids, q_seg_pos=self.q_pos, kv_seg_ids=self.kv_ids,
             kv_seg_pos=self.kv_pos, cu_seqlens_q=self.cu_q, cu_seqlens_kv=self.cu_kv,
             bias=self.bias, dq_mode=dq_mode, force_general_path=force_general,
-            window=c.window, bottom_right=c.bottom_right)
+            window=c.window, bottom_right=c.bottom_right, dtype=c.dtype)
         self.ws_fwd = torch.zeros(max(A.attn_fwd_workspace_size(self.params), 256),
                                   dtype=torch.uint8, device="cuda")
         self.ws_bwd = torch.zeros(max(A.attn_bwd_workspace_size(self.params), 256),
@@ -59,7 +68,7 @@ class DevCase:
     def forward(self, canary=True):
         c = self.case
         fill = float("nan") if canary else 0.0
-        self.o = torch.full((c.B * c.Sq, c.Hq, c.d_v), fill, dtype=torch.bfloat16, device="cuda")
+        self.o = torch.full((c.B * c.Sq, c.Hq, c.d_v), fill, dtype=torch_dtype(c), device="cuda")
         self.lse = torch.full((c.B, c.Hq, c.Sq), fill, dtype=torch.float32, device="cuda")
         A.attn_fwd(self.params, self.o, self.lse, self.ws_fwd)
         st, stats = A.attn_read_status(self.ws_fwd)
@@ -72,7 +81,7 @@ class DevCase:
         fill = float("nan") if canary else 0.0
 
         def z(*shape):
-            return torch.full(shape, fill, dtype=torch.bfloat16, device="cuda")
+            return torch.full(shape, fill, dtype=torch_dtype(c), device="cuda")
 
         if c.layout == "3HD":
             W = c.Hq * c.d_qk + c.Hkv * c.d_qk + c.Hkv * c.d_v
@@ -91,7 +100,7 @@ class DevCase:
         dbias = None
         if c.bias is not None and want_dbias:
             dbias = torch.full(c.bias.shape, float("nan") if canary else 0.0,
-                               dtype=torch.bfloat16, device="cuda")
+                               dtype=torch_dtype(c), device="cuda")
         A.attn_bwd(self.params, self.o, self.do, self.lse, dq, dk, dv, dbias, self.ws_bwd)
         st, stats = A.attn_read_status(self.ws_bwd)
         assert st == 0, f"device status {st}"

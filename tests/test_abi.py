@@ -199,3 +199,13 @@ def test_band_validation(lib):
                       Hkv=1, d_qk=64, d_v=64, scale=0.1, q=None, window=(None, 0),
                       bottom_right=True)
     assert (m.band, m.window_left, m.window_right, m.bottom_right) == (1, -1, 0, 1)
+
+
+def test_dtype_validation(lib):
+    p = params()
+    for dt, ok in ((0, True), (1, True), (2, False), (-1, False)):
+        p.dtype = dt
+        assert (A.attn_fwd_workspace_size(p) > 0) == ok
+    m = A.make_params(layout="HD_HD_HD", fmt="BSHD", mask="NONE", B=1, Sq=8, Skv=8, Hq=1, Hkv=1,
+                      d_qk=64, d_v=64, scale=0.1, q=None, dtype="fp16")
+    assert m.dtype == 1

@@ -373,3 +373,27 @@ def _bwd_ws_size(params):
     from bwd_tcgen05_tma_gb300 import attn as A
 
     return A.attn_bwd_workspace_size(params)
+
+
+def test_backward_gradients_only_16_byte_aligned():
+    """Gradient buffers that start 16 bytes past a 32-byte boundary (the ABI
+    asks for 16): the epilogues then take their 16-byte stores, and the
+    gradients are the bits of the aligned call."""
+    from gpu_util import DevCase
+
+    from bwd_tcgen05_tma_gb300 import attn as A
+
+    case = CASES["thd_gqa_3hd"]()
+    d = DevCase(case, dq_mode="deterministic")
+    d.forward()
+    g_ref, _ = d.backward()
+    ref = g_ref["dqkv"].clone()
+    W = ref.shape[1]
+    big = torch.full((ref.numel() + 16,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert big.data_ptr() % 32 == 0
+    dqkv = big[8:8 + ref.numel()].view(ref.shape)  # 16 bytes past the boundary
+    assert dqkv.data_ptr() % 32 == 16
+    A.attn_bwd(d.params, d.o, d.do, d.lse, dqkv, None, None, None, d.ws_bwd)
+    st, _ = A.attn_read_status(d.ws_bwd)
+    assert st == 0 and W == dqkv.shape[1]
+    assert torch.equal(dqkv.view(torch.int16), ref.view(torch.int16))

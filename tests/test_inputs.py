@@ -50,3 +50,15 @@ def test_cross_recipe_independent_metadata():
     assert c.q_ids.shape == (2, 4096) and c.kv_ids.shape == (2, 8192)
     assert np.all(c.q_ids > 0) and np.all(c.kv_ids > 0)
     assert abs(float(c.bias.std()) - 0.5) < 0.01
+
+
+def test_fp16_inputs_are_fp16_values():
+    """Cases of the fp16 element type hold float32 copies of fp16 values
+    (exactly representable, so both sides read the same numbers)."""
+    c = I.synth("f", B=1, Sq=64, Skv=64, Hq=2, Hkv=1, d_qk=64, d_v=64, layout="HD_HD_HD",
+                fmt="BSHD", causal=True, seed=3, dtype="fp16", bias_shape=(1, 2, 64, 64))
+    for x in (c.buffers["q"], c.buffers["k"], c.buffers["v"], c.do, c.bias):
+        assert np.array_equal(x.astype(np.float16).astype(np.float32), x)
+    assert c.dtype == "fp16"
+    assert np.array_equal(I.f16_round(np.float32([1.0 + 2.0 ** -11, 65504.0])),
+                          np.float32([1.0, 65504.0]))
