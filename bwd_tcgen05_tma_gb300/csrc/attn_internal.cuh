@@ -111,15 +111,6 @@ __device__ __forceinline__ bool ring_pop(ItemRing* r, uint32_t n, int32_t& item)
   return true;
 }
 
-// Single-thread consumer variant (MMA issuer).
-__device__ __forceinline__ bool ring_pop1(ItemRing* r, uint32_t n, int32_t& item) {
-  const int s = n % kItemRing;
-  if (!sm103::mbar_wait(&r->full[s], (n / kItemRing) & 1)) return false;
-  item = *reinterpret_cast<volatile int32_t*>(&r->item[s]);
-  sm103::mbar_arrive(&r->empty[s]);
-  return true;
-}
-
 // Whole-warp consumer that counts as one arrival (the warp-wide MMA issuers):
 // every lane waits, lane 0 reads the entry and releases the slot, and the
 // item reaches every lane as a warp-uniform value.

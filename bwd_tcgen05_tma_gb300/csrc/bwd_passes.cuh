@@ -240,117 +240,109 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f32acc(E::kMmaFmt, 128, kBwdQ, false, false);
-      constexpr uint32_t id_dv = idesc_f32acc(E::kMmaFmt, 128, DV, false, true);
-      constexpr uint32_t id_dk = idesc_f32acc(E::kMmaFmt, 128, DQK, false, true);
-      constexpr uint32_t id_dq = idesc_f32acc(E::kMmaFmt, 128, kBwdQ, true, true);
-      // operand descriptors are built once; each MMA only adds a constant offset
-      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);      // K, K-major
-      const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);   // K^T, MN-major
-      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
-      const uint64_t ds_km = sdesc_sw128(smem_u32(sm + L::kDSOff), 16, 1024);
-      const uint64_t ds_mn = sdesc_sw128(smem_u32(sm + L::kDSOff), 8192, 1024);
-      const uint64_t st_km = sdesc_sw128(smem_u32(sm + L::kStageOff), 16, 1024);   // Q / dO tiles
-      const uint64_t st_mn = sdesc_sw128(smem_u32(sm + L::kStageOff), 8192, 1024);
-      uint32_t st = 0, kvc = 0, gc = 0;
-      bool ok = true;
-      auto stage_off16 = [&](uint32_t x) -> uint32_t {
-        return static_cast<uint32_t>(((x % NS) * L::kStageBytes) >> 4);
-      };
-      auto issue_s = [&](uint32_t x) -> bool {  // S^T = K Q^T into buffer x & 1
-        if (!mbar_wait(&bars->qd_full[x % NS], (x / NS) & 1)) return false;
-        // buffer x & 1 still holds P^T(x - 2) until dV(x - 2) has read it
-        if (x >= 2 && !mbar_wait(&bars->p_free[x & 1], ((x >> 1) - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t qd = st_km + stage_off16(x);
-        const uint32_t dt = tmem + L::kColS + 64 * (x & 1);
-#pragma unroll
-        for (int ks = 0; ks < DQK / 16; ++ks)
-          mma_ss(dt, k_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                 qd + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id_s, ks > 0);
-        mma_commit(&bars->s_full[x & 1]);
-        ATTN_TL(10, x);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t x) -> bool {  // dP^T = V dO^T
-        if (x > 0 && !mbar_wait(&bars->dp_free, (x - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t od = st_km + stage_off16(x) + (L::kQBytes >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DV / 16; ++ks)
-          mma_ss(tmem + L::kColDP, v_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                 od + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), id_s, ks > 0);
-        mma_commit(&bars->dp_full);
-        ATTN_TL(11, x);
-        return true;
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-        const DkdvItem w = dkdv_item(a, idx);
-        for (int b = w.b0; b < w.b1 && ok; ++b) {
-          for (int g = w.g0; g < w.g1 && ok; ++g) {
-            int q_lo;
-            const int nq = dkdv_q_tiles(a, b, w.t, q_lo);
-            if (nq == 0) continue;
-            const uint32_t nsteps = (uint32_t)nq * G;
-            if (!(ok = mbar_wait(&bars->kv_full, kvc & 1))) break;
-            ++kvc;
-            if (!(ok = issue_s(st))) break;
-            if (!(ok = issue_dp(st))) break;
-            for (uint32_t u = 0; u < nsteps; ++u) {
-              const uint32_t cur = st + u;
-              if (u + 1 < nsteps && !(ok = issue_s(cur + 1))) break;
-              if (!(ok = mbar_wait(&bars->p_ready[cur & 1], (cur >> 1) & 1))) break;
-              ATTN_TL(12, cur);
-              if (u == 0 && gc > 0 && !(ok = mbar_wait(&bars->acc_empty, (gc - 1) & 1))) break;
+    // The whole warp runs this loop on warp-uniform values; one elected lane
+    // issues each GEMM's MMAs from a single asm statement.
+    constexpr uint32_t id_s = idesc_f32acc(E::kMmaFmt, 128, kBwdQ, false, false);
+    constexpr uint32_t id_dv = idesc_f32acc(E::kMmaFmt, 128, DV, false, true);
+    constexpr uint32_t id_dk = idesc_f32acc(E::kMmaFmt, 128, DQK, false, true);
+    constexpr uint32_t id_dq = idesc_f32acc(E::kMmaFmt, 128, kBwdQ, true, true);
+    const uint32_t tm = warp_uniform(tmem);
+    // operand descriptors are built once; each GEMM only adds a stage offset
+    const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);      // K, K-major
+    const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);   // K^T, MN-major
+    const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
+    const uint64_t ds_km = sdesc_sw128(smem_u32(sm + L::kDSOff), 16, 1024);
+    const uint64_t ds_mn = sdesc_sw128(smem_u32(sm + L::kDSOff), 8192, 1024);
+    const uint64_t st_km = sdesc_sw128(smem_u32(sm + L::kStageOff), 16, 1024);   // Q / dO tiles
+    const uint64_t st_mn = sdesc_sw128(smem_u32(sm + L::kStageOff), 8192, 1024);
+    uint32_t st = 0, kvc = 0, gc = 0;
+    bool ok = true;
+    auto stage_off16 = [&](uint32_t x) -> uint32_t {
+      return static_cast<uint32_t>(((x % NS) * L::kStageBytes) >> 4);
+    };
+    // K-major operands: K / V tiles of 128 rows (chunks 16 KB apart), Q / dO
+    // stage tiles of 64 rows (chunks 8 KB apart)
+    auto issue_s = [&](uint32_t x) -> bool {  // S^T = K Q^T into buffer x & 1
+      if (!mbar_wait_warp(&bars->qd_full[x % NS], (x / NS) & 1)) return false;
+      // buffer x & 1 still holds P^T(x - 2) until dV(x - 2) has read it
+      if (x >= 2 && !mbar_wait_warp(&bars->p_free[x & 1], ((x >> 1) - 1) & 1)) return false;
+      tc_fence_after();
+      mma_ss_warp<DQK / 16, 4, 2, 1018, 2, 506>(tm + L::kColS + 64 * (x & 1), k_km,
+                                                 st_km + stage_off16(x), id_s, 0u);
+      mma_commit_warp(&bars->s_full[x & 1]);
+      ATTN_TL(10, x);
+      return true;
+    };
+    auto issue_dp = [&](uint32_t x) -> bool {  // dP^T = V dO^T
+      if (x > 0 && !mbar_wait_warp(&bars->dp_free, (x - 1) & 1)) return false;
+      tc_fence_after();
+      mma_ss_warp<DV / 16, 4, 2, 1018, 2, 506>(tm + L::kColDP, v_km,
+                                                st_km + stage_off16(x) + (L::kQBytes >> 4), id_s, 0u);
+      mma_commit_warp(&bars->dp_full);
+      ATTN_TL(11, x);
+      return true;
+    };
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) ||
+          !(ok = ring_pop_warp1(ring, rn, idx)) || idx < 0)
+        break;
+      const DkdvItem w = dkdv_item(a, idx);
+      for (int b = w.b0; b < w.b1 && ok; ++b) {
+        for (int g = w.g0; g < w.g1 && ok; ++g) {
+          int q_lo;
+          const int nq = warp_uniform(dkdv_q_tiles(a, b, w.t, q_lo));
+          if (nq == 0) continue;
+          const uint32_t nsteps = (uint32_t)nq * G;
+          if (!(ok = mbar_wait_warp(&bars->kv_full, kvc & 1))) break;
+          ++kvc;
+          if (!(ok = issue_s(st))) break;
+          if (!(ok = issue_dp(st))) break;
+          for (uint32_t u = 0; u < nsteps; ++u) {
+            const uint32_t cur = st + u;
+            if (u + 1 < nsteps && !(ok = issue_s(cur + 1))) break;
+            if (!(ok = mbar_wait_warp(&bars->p_ready[cur & 1], (cur >> 1) & 1))) break;
+            ATTN_TL(12, cur);
+            if (u == 0 && gc > 0 && !(ok = mbar_wait_warp(&bars->acc_empty, (gc - 1) & 1))) break;
+            tc_fence_after();
+            const uint64_t q_mn = st_mn + stage_off16(cur);
+            const uint64_t o_mn = q_mn + (L::kQBytes >> 4);
+            // dV += P^T dO, A = packed P^T from tensor memory (query columns
+            // [0,32) at S^T columns [0,16), [32,64) at [32,48))
+            mma_ts_warp<kBwdQ / 16, 2, 8, 24, 128, 128>(tm + L::kColDV, tm + L::kColS + 64 * (cur & 1),
+                                                        o_mn, id_dv, u > 0 ? 1u : 0u);
+            mma_commit_warp(&bars->p_free[cur & 1]);
+            if (u + 1 < nsteps && !(ok = issue_dp(cur + 1))) break;
+            if (!(ok = mbar_wait_warp(&bars->ds_ready, cur & 1))) break;
+            ATTN_TL(14, cur);
+            tc_fence_after();
+            // dK += dS^T Q
+            mma_ss_warp<kBwdQ / 16, 4, 2, 2, 128, 128>(tm + L::kColDK, ds_km, q_mn, id_dk,
+                                                       u > 0 ? 1u : 0u);
+            if constexpr (ATOMIC) {  // dQ^T = K^T dS^T
+              if (cur >= 1 && !(ok = mbar_wait_warp(&bars->dq_free, (cur - 1) & 1))) break;
               tc_fence_after();
-              const uint64_t q_mn = st_mn + stage_off16(cur);
-              const uint64_t o_mn = q_mn + (L::kQBytes >> 4);
-              // P^T, packed bf16: query columns [0,32) at S^T columns [0,16), [32,64) at [32,48)
-              const uint32_t p_tm = tmem + L::kColS + 64 * (cur & 1);
-#pragma unroll
-              for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dV += P^T dO  (A from tensor memory)
-                mma_ts(tmem + L::kColDV, p_tm + ks * 8 + (ks >> 1) * 16, o_mn + ((ks * 2048) >> 4),
-                       id_dv, (u > 0 || ks > 0));
-              mma_commit(&bars->p_free[cur & 1]);
-              if (u + 1 < nsteps && !(ok = issue_dp(cur + 1))) break;
-              if (!(ok = mbar_wait(&bars->ds_ready, cur & 1))) break;
-              ATTN_TL(14, cur);
-              tc_fence_after();
-#pragma unroll
-              for (int ks = 0; ks < kBwdQ / 16; ++ks)  // dK += dS^T Q
-                mma_ss(tmem + L::kColDK, ds_km + ((ks * 32) >> 4), q_mn + ((ks * 2048) >> 4), id_dk,
-                       (u > 0 || ks > 0));
-              if constexpr (ATOMIC) {  // dQ^T = K^T dS^T
-                if (cur >= 1 && !(ok = mbar_wait(&bars->dq_free, (cur - 1) & 1))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks)
-                  mma_ss(tmem + L::kColDQ, k_mn + ((ks * 2048) >> 4), ds_mn + ((ks * 2048) >> 4),
-                         id_dq, ks > 0);
-                mma_commit(&bars->dq_full);
-              }
-              mma_commit(&bars->ds_free);
-              mma_commit(&bars->qd_empty[cur % NS]);
-              ATTN_TL(15, cur);
+              mma_ss_warp<kTile / 16, 4, 128, 128, 128, 128>(tm + L::kColDQ, k_mn, ds_mn, id_dq, 0u);
+              mma_commit_warp(&bars->dq_full);
             }
-            if (!ok) break;
-            mma_commit(&bars->acc_full);
-            mma_commit(&bars->kv_empty);
-            ++gc;
-            st += nsteps;
+            mma_commit_warp(&bars->ds_free);
+            mma_commit_warp(&bars->qd_empty[cur % NS]);
+            ATTN_TL(15, cur);
           }
+          if (!ok) break;
+          mma_commit_warp(&bars->acc_full);
+          mma_commit_warp(&bars->kv_empty);
+          ++gc;
+          st += nsteps;
         }
       }
-      if (!ok) {
-        report_timeout(a, 0x130);
-        *abort_flag = 1;
-      }
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 200000000ull);
     }
+    if (!ok && lane == 0) {
+      report_timeout(a, 0x130);
+      *abort_flag = 1;
+    }
+    mma_commit_warp(&bars->drain);
+    mbar_wait(&bars->drain, 0, 200000000ull);
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P / dS warps
     // two warpgroups: each thread owns KV row j (TMEM lane j) and one half of
@@ -820,88 +812,84 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f32acc(E::kMmaFmt, 128, kTile, false, false);
-      constexpr uint32_t id_dq = idesc_f32acc(E::kMmaFmt, 128, DQK, false, true);
-      // operand descriptors are built once; each MMA only adds a constant offset
-      const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
-      const uint64_t o_km = sdesc_sw128(smem_u32(sm + L::kOOff), 16, 1024);
-      const uint64_t s_km = sdesc_sw128(smem_u32(sm + L::kSOff), 16, 1024);
-      const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
-      const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);
-      const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
-      uint32_t kt = 0, it = 0;
-      bool ok = true;
-      auto issue_s = [&](uint32_t k) -> bool {  // S = Q K^T
-        const int ks_ = k % KS;
-        if (!mbar_wait(&bars->k_full[ks_], (k / KS) & 1)) return false;
-        if (k > 0 && !mbar_wait(&bars->s_free, (k - 1) & 1)) return false;
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this loop on warp-uniform values; one elected lane
+    // issues each GEMM's MMAs from a single asm statement.
+    constexpr uint32_t id_s = idesc_f32acc(E::kMmaFmt, 128, kTile, false, false);
+    constexpr uint32_t id_dq = idesc_f32acc(E::kMmaFmt, 128, DQK, false, true);
+    const uint32_t tm = warp_uniform(tmem);
+    // operand descriptors are built once; each GEMM only adds a stage offset
+    const uint64_t q_km = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+    const uint64_t o_km = sdesc_sw128(smem_u32(sm + L::kOOff), 16, 1024);
+    const uint64_t s_km = sdesc_sw128(smem_u32(sm + L::kSOff), 16, 1024);
+    const uint64_t k_km = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+    const uint64_t k_mn = sdesc_sw128(smem_u32(sm + L::kKOff), 16384, 1024);
+    const uint64_t v_km = sdesc_sw128(smem_u32(sm + L::kVOff), 16, 1024);
+    uint32_t kt = 0, it = 0;
+    bool ok = true;
+    auto issue_s = [&](uint32_t k) -> bool {  // S = Q K^T
+      const int ks_ = k % KS;
+      if (!mbar_wait_warp(&bars->k_full[ks_], (k / KS) & 1)) return false;
+      if (k > 0 && !mbar_wait_warp(&bars->s_free, (k - 1) & 1)) return false;
+      tc_fence_after();
+      const uint64_t kd = k_km + static_cast<uint32_t>((ks_ * L::kKBytes) >> 4);
+      mma_ss_warp<DQK / 16, 4, 2, 1018, 2, 1018>(tm + L::kColS, q_km, kd, id_s, 0u);
+      mma_commit_warp(&bars->s_full);
+      return true;
+    };
+    auto issue_dp = [&](uint32_t k) -> bool {  // dP = dO V^T
+      const int vs = k % VS;
+      if (!mbar_wait_warp(&bars->v_full[vs], (k / VS) & 1)) return false;
+      if (k > 0 && !mbar_wait_warp(&bars->dp_free, (k - 1) & 1)) return false;
+      tc_fence_after();
+      const uint64_t vd = v_km + static_cast<uint32_t>((vs * L::kVBytes) >> 4);
+      mma_ss_warp<DV / 16, 4, 2, 1018, 2, 1018>(tm + L::kColDP, o_km, vd, id_s, 0u);
+      mma_commit_warp(&bars->dp_full);
+      mma_commit_warp(&bars->v_empty[vs]);
+      return true;
+    };
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) ||
+          !(ok = ring_pop_warp1(ring, rn, idx)) || idx < 0)
+        break;
+      int b, t, h, kv_lo, n;
+      item_of(idx, b, t, h, kv_lo, n);
+      n = warp_uniform(n);
+      if (n == 0) continue;
+      if (!(ok = mbar_wait_warp(&bars->q_full, it & 1))) break;
+      if (!(ok = issue_s(kt)) || !(ok = issue_dp(kt))) break;
+      for (int j = 0; j < n; ++j) {
+        const uint32_t k = kt + j;
+        const bool more = j + 1 < n;
+        if (KS >= 2 && more) {
+          if (!(ok = issue_s(k + 1)) || !(ok = issue_dp(k + 1))) break;
+        }
+        if (!more) mma_commit_warp(&bars->q_empty);  // last S / dP of the item issued
+        if (!(ok = mbar_wait_warp(&bars->ds_ready, k & 1))) break;
+        if (j == 0 && it > 0 && !(ok = mbar_wait_warp(&bars->acc_empty, (it - 1) & 1))) break;
         tc_fence_after();
-        const uint64_t kd = k_km + static_cast<uint32_t>((ks_ * L::kKBytes) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DQK / 16; ++ks) {
-          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + L::kColS, q_km + off16, kd + off16, id_s, ks > 0);
+        // dQ += dS K: A = dS (128 x 128 tile in shared memory), B = K MN-major
+        const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
+        mma_ss_warp<kTile / 16, 4, 2, 1018, 128, 128>(tm + L::kColDQ, s_km, kd, id_dq,
+                                                      j > 0 ? 1u : 0u);
+        mma_commit_warp(&bars->ds_free);
+        mma_commit_warp(&bars->k_empty[k % KS]);
+        if (KS == 1 && more) {
+          if (!(ok = issue_s(k + 1)) || !(ok = issue_dp(k + 1))) break;
         }
-        mma_commit(&bars->s_full);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t k) -> bool {  // dP = dO V^T
-        const int vs = k % VS;
-        if (!mbar_wait(&bars->v_full[vs], (k / VS) & 1)) return false;
-        if (k > 0 && !mbar_wait(&bars->dp_free, (k - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t vd = v_km + static_cast<uint32_t>((vs * L::kVBytes) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < DV / 16; ++ks) {
-          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + L::kColDP, o_km + off16, vd + off16, id_s, ks > 0);
-        }
-        mma_commit(&bars->dp_full);
-        mma_commit(&bars->v_empty[vs]);
-        return true;
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-        int b, t, h, kv_lo, n;
-        item_of(idx, b, t, h, kv_lo, n);
-        if (n == 0) continue;
-        if (!(ok = mbar_wait(&bars->q_full, it & 1))) break;
-        if (!(ok = issue_s(kt)) || !(ok = issue_dp(kt))) break;
-        for (int j = 0; j < n; ++j) {
-          const uint32_t k = kt + j;
-          const bool more = j + 1 < n;
-          if (KS >= 2 && more) {
-            if (!(ok = issue_s(k + 1)) || !(ok = issue_dp(k + 1))) break;
-          }
-          if (!more) mma_commit(&bars->q_empty);  // last S / dP of the item issued
-          if (!(ok = mbar_wait(&bars->ds_ready, k & 1))) break;
-          if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->acc_empty, (it - 1) & 1))) break;
-          tc_fence_after();
-          const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)  // dQ += dS K
-            mma_ss(tmem + L::kColDQ, s_km + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                   kd + ((ks * 2048) >> 4), id_dq, (j > 0 || ks > 0));
-          mma_commit(&bars->ds_free);
-          mma_commit(&bars->k_empty[k % KS]);
-          if (KS == 1 && more) {
-            if (!(ok = issue_s(k + 1)) || !(ok = issue_dp(k + 1))) break;
-          }
-        }
-        if (!ok) break;
-        mma_commit(&bars->acc_full);
-        kt += n;
-        ++it;
       }
-      if (!ok) {
-        report_timeout(a, 0x230);
-        *abort_flag = 1;
-      }
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 200000000ull);
+      if (!ok) break;
+      mma_commit_warp(&bars->acc_full);
+      kt += n;
+      ++it;
     }
+    if (!ok && lane == 0) {
+      report_timeout(a, 0x230);
+      *abort_flag = 1;
+    }
+    mma_commit_warp(&bars->drain);
+    mbar_wait(&bars->drain, 0, 200000000ull);
   } else if (warp >= 4) {
     const int r = tid - 128;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;

@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
     // dK += dS^T(x) Q(x): A = packed dS^T (query columns [0,64) at dP^T columns
     // [0,32), [64,128) at [64,96)), B = Q(x) MN-major; K = 128 query rows
     auto issue_dk = [&](uint32_t x, bool first) {
-      mma_ts_warp<kQ / 16, 8, 40, 128, 128>(tm + L::kColDK, tm + L::kColDP, q_mn + qoff16(x), id_dk,
+      mma_ts_warp<kQ / 16, 4, 8, 40, 128, 128>(tm + L::kColDK, tm + L::kColDP, q_mn + qoff16(x), id_dk,
                                             first ? 0u : 1u);
       mma_commit_warp(&bars->q_empty[x % NQ]);
     };
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
             if (!(ok = mbar_wait_warp(&bars->q_full[cur % NQ], (cur / NQ) & 1))) break;
             tc_fence_after();
             // S^T(cur) = K Q^T  (over P^T(cur-1), read by dV(cur-1) issued earlier)
-            mma_ss_warp<DQK / 16, 2, 1018, 2, 1018>(tm + L::kColS, k_km, q_km + qoff16(cur), id_s,
+            mma_ss_warp<DQK / 16, 4, 2, 1018, 2, 1018>(tm + L::kColS, k_km, q_km + qoff16(cur), id_s,
                                                     0u);
             mma_commit_warp(&bars->s_full);
             ATTN_TL(10, cur);
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
             if (!(ok = mbar_wait_warp(&bars->o_full[cur % NO], (cur / NO) & 1))) break;
             tc_fence_after();
             // dP^T(cur) = V dO^T  (over dS^T(cur-1), read by dK(cur-1) just issued)
-            mma_ss_warp<DV / 16, 2, 1018, 2, 1018>(tm + L::kColDP, v_km, o_km + ooff16(cur), id_p,
+            mma_ss_warp<DV / 16, 4, 2, 1018, 2, 1018>(tm + L::kColDP, v_km, o_km + ooff16(cur), id_p,
                                                    0u);
             mma_commit_warp(&bars->dp_full);
             ATTN_TL(11, cur);
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
             ATTN_TL(12, cur);
             if (u == 0 && gc > 0 && !(ok = mbar_wait_warp(&bars->acc_empty, (gc - 1) & 1))) break;
             tc_fence_after();
-            mma_ts_warp<kQ / 16, 8, 40, 128, 128>(tm + L::kColDV, tm + L::kColS, o_mn + ooff16(cur),
+            mma_ts_warp<kQ / 16, 4, 8, 40, 128, 128>(tm + L::kColDV, tm + L::kColS, o_mn + ooff16(cur),
                                                   id_dv, u > 0 ? 1u : 0u);
             mma_commit_warp(&bars->o_empty[cur % NO]);
             ATTN_TL(13, cur);

@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
       if (!mbar_wait_warp(&bars->k_full[s_], (k / KS) & 1)) return false;
       tc_fence_after();
       const uint64_t kd = k_km + static_cast<uint32_t>((s_ * L::kKBytes) >> 4);
-      mma_ts_warp<DQK / 16, 8, 8, 2, 1018>(tm + L::kColS, tm + L::kColQ, kd, id_s, 0u);
+      mma_ts_warp<DQK / 16, 4, 8, 8, 2, 1018>(tm + L::kColS, tm + L::kColQ, kd, id_s, 0u);
       mma_commit_warp(&bars->s_full);
       return true;
     };
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
       if (!mbar_wait_warp(&bars->v_full[s_], (k / VS) & 1)) return false;
       tc_fence_after();
       const uint64_t vd = v_km + static_cast<uint32_t>((s_ * L::kVBytes) >> 4);
-      mma_ts_warp<DV / 16, 8, 8, 2, 1018>(tm + L::kColDP, tm + L::kColO, vd, id_s, 0u);
+      mma_ts_warp<DV / 16, 4, 8, 8, 2, 1018>(tm + L::kColDP, tm + L::kColO, vd, id_s, 0u);
       mma_commit_warp(&bars->dp_full);
       mma_commit_warp(&bars->v_empty[s_]);
       return true;
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
           {  // dQ += dS K: A = packed dS (key columns [0,64) at dP columns [0,32),
              // [64,128) at [64,96)), B = K(k) MN-major, K = 128 keys
             const uint64_t kd = k_mn + static_cast<uint32_t>(((k % KS) * L::kKBytes) >> 4);
-            mma_ts_warp<kTile / 16, 8, 40, 128, 128>(tm + L::kColDQ, tm + L::kColDP, kd, id_dq,
+            mma_ts_warp<kTile / 16, 4, 8, 40, 128, 128>(tm + L::kColDQ, tm + L::kColDP, kd, id_dq,
                                                      j > 0 ? 1u : 0u);
             // S(k) was complete before dS(k) existed: K(k) is free after this
             mma_commit_warp(&bars->k_empty[k % KS]);

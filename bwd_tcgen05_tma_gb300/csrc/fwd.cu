@@ -214,74 +214,71 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f32acc(E::kMmaFmt, 128, kTile, false, false);
-      constexpr uint32_t idesc_o = idesc_f32acc(E::kMmaFmt, 128, DV, false, true);
-      // operand descriptors are built once; each MMA only adds a constant offset
-      const uint64_t q_desc = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
-      const uint64_t p_desc = sdesc_sw128(smem_u32(sm + L::kPOff), 16, 1024);
-      const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
-      const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm + L::kVOff), 16384, 1024);
-      uint32_t kt = 0, it = 0;
-      bool ok = true;
-      auto issue_s = [&](uint32_t k) -> bool {
-        const int s = k % L::kKStages, sb = k & 1;
-        if (!mbar_wait(&bars->k_full[s], (k / L::kKStages) & 1)) return false;
-        if (k >= 2 && !mbar_wait(&bars->s_empty[sb], ((k >> 1) - 1) & 1)) return false;
+    // The whole warp runs this loop on warp-uniform values; one elected lane
+    // issues each GEMM's MMAs from a single asm statement.
+    constexpr uint32_t idesc_s = idesc_f32acc(E::kMmaFmt, 128, kTile, false, false);
+    constexpr uint32_t idesc_o = idesc_f32acc(E::kMmaFmt, 128, DV, false, true);
+    const uint32_t tm = warp_uniform(tmem);
+    // operand descriptors are built once; each GEMM only adds a stage offset
+    const uint64_t q_desc = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+    const uint64_t p_desc = sdesc_sw128(smem_u32(sm + L::kPOff), 16, 1024);
+    const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm + L::kKOff), 16, 1024);
+    const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm + L::kVOff), 16384, 1024);
+    uint32_t kt = 0, it = 0;
+    bool ok = true;
+    auto issue_s = [&](uint32_t k) -> bool {
+      const int s = k % L::kKStages, sb = k & 1;
+      if (!mbar_wait_warp(&bars->k_full[s], (k / L::kKStages) & 1)) return false;
+      if (k >= 2 && !mbar_wait_warp(&bars->s_empty[sb], ((k >> 1) - 1) & 1)) return false;
+      tc_fence_after();
+      const uint64_t kd = k_desc0 + static_cast<uint64_t>((s * L::kKBytes) >> 4);
+      mma_ss_warp<DQK / 16, 4, 2, 1018, 2, 1018>(tm + L::kColS + sb * kTile, q_desc, kd, idesc_s,
+                                                 0u);
+      mma_commit_warp(&bars->s_full[sb]);
+      mma_commit_warp(&bars->k_empty[s]);
+      return true;
+    };
+    for (uint32_t rn = 0;; ++rn) {
+      int32_t idx;
+      if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) ||
+          !(ok = ring_pop_warp1(ring, rn, idx)) || idx < 0)
+        break;
+      const FwdItem w = fwd_item(a, idx);
+      const int n = warp_uniform(w.n);
+      if (n == 0) continue;
+      if (!(ok = mbar_wait_warp(&bars->q_full, it & 1))) break;
+      if (!(ok = issue_s(kt))) break;
+      for (int j = 0; j < n; ++j) {
+        const uint32_t k = kt + j;
+        if (j + 1 < n) {
+          if (!(ok = issue_s(k + 1))) break;
+        } else {
+          mma_commit_warp(&bars->q_empty);  // every S MMA of this item has been issued
+        }
+        if (!(ok = mbar_wait_warp(&bars->p_full[k & 1], (k >> 1) & 1))) break;
+        if (j == 0 && it > 0 && !(ok = mbar_wait_warp(&bars->o_empty, (it - 1) & 1))) break;
+        const int s = k % L::kVStages;
+        if (!(ok = mbar_wait_warp(&bars->v_full[s], (k / L::kVStages) & 1))) break;
         tc_fence_after();
-        const uint64_t kd = k_desc0 + static_cast<uint64_t>((s * L::kKBytes) >> 4);
-        const uint32_t dt = tmem + L::kColS + sb * kTile;
-#pragma unroll
-        for (int ks = 0; ks < DQK / 16; ++ks) {
-          const uint32_t off16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-          mma_ss(dt, q_desc + off16, kd + off16, idesc_s, ks > 0);
-        }
-        mma_commit(&bars->s_full[sb]);
-        mma_commit(&bars->k_empty[s]);
-        return true;
-      };
-      for (uint32_t rn = 0;; ++rn) {
-        int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_pop1(ring, rn, idx)) || idx < 0) break;
-        const FwdItem w = fwd_item(a, idx);
-        if (w.n == 0) continue;
-        if (!(ok = mbar_wait(&bars->q_full, it & 1))) break;
-        if (!(ok = issue_s(kt))) break;
-        for (int j = 0; j < w.n; ++j) {
-          const uint32_t k = kt + j;
-          if (j + 1 < w.n) {
-            if (!(ok = issue_s(k + 1))) break;
-          } else {
-            mma_commit(&bars->q_empty);  // every S MMA of this item has been issued
-          }
-          if (!(ok = mbar_wait(&bars->p_full[k & 1], (k >> 1) & 1))) break;
-          if (j == 0 && it > 0 && !(ok = mbar_wait(&bars->o_empty, (it - 1) & 1))) break;
-          const int s = k % L::kVStages;
-          if (!(ok = mbar_wait(&bars->v_full[s], (k / L::kVStages) & 1))) break;
-          tc_fence_after();
-          const uint64_t vd = v_desc0 + static_cast<uint64_t>((s * L::kVBytes) >> 4);
-          const uint64_t pd = p_desc + static_cast<uint32_t>(((k % L::kPStages) * L::kPBytes) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks) {
-            const uint32_t poff16 = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-            mma_ss(tmem + L::kColO, pd + poff16, vd + static_cast<uint32_t>(ks * (2048 >> 4)),
-                   idesc_o, (j > 0 || ks > 0));
-          }
-          mma_commit(&bars->pv_done);
-          mma_commit(&bars->v_empty[s]);
-        }
-        if (!ok) break;
-        mma_commit(&bars->o_full);  // O of this item complete once these land
-        kt += w.n;
-        ++it;
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>((s * L::kVBytes) >> 4);
+        const uint64_t pd = p_desc + static_cast<uint32_t>(((k % L::kPStages) * L::kPBytes) >> 4);
+        // O += P V: A = P (shared memory, K-major), B = V MN-major
+        mma_ss_warp<kTile / 16, 4, 2, 1018, 128, 128>(tm + L::kColO, pd, vd, idesc_o,
+                                                      j > 0 ? 1u : 0u);
+        mma_commit_warp(&bars->pv_done);
+        mma_commit_warp(&bars->v_empty[s]);
       }
-      if (!ok) {
-        report_timeout(a, 0x20);
-        *abort_flag = 1;
-      }
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 200000000ull);
+      if (!ok) break;
+      mma_commit_warp(&bars->o_full);  // O of this item complete once these land
+      kt += n;
+      ++it;
     }
+    if (!ok && lane == 0) {
+      report_timeout(a, 0x20);
+      *abort_flag = 1;
+    }
+    mma_commit_warp(&bars->drain);
+    mbar_wait(&bars->drain, 0, 200000000ull);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int r = tid - 128;

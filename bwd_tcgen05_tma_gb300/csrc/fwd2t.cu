@@ -322,13 +322,13 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       auto issue_s = [&](int x, uint32_t qs, uint32_t kc) {
         const uint64_t qd = q_km + static_cast<uint32_t>(((qs * 2 + x) * L::kQStage) >> 4);
         const uint64_t kd = kv_km + stage_off(kc);
-        mma_ss_warp<DQK / 16, 2, 1018, 2, 1018>(tm + L::kColS + x * kTile, qd, kd, id_s, 0u);
+        mma_ss_warp<DQK / 16, 4, 2, 1018, 2, 1018>(tm + L::kColS + x * kTile, qd, kd, id_s, 0u);
         mma_commit_warp(&bars->s_full[x]);
       };
       // O_X += P_X V; V at ring position vc; P_X packed over S_X
       auto issue_pv = [&](int x, uint32_t vc, bool first) {
         const uint64_t vd = kv_mn + stage_off(vc);
-        mma_ts_warp<kTile / 16, 8, 8, 128, 128>(tm + L::kColO + x * kTile, tm + L::kColS + x * kTile,
+        mma_ts_warp<kTile / 16, 4, 8, 8, 128, 128>(tm + L::kColO + x * kTile, tm + L::kColS + x * kTile,
                                                 vd, id_o, first ? 0u : 1u);
       };
       uint32_t rn = 0;

@@ -191,28 +191,6 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_fmt, int M, int 
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]; one instruction covers K = 16.
-SM103_DEV void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                      uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]; A holds bf16 pairs packed in 32-bit columns.
-SM103_DEV void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                      uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- warp-collective MMA issue
 // The issuing warp runs its loop converged, on warp-uniform values, and one
 // elected lane issues.  All K slices of one GEMM (K = 16 * NK) go out from one
@@ -224,84 +202,196 @@ SM103_DEV void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t
 // this GPU); issued this way it stays at the tensor core's 64 clk.
 //
 // Steps (16-byte units for descriptors, columns for tensor-memory addresses)
-// from slice k-1 to slice k: S for k = 1..3, 5..7 and J for k = 4.
-//   K-major 128-byte-swizzled tile, 64-column chunks 16 KB apart:  S 2,  J 1018
-//   MN-major 128-byte-swizzled tile (16 rows of 128 B per slice):  S 128, J 128
-//   packed 16-bit pairs in tensor memory, contiguous:              S 8,  J 8
-//   the same in two 32-column halves 64 columns apart:             S 8,  J 40
+// from slice k-1 to slice k, with the period JP of the jumps:
+//   K-major 128-byte-swizzled tile of R rows, 64-column chunks R*128 B apart:
+//                                          JP 4, S 2, J (R*128 - 96) / 16
+//   MN-major 128-byte-swizzled tile (16 rows of 128 B per slice): S = J = 128
+//   packed 16-bit pairs in tensor memory, contiguous:              S = J = 8
+//   the same in 32-column halves 64 columns apart:   JP 4, S 8, J 40
 #define SM103_MMA_F16 "@e tcgen05.mma.cta_group::1.kind::f16 "
-#define SM103_SS_STEP(ai, bi)                                                        \
-  "add.u32 alo, alo, %" #ai ";\n\tadd.u32 blo, blo, %" #bi ";\n\t"                \
-  "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16           \
-  "[%0], ad, bd, %3, p1;\n\t"
-#define SM103_TS_STEP(ai, bi)                                                        \
-  "add.u32 at, at, %" #ai ";\n\tadd.u32 blo, blo, %" #bi ";\n\t"                  \
-  "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+
+// Operand step before K slice k: J when k is a multiple of the period JP
+// (a jump to the next 64-column chunk or tensor-memory half), S otherwise.
+template <int K, int JP, int S, int J>
+__host__ __device__ constexpr int step() {
+  return (K % JP == 0) ? J : S;
+}
 
 // D[tmem] (+)= A[smem] B[smem] over NK K-slices; the first slice accumulates
-// iff `accumulate`, the others always.
-template <int NK, int AS, int AJ, int BS, int BJ>
+// iff `accumulate`, the others always.  Steps: see step().
+template <int NK, int JP, int AS, int AJ, int BS, int BJ>
 SM103_DEV void mma_ss_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                            uint32_t accumulate) {
-  static_assert(NK == 4 || NK == 8, "K slices per GEMM");
-  if constexpr (NK == 8) {
+  static_assert(NK == 4 || NK == 8 || NK == 12, "K slices per GEMM");
+  if constexpr (NK == 4) {
     asm volatile(
         "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 alo, ahi, blo, bhi;\n\t.reg .b64 ad, bd;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
-        "mov.b64 {alo, ahi}, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t" SM103_MMA_F16
-        "[%0], %1, %2, %3, p0;\n\t" SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8)
-            SM103_SS_STEP(7, 9) SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) "}" ::"r"(
-                d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u), "n"(AS), "n"(AJ), "n"(BS),
-        "n"(BJ)
+        "mov.b64 {alo, ahi}, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t"
+        SM103_MMA_F16 "[%0], %1, %2, %3, p0;\n\t"
+        "add.u32 alo, alo, %6;\n\tadd.u32 blo, blo, %9;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %7;\n\tadd.u32 blo, blo, %10;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %8;\n\tadd.u32 blo, blo, %11;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u),
+        "n"(step<1, JP, AS, AJ>()), "n"(step<2, JP, AS, AJ>()), "n"(step<3, JP, AS, AJ>()),
+        "n"(step<1, JP, BS, BJ>()), "n"(step<2, JP, BS, BJ>()), "n"(step<3, JP, BS, BJ>())
+        : "memory");
+  } else if constexpr (NK == 8) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 alo, ahi, blo, bhi;\n\t.reg .b64 ad, bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+        "mov.b64 {alo, ahi}, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t"
+        SM103_MMA_F16 "[%0], %1, %2, %3, p0;\n\t"
+        "add.u32 alo, alo, %6;\n\tadd.u32 blo, blo, %13;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %7;\n\tadd.u32 blo, blo, %14;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %8;\n\tadd.u32 blo, blo, %15;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %9;\n\tadd.u32 blo, blo, %16;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %10;\n\tadd.u32 blo, blo, %17;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %11;\n\tadd.u32 blo, blo, %18;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %12;\n\tadd.u32 blo, blo, %19;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u),
+        "n"(step<1, JP, AS, AJ>()), "n"(step<2, JP, AS, AJ>()), "n"(step<3, JP, AS, AJ>()), "n"(step<4, JP, AS, AJ>()), "n"(step<5, JP, AS, AJ>()), "n"(step<6, JP, AS, AJ>()), "n"(step<7, JP, AS, AJ>()),
+        "n"(step<1, JP, BS, BJ>()), "n"(step<2, JP, BS, BJ>()), "n"(step<3, JP, BS, BJ>()), "n"(step<4, JP, BS, BJ>()), "n"(step<5, JP, BS, BJ>()), "n"(step<6, JP, BS, BJ>()), "n"(step<7, JP, BS, BJ>())
         : "memory");
   } else {
     asm volatile(
         "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 alo, ahi, blo, bhi;\n\t.reg .b64 ad, bd;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
-        "mov.b64 {alo, ahi}, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t" SM103_MMA_F16
-        "[%0], %1, %2, %3, p0;\n\t" SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) SM103_SS_STEP(6, 8) "}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u), "n"(AS), "n"(AJ), "n"(BS),
-        "n"(BJ)
+        "mov.b64 {alo, ahi}, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t"
+        SM103_MMA_F16 "[%0], %1, %2, %3, p0;\n\t"
+        "add.u32 alo, alo, %6;\n\tadd.u32 blo, blo, %17;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %7;\n\tadd.u32 blo, blo, %18;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %8;\n\tadd.u32 blo, blo, %19;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %9;\n\tadd.u32 blo, blo, %20;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %10;\n\tadd.u32 blo, blo, %21;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %11;\n\tadd.u32 blo, blo, %22;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %12;\n\tadd.u32 blo, blo, %23;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %13;\n\tadd.u32 blo, blo, %24;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %14;\n\tadd.u32 blo, blo, %25;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %15;\n\tadd.u32 blo, blo, %26;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "add.u32 alo, alo, %16;\n\tadd.u32 blo, blo, %27;\n\t"
+        "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], ad, bd, %3, p1;\n\t"
+        "}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u),
+        "n"(step<1, JP, AS, AJ>()), "n"(step<2, JP, AS, AJ>()), "n"(step<3, JP, AS, AJ>()), "n"(step<4, JP, AS, AJ>()), "n"(step<5, JP, AS, AJ>()), "n"(step<6, JP, AS, AJ>()), "n"(step<7, JP, AS, AJ>()), "n"(step<8, JP, AS, AJ>()), "n"(step<9, JP, AS, AJ>()), "n"(step<10, JP, AS, AJ>()), "n"(step<11, JP, AS, AJ>()),
+        "n"(step<1, JP, BS, BJ>()), "n"(step<2, JP, BS, BJ>()), "n"(step<3, JP, BS, BJ>()), "n"(step<4, JP, BS, BJ>()), "n"(step<5, JP, BS, BJ>()), "n"(step<6, JP, BS, BJ>()), "n"(step<7, JP, BS, BJ>()), "n"(step<8, JP, BS, BJ>()), "n"(step<9, JP, BS, BJ>()), "n"(step<10, JP, BS, BJ>()), "n"(step<11, JP, BS, BJ>())
         : "memory");
   }
 }
 
 // D[tmem] (+)= A[tmem] B[smem] over NK K-slices (A: packed 16-bit pairs).
-template <int NK, int AS, int AJ, int BS, int BJ>
+template <int NK, int JP, int AS, int AJ, int BS, int BJ>
 SM103_DEV void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                            uint32_t accumulate) {
-  static_assert(NK == 4 || NK == 8, "K slices per GEMM");
-  if constexpr (NK == 8) {
+  static_assert(NK == 4 || NK == 8 || NK == 12, "K slices per GEMM");
+  if constexpr (NK == 4) {
     asm volatile(
         "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 at, blo, bhi;\n\t.reg .b64 bd;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
-        "mov.b32 at, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t" SM103_MMA_F16
-        "[%0], [%1], %2, %3, p0;\n\t" SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8)
-            SM103_TS_STEP(7, 9) SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) "}" ::"r"(
-                d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u), "n"(AS), "n"(AJ), "n"(BS),
-        "n"(BJ)
+        "mov.b32 at, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t"
+        SM103_MMA_F16 "[%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 at, at, %6;\n\tadd.u32 blo, blo, %9;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %7;\n\tadd.u32 blo, blo, %10;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %8;\n\tadd.u32 blo, blo, %11;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u),
+        "n"(step<1, JP, AS, AJ>()), "n"(step<2, JP, AS, AJ>()), "n"(step<3, JP, AS, AJ>()),
+        "n"(step<1, JP, BS, BJ>()), "n"(step<2, JP, BS, BJ>()), "n"(step<3, JP, BS, BJ>())
+        : "memory");
+  } else if constexpr (NK == 8) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 at, blo, bhi;\n\t.reg .b64 bd;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+        "mov.b32 at, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t"
+        SM103_MMA_F16 "[%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 at, at, %6;\n\tadd.u32 blo, blo, %13;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %7;\n\tadd.u32 blo, blo, %14;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %8;\n\tadd.u32 blo, blo, %15;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %9;\n\tadd.u32 blo, blo, %16;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %10;\n\tadd.u32 blo, blo, %17;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %11;\n\tadd.u32 blo, blo, %18;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %12;\n\tadd.u32 blo, blo, %19;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u),
+        "n"(step<1, JP, AS, AJ>()), "n"(step<2, JP, AS, AJ>()), "n"(step<3, JP, AS, AJ>()), "n"(step<4, JP, AS, AJ>()), "n"(step<5, JP, AS, AJ>()), "n"(step<6, JP, AS, AJ>()), "n"(step<7, JP, AS, AJ>()),
+        "n"(step<1, JP, BS, BJ>()), "n"(step<2, JP, BS, BJ>()), "n"(step<3, JP, BS, BJ>()), "n"(step<4, JP, BS, BJ>()), "n"(step<5, JP, BS, BJ>()), "n"(step<6, JP, BS, BJ>()), "n"(step<7, JP, BS, BJ>())
         : "memory");
   } else {
     asm volatile(
         "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 at, blo, bhi;\n\t.reg .b64 bd;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
-        "mov.b32 at, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t" SM103_MMA_F16
-        "[%0], [%1], %2, %3, p0;\n\t" SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) SM103_TS_STEP(6, 8) "}" ::"r"(
-            d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u), "n"(AS), "n"(AJ), "n"(BS),
-        "n"(BJ)
+        "mov.b32 at, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t"
+        SM103_MMA_F16 "[%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 at, at, %6;\n\tadd.u32 blo, blo, %17;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %7;\n\tadd.u32 blo, blo, %18;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %8;\n\tadd.u32 blo, blo, %19;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %9;\n\tadd.u32 blo, blo, %20;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %10;\n\tadd.u32 blo, blo, %21;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %11;\n\tadd.u32 blo, blo, %22;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %12;\n\tadd.u32 blo, blo, %23;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %13;\n\tadd.u32 blo, blo, %24;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %14;\n\tadd.u32 blo, blo, %25;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %15;\n\tadd.u32 blo, blo, %26;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "add.u32 at, at, %16;\n\tadd.u32 blo, blo, %27;\n\t"
+        "mov.b64 bd, {blo, bhi};\n\t" SM103_MMA_F16 "[%0], [at], bd, %3, p1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u),
+        "n"(step<1, JP, AS, AJ>()), "n"(step<2, JP, AS, AJ>()), "n"(step<3, JP, AS, AJ>()), "n"(step<4, JP, AS, AJ>()), "n"(step<5, JP, AS, AJ>()), "n"(step<6, JP, AS, AJ>()), "n"(step<7, JP, AS, AJ>()), "n"(step<8, JP, AS, AJ>()), "n"(step<9, JP, AS, AJ>()), "n"(step<10, JP, AS, AJ>()), "n"(step<11, JP, AS, AJ>()),
+        "n"(step<1, JP, BS, BJ>()), "n"(step<2, JP, BS, BJ>()), "n"(step<3, JP, BS, BJ>()), "n"(step<4, JP, BS, BJ>()), "n"(step<5, JP, BS, BJ>()), "n"(step<6, JP, BS, BJ>()), "n"(step<7, JP, BS, BJ>()), "n"(step<8, JP, BS, BJ>()), "n"(step<9, JP, BS, BJ>()), "n"(step<10, JP, BS, BJ>()), "n"(step<11, JP, BS, BJ>())
         : "memory");
   }
 }
 
-// The commit below, issued by the elected lane of a converged warp.
+// Arrive on `bar` once every tcgen05 op issued so far by the warp is done;
+// issued by the elected lane of a converged warp.
 SM103_DEV void mma_commit_warp(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
@@ -313,14 +403,6 @@ SM103_DEV void mma_commit_warp(uint64_t* bar) {
 // Lane 0's value, known to the compiler to be the same in every lane.
 SM103_DEV int warp_uniform(int v) { return __shfl_sync(0xffffffffu, v, 0); }
 SM103_DEV uint32_t warp_uniform(uint32_t v) { return __shfl_sync(0xffffffffu, v, 0); }
-
-// Arrive on `bar` once every tcgen05 op issued so far by this thread is done.
-SM103_DEV void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
 
 // ---------------------------------------------------------------- TMEM ld/st
 // 32x32b shape: thread t of a warp accesses TMEM lane (32 * (warp % 4) + t);
