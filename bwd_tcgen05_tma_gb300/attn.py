@@ -54,12 +54,13 @@ class attn_params_t(ctypes.Structure):
         ("band", c_i32), ("window_left", c_i32), ("window_right", c_i32),
         ("bottom_right", c_i32),
         ("dtype", c_i32),
+        ("test_wait_timeout", c_i32),
     ]
 
 
 class attn_stats_t(ctypes.Structure):
     _fields_ = [("status", c_i32), ("path", c_i32), ("reason", c_i32), ("dq_mode", c_i32),
-                ("tile_pairs", c_i64)]
+                ("tile_pairs", c_i64), ("wait_site", c_i32), ("reserved", c_i32)]
 
 
 class attn_resolved_t(ctypes.Structure):

@@ -254,6 +254,7 @@ CUtensorMapDataType map_type(const attn_params_t* p) {
 
 void fill_common(KernelArgs& a, const attn_params_t* p, char* ws, const Plan& pl) {
   a.elem_f16 = p->dtype == ATTN_DTYPE_FP16 ? 1 : 0;
+  a.test_stall = p->test_wait_timeout != 0 ? 1 : 0;
   a.B = p->B; a.Sq = p->Sq; a.Skv = p->Skv; a.Hq = p->Hq; a.Hkv = p->Hkv;
   a.d_qk = p->d_qk; a.d_v = p->d_v;
   const bool causal = p->mask == ATTN_MASK_CAUSAL || p->mask == ATTN_MASK_PADDING_CAUSAL;
@@ -604,6 +605,8 @@ attn_status_t attn_read_status(const void* ws, void* stream, attn_stats_t* stats
     stats->reason = h.reason;
     stats->dq_mode = h.dq_mode;
     stats->tile_pairs = h.tile_pairs;
+    stats->wait_site = h.status != 0 ? h.where : 0;
+    stats->reserved = 0;
   }
   return h.status == 0 ? ATTN_OK : static_cast<attn_status_t>(h.status);
 }

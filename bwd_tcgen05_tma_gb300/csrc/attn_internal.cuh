@@ -267,6 +267,7 @@ struct KernelArgs {
   float* dbias_acc;   // fp32 like the bias (bias broadcast along batch or heads)
   int dbias_mode;     // 0 none, 1 write bf16 directly, 2 accumulate in fp32
   int elem_f16;        // element type: 0 bf16, 1 fp16
+  int test_stall;      // testing knob: the forward's scheduler hands out no work
   int grad_st32;       // 1: dQ/dK/dV rows start 32-byte aligned (256-bit stores)
   int dkdv_batch_loop;  // 1: one dK/dV work item loops over every batch row
   int dkdv_head_loop;   // 1: one dK/dV work item loops over every KV head

@@ -410,8 +410,10 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       // ------------------------------------------------------------ scheduler
       // Claims work items from the global counter, looks up each one's key
       // range and publishes them in order; every other role takes them from
-      // the ring, so the latency of the claim is off their paths.
-      if (lane == 0) {
+      // the ring, so the latency of the claim is off their paths.  (The
+      // failure-path test knob keeps it from publishing anything: every other
+      // role's bounded wait for work then runs out and the CTA unwinds.)
+      if (lane == 0 && !a.test_stall) {
         for (uint32_t pub = 0;; ++pub) {
           const int4 e = f2_entry(a, atomicAdd(&a.hdr->next_item[0], 1), n_items);
           if (*abort_flag) break;

@@ -187,6 +187,14 @@ typedef struct {
    * of the same computation (the pages use bf16 only); ATTN_ERR_INVALID_ARG
    * for other values. */
   int32_t dtype;
+  /* Testing knob for the failure path (zero in normal use).  Nonzero: the
+   * forward kernel for query heads in pairs (even GQA group size, head dims
+   * <= 128) hands out no work, so every bounded wait for work runs out
+   * (after about 2 s); the kernel records ATTN_ERR_DEVICE_TIMEOUT and the
+   * first wait that ran out, frees its tensor memory and exits without
+   * writing O or LSE.  attn_read_status reports it; the next call on the
+   * workspace starts from a clear status.  No fault, trap or endless wait. */
+  int32_t test_wait_timeout;
 } attn_params_t;
 
 /* Which metadata path the device chose (read back by attn_read_status). */
@@ -214,6 +222,12 @@ typedef struct {
   int32_t reason;        /* attn_path_reason_t */
   int32_t dq_mode;       /* dQ mode actually used by the last backward */
   int64_t tile_pairs;    /* (query tile, KV tile) pairs scheduled by the last call */
+  int32_t wait_site;     /* with ATTN_ERR_DEVICE_TIMEOUT: the first bounded wait
+                            that ran out (kernel and role code: 0x6.. forward
+                            over head pairs, 0x3.. 128-row dK/dV, 0x4.. dQ,
+                            0x1.. / 0x2.. the other backward passes, 0x0.. the
+                            other forward, 0x30. metadata); 0 otherwise */
+  int32_t reserved;
 } attn_stats_t;
 
 /* Workspace bytes the forward / backward needs for these parameters (0 on
