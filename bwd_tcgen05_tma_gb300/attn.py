@@ -7,6 +7,7 @@ fallback implementation.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -22,11 +23,13 @@ DQ_MODES = {"atomic": 0, "deterministic": 1}
 DTYPES = {"bf16": 0, "fp16": 1}
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_SHAPE_MISMATCH", 4: "ATTN_ERR_WORKSPACE_TOO_SMALL", 5: "ATTN_ERR_CUDA",
-          6: "ATTN_ERR_DEVICE_TIMEOUT"}
+          6: "ATTN_ERR_DEVICE_TIMEOUT", 7: "ATTN_ERR_DEVICE_BOUNDS"}
+BUILD_DEVICE_CHECKS = 1
 EXPORTED = ("attn_abi_version", "attn_status_string", "attn_fwd_workspace_size",
             "attn_bwd_workspace_size", "attn_resolve_layout", "attn_fwd", "attn_bwd",
             "attn_read_status", "attn_set_trace_events", "attn_event_create",
-            "attn_event_destroy", "attn_event_elapsed_ms", "attn_fwd_noalloc")
+            "attn_event_destroy", "attn_event_elapsed_ms", "attn_fwd_noalloc",
+            "attn_build_flags")
 FWD_NOALLOC_SCRATCH_BYTES = 4 << 20
 TRACE_SLOTS = ("meta", "fwd", "bwd_pre", "dkdv", "dq", "dbias")
 
@@ -83,6 +86,7 @@ def load_library(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     P = ctypes.POINTER(attn_params_t)
     lib.attn_abi_version.restype = c_i32
+    lib.attn_build_flags.restype = c_i32
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [c_i32]
     lib.attn_fwd_workspace_size.restype = c_sz
@@ -111,6 +115,20 @@ def load_library(path: str = LIB_PATH):
         raise RuntimeError("attention library ABI version mismatch")
     _lib = lib
     return lib
+
+
+@contextlib.contextmanager
+def library_scope(path: str):
+    """Route every call made inside the block to the library at ``path`` (for
+    example the checking build, ``build.build(debug=True)``); the library
+    loaded before is restored afterwards."""
+    global _lib
+    prev = _lib
+    _lib = None
+    try:
+        yield load_library(path)
+    finally:
+        _lib = prev
 
 
 class AttnError(RuntimeError):

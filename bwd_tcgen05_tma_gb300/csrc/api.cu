@@ -363,6 +363,14 @@ extern "C" {
 
 int32_t attn_abi_version(void) { return ATTN_PARAMS_VERSION; }
 
+int32_t attn_build_flags(void) {
+#ifdef ATTN_DEBUG
+  return ATTN_BUILD_DEVICE_CHECKS;
+#else
+  return 0;
+#endif
+}
+
 attn_status_t attn_event_create(void** event) {
   if (!event) return ATTN_ERR_INVALID_ARG;
   cudaEvent_t e = nullptr;
@@ -409,6 +417,7 @@ const char* attn_status_string(attn_status_t s) {
     case ATTN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case ATTN_ERR_DEVICE_BOUNDS: return "device-side bounds check failed (access skipped)";
   }
   return "unknown status";
 }

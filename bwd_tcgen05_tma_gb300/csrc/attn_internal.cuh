@@ -8,6 +8,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "debug_checks.h"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -60,13 +61,13 @@ constexpr int kBwdQ = 64;    // query tile of the dK/dV pass
 
 // Workspace header (first 256 bytes of every workspace).
 struct WsHeader {
-  int32_t status;      // device-side attn_status_t (timeouts)
+  int32_t status;      // device-side attn_status_t (timeouts, failed bounds checks)
   int32_t path;        // 0 fast, 1 general
   int32_t reason;      // attn_path_reason_t
   int32_t dq_mode;     // dQ mode used
   int64_t tile_pairs;  // scheduled (query tile, KV tile) pairs
   int32_t mismatch;    // bit0 ids differ, bit1 pos differ, bit2 nonstandard pos
-  int32_t where;       // debug: which wait timed out (role * 16 + barrier)
+  int32_t where;       // site of the first device-side error (wait or bounds check)
   int32_t next_item[4];  // work-item counters of the persistent kernels (zeroed per call)
   uint32_t meta_barrier;  // arrivals at the metadata kernel's grid barriers (zeroed per call)
 };
@@ -415,10 +416,72 @@ __device__ __forceinline__ void warp_max_logit(float* out, float row_max_log2) {
   if ((threadIdx.x & 31) == 0 && v > -INFINITY) atomic_max_f32(out, v * 0.6931471805599453f);
 }
 
-// Records a timed-out wait; the first one (by arrival) keeps its location.
+// Records a device-side error; the first one (by arrival) keeps its status
+// and its site.
+__device__ __forceinline__ void report_device_error(const KernelArgs& a, int status, int where) {
+  if (atomicCAS(&a.hdr->status, 0, status) == 0) atomicExch(&a.hdr->where, where);
+}
+
+// A timed-out wait.
 __device__ __forceinline__ void report_timeout(const KernelArgs& a, int where) {
-  atomicExch(&a.hdr->status, 6 /* ATTN_ERR_DEVICE_TIMEOUT */);
-  atomicCAS(&a.hdr->where, 0, where);
+  report_device_error(a, 6 /* ATTN_ERR_DEVICE_TIMEOUT */, where);
+}
+
+// Bounds checks of the checking build.  `ATTN_CHECK(a, cond, site)` is true
+// when the access it guards may go ahead: with -DATTN_DEBUG it evaluates
+// cond and, when cond fails, records ATTN_ERR_DEVICE_BOUNDS at `site` (codes
+// 0x7K.., K the kernel as in the wait sites) and the access is skipped;
+// otherwise it is the constant true and cond is not evaluated.
+#ifdef ATTN_DEBUG
+__device__ __forceinline__ bool debug_check(const KernelArgs& a, bool ok, int site) {
+  if (!ok) report_device_error(a, 7 /* ATTN_ERR_DEVICE_BOUNDS */, site);
+  return ok;
+}
+#define ATTN_CHECK(a, cond, site) (::attn::debug_check((a), (cond), (site)))
+#else
+#define ATTN_CHECK(a, cond, site) true
+#endif
+using attn_dbg::span_ok;
+using attn_dbg::tma_box_ok;
+using attn_dbg::row_span_ok;
+
+// The box of a tiled copy through one of the argument block's tensor maps
+// (16-bit tensors in 64-column boxes, the fp32 dQ accumulator in 32-column
+// boxes; `rows` = the box's row count) lies where the copy engine allows it.
+__device__ __forceinline__ bool box_ok(const KernelArgs& a, const CUtensorMap* m, int x, int y,
+                                       int64_t z, int rows, bool store = false) {
+  const int64_t tq = (int64_t)a.B * a.Sq, tkv = (int64_t)a.B * a.Skv;
+  if (m == &a.tm_q) return tma_box_ok(x, 64, a.d_qk, 2, y, a.Hq, z, rows, tq, store);
+  if (m == &a.tm_k) return tma_box_ok(x, 64, a.d_qk, 2, y, a.Hkv, z, rows, tkv, store);
+  if (m == &a.tm_v) return tma_box_ok(x, 64, a.d_v, 2, y, a.Hkv, z, rows, tkv, store);
+  if (m == &a.tm_do) return tma_box_ok(x, 64, a.d_v, 2, y, a.Hq, z, rows, tq, store);
+  if (m == &a.tm_dqacc) return tma_box_ok(x, 32, a.d_qk, 4, y, a.Hq, z, rows, tq, store);
+  return false;
+}
+
+// Gradient rows: n elements from column `col` of token row `row` of dQ
+// (query tokens, Hq heads of d_qk), dK (key tokens, Hkv heads of d_qk) or dV
+// (key tokens, Hkv heads of d_v), written through `p` with `vec`-byte stores.
+__device__ __forceinline__ bool dq_span_ok(const KernelArgs& a, int64_t row, int64_t col, int n,
+                                           const void* p, int vec) {
+  return row_span_ok(row, (int64_t)a.B * a.Sq, col, n, (int64_t)a.Hq * a.d_qk,
+                     reinterpret_cast<uint64_t>(p), vec);
+}
+__device__ __forceinline__ bool dk_span_ok(const KernelArgs& a, int64_t row, int64_t col, int n,
+                                           const void* p, int vec) {
+  return row_span_ok(row, (int64_t)a.B * a.Skv, col, n, (int64_t)a.Hkv * a.d_qk,
+                     reinterpret_cast<uint64_t>(p), vec);
+}
+__device__ __forceinline__ bool dv_span_ok(const KernelArgs& a, int64_t row, int64_t col, int n,
+                                           const void* p, int vec) {
+  return row_span_ok(row, (int64_t)a.B * a.Skv, col, n, (int64_t)a.Hkv * a.d_v,
+                     reinterpret_cast<uint64_t>(p), vec);
+}
+// One element (row, key) of the bias gradient dBias [bias_b, bias_h, Sq, Skv]
+// (fp32 accumulator or the output itself) at flat row `brow` = (b * bias_h + h)
+// * Sq + query.
+__device__ __forceinline__ bool dbias_ok(const KernelArgs& a, int64_t brow, int64_t key) {
+  return brow >= 0 && brow < (int64_t)a.bias_b * a.bias_h * a.Sq && key >= 0 && key < a.Skv;
 }
 
 // ---------------------------------------------------------------- dK/dV work items

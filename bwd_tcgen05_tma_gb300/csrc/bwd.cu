@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const KernelArgs a, int dq
     const int h = v / kPreTok, j = v - h * kPreTok;
     const int64_t t = t0 + j;
     float part = 0.f;  // this token's share of the sink gradient
-    if (v < a.Hq * kPreTok && t < ntok) {
+    if (v < a.Hq * kPreTok && t < ntok &&
+        ATTN_CHECK(a, span_ok(((t / a.Sq) * a.Hq + h) * a.Sq + t % a.Sq, 1, ntok * a.Hq), 0x7201)) {
       const int b = static_cast<int>(t / a.Sq), i = static_cast<int>(t - (int64_t)b * a.Sq);
       const int64_t idx = ((int64_t)b * a.Hq + h) * a.Sq + i;
       const float D = dsm[j][h];
@@ -156,7 +157,8 @@ __global__ void dq_convert_kernel(const KernelArgs a) {
     o.y = E::pack(x0.z, x0.w);
     o.z = E::pack(x1.x, x1.y);
     o.w = E::pack(x1.z, x1.w);
-    *reinterpret_cast<uint4*>(a.dq + tok * a.dq_stride + e) = o;
+    if (ATTN_CHECK(a, dq_span_ok(a, tok, e, 8, a.dq + tok * a.dq_stride + e, 16), 0x7202))
+      *reinterpret_cast<uint4*>(a.dq + tok * a.dq_stride + e) = o;
   }
 }
 

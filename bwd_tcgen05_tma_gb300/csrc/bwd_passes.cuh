@@ -158,10 +158,12 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
             mbar_arrive_expect_tx(&bars->kv_full, L::kKBytes + L::kVBytes);
 #pragma unroll
             for (int c = 0; c < DQK / 64; ++c)
-              tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
+              if (ATTN_CHECK(a, box_ok(a, &a.tm_k, c * 64, g, krow, kTile), 0x7501))
+                tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
 #pragma unroll
             for (int c = 0; c < DV / 64; ++c)
-              tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
+              if (ATTN_CHECK(a, box_ok(a, &a.tm_v, c * 64, g, krow, kTile), 0x7502))
+                tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
             ++kvc;
             for (int hh = 0; hh < G && ok; ++hh) {
               const int h = g * G + hh;
@@ -175,11 +177,13 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
                 mbar_arrive_expect_tx(&bars->qd_full[stage], L::kStageBytes);
 #pragma unroll
                 for (int c = 0; c < DQK / 64; ++c)
-                  tma_load_3d(qs + c * 8192, &a.tm_q, &bars->qd_full[stage], c * 64, h, qrow);
+                  if (ATTN_CHECK(a, box_ok(a, &a.tm_q, c * 64, h, qrow, kBwdQ), 0x7503))
+                    tma_load_3d(qs + c * 8192, &a.tm_q, &bars->qd_full[stage], c * 64, h, qrow);
 #pragma unroll
                 for (int c = 0; c < DV / 64; ++c)
-                  tma_load_3d(qs + L::kQBytes + c * 8192, &a.tm_do, &bars->qd_full[stage], c * 64,
-                              h, qrow);
+                  if (ATTN_CHECK(a, box_ok(a, &a.tm_do, c * 64, h, qrow, kBwdQ), 0x7504))
+                    tma_load_3d(qs + L::kQBytes + c * 8192, &a.tm_do, &bars->qd_full[stage], c * 64,
+                                h, qrow);
                 ATTN_TL(1, st);
               }
             }
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
               {
                 uint32_t u[32];
                 tmem_ld32x32b_x32(s_tm + c0h, u);
-                tmem_ld_wait();
+                tmem_ld_wait(u);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(u[e]) * a.scale_log2;
               }
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
               {
                 uint32_t u[32];
                 tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + c0h, u);
-                tmem_ld_wait();
+                tmem_ld_wait(u);
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
                   const float4 d4 = *reinterpret_cast<const float4*>(&V.D[c0h + e]);
@@ -496,7 +500,10 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
               fence_proxy_async_smem();
               mbar_arrive(&bars->ds_ready);
               if (j == 0 && half == 0) ATTN_TL(24, cur);
-              if (DBIAS != 0 && row_ok) {
+              if (DBIAS != 0 && row_ok &&
+                  ATTN_CHECK(a, dbias_ok(a, bias_base + q0 + c0h, kj) &&
+                                    dbias_ok(a, bias_base + min(q0 + c0h + 31, a.Sq - 1), kj),
+                             0x7505)) {
                 if (DBIAS == 1) {
                   bf16* dp = a.dbias + (bias_base + q0 + c0h) * a.Skv + kj;
 #pragma unroll
@@ -549,7 +556,9 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
           bf16* dv_row = a.dv + ((int64_t)b * a.Skv + kj) * a.dv_stride + (int64_t)g * DV;
           bf16* dk_row = a.dk + ((int64_t)b * a.Skv + kj) * a.dk_stride + (int64_t)g * DQK;
           if (nq == 0) {
-            if (row_ok) {
+            if (row_ok && ATTN_CHECK(a, dv_span_ok(a, (int64_t)b * a.Skv + kj, (int64_t)g * DV, DV, dv_row, 16) &&
+                                            dk_span_ok(a, (int64_t)b * a.Skv + kj, (int64_t)g * DQK, DQK, dk_row, 16),
+                                     0x7506)) {
 #pragma unroll
               for (int c = 0; c < DV; c += 8)
                 *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0, 0, 0, 0);
@@ -572,7 +581,7 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
                 uint32_t u0[32], u1[32];
                 tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ, u0);
                 tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + 32, u1);
-                tmem_ld_wait();
+                tmem_ld_wait(u0, u1);
                 tc_fence_before();
                 mbar_arrive(&bars->dq_free);
                 // the previous tile's reduce must have finished reading the staging buffer
@@ -592,8 +601,10 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
                     const int q0 = q_lo + s * kBwdQ;
 #pragma unroll
                     for (int bx = 0; bx < DQK / 32; ++bx)
-                      tma_reduce_add_3d(&a.tm_dqacc, stg + bx * (kBwdQ * 32), bx * 32, h,
-                                        b * a.Sq + q0);
+                      if (ATTN_CHECK(a, box_ok(a, &a.tm_dqacc, bx * 32, h, (int64_t)b * a.Sq + q0, kBwdQ, true),
+                                     0x7507))
+                        tma_reduce_add_3d(&a.tm_dqacc, stg + bx * (kBwdQ * 32), bx * 32, h,
+                                          b * a.Sq + q0);
                     bulk_commit_group();
                     bulk_wait_read_all();
                     mbar_arrive(&bars->stg_free);
@@ -611,8 +622,9 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
           for (int q = 0; q < DV / 32; ++q) {
             uint32_t u[32];
             tmem_ld32x32b_x32(tmem + lane_base + L::kColDV + q * 32, u);
-            tmem_ld_wait();
-            if (row_ok) {
+            tmem_ld_wait(u);
+            if (row_ok && ATTN_CHECK(a, dv_span_ok(a, (int64_t)b * a.Skv + kj, (int64_t)g * DV + q * 32, 32,
+                                                   dv_row + q * 32, 16), 0x7508)) {
 #pragma unroll
               for (int c = 0; c < 32; c += 8) {
                 uint4 v;
@@ -628,8 +640,9 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
           for (int q = 0; q < DQK / 32; ++q) {
             uint32_t u[32];
             tmem_ld32x32b_x32(tmem + lane_base + L::kColDK + q * 32, u);
-            tmem_ld_wait();
-            if (row_ok) {
+            tmem_ld_wait(u);
+            if (row_ok && ATTN_CHECK(a, dk_span_ok(a, (int64_t)b * a.Skv + kj, (int64_t)g * DQK + q * 32, 32,
+                                                   dk_row + q * 32, 16), 0x7509)) {
               const float sc = a.scale;
 #pragma unroll
               for (int c = 0; c < 32; c += 8) {
@@ -773,10 +786,12 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
         mbar_arrive_expect_tx(&bars->q_full, L::kQBytes + L::kOBytes);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->q_full, c * 64, h, qrow);
+          if (ATTN_CHECK(a, box_ok(a, &a.tm_q, c * 64, h, qrow, kTile), 0x7601))
+            tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->q_full, c * 64, h, qrow);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sm + L::kOOff + c * 16384, &a.tm_do, &bars->q_full, c * 64, h, qrow);
+          if (ATTN_CHECK(a, box_ok(a, &a.tm_do, c * 64, h, qrow, kTile), 0x7602))
+            tma_load_3d(sm + L::kOOff + c * 16384, &a.tm_do, &bars->q_full, c * 64, h, qrow);
         ++it;
         const int g = h / (a.Hq / a.Hkv);
         for (int j = 0; j < n; ++j, ++kt) {
@@ -787,16 +802,18 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
           mbar_arrive_expect_tx(&bars->k_full[ks], L::kKBytes);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(sm + L::kKOff + ks * L::kKBytes + c * 16384, &a.tm_k, &bars->k_full[ks],
-                        c * 64, g, krow);
+            if (ATTN_CHECK(a, box_ok(a, &a.tm_k, c * 64, g, krow, kTile), 0x7603))
+              tma_load_3d(sm + L::kKOff + ks * L::kKBytes + c * 16384, &a.tm_k, &bars->k_full[ks],
+                          c * 64, g, krow);
           ++k_loads;
           if (kt >= (uint32_t)VS && !(ok = mbar_wait(&bars->v_empty[vs], ((kt / VS) - 1) & 1)))
             break;
           mbar_arrive_expect_tx(&bars->v_full[vs], L::kVBytes);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(sm + L::kVOff + vs * L::kVBytes + c * 16384, &a.tm_v, &bars->v_full[vs],
-                        c * 64, g, krow);
+            if (ATTN_CHECK(a, box_ok(a, &a.tm_v, c * 64, g, krow, kTile), 0x7604))
+              tma_load_3d(sm + L::kVOff + vs * L::kVBytes + c * 16384, &a.tm_v, &bars->v_full[vs],
+                          c * 64, g, krow);
         }
       }
       if (!ok) {
@@ -908,7 +925,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
       const int64_t grow = (int64_t)b * a.Sq + i;
       bf16* dq_row = a.dq + grow * a.dq_stride + (int64_t)h * DQK;
       if (n == 0) {
-        if (row_ok) {
+        if (row_ok && ATTN_CHECK(a, dq_span_ok(a, grow, (int64_t)h * DQK, DQK, dq_row, 16), 0x7605)) {
 #pragma unroll
           for (int c = 0; c < DQK; c += 8)
             *reinterpret_cast<uint4*>(dq_row + c) = make_uint4(0, 0, 0, 0);
@@ -945,7 +962,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
         for (int q = 0; q < kTile / 32; ++q) {
           uint32_t u[32];
           tmem_ld32x32b_x32(tmem + lane_base + L::kColS + q * 32, u);
-          tmem_ld_wait();
+          tmem_ld_wait(u);
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[q * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
         }
@@ -971,7 +988,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
         for (int q = 0; q < kTile / 32; ++q) {
           uint32_t u[32];
           tmem_ld32x32b_x32(tmem + lane_base + L::kColDP + q * 32, u);
-          tmem_ld_wait();
+          tmem_ld_wait(u);
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[q * 32 + e] *= (__uint_as_float(u[e]) - Di);
         }
@@ -998,8 +1015,9 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
       for (int q = 0; q < DQK / 32; ++q) {
         uint32_t u[32];
         tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + q * 32, u);
-        tmem_ld_wait();
-        if (row_ok) {
+        tmem_ld_wait(u);
+        if (row_ok && ATTN_CHECK(a, dq_span_ok(a, grow, (int64_t)h * DQK + q * 32, 32, dq_row + q * 32, 16),
+                                 0x7606)) {
           const float sc = a.scale;
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {

@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 mbar_arrive_expect_tx(&bars->q_full[sq], L::kQBytes);
 #pragma unroll
                 for (int c = 0; c < DQK / 64; ++c)
-                  tma_load_3d(qs + c * 16384, &a.tm_q, &bars->q_full[sq], c * 64, h, qrow);
+                  if (ATTN_CHECK(a, box_ok(a, &a.tm_q, c * 64, h, qrow, kQ), 0x7301))
+                    tma_load_3d(qs + c * 16384, &a.tm_q, &bars->q_full[sq], c * 64, h, qrow);
                 ++q_issued;
                 ATTN_TL(1, st);
                 if (hh == 0 && s == 0) {
@@ -168,10 +169,12 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                   mbar_arrive_expect_tx(&bars->kv_full, L::kKBytes + L::kVBytes);
 #pragma unroll
                   for (int c = 0; c < DQK / 64; ++c)
-                    tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
+                    if (ATTN_CHECK(a, box_ok(a, &a.tm_k, c * 64, g, krow, kTile), 0x7302))
+                      tma_load_3d(sm + L::kKOff + c * 16384, &a.tm_k, &bars->kv_full, c * 64, g, krow);
 #pragma unroll
                   for (int c = 0; c < DV / 64; ++c)
-                    tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
+                    if (ATTN_CHECK(a, box_ok(a, &a.tm_v, c * 64, g, krow, kTile), 0x7303))
+                      tma_load_3d(sm + L::kVOff + c * 16384, &a.tm_v, &bars->kv_full, c * 64, g, krow);
                   ++kvc;
                 }
                 if (st >= (uint32_t)NO &&
@@ -181,7 +184,8 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 mbar_arrive_expect_tx(&bars->o_full[so], L::kOBytes);
 #pragma unroll
                 for (int c = 0; c < DV / 64; ++c)
-                  tma_load_3d(os + c * 16384, &a.tm_do, &bars->o_full[so], c * 64, h, qrow);
+                  if (ATTN_CHECK(a, box_ok(a, &a.tm_do, c * 64, h, qrow, kQ), 0x7304))
+                    tma_load_3d(os + c * 16384, &a.tm_do, &bars->o_full[so], c * 64, h, qrow);
                 ++o_issued;
                 ATTN_TL(2, st);
               }
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 } else {
                   uint32_t u[32];
                   tmem_ld32x32b_x32(s_tm + q * 32, u);
-                  tmem_ld_wait();
+                  tmem_ld_wait(u);
                   float x[32];
                   if (HAS_BIAS) {
 #pragma unroll
@@ -504,7 +508,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 }
                 uint32_t u[32];
                 tmem_ld32x32b_x32(dp_tm + q * 32, u);
-                tmem_ld_wait();
+                tmem_ld_wait(u);
                 uint32_t pk[16];
                 if (DBIAS == 0) {
                   // dP - D in fp32, then one packed bf16 product with P (already
@@ -539,7 +543,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pk[e] = E::pack(ds[2 * e], ds[2 * e + 1]);
                 tmem_st32x32b_x16(dp_tm + q * 16, pk);
-                if (DBIAS != 0 && row_ok) {
+                if (DBIAS != 0 && row_ok &&
+                    ATTN_CHECK(a, dbias_ok(a, bias_base + qh + q * 32, kj) &&
+                                      dbias_ok(a, bias_base + min(qh + q * 32 + 31, a.Sq - 1), kj),
+                               0x7305)) {
                   if (DBIAS == 1) {
                     bf16* dpb = a.dbias + (bias_base + qh + q * 32) * a.Skv + kj;
 #pragma unroll
@@ -598,7 +605,9 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
           bf16* dv_row = a.dv + ((int64_t)b * a.Skv + kj) * a.dv_stride + (int64_t)g * DV;
           bf16* dk_row = a.dk + ((int64_t)b * a.Skv + kj) * a.dk_stride + (int64_t)g * DQK;
           if (nq == 0) {
-            if (row_ok) {
+            if (row_ok && ATTN_CHECK(a, dv_span_ok(a, (int64_t)b * a.Skv + kj, (int64_t)g * DV, DV, dv_row, 16) &&
+                                            dk_span_ok(a, (int64_t)b * a.Skv + kj, (int64_t)g * DQK, DQK, dk_row, 16),
+                                     0x7306)) {
 #pragma unroll
               for (int c = 0; c < DV; c += 8)
                 *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0, 0, 0, 0);
@@ -614,7 +623,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
           for (int q = 0; q < DV / 32; ++q) {
             uint32_t u[32];
             tmem_ld32x32b_x32(tmem + lane_base + L::kColDV + q * 32, u);
-            tmem_ld_wait();
+            tmem_ld_wait(u);
             if (row_ok) {
 #pragma unroll
               for (int c = 0; c < 32; c += 16) {
@@ -622,7 +631,9 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                   w[e] = E::pack(__uint_as_float(u[c + 2 * e]), __uint_as_float(u[c + 2 * e + 1]));
-                store16_elems(dv_row + q * 32 + c, w, a.grad_st32 != 0);
+                if (ATTN_CHECK(a, dv_span_ok(a, (int64_t)b * a.Skv + kj, (int64_t)g * DV + q * 32 + c, 16,
+                                             dv_row + q * 32 + c, a.grad_st32 ? 32 : 16), 0x7307))
+                  store16_elems(dv_row + q * 32 + c, w, a.grad_st32 != 0);
               }
             }
           }
@@ -630,7 +641,7 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
           for (int q = 0; q < DQK / 32; ++q) {
             uint32_t u[32];
             tmem_ld32x32b_x32(tmem + lane_base + L::kColDK + q * 32, u);
-            tmem_ld_wait();
+            tmem_ld_wait(u);
             if (row_ok) {
               const float sc = a.scale;
 #pragma unroll
@@ -639,7 +650,9 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                   w[e] = E::pack(__uint_as_float(u[c + 2 * e]) * sc, __uint_as_float(u[c + 2 * e + 1]) * sc);
-                store16_elems(dk_row + q * 32 + c, w, a.grad_st32 != 0);
+                if (ATTN_CHECK(a, dk_span_ok(a, (int64_t)b * a.Skv + kj, (int64_t)g * DQK + q * 32 + c, 16,
+                                             dk_row + q * 32 + c, a.grad_st32 ? 32 : 16), 0x7308))
+                  store16_elems(dk_row + q * 32 + c, w, a.grad_st32 != 0);
               }
             }
           }

@@ -164,10 +164,12 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
         mbar_arrive_expect_tx(&bars->qo_full, L::kQBytes + L::kOBytes);
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->qo_full, c * 64, h, qrow);
+          if (ATTN_CHECK(a, box_ok(a, &a.tm_q, c * 64, h, qrow, kTile), 0x7401))
+            tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->qo_full, c * 64, h, qrow);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(sm + L::kOOff + c * 16384, &a.tm_do, &bars->qo_full, c * 64, h, qrow);
+          if (ATTN_CHECK(a, box_ok(a, &a.tm_do, c * 64, h, qrow, kTile), 0x7402))
+            tma_load_3d(sm + L::kOOff + c * 16384, &a.tm_do, &bars->qo_full, c * 64, h, qrow);
         ++it;
         const int g = h / (a.Hq / a.Hkv);
         for (int j = 0; j < n; ++j, ++kt) {
@@ -178,16 +180,18 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
           mbar_arrive_expect_tx(&bars->k_full[ks], L::kKBytes);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(sm + L::kKOff + ks * L::kKBytes + c * 16384, &a.tm_k, &bars->k_full[ks],
-                        c * 64, g, krow);
+            if (ATTN_CHECK(a, box_ok(a, &a.tm_k, c * 64, g, krow, kTile), 0x7403))
+              tma_load_3d(sm + L::kKOff + ks * L::kKBytes + c * 16384, &a.tm_k, &bars->k_full[ks],
+                          c * 64, g, krow);
           ++k_issued;
           if (kt >= (uint32_t)VS && !(ok = mbar_wait(&bars->v_empty[vs], ((kt / VS) - 1) & 1)))
             break;
           mbar_arrive_expect_tx(&bars->v_full[vs], L::kVBytes);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(sm + L::kVOff + vs * L::kVBytes + c * 16384, &a.tm_v, &bars->v_full[vs],
-                        c * 64, g, krow);
+            if (ATTN_CHECK(a, box_ok(a, &a.tm_v, c * 64, g, krow, kTile), 0x7404))
+              tma_load_3d(sm + L::kVOff + vs * L::kVBytes + c * 16384, &a.tm_v, &bars->v_full[vs],
+                          c * 64, g, krow);
           ++v_issued;
         }
       }
@@ -310,7 +314,9 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
       const bool row_ok = i < a.Sq;
       const int64_t grow = (int64_t)b * a.Sq + i;
       if (n == 0) {  // no key visible to the tile: dQ rows are exactly zero
-        if (half == 0 && row_ok) {
+        if (half == 0 && row_ok &&
+            ATTN_CHECK(a, dq_span_ok(a, grow, (int64_t)h * DQK, DQK,
+                                     a.dq + grow * a.dq_stride + (int64_t)h * DQK, 16), 0x7405)) {
           bf16* dq_row = a.dq + grow * a.dq_stride + (int64_t)h * DQK;
 #pragma unroll
           for (int c = 0; c < DQK; c += 8)
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
           }
           uint32_t u[32];
           tmem_ld32x32b_x32(s_tm + q * 32, u);
-          tmem_ld_wait();
+          tmem_ld_wait(u);
           float x[32];
           if (HAS_BIAS) {
 #pragma unroll
@@ -433,7 +439,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
           } else {
             uint32_t u[32];
             tmem_ld32x32b_x32(dp_tm + q * 32, u);
-            tmem_ld_wait();
+            tmem_ld_wait(u);
             // dP - D in fp32, then one packed bf16 product with P (already bf16)
             const float2 d2 = make_float2(Di, Di);
 #pragma unroll
@@ -480,7 +486,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
       for (int q = 0; q < DQK / 32; ++q) {
         uint32_t u[32];
         tmem_ld32x32b_x32(tmem + lane_base + L::kColDQ + q * 32, u);
-        tmem_ld_wait();
+        tmem_ld_wait(u);
         if (row_ok) {
           const float sc = a.scale;
 #pragma unroll
@@ -489,7 +495,9 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               w[e] = E::pack(__uint_as_float(u[c + 2 * e]) * sc, __uint_as_float(u[c + 2 * e + 1]) * sc);
-            store16_elems(dq_row + q * 32 + c, w, a.grad_st32 != 0);
+            if (ATTN_CHECK(a, dq_span_ok(a, (int64_t)b * a.Sq + i, (int64_t)h * DQK + q * 32 + c, 16,
+                                         dq_row + q * 32 + c, a.grad_st32 ? 32 : 16), 0x7406))
+              store16_elems(dq_row + q * 32 + c, w, a.grad_st32 != 0);
           }
         }
       }

@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         const int qrow = w.b * a.Sq + w.t * kTile;
 #pragma unroll
         for (int c = 0; c < DQK / 64; ++c)
-          tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->q_full, c * 64, w.h, qrow);
+          if (ATTN_CHECK(a, box_ok(a, &a.tm_q, c * 64, w.h, qrow, kTile), 0x7001))
+            tma_load_3d(sm + L::kQOff + c * 16384, &a.tm_q, &bars->q_full, c * 64, w.h, qrow);
         const int g = w.h / (a.Hq / a.Hkv);
         for (int j = 0; j < w.n; ++j, ++kt) {
           const int krow = w.b * a.Skv + w.kv_lo + j * kTile;
@@ -185,7 +186,8 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
           mbar_arrive_expect_tx(&bars->k_full[ks], L::kKBytes);
 #pragma unroll
           for (int c = 0; c < DQK / 64; ++c)
-            tma_load_3d(kst + c * 16384, &a.tm_k, &bars->k_full[ks], c * 64, g, krow);
+            if (ATTN_CHECK(a, box_ok(a, &a.tm_k, c * 64, g, krow, kTile), 0x7002))
+              tma_load_3d(kst + c * 16384, &a.tm_k, &bars->k_full[ks], c * 64, g, krow);
           ++k_loads;
           if (kt >= (uint32_t)L::kVStages &&
               !(ok = mbar_wait(&bars->v_empty[vs], ((kt / L::kVStages) - 1) & 1)))
@@ -194,7 +196,8 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
           mbar_arrive_expect_tx(&bars->v_full[vs], L::kVBytes);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(vst + c * 16384, &a.tm_v, &bars->v_full[vs], c * 64, g, krow);
+            if (ATTN_CHECK(a, box_ok(a, &a.tm_v, c * 64, g, krow, kTile), 0x7003))
+              tma_load_3d(vst + c * 16384, &a.tm_v, &bars->v_full[vs], c * 64, g, krow);
         }
         if (!ok) break;
         ++it;
@@ -298,7 +301,9 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
       bf16* orow = a.o + (grow * a.Hq + w.h) * DV;
       float* lse_out = a.lse + ((int64_t)w.b * a.Hq + w.h) * a.Sq + i;
       if (w.n == 0) {
-        if (row_ok) {
+        if (row_ok && ATTN_CHECK(a, span_ok(orow - a.o, DV, (int64_t)a.B * a.Sq * a.Hq * DV) &&
+                                        span_ok(lse_out - a.lse, 1, (int64_t)a.B * a.Hq * a.Sq),
+                                 0x7004)) {
 #pragma unroll
           for (int c = 0; c < DV; c += 8)
             *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         for (int q = 0; q < kTile / 32; ++q) {
           uint32_t u[32];
           tmem_ld32x32b_x32(tmem + lane_base + L::kColS + sb * kTile + q * 32, u);
-          tmem_ld_wait();
+          tmem_ld_wait(u);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float2 y = mul_f32x2(make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])),
@@ -388,7 +393,7 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
             uint32_t u[32];
             const uint32_t ta = tmem + lane_base + L::kColO + q * 32;
             tmem_ld32x32b_x32(ta, u);
-            tmem_ld_wait();
+            tmem_ld_wait(u);
 #pragma unroll
             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
             tmem_st32x32b_x32(ta, u);
@@ -441,8 +446,9 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
       for (int q = 0; q < DV / 32; ++q) {
         uint32_t u[32];
         tmem_ld32x32b_x32(tmem + lane_base + L::kColO + q * 32, u);
-        tmem_ld_wait();
-        if (row_ok) {
+        tmem_ld_wait(u);
+        if (row_ok && ATTN_CHECK(a, span_ok(orow + q * 32 - a.o, 32, (int64_t)a.B * a.Sq * a.Hq * DV),
+                                 0x7005)) {
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint4 v;
@@ -454,8 +460,10 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
           }
         }
       }
-      if (row_ok) *lse_out = (l_fin > 0.f) ? (m_fin + __log2f(l_fin)) * kLn2 : -INFINITY;
-      if (a.max_logit) warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + w.h, row_max);
+      if (row_ok && ATTN_CHECK(a, span_ok(lse_out - a.lse, 1, (int64_t)a.B * a.Hq * a.Sq), 0x7006))
+        *lse_out = (l_fin > 0.f) ? (m_fin + __log2f(l_fin)) * kLn2 : -INFINITY;
+      if (a.max_logit && ATTN_CHECK(a, span_ok((int64_t)w.b * a.Hq + w.h, 1, (int64_t)a.B * a.Hq), 0x7007))
+        warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + w.h, row_max);
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
       kt += w.n;

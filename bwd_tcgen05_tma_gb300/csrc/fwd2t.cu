@@ -223,7 +223,8 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           uint8_t* dst = sm + L::kKVOff + s * L::kKVBytes;
           mbar_arrive_expect_tx(&bars->kv_full[s], kTile * ncols * 2);
           for (int c = 0; c < ncols / 64; ++c)
-            tma_load_3d(dst + c * 16384, m, &bars->kv_full[s], c * 64, g, krow);
+            if (ATTN_CHECK(a, box_ok(a, m, c * 64, g, krow, kTile), 0x7101))
+              tma_load_3d(dst + c * 16384, m, &bars->kv_full[s], c * 64, g, krow);
           ++kvc;
           return true;
         };
@@ -242,7 +243,8 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
             uint8_t* dst = sm + L::kQOff + (qs * 2 + x) * L::kQStage;
   #pragma unroll
             for (int c = 0; c < DQK / 64; ++c)
-              tma_load_3d(dst + c * 16384, &a.tm_q, &bars->q_full[qs], c * 64, w.h0 + x, qrow);
+              if (ATTN_CHECK(a, box_ok(a, &a.tm_q, c * 64, w.h0 + x, qrow, kTile), 0x7102))
+                tma_load_3d(dst + c * 16384, &a.tm_q, &bars->q_full[qs], c * 64, w.h0 + x, qrow);
           }
           ++qi;
           return true;
@@ -378,6 +380,10 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
             issue_pv(x, vc, j == 0);
             ATTN_TL(40 + x, k);
             if (!more) mma_commit_warp(&bars->o_full[x]);
+            // V(j) is read by both P V and by nothing after them: its stage
+            // goes back to the producer now, not after the next S as well,
+            // so that K(j+2) starts loading one S earlier
+            if (x == 1) mma_commit_warp(&bars->kv_empty[vc % NKV]);
             if (!go_on) continue;
             // the next S over P_X(j), after P_X(j) V (same issuer, in-order pipe)
             if (x == 0) {
@@ -390,7 +396,6 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
             ATTN_TL(32 + x, k + 1);
           }
           if (!ok) break;
-          mma_commit_warp(&bars->kv_empty[vc % NKV]);  // V(j) read by both P V
           if (go_on) mma_commit_warp(&bars->kv_empty[(vc + 1) % NKV]);  // the next K by both S
           kvc += go_on ? 2 : 1;
         }
@@ -476,7 +481,9 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       float* lse_out = a.lse + ((int64_t)R.b * a.Hq + h) * a.Sq + i;
       struct { int b, n, kv_lo; } w = {R.b, e.y, e.z};
       if (w.n == 0) {
-        if (row_ok) {
+        if (row_ok && ATTN_CHECK(a, span_ok(orow - a.o, DV, (int64_t)a.B * a.Sq * a.Hq * DV) &&
+                                        span_ok(lse_out - a.lse, 1, (int64_t)a.B * a.Hq * a.Sq),
+                                 0x7106)) {
 #pragma unroll
           for (int c = 0; c < DV; c += 8)
             *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
@@ -517,7 +524,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         uint32_t u[4][32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32x32b_x32(s_tm + q * 32, u[q]);
-        tmem_ld_wait();
+        tmem_ld_wait(u);
         // pass 1: the row max over valid keys (log2 units)
         float mx8[8];
 #pragma unroll
@@ -566,7 +573,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
           for (int q = 0; q < DV / 32; ++q) {
             uint32_t o[32];
             tmem_ld32x32b_x32(o_tm + q * 32, o);
-            tmem_ld_wait();
+            tmem_ld_wait(o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
             tmem_st32x32b_x32(o_tm + q * 32, o);
@@ -608,7 +615,7 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
       for (int q = 0; q < DV / 32; ++q) {
         uint32_t u[32];
         tmem_ld32x32b_x32(o_tm + q * 32, u);
-        tmem_ld_wait();
+        tmem_ld_wait(u);
         const uint32_t row = smem_u32(stg + (q >> 1) * 16384 + r * 128);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -630,12 +637,16 @@ __global__ void __launch_bounds__(384, 1) fwd2t_kernel(const __grid_constant__ K
         const F2Item wi = f2_item(a, e.x);
 #pragma unroll
         for (int c = 0; c < DV / 64; ++c)
-          tma_store_4d(&a.tm_o, stg + c * 16384, c * 64, h, wi.t * kTile, wi.b);
+          if (ATTN_CHECK(a, tma_box_ok(c * 64, 64, DV, 2, h, a.Hq, wi.t * kTile, kTile, a.Sq, true) &&
+                                wi.b >= 0 && wi.b < a.B, 0x7103))
+            tma_store_4d(&a.tm_o, stg + c * 16384, c * 64, h, wi.t * kTile, wi.b);
         bulk_commit_group();
         store_stage = static_cast<int>(it & 1);
       }
-      if (row_ok) *lse_out = (l_fin > 0.f) ? (m_fin + __log2f(l_fin)) * kLn2 : -INFINITY;
-      if (a.max_logit) warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + h, row_max);
+      if (row_ok && ATTN_CHECK(a, span_ok(lse_out - a.lse, 1, (int64_t)a.B * a.Hq * a.Sq), 0x7104))
+        *lse_out = (l_fin > 0.f) ? (m_fin + __log2f(l_fin)) * kLn2 : -INFINITY;
+      if (a.max_logit && ATTN_CHECK(a, span_ok((int64_t)w.b * a.Hq + h, 1, (int64_t)a.B * a.Hq), 0x7105))
+        warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + h, row_max);
       tc_fence_before();
       mbar_arrive(&bars->o_empty[x]);
       if (lane == 0 && warp == 4) ATTN_TL(48, it);

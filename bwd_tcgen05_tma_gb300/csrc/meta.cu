@@ -415,7 +415,9 @@ __device__ void meta_ranges(const KernelArgs& a, const MetaIn& in) {
     }
     lo = warp_min(lo);
     hi = warp_max(hi);
-    if (lane == 0) {
+    if (lane == 0 &&
+        ATTN_CHECK(a, span_ok(w2, 1, (int64_t)a.B * (qside ? a.n_qt : a.n_kt)), 0x7801) &&
+        ATTN_CHECK(a, hi <= lo || (lo >= 0 && hi <= S_oth), 0x7802)) {
       const int2 r = (hi > lo) ? make_int2(lo, hi) : make_int2(0, 0);
       if (qside) {
         const_cast<int2*>(a.q_tile_range)[w2] = r;

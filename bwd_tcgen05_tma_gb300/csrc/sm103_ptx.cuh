@@ -431,7 +431,35 @@ SM103_DEV void tmem_ld32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
-SM103_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// tcgen05.ld fills its registers asynchronously: they hold the loaded values
+// once tcgen05.wait::ld has returned, but the compiler sees them as set by
+// the load itself and is free to move their uses above a wait that does not
+// name them.  So the wait takes the loaded registers as operands ("+r"): every
+// later use then depends on it.  Further arrays loaded before the same wait
+// pass through an empty statement placed after it (volatile statements keep
+// their order).
+#define SM103_RW8(a, o) "+r"(a[o + 0]), "+r"(a[o + 1]), "+r"(a[o + 2]), "+r"(a[o + 3]), \
+                        "+r"(a[o + 4]), "+r"(a[o + 5]), "+r"(a[o + 6]), "+r"(a[o + 7])
+SM103_DEV void tmem_ld_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : SM103_RW8(r, 0), SM103_RW8(r, 8)::"memory");
+}
+SM103_DEV void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : SM103_RW8(r, 0), SM103_RW8(r, 8), SM103_RW8(r, 16), SM103_RW8(r, 24)::"memory");
+}
+SM103_DEV void tmem_ld_after_wait(uint32_t (&r)[32]) {
+  asm volatile("" : SM103_RW8(r, 0), SM103_RW8(r, 8), SM103_RW8(r, 16), SM103_RW8(r, 24)::"memory");
+}
+SM103_DEV void tmem_ld_wait(uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+  tmem_ld_wait(r0);
+  tmem_ld_after_wait(r1);
+}
+template <int N>
+SM103_DEV void tmem_ld_wait(uint32_t (&r)[N][32]) {
+  tmem_ld_wait(r[0]);
+#pragma unroll
+  for (int i = 1; i < N; ++i) tmem_ld_after_wait(r[i]);
+}
 
 SM103_DEV void tmem_st32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(

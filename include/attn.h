@@ -66,7 +66,11 @@ typedef enum {
   ATTN_ERR_SHAPE_MISMATCH = 3,      /* segment ids/pos (or Q/KV) shapes disagree */
   ATTN_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the *_workspace_size() value */
   ATTN_ERR_CUDA = 5,                /* a CUDA runtime call failed (launch, attribute) */
-  ATTN_ERR_DEVICE_TIMEOUT = 6       /* a kernel wait ran past its limit (read via
+  ATTN_ERR_DEVICE_TIMEOUT = 6,      /* a kernel wait ran past its limit (read via
+                                       attn_read_status) */
+  ATTN_ERR_DEVICE_BOUNDS = 7        /* checking build only (attn_build_flags):
+                                       a device-side bounds check failed and its
+                                       access was skipped (read via
                                        attn_read_status) */
 } attn_status_t;
 
@@ -217,7 +221,8 @@ typedef enum {
 } attn_path_reason_t;
 
 typedef struct {
-  int32_t status;        /* attn_status_t of the device side (timeouts) */
+  int32_t status;        /* attn_status_t of the device side (timeouts, failed
+                            bounds checks of the checking build) */
   int32_t path;          /* attn_path_t of the last call using this workspace */
   int32_t reason;        /* attn_path_reason_t */
   int32_t dq_mode;       /* dQ mode actually used by the last backward */
@@ -226,7 +231,12 @@ typedef struct {
                             that ran out (kernel and role code: 0x6.. forward
                             over head pairs, 0x3.. 128-row dK/dV, 0x4.. dQ,
                             0x1.. / 0x2.. the other backward passes, 0x0.. the
-                            other forward, 0x30. metadata); 0 otherwise */
+                            other forward, 0x30. metadata); with
+                            ATTN_ERR_DEVICE_BOUNDS: the first failed check
+                            (0x7K.., K the kernel: 0 other forward, 1 forward
+                            over head pairs, 2 preprocess and conversions,
+                            3 128-row dK/dV, 4 dQ, 5 64-row dK/dV, 6 192-wide
+                            dQ, 8 metadata); 0 otherwise */
   int32_t reserved;
 } attn_stats_t;
 
@@ -336,6 +346,20 @@ attn_status_t attn_event_elapsed_ms(const void* start, const void* end, float* m
 attn_status_t attn_fwd_noalloc(const attn_params_t* p, void* o, float* lse, void* stream);
 
 int32_t attn_abi_version(void);
+
+/* Properties of this build of the library, as bit flags:
+ *  ATTN_BUILD_DEVICE_CHECKS  the checking build (libattn_sm103_debug.so,
+ *    compiled with ATTN_DEBUG; the pages have no counterpart, it stands in for
+ *    a memory checker): before every tensor-map copy and every global store a
+ *    kernel checks the copy's coordinates (16-byte-aligned innermost
+ *    coordinate, box inside the row, existing head, no store starting at a
+ *    negative row) or the store's element range against the tensor's size.
+ *    A failed check records ATTN_ERR_DEVICE_BOUNDS and the check's site in
+ *    the workspace status and skips the access (no trap); waits that then go
+ *    unanswered run out and the kernel unwinds as for a timeout.  Same entry
+ *    points and results, slower. */
+#define ATTN_BUILD_DEVICE_CHECKS 1
+int32_t attn_build_flags(void);
 
 #ifdef __cplusplus
 }
