@@ -26,7 +26,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 struct Plan {
   size_t hdr, q_id, q_pos, seg_lo, seg_hi, kv_id, kv_pos, kv_seg_lo, kv_seg_hi;
-  size_t q_chunk, kv_chunk, q_range, kv_range, meta_scan;
+  size_t q_chunk, kv_chunk, q_range, kv_range, q_order, meta_scan;
   size_t fwd_total;
   size_t lse2, dvec, dq_acc, dbias_acc, sink_part;
   size_t bwd_total;
@@ -59,6 +59,7 @@ Plan make_plan(const attn_params_t* p) {
   pl.kv_chunk = o; o = up(o + B * nkc * sizeof(ChunkInfo));
   pl.q_range = o; o = up(o + B * nqt * sizeof(int2));
   pl.kv_range = o; o = up(o + B * nkt * sizeof(int2));
+  pl.q_order = o; o = up(o + B * nqt * 4);
   pl.meta_scan = o; o = up(o + 2 * B * ((std::max(Sq, Skv) + 1023) / 1024) * sizeof(int2));
   pl.fwd_total = o;
   pl.lse2 = o; o = up(o + B * p->Hq * Sq * 4);
@@ -280,6 +281,7 @@ void fill_common(KernelArgs& a, const attn_params_t* p, char* ws, const Plan& pl
   a.meta_scan = reinterpret_cast<int2*>(ws + pl.meta_scan);
   a.q_tile_range = reinterpret_cast<int2*>(ws + pl.q_range);
   a.kv_tile_range = reinterpret_cast<int2*>(ws + pl.kv_range);
+  a.q_order = reinterpret_cast<int32_t*>(ws + pl.q_order);
   a.bias = static_cast<const bf16*>(p->bias);
   a.bias_b = p->bias_b;
   a.bias_h = p->bias_h;

@@ -70,6 +70,7 @@ struct WsHeader {
   int32_t where;       // site of the first device-side error (wait or bounds check)
   int32_t next_item[4];  // work-item counters of the persistent kernels (zeroed per call)
   uint32_t meta_barrier;  // arrivals at the metadata kernel's grid barriers (zeroed per call)
+  uint32_t meta_done;     // metadata blocks past their last pass (zeroed per call)
 };
 
 // Dynamic work distribution inside a persistent CTA: one thread claims items
@@ -90,14 +91,25 @@ __device__ __forceinline__ void ring_init(ItemRing* r, uint32_t consumers) {
 }
 
 // Producer side: claim the next item (or -1 once exhausted) and publish it as
-// the n-th entry of the ring.  Returns false if the wait for a free slot timed out.
+// the n-th entry of the ring.  With `order`, claim v stands for item
+// order[v / per] * per + v % per (items grouped `per` to a tile, the tiles
+// handed out in the order given).  Returns false if the wait for a free slot
+// timed out.
 __device__ __forceinline__ bool ring_push(ItemRing* r, uint32_t n, int32_t* counter, int n_items,
-                                          int32_t& item) {
+                                          int32_t& item, const int32_t* order = nullptr,
+                                          int per = 1) {
   const int s = n % kItemRing;
   if (n >= (uint32_t)kItemRing && !sm103::mbar_wait(&r->empty[s], ((n / kItemRing) - 1) & 1))
     return false;
   const int32_t v = atomicAdd(counter, 1);
-  item = (v < n_items) ? v : -1;
+  if (v >= n_items) {
+    item = -1;
+  } else if (order) {
+    const int32_t g = v / per;
+    item = order[g] * per + (v - g * per);
+  } else {
+    item = v;
+  }
   *reinterpret_cast<volatile int32_t*>(&r->item[s]) = item;
   sm103::mbar_arrive(&r->full[s]);  // release: the item is visible to waiters
   return true;
@@ -237,6 +249,9 @@ struct KernelArgs {
   const int2* meta_scan;      // [2][B][chunks of 1024] first/last run boundary per chunk
   const int2* q_tile_range;   // [B*n_qt]  KV token range of each 128-row query tile
   const int2* kv_tile_range;  // [B*n_kt]  query token range of each 128-row KV tile
+  // query tiles (b * n_qt + t) in order of decreasing KV-tile count: the
+  // persistent passes over query tiles hand out their longest items first
+  const int32_t* q_order;     // [B*n_qt]
   float* max_logit;  // forward only: fp32 [B, Hq] or null
   const float* sink;  // fp32 [Hq] sink logits or null
   float* dsink;       // backward only: fp32 [Hq] or null

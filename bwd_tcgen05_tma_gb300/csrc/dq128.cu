@@ -131,13 +131,15 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
   const bool general = path_general(a);
 
   // causal work is heaviest in the last query tiles: hand those out first
+  // item = (query tile w = b * n_qt + t, head h), numbered w * Hq + h; the
+  // producer claims them with the query tiles in the metadata pass's order
+  // (longest first)
   auto item_of = [&](int idx, int& b, int& t, int& h, int& kv_lo, int& n) {
-    const int per_t = a.B * a.Hq;
-    const int t_rev = idx / per_t, rem = idx - t_rev * per_t;
-    t = a.n_qt - 1 - t_rev;
-    b = rem / a.Hq;
-    h = rem - b * a.Hq;
-    const int2 r = a.q_tile_range[b * a.n_qt + t];
+    const int w = idx / a.Hq;
+    h = idx - w * a.Hq;
+    b = w / a.n_qt;
+    t = w - b * a.n_qt;
+    const int2 r = a.q_tile_range[w];
     kv_lo = r.x;
     n = (r.y > r.x) ? (r.y - r.x + kTile - 1) / kTile : 0;
   };
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
       bool ok = true;
       for (uint32_t rn = 0;; ++rn) {
         int32_t idx;
-        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[2], n_items, idx)) ||
+        if (!ok || *abort_flag || !(ok = ring_push(ring, rn, &a.hdr->next_item[2], n_items, idx, a.q_order, a.Hq)) ||
             idx < 0)
           break;
         int b, t, h, kv_lo, n;

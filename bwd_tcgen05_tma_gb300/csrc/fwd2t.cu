@@ -59,25 +59,28 @@ struct F2Item {
   int b, t, h0;
 };
 
-// item = (query tile, head pair), longest causal tiles first
+// item = (query tile w = b * n_qt + t, head pair), numbered w * (Hq / 2) + pair
 __device__ __forceinline__ F2Item f2_item(const KernelArgs& a, int idx) {
   const int hp = a.Hq / 2;
-  const int per_t = a.B * hp;
-  const int t_rev = idx / per_t, rem = idx - t_rev * per_t;
+  const int w = idx / hp;
   F2Item it;
-  it.t = a.n_qt - 1 - t_rev;
-  it.b = rem / hp;
-  it.h0 = 2 * (rem - it.b * hp);
+  it.b = w / a.n_qt;
+  it.t = w - it.b * a.n_qt;
+  it.h0 = 2 * (idx - w * hp);
   return it;
 }
 
-// Ring entry of item idx: (idx, key tiles, first key, 0); (-1, 0, 0, 0) past the end.
-__device__ __forceinline__ int4 f2_entry(const KernelArgs& a, int idx, int n_items) {
-  if (idx >= n_items) return make_int4(-1, 0, 0, 0);
-  const F2Item w = f2_item(a, idx);
-  const int2 r = a.q_tile_range[w.b * a.n_qt + w.t];
+// Ring entry of the c-th claim: (item, key tiles, first key, 0), or
+// (-1, 0, 0, 0) past the end.  Claims walk the query tiles in the metadata
+// pass's order (longest first), the head pairs of a tile one after another.
+__device__ __forceinline__ int4 f2_entry(const KernelArgs& a, int c, int n_items) {
+  if (c >= n_items) return make_int4(-1, 0, 0, 0);
+  const int hp = a.Hq / 2;
+  const int rank = c / hp;
+  const int w = a.q_order[rank];
+  const int2 r = a.q_tile_range[w];
   const int n = (r.y > r.x) ? (r.y - r.x + kTile - 1) / kTile : 0;
-  return make_int4(idx, n, r.x, 0);
+  return make_int4(w * hp + (c - rank * hp), n, r.x, 0);
 }
 
 // Per-row state of one softmax thread for one item.

@@ -157,11 +157,14 @@ struct MetaIn {
   int nblk;  // 1024-token blocks of the longer side
 };
 
+constexpr int kOrderBins = kMetaThreads;  // tile counts 0 .. kOrderBins - 1 (larger ones clamp)
+
 struct MetaShared {
   int sh[32];
   int shl[32];
   int carry_start, carry_end;
   int flag;
+  int bins[kOrderBins];
 };
 
 // Pass 1 for one (block, row, side) unit.
@@ -431,6 +434,56 @@ __device__ void meta_ranges(const KernelArgs& a, const MetaIn& in) {
   }
 }
 
+// Pass 5, run by the last block to finish pass 4: the query tiles in order
+// of decreasing KV-tile count (a counting sort; the order among equal counts
+// is not fixed and does not matter).  The persistent passes over query tiles
+// map their claim counter through it, so the longest items go out first and
+// the end of the grid is made of short ones.
+__device__ void meta_order(const KernelArgs& a, MetaShared& sm) {
+  const int n = a.B * a.n_qt;
+  auto key = [&](int w) -> int {
+    const int2 r = __ldcg(a.q_tile_range + w);  // written by other blocks: from L2
+    const int c = (r.y > r.x) ? (r.y - r.x + kTile - 1) / kTile : 0;
+    return min(c, kOrderBins - 1);
+  };
+  sm.bins[threadIdx.x] = 0;
+  __syncthreads();
+  for (int w = threadIdx.x; w < n; w += blockDim.x) atomicAdd(&sm.bins[key(w)], 1);
+  __syncthreads();
+  // start of each count's run: thread i owns count kOrderBins - 1 - i, so an
+  // exclusive prefix sum in thread order runs over decreasing counts
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int mine = sm.bins[kOrderBins - 1 - threadIdx.x];
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) sm.sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = sm.sh[lane];
+    int ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += v;
+    }
+    sm.shl[lane] = ti - t;  // exclusive over warps
+  }
+  __syncthreads();
+  const int start = sm.shl[warp] + incl - mine;
+  __syncthreads();
+  sm.bins[kOrderBins - 1 - threadIdx.x] = start;
+  __syncthreads();
+  int32_t* out = const_cast<int32_t*>(a.q_order);
+  for (int w = threadIdx.x; w < n; w += blockDim.x) {
+    const int pos = atomicAdd(&sm.bins[key(w)], 1);
+    if (ATTN_CHECK(a, span_ok(pos, 1, n), 0x7803)) out[pos] = w;
+  }
+}
+
 __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const KernelArgs a, const MetaIn in) {
   __shared__ MetaShared sm;
   sm103::grid_dep_launch();  // the forward may be scheduled now; it waits for this grid to finish
@@ -454,6 +507,16 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const KernelArgs a, 
   meta_match_chunks(a);
   if (!grid_barrier(a, 3, &sm.flag)) return;
   meta_ranges(a, in);
+  // the last block past pass 4 sees every tile range and orders the tiles
+  __threadfence();  // this thread's ranges reach L2 before the block counts itself done
+  __syncthreads();
+  if (threadIdx.x == 0)
+    sm.flag = (atomicAdd(&a.hdr->meta_done, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (sm.flag) {
+    __threadfence();
+    meta_order(a, sm);
+  }
 }
 
 int meta_max_blocks() {
