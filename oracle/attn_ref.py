@@ -49,6 +49,9 @@ What it computes (all in float64 on bf16-valued inputs):
 * Optionally per-head sink logits that join every softmax row as a column
   without a value vector, and their gradient (``attention_forward``,
   ``sink_gradient``; reading stated there).
+* An FP8 forward (``attention_forward_fp8``): Q, K, V given as E4M3 values with
+  one descale factor per tensor, P quantised to E4M3 before it meets V
+  (``e4m3_round``); reading stated there.
 
 Rows are processed one block of queries at a time and each block only touches
 the keys that are valid for at least one of its rows; since every softmax row is
@@ -269,6 +272,82 @@ def attention_forward(q, k, v, id_q, pos_q, id_kv, pos_kv, causal, scale, bias=N
                 if cols.size == 0:
                     continue
                 o[b, r0:r1, h] = p @ v[b, cols, g]
+    return o, lse
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) forward
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0  # 1.75 * 2^8: the largest finite E4M3 value
+P_SCALE = 256.0   # P is quantised as E4M3(256 * p), so p = 1 maps to 256
+
+
+def e4m3_round(x):
+    """Nearest E4M3 value (ties to even), saturating at +-448, from the format:
+    1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; no infinities;
+    normal values (1 + m/8) 2^e for e in [-6, 8] (the top code of e = 8 is
+    NaN, so the largest is 1.75 * 2^8 = 448), subnormal values k 2^-9 for
+    k = 0..7.  In every binade [2^e, 2^(e+1)) the spacing is 2^(e-3); below
+    2^-6 it is 2^-9."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)
+    quantum = np.exp2(e - 3)  # 2^-9 in the subnormal range (e clamped to -6)
+    r = np.rint(a / quantum) * quantum  # np.rint rounds halves to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(np.isnan(x), np.nan, np.copysign(r, x))
+
+
+def attention_forward_fp8(q8, k8, v8, descale_q, descale_k, descale_v, id_q, pos_q, id_kv,
+                          pos_kv, causal, scale, row_block=256):
+    """O [B,Sq,Hq,d_v] and LSE [B,Hq,Sq] of the FP8 forward.
+
+    The pages define attention in bf16 only; SURVEY's next step is an FP8
+    forward of the same computation.  Reading taken (the plainest one that
+    keeps every product in the 8-bit format):
+
+      inputs      q8, k8, v8 hold E4M3 values; the tensors they stand for are
+                  descale_q * q8, descale_k * k8, descale_v * v8
+      scores      S_ij = scale * descale_q * descale_k * <q8_i, k8_j>   (exact)
+      max, sum    m_i = max_j S_ij over valid j;  p_ij = exp(S_ij - m_i);
+                  l_i = sum_j p_ij  (p itself, before any rounding)
+      P to E4M3   P8_ij = E4M3(256 p_ij)  (p <= 1, so P8 <= 256 < 448)
+      output      O_i = descale_v * sum_j P8_ij v8_j / (256 l_i),
+                  LSE_i = m_i + ln l_i;  O_i = 0, LSE_i = -inf without valid j
+
+    The quantisation of P is taken against the row's final maximum (every
+    p_ij <= 1), so the result does not depend on how the keys are blocked.
+    Everything else is float64."""
+    B, Sq, Hq, _ = q8.shape
+    _, Skv, Hkv, d_v = v8.shape
+    group = Hq // Hkv
+    sc = scale * descale_q * descale_k
+    o = np.zeros((B, Sq, Hq, d_v))
+    lse = np.full((B, Hq, Sq), -np.inf)
+    for b in range(B):
+        mask = valid_pairs(id_q[b], pos_q[b], id_kv[b], pos_kv[b], causal)
+        for h in range(Hq):
+            g = h // group
+            for r0 in range(0, Sq, row_block):
+                r1 = min(Sq, r0 + row_block)
+                mrow = mask[r0:r1]
+                cols = np.nonzero(mrow.any(axis=0))[0]
+                if cols.size == 0:
+                    continue
+                s = sc * (q8[b, r0:r1, h] @ k8[b, cols, g].T)
+                s = np.where(mrow[:, cols], s, -np.inf)
+                m = s.max(axis=1)
+                fin = np.isfinite(m)
+                p = np.zeros_like(s)
+                p[fin] = np.exp(s[fin] - m[fin, None])
+                l = p.sum(axis=1)
+                p8 = e4m3_round(P_SCALE * p)
+                out = np.zeros((r1 - r0, d_v))
+                out[fin] = descale_v * (p8[fin] @ v8[b, cols, g]) / (P_SCALE * l[fin, None])
+                o[b, r0:r1, h] = out
+                lse[b, h, r0:r1][fin] = m[fin] + np.log(l[fin])
     return o, lse
 
 
