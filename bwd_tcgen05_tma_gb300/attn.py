@@ -14,13 +14,13 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_sm103.so")
 
-ATTN_PARAMS_VERSION = 5
+ATTN_PARAMS_VERSION = 6
 
 LAYOUTS = {"3HD": 0, "HD_2HD": 1, "HD_HD_HD": 2}
 FORMATS = {"BSHD": 0, "THD_SEGMENTS": 1, "THD_CU_SEQLENS": 2}
 MASKS = {"NONE": 0, "CAUSAL": 1, "PADDING": 2, "PADDING_CAUSAL": 3}
 DQ_MODES = {"atomic": 0, "deterministic": 1}
-DTYPES = {"bf16": 0, "fp16": 1}
+DTYPES = {"bf16": 0, "fp16": 1, "fp8_e4m3": 2}
 STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
           3: "ATTN_ERR_SHAPE_MISMATCH", 4: "ATTN_ERR_WORKSPACE_TOO_SMALL", 5: "ATTN_ERR_CUDA",
           6: "ATTN_ERR_DEVICE_TIMEOUT", 7: "ATTN_ERR_DEVICE_BOUNDS"}
@@ -58,6 +58,7 @@ class attn_params_t(ctypes.Structure):
         ("bottom_right", c_i32),
         ("dtype", c_i32),
         ("test_wait_timeout", c_i32),
+        ("descale_q", c_f32), ("descale_k", c_f32), ("descale_v", c_f32),
     ]
 
 
@@ -155,13 +156,15 @@ def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, 
                 q_seg_ids=None, q_seg_pos=None, kv_seg_ids=None, kv_seg_pos=None,
                 cu_seqlens_q=None, cu_seqlens_kv=None, bias=None, dq_mode="deterministic",
                 force_general_path=False, metadata_from_forward=False, max_logit=None,
-                sink=None, dsink=None, window=None, bottom_right=False, dtype="bf16"):
+                sink=None, dsink=None, window=None, bottom_right=False, dtype="bf16",
+                descale=(1.0, 1.0, 1.0)):
     """Fill an ``attn_params_t`` from tensors (any object with data_ptr/shape).
     max_logit: optional fp32 [B, Hq] tensor the forward fills; sink: optional
     fp32 [Hq] sink logits; dsink: optional fp32 [Hq] tensor the backward fills
     with their gradient; window: optional (left, right) band, None for an
-    unbounded side; bottom_right: align positions by Skv - Sq; dtype: "bf16" or
-    "fp16", the element type of every 16-bit tensor (see attn.h)."""
+    unbounded side; bottom_right: align positions by Skv - Sq; dtype: "bf16",
+    "fp16" or "fp8_e4m3" (forward only: Q / K / V as E4M3 codes, O in bf16);
+    descale: the (q, k, v) factors the E4M3 codes stand scaled by (see attn.h)."""
     p = attn_params_t()
     p.struct_version = ATTN_PARAMS_VERSION
     p.fmt = FORMATS[fmt]
@@ -202,6 +205,7 @@ def make_params(*, layout, fmt, mask, B, Sq, Skv, Hq, Hkv, d_qk, d_v, scale, q, 
         p.window_right = -1 if right is None else int(right)
     p.bottom_right = 1 if bottom_right else 0
     p.dtype = DTYPES[dtype]
+    p.descale_q, p.descale_k, p.descale_v = (float(x) for x in descale)
     return p
 
 

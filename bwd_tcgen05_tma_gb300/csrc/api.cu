@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -26,7 +27,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 struct Plan {
   size_t hdr, q_id, q_pos, seg_lo, seg_hi, kv_id, kv_pos, kv_seg_lo, kv_seg_hi;
-  size_t q_chunk, kv_chunk, q_range, kv_range, q_order, meta_scan;
+  size_t q_chunk, kv_chunk, q_range, kv_range, q_order, meta_scan, vt;
   size_t fwd_total;
   size_t lse2, dvec, dq_acc, dbias_acc, sink_part;
   size_t bwd_total;
@@ -35,6 +36,14 @@ struct Plan {
 bool effective_atomic(const attn_params_t* p) {
   return p->dq_mode == ATTN_DQ_ATOMIC && p->d_qk <= 128;
 }
+
+// Bytes per element of Q / K / V.
+int64_t elem_bytes(const attn_params_t* p) { return p->dtype == ATTN_DTYPE_FP8_E4M3 ? 1 : 2; }
+
+// Keys per row of a transposed-V plane (FP8 forward): Skv rounded up to a
+// whole tile, plus one tile, so that a 128-key box starting at any key below
+// Skv stays inside the row.
+int64_t vt_pad(const attn_params_t* p) { return ((p->Skv + kTile - 1) / kTile) * kTile + kTile; }
 
 bool dbias_needs_acc(const attn_params_t* p) {
   return p->bias != nullptr && ((p->bias_b == 1 && p->B > 1) || (p->bias_h == 1 && p->Hq > 1));
@@ -61,6 +70,8 @@ Plan make_plan(const attn_params_t* p) {
   pl.kv_range = o; o = up(o + B * nkt * sizeof(int2));
   pl.q_order = o; o = up(o + B * nqt * 4);
   pl.meta_scan = o; o = up(o + 2 * B * ((std::max(Sq, Skv) + 1023) / 1024) * sizeof(int2));
+  pl.vt = o;  // FP8 forward only: V^T planes [B * Hkv][d_v][vt_pad], one byte each
+  if (p->dtype == ATTN_DTYPE_FP8_E4M3) o = up(o + B * (size_t)p->Hkv * p->d_v * vt_pad(p));
   pl.fwd_total = o;
   pl.lse2 = o; o = up(o + B * p->Hq * Sq * 4);
   pl.dvec = o; o = up(o + B * p->Hq * Sq * 4);
@@ -123,7 +134,14 @@ attn_status_t validate(const attn_params_t* p) {
   }
   const bool causal = p->mask == ATTN_MASK_CAUSAL || p->mask == ATTN_MASK_PADDING_CAUSAL;
   if (p->band && causal && p->window_right > 0) return ATTN_ERR_INVALID_ARG;
-  if (p->dtype != ATTN_DTYPE_BF16 && p->dtype != ATTN_DTYPE_FP16) return ATTN_ERR_INVALID_ARG;
+  if (p->dtype != ATTN_DTYPE_BF16 && p->dtype != ATTN_DTYPE_FP16 && p->dtype != ATTN_DTYPE_FP8_E4M3)
+    return ATTN_ERR_INVALID_ARG;
+  if (p->dtype == ATTN_DTYPE_FP8_E4M3) {
+    const float d[3] = {p->descale_q, p->descale_k, p->descale_v};
+    for (float x : d)
+      if (!(x > 0.f) || !std::isfinite(x)) return ATTN_ERR_INVALID_ARG;
+    if (p->d_qk != 128 || p->d_v != 128 || p->bias || p->sink) return ATTN_ERR_UNSUPPORTED;
+  }
   if (p->bias) {
     if (!aligned16(p->bias)) return ATTN_ERR_INVALID_ARG;
     if (!(p->bias_b == 1 || p->bias_b == p->B) || !(p->bias_h == 1 || p->bias_h == p->Hq))
@@ -135,19 +153,20 @@ attn_status_t validate(const attn_params_t* p) {
 attn_status_t resolve(const attn_params_t* p, void* dq, void* dk, void* dv, attn_resolved_t* r) {
   const char* q = static_cast<const char*>(p->q);
   const int64_t Hq = p->Hq, Hkv = p->Hkv, dqk = p->d_qk, dvv = p->d_v;
+  const int64_t es = elem_bytes(p);  // byte offsets of the packed slices
   std::memset(r, 0, sizeof(*r));
   switch (p->layout) {
     case ATTN_LAYOUT_3HD: {
       const int64_t W = Hq * dqk + Hkv * dqk + Hkv * dvv;
       r->q = q;
-      r->k = q + Hq * dqk * 2;
-      r->v = q + (Hq * dqk + Hkv * dqk) * 2;
+      r->k = q + Hq * dqk * es;
+      r->v = q + (Hq * dqk + Hkv * dqk) * es;
       r->q_token_stride = r->k_token_stride = r->v_token_stride = W;
       if (dq) {
         char* d = static_cast<char*>(dq);
         r->dq = d;
-        r->dk = d + Hq * dqk * 2;
-        r->dv = d + (Hq * dqk + Hkv * dqk) * 2;
+        r->dk = d + Hq * dqk * es;
+        r->dv = d + (Hq * dqk + Hkv * dqk) * es;
       }
       break;
     }
@@ -155,13 +174,13 @@ attn_status_t resolve(const attn_params_t* p, void* dq, void* dk, void* dv, attn
       const char* k = static_cast<const char*>(p->k);
       r->q = q;
       r->k = k;
-      r->v = k + Hkv * dvv * 2;  // stride from v_head_dim
+      r->v = k + Hkv * dvv * es;  // stride from v_head_dim
       r->q_token_stride = Hq * dqk;
       r->k_token_stride = r->v_token_stride = 2 * Hkv * dvv;
       r->dq = dq;
       if (dk) {
         r->dk = dk;
-        r->dv = static_cast<char*>(dk) + Hkv * dvv * 2;
+        r->dv = static_cast<char*>(dk) + Hkv * dvv * es;
       }
       break;
     }
@@ -203,6 +222,35 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int D,
   cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, type, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over a token-major tensor of one-byte elements (FP8): dims {D, H,
+// T}, box {128, 1, rows} (one 128-byte swizzle row per token).
+bool make_map8(CUtensorMap* m, const void* base, int D, int H, int64_t T, int64_t tok_stride,
+               int rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)tok_stride};
+  cuuint32_t box[3] = {128, 1, (cuuint32_t)rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over the transposed-V planes of the FP8 forward: dims {vt_pad
+// keys, d_v, planes}, box {128 keys, 128 dims, 1}.
+bool make_map_vt(CUtensorMap* m, const void* base, int64_t pad, int d_v, int64_t planes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)pad, (cuuint64_t)d_v, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)pad, (cuuint64_t)(pad * d_v)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -461,6 +509,29 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
   KernelArgs a;
   std::memset(&a, 0, sizeof(a));
   fill_common(a, p, static_cast<char*>(ws), pl);
+  if (p->dtype == ATTN_DTYPE_FP8_E4M3) {
+    // V^T planes first (they depend on nothing the metadata pass writes),
+    // then the metadata, then the two-pass forward
+    a.vt = reinterpret_cast<uint8_t*>(static_cast<char*>(ws) + pl.vt);
+    a.vt_pad = static_cast<int>(vt_pad(p));
+    a.vt_src = static_cast<const uint8_t*>(r.v);
+    a.vt_src_stride = r.v_token_stride;
+    a.fp8_sc2 = p->scale * p->descale_q * p->descale_k * 1.4426950408889634f;
+    a.fp8_dv = p->descale_v;
+    if (!make_map8(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
+        !make_map8(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
+        !make_map_vt(&a.tm_v, a.vt, a.vt_pad, p->d_v, (int64_t)p->B * p->Hkv))
+      return ATTN_ERR_CUDA;
+    a.o = static_cast<bf16*>(o);
+    a.lse = lse;
+    a.max_logit = p->max_logit;
+    trace(ATTN_TRACE_FWD, false, st);
+    if (launch_vt_transpose(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
+    if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
+    if (launch_fwd_fp8(a, sm_count(), st) != cudaSuccess) return ATTN_ERR_CUDA;
+    trace(ATTN_TRACE_FWD, true, st);
+    return ATTN_OK;
+  }
   const CUtensorMapDataType mt = map_type(p);
   if (!make_map(&a.tm_q, mt, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
       !make_map(&a.tm_k, mt, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
@@ -483,6 +554,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
                        void* stream) {
   attn_status_t s = validate(p);
   if (s != ATTN_OK) return s;
+  if (p->dtype == ATTN_DTYPE_FP8_E4M3) return ATTN_ERR_UNSUPPORTED;  // forward only
   if (!o || !d_o || !lse || !ws || !aligned16(o) || !aligned16(d_o) ||
       (reinterpret_cast<uintptr_t>(ws) % kAlign))
     return ATTN_ERR_INVALID_ARG;
@@ -667,6 +739,7 @@ extern "C" attn_status_t attn_fwd_noalloc(const attn_params_t* p, void* o, float
                                           void* stream) {
   attn_status_t s = validate(p);
   if (s != ATTN_OK) return s;
+  if (p->dtype == ATTN_DTYPE_FP8_E4M3) return ATTN_ERR_UNSUPPORTED;  // workspace entry points only
   if (!o || !lse || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
   const Plan pl = make_plan(p);
   if (pl.fwd_total > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE_TOO_SMALL;

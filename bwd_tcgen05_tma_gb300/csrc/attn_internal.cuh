@@ -287,6 +287,15 @@ struct KernelArgs {
   int grad_st32;       // 1: dQ/dK/dV rows start 32-byte aligned (256-bit stores)
   int dkdv_batch_loop;  // 1: one dK/dV work item loops over every batch row
   int dkdv_head_loop;   // 1: one dK/dV work item loops over every KV head
+
+  // FP8 (E4M3) forward: tm_q / tm_k map the one-byte Q and K, tm_v the
+  // transposed V in the workspace (planes of [128 d][vt_pad keys])
+  float fp8_sc2;               // scale * descale_q * descale_k * log2(e)
+  float fp8_dv;                // descale_v
+  const uint8_t* vt_src;       // V (E4M3), its token-row stride in elements
+  int64_t vt_src_stride;
+  uint8_t* vt;                 // [B * Hkv][128][vt_pad]
+  int vt_pad;                  // keys per plane row: Skv rounded up to 128, plus 128
 };
 
 // Opt-in timeline for pipeline debugging (-DATTN_TIMELINE builds only): the
@@ -563,6 +572,9 @@ cudaError_t launch_meta(const KernelArgs& a, int fmt, const int32_t* q_ids, cons
 cudaError_t launch_fwd(const KernelArgs& a, int num_sms, cudaStream_t st);
 // Forward over pairs of query heads of one KV group (even group size, d <= 128).
 cudaError_t launch_fwd2t(const KernelArgs& a, int num_sms, cudaStream_t st);
+// FP8 forward (d_qk = d_v = 128) and the transposed copy of V it reads.
+cudaError_t launch_vt_transpose(const KernelArgs& a, cudaStream_t st);
+cudaError_t launch_fwd_fp8(const KernelArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st);
 cudaError_t launch_sink_reduce(const KernelArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const KernelArgs& a, bool atomic_dq, int num_sms, cudaStream_t st);

@@ -304,6 +304,30 @@ SM103_DEV void mma_ss_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint
   }
 }
 
+// kind::f8f6f4 with both operands one 128-byte-swizzled K-major row of 128
+// one-byte elements per M / N row: four K slices of 32, 32 bytes apart.
+SM103_DEV void mma_f8_ss4_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0, p1;\n\t.reg .b32 alo, ahi, blo, bhi;\n\t.reg .b64 ad, bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.ne.b32 p1, %5, 0;\n\t"
+      "mov.b64 {alo, ahi}, %1;\n\tmov.b64 {blo, bhi}, %2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p0;\n\t"
+      "add.u32 alo, alo, 2;\n\tadd.u32 blo, blo, 2;\n\t"
+      "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %3, p1;\n\t"
+      "add.u32 alo, alo, 2;\n\tadd.u32 blo, blo, 2;\n\t"
+      "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %3, p1;\n\t"
+      "add.u32 alo, alo, 2;\n\tadd.u32 blo, blo, 2;\n\t"
+      "mov.b64 ad, {alo, ahi};\n\tmov.b64 bd, {blo, bhi};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %3, p1;\n\t"
+      "}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(1u)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] B[smem] over NK K-slices (A: packed 16-bit pairs).
 template <int NK, int JP, int AS, int AJ, int BS, int BJ>
 SM103_DEV void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,

@@ -64,8 +64,27 @@ def f16_round(x):
     return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
 
 
+def e4m3_codes(x):
+    """E4M3 codes (uint8) of float32 values within +-448, by PyTorch's
+    float8_e4m3fn conversion (round to nearest even)."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def e4m3_value(codes):
+    """float32 values of E4M3 codes."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.float().numpy()
+
+
 def round_to(x, dtype):
-    """Nearest value of the element type ("bf16" or "fp16"), as float32."""
+    """Nearest value of the element type ("bf16", "fp16" or "fp8_e4m3"), as float32."""
+    if dtype == "fp8_e4m3":
+        return e4m3_value(e4m3_codes(x))
     return bf16_round(x) if dtype == "bf16" else f16_round(x)
 
 
@@ -204,9 +223,12 @@ def synth(name, *, B, Sq, Skv, Hq, Hkv, d_qk, d_v, layout, fmt, causal, seed,
                 ki[b], kp[b] = ids_pos_from_lengths(klens, Skv)
         c.q_ids, c.q_pos, c.kv_ids, c.kv_pos = qi, qp, ki, kp
     c.buffers = make_buffers(rng, layout, B, Sq, Skv, Hq, Hkv, d_qk, d_v, dtype)
-    c.do = _normal_bf16(rng, (B, Sq, Hq, d_v), dtype=dtype)
+    # dO and the bias stay 16-bit when Q / K / V are E4M3 (the FP8 path is a
+    # forward; O is bf16)
+    dt16 = "bf16" if dtype == "fp8_e4m3" else dtype
+    c.do = _normal_bf16(rng, (B, Sq, Hq, d_v), dtype=dt16)
     if bias_shape is not None:
-        c.bias = _normal_bf16(rng, bias_shape, std=bias_std, dtype=dtype)
+        c.bias = _normal_bf16(rng, bias_shape, std=bias_std, dtype=dt16)
     return c
 
 

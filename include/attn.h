@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define ATTN_PARAMS_VERSION 5
+#define ATTN_PARAMS_VERSION 6
 
 typedef enum {
   ATTN_OK = 0,
@@ -113,7 +113,20 @@ typedef enum {
 typedef enum { ATTN_DQ_ATOMIC = 0, ATTN_DQ_DETERMINISTIC = 1 } attn_dq_mode_t;
 
 /* 16-bit element type of Q/K/V/O/dO/bias and of all gradients. */
-typedef enum { ATTN_DTYPE_BF16 = 0, ATTN_DTYPE_FP16 = 1 } attn_dtype_t;
+/* Element types.  ATTN_DTYPE_FP8_E4M3: forward only, Q / K / V hold E4M3
+ * codes (one byte each) standing for descale_q * Q, descale_k * K and
+ * descale_v * V; O is written in bf16 and LSE in fp32.  Reading (the pages use
+ * bf16 only): scores are the exact products of the E4M3 values accumulated in
+ * fp32, P enters P V as E4M3(256 p) with p = exp(s - m) against the row's
+ * final maximum m, the normaliser l sums the p before rounding, and
+ * O = descale_v * sum_j P8_j V_j / (256 l).  Needs d_qk = d_v = 128, no bias,
+ * no sink (ATTN_ERR_UNSUPPORTED otherwise, and from attn_bwd and
+ * attn_fwd_noalloc). */
+typedef enum {
+  ATTN_DTYPE_BF16 = 0,
+  ATTN_DTYPE_FP16 = 1,
+  ATTN_DTYPE_FP8_E4M3 = 2
+} attn_dtype_t;
 
 typedef struct {
   int32_t struct_version; /* = ATTN_PARAMS_VERSION */
@@ -187,9 +200,10 @@ typedef struct {
   int32_t window_left;
   int32_t window_right;
   int32_t bottom_right;
-  /* attn_dtype_t of every 16-bit tensor (zero: bf16).  An adjacent precision
-   * of the same computation (the pages use bf16 only); ATTN_ERR_INVALID_ARG
-   * for other values. */
+  /* attn_dtype_t of Q, K, V, O, dO, bias and the gradients (zero: bf16).  An
+   * adjacent precision of the same computation (the pages use bf16 only);
+   * with ATTN_DTYPE_FP8_E4M3, Q / K / V are E4M3 and O is bf16 (see
+   * attn_dtype_t).  ATTN_ERR_INVALID_ARG for other values. */
   int32_t dtype;
   /* Testing knob for the failure path (zero in normal use).  Nonzero: the
    * forward kernel for query heads in pairs (even GQA group size, head dims
@@ -199,6 +213,12 @@ typedef struct {
    * writing O or LSE.  attn_read_status reports it; the next call on the
    * workspace starts from a clear status.  No fault, trap or endless wait. */
   int32_t test_wait_timeout;
+  /* ATTN_DTYPE_FP8_E4M3 only: the factors the E4M3 Q, K, V codes stand
+   * scaled by (the tensors are descale_x times the codes' values); positive
+   * and finite (ATTN_ERR_INVALID_ARG otherwise).  Ignored for other types. */
+  float descale_q;
+  float descale_k;
+  float descale_v;
 } attn_params_t;
 
 /* Which metadata path the device chose (read back by attn_read_status). */

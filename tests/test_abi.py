@@ -203,9 +203,51 @@ def test_band_validation(lib):
 
 def test_dtype_validation(lib):
     p = params()
-    for dt, ok in ((0, True), (1, True), (2, False), (-1, False)):
+    p.descale_q = p.descale_k = p.descale_v = 1.0
+    for dt, ok in ((0, True), (1, True), (2, True), (3, False), (-1, False)):
         p.dtype = dt
         assert (A.attn_fwd_workspace_size(p) > 0) == ok
+
+
+def test_fp8_forward_validation(lib):
+    """E4M3 forward: descale factors positive and finite (INVALID_ARG),
+    head dims 128 and no bias or sink (UNSUPPORTED), forward only (the
+    backward and the no-allocation entry point return UNSUPPORTED), and a
+    workspace that holds the transposed V planes."""
+    def fp8(**kw):
+        p = params(**kw)
+        p.dtype = 2
+        p.descale_q, p.descale_k, p.descale_v = 0.5, 2.0, 1.0
+        return p
+
+    p = fp8()
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) > 0
+    pb = params()
+    # one byte per element of V^T: B * Hkv * d_v * (Skv rounded to 128, plus 128)
+    assert (A.attn_fwd_workspace_size(p) - A.attn_fwd_workspace_size(pb)
+            >= 2 * 2 * 128 * (256 + 128))
+    for field, val in (("descale_q", 0.0), ("descale_k", -1.0), ("descale_v", float("inf")),
+                       ("descale_v", float("nan"))):
+        q = fp8()
+        setattr(q, field, val)
+        assert A.attn_fwd_workspace_size(q) == 0, field
+        assert lib.attn_resolve_layout(ctypes.byref(q), None, None, None,
+                                       ctypes.byref(A.attn_resolved_t())) == 1
+    r = A.attn_resolved_t()
+    assert lib.attn_resolve_layout(ctypes.byref(fp8(d_qk=64, d_v=64)), None, None, None,
+                                   ctypes.byref(r)) == 2
+    q = fp8()
+    q.bias = FAKE
+    q.bias_b, q.bias_h = 1, 8
+    assert lib.attn_resolve_layout(ctypes.byref(q), None, None, None, ctypes.byref(r)) == 2
+    assert _bwd(lib, fp8()) == 2
+    assert lib.attn_fwd_noalloc(ctypes.byref(fp8()), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE),
+                                None) == 2
+    # packed layouts resolve with one-byte elements
+    q = fp8(layout="3HD")
+    assert lib.attn_resolve_layout(ctypes.byref(q), None, None, None, ctypes.byref(r)) == 0
+    assert r.k - r.q == 8 * 128 and r.v - r.q == (8 + 2) * 128
+    assert r.q_token_stride == (8 + 2 + 2) * 128
     m = A.make_params(layout="HD_HD_HD", fmt="BSHD", mask="NONE", B=1, Sq=8, Skv=8, Hq=1, Hkv=1,
                       d_qk=64, d_v=64, scale=0.1, q=None, dtype="fp16")
     assert m.dtype == 1

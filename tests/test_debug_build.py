@@ -78,3 +78,12 @@ def test_no_check_fires_fp16(debug_lib):
     case = _case("c129h", B=1, Sq=129, Skv=129, Hq=4, Hkv=2, d_qk=64, d_v=64, seed=87,
                  dtype="fp16")
     _run(case, "atomic", False)
+
+
+def test_no_check_fires_fp8(debug_lib):
+    """The E4M3 forward on segments whose starts are not 16-aligned, packed
+    QKV, GQA, causal: every copy (keys are the innermost coordinate of the
+    transposed-V copies) and store passes its check."""
+    from test_fp8 import CASES as FP8_CASES, _run as fp8_run
+
+    fp8_run(FP8_CASES["thd_gqa_3hd"]())
