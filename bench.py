@@ -76,8 +76,9 @@ KERNEL_SOURCES = {
     "dq": ("dq128.cu",),
     "fwd": ("fwd2t.cu",),
     "bwd_pre": ("bwd.cu",),
+    "fwd_fp8": ("fwd_fp8.cu",),
 }
-COMMON_SOURCES = ("attn_internal.cuh", "sm103_ptx.cuh")
+COMMON_SOURCES = ("attn_internal.cuh", "sm103_ptx.cuh", "debug_checks.h")
 
 
 def source_hash(kernel):
@@ -253,6 +254,47 @@ class Problem:
         if s != 0:
             raise RuntimeError(f"device status {s}")
         return st
+
+
+class Fp8Forward:
+    """The E4M3 forward on the same workload: Q / K / V rounded to E4M3 codes
+    (descale factors 1), O in bf16.  Runs only where the FP8 path applies
+    (d_qk = d_v = 128, no bias)."""
+
+    def __init__(self, case, prob):
+        import torch
+
+        from bwd_tcgen05_tma_gb300 import attn as A
+        from bwd_tcgen05_tma_gb300 import inputs as I
+
+        c = case
+        self.codes = {k: torch.from_numpy(I.e4m3_codes(v)).cuda() for k, v in c.buffers.items()}
+        t = self.codes
+        q, k, v = {"3HD": (t.get("qkv"), None, None), "HD_2HD": (t.get("q"), t.get("kv"), None),
+                   "HD_HD_HD": (t.get("q"), t.get("k"), t.get("v"))}[c.layout]
+        d = prob.dev  # the metadata tensors of the 16-bit problem, kept alive there
+        self.params = A.make_params(
+            layout=c.layout, fmt=c.fmt, mask=c.mask, B=c.B, Sq=c.Sq, Skv=c.Skv, Hq=c.Hq,
+            Hkv=c.Hkv, d_qk=c.d_qk, d_v=c.d_v, scale=c.scale, q=q, k=k, v=v,
+            q_seg_ids=d.get("q_ids"), q_seg_pos=d.get("q_pos"), kv_seg_ids=d.get("kv_ids"),
+            kv_seg_pos=d.get("kv_pos"), dtype="fp8_e4m3", descale=(1.0, 1.0, 1.0))
+        self.ws = torch.empty(A.attn_fwd_workspace_size(self.params), dtype=torch.uint8,
+                              device="cuda")
+        self.o = torch.empty((c.B * c.Sq, c.Hq, c.d_v), dtype=torch.bfloat16, device="cuda")
+        self.lse = torch.empty((c.B, c.Hq, c.Sq), dtype=torch.float32, device="cuda")
+        self.A = A
+
+    @staticmethod
+    def applies(case):
+        return case.d_qk == 128 and case.d_v == 128 and case.bias is None
+
+    def fwd(self):
+        self.A.attn_fwd(self.params, self.o, self.lse, self.ws)
+
+    def check_status(self):
+        s, _ = self.A.attn_read_status(self.ws)
+        if s != 0:
+            raise RuntimeError(f"device status {s} (FP8 forward)")
 
 
 class E2EPipeline:
@@ -614,6 +656,23 @@ def main():
         line["other_dq_mode"] = {"dq_mode": other, "value": aggregate_tflops(world, total_flops, t_d),
                                  "unit": "TFLOP/s", "ms_per_step": t_d}
         del alt
+        if Fp8Forward.applies(case):
+            # the FP8 forward (metadata, V transpose, two-pass forward) beside
+            # the bf16 one; its tensor peak is the bf16 one times the nominal
+            # dense ratio 4.5 / 2.25 PFLOP/s
+            f8 = Fp8Forward(case, prob)
+            for _ in range(3):
+                f8.fwd()
+            t_8 = max_over_ranks(timed(f8.fwd, max(20, args.steps // 4), stream, barrier))
+            f8.check_status()
+            v8 = aggregate_tflops(world, fwd_flops, t_8)
+            line["fp8_forward"] = {
+                "value": v8, "unit": "TFLOP/s", "ms": t_8, "dtype": "e4m3 (O bf16)",
+                "flops": "the bf16 forward's (4 d per unmasked pair and head; the row-maximum "
+                         "pass recomputes S and is not credited)",
+                "pct_of_fp8_peak": v8 / (2.0 * peak),
+                "peak_basis": f"2 x {peak_key} = {2.0 * peak} TFLOP/s (nominal fp8/bf16 ratio)"}
+            del f8
 
     if not args.no_e2e:
         pipe = E2EPipeline([prob, Problem(case, args.dq_mode, args.force_general)])
