@@ -287,6 +287,7 @@ struct KernelArgs {
   int grad_st32;       // 1: dQ/dK/dV rows start 32-byte aligned (256-bit stores)
   int dkdv_batch_loop;  // 1: one dK/dV work item loops over every batch row
   int dkdv_head_loop;   // 1: one dK/dV work item loops over every KV head
+  int dkdv_bq;          // query-tile rows of the dK/dV pass in use (128 or 64)
 
   // FP8 (E4M3) forward: tm_q / tm_k map the one-byte Q and K, tm_v the
   // transposed V in the workspace (planes of [128 d][vt_pad keys])
@@ -541,6 +542,43 @@ __device__ __forceinline__ int dkdv_q_tiles(const KernelArgs& a, int b, int t, i
   const int2 r = a.kv_tile_range[b * a.n_kt + t];
   q_lo = r.x;
   return (r.y > r.x) ? (r.y - r.x + BQ - 1) / BQ : 0;
+}
+
+// Broadcast dBias (an fp32 accumulator summed over batch rows and/or heads):
+// the dK/dV pass that owns KV tile t writes the query rows its BQ-row query
+// tiles cover, [q_lo, q_lo + nq * BQ) within [0, Sq), for every batch row it
+// visits.  The first (batch row, head) of a work item to reach a row stores
+// it, the later ones add to it, and the conversion writes 0 where no pass
+// wrote, so the accumulator needs no clearing.
+//
+// Rows [i0, i0 + 32) of the current (batch row b, head g * G + hh) step that
+// an earlier step of the same work item has written already, as a bit mask.
+template <int BQ>
+__device__ __forceinline__ uint32_t dbias_rows_written_before(const KernelArgs& a, int b0, int b,
+                                                              int g0, int g, int hh, int t, int i0) {
+  if (a.bias_h == 1 && (g > g0 || hh > 0)) return ~0u;  // the item's first head wrote them
+  uint32_t seen = 0u;
+  if (a.bias_b == 1) {
+    for (int bp = b0; bp < b; ++bp) {
+      int q_lo;
+      const int nq = dkdv_q_tiles<BQ>(a, bp, t, q_lo);
+      if (nq > 0) seen |= static_cast<uint32_t>(range_bits64(q_lo - i0, q_lo + nq * BQ - i0));
+    }
+  }
+  return seen;
+}
+
+// Whether any dK/dV step wrote query row i of accumulator slice bb for KV
+// tile t (the batch rows summed into slice bb: bb itself, or all of them when
+// the bias is broadcast over the batch).
+__device__ __forceinline__ bool dbias_row_written(const KernelArgs& a, int bb, int i, int t) {
+  const int b0 = a.bias_b > 1 ? bb : 0, b1 = a.bias_b > 1 ? bb + 1 : a.B;
+  for (int b = b0; b < b1; ++b) {
+    const int2 r = a.kv_tile_range[b * a.n_kt + t];
+    if (r.y > r.x && i >= r.x && i < r.x + ((r.y - r.x + a.dkdv_bq - 1) / a.dkdv_bq) * a.dkdv_bq)
+      return true;
+  }
+  return false;
 }
 
 

@@ -164,20 +164,34 @@ __global__ void dq_convert_kernel(const KernelArgs a) {
 
 template <class E>
 __global__ void dbias_convert_kernel(const KernelArgs a) {
-  // four elements per thread and step: one 16-byte load, one 8-byte store
-  // (both buffers are 16-byte aligned); the last n % 4 elements one by one
+  // Elements no dK/dV step wrote are 0 and are not read (the accumulator is
+  // not cleared).  With Skv a multiple of 4, four elements of one row per
+  // thread and step: one 16-byte load, one 8-byte store (both buffers are
+  // 16-byte aligned, and the four share a KV tile); otherwise one by one.
   const int64_t n = (int64_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
-  const int64_t n4 = n / 4;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t t0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  for (int64_t v = t0; v < n4; v += stride) {
-    const float4 x = reinterpret_cast<const float4*>(a.dbias_acc)[v];
-    uint2 o;
-    o.x = E::pack(x.x, x.y);
-    o.y = E::pack(x.z, x.w);
-    reinterpret_cast<uint2*>(a.dbias)[v] = o;
+  const int64_t plane = (int64_t)a.bias_h * a.Sq * a.Skv;
+  auto written = [&](int64_t v) -> bool {
+    const int64_t row = v / a.Skv;
+    const int j = static_cast<int>(v - row * a.Skv);
+    const int i = static_cast<int>(row % a.Sq);
+    return dbias_row_written(a, static_cast<int>(v / plane), i, j / kTile);
+  };
+  if (a.Skv % 4 == 0) {
+    const int64_t n4 = n / 4;
+    for (int64_t v = t0; v < n4; v += stride) {
+      uint2 o = make_uint2(0u, 0u);
+      if (written(4 * v)) {
+        const float4 x = reinterpret_cast<const float4*>(a.dbias_acc)[v];
+        o.x = E::pack(x.x, x.y);
+        o.y = E::pack(x.z, x.w);
+      }
+      reinterpret_cast<uint2*>(a.dbias)[v] = o;
+    }
+  } else {
+    for (int64_t v = t0; v < n; v += stride) E::st(a.dbias + v, written(v) ? a.dbias_acc[v] : 0.f);
   }
-  for (int64_t v = 4 * n4 + t0; v < n; v += stride) E::st(a.dbias + v, a.dbias_acc[v]);
 }
 
 int blocks_for(int64_t n, int per_block) {
@@ -196,10 +210,7 @@ cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st
   if (a.dbias_mode == 1) {
     e = cudaMemsetAsync(a.dbias, 0, nb * sizeof(bf16), st);
     if (e != cudaSuccess) return e;
-  } else if (a.dbias_mode == 2) {
-    e = cudaMemsetAsync(a.dbias_acc, 0, nb * sizeof(float), st);
-    if (e != cudaSuccess) return e;
-  }
+  }  // the fp32 accumulator of a broadcast dBias is not cleared: see dbias_row_written
   const int mode = zero_dq_acc ? 0 : 1;
   if (a.Hq > kPreMaxH) return cudaErrorInvalidValue;  // rejected on the host before launch
   const int64_t ntok = (int64_t)a.B * a.Sq;

@@ -554,14 +554,20 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                       if (qh + q * 32 + c < a.Sq) E::st(dpb + (int64_t)c * a.Skv, ds[c]);
                   } else {
                     float* dpb = a.dbias_acc + (bias_base + qh + q * 32) * a.Skv + kj;
-                    // eight loads in flight before their stores (a store between
-                    // two loads would serialise them: the addresses may alias)
+                    // rows no earlier step of this item wrote start from 0 (the
+                    // accumulator is not cleared); eight loads in flight before
+                    // their stores (a store between two loads would serialise
+                    // them: the addresses may alias)
+                    const uint32_t seen =
+                        dbias_rows_written_before<kQ>(a, w.b0, b, w.g0, g, hh, w.t, qh + q * 32);
 #pragma unroll
                     for (int c8 = 0; c8 < 32; c8 += 8) {
                       float acc[8];
 #pragma unroll
                       for (int c = 0; c < 8; ++c)
-                        acc[c] = (qh + q * 32 + c8 + c < a.Sq) ? dpb[(int64_t)(c8 + c) * a.Skv] : 0.f;
+                        acc[c] = (qh + q * 32 + c8 + c < a.Sq && ((seen >> (c8 + c)) & 1u))
+                                     ? dpb[(int64_t)(c8 + c) * a.Skv]
+                                     : 0.f;
 #pragma unroll
                       for (int c = 0; c < 8; ++c)
                         if (qh + q * 32 + c8 + c < a.Sq)
