@@ -31,7 +31,7 @@ using namespace sm103;
 constexpr float kLog2eP = 1.4426950408889634f;
 
 // =========================================================== dK / dV pass
-template <int DQK, int DV, bool ATOMIC>
+template <int DQK, int DV, bool ATOMIC, bool HAS_BIAS = false>
 struct DkdvLayout {
   static constexpr int kKBytes = kTile * DQK * 2;
   static constexpr int kVBytes = kTile * DV * 2;
@@ -40,18 +40,23 @@ struct DkdvLayout {
   static constexpr int kDSBytes = kTile * kBwdQ * 2;
   static constexpr int kDQStageBytes = ATOMIC ? kBwdQ * DQK * 4 : 0;  // fp32 dQ tile for TMA reduce
   static constexpr int kStageBytes = kQBytes + kOBytes;
+  // one stage's bias tile, 64 query rows x 128 keys, rows of 256 bytes
+  static constexpr int kBiasBytes = HAS_BIAS ? kBwdQ * kTile * 2 : 0;
+  static constexpr int kPerStage = kStageBytes + kBiasBytes + 1024;
   static constexpr int kFixed = kKBytes + kVBytes + kDSBytes + kDQStageBytes;
-  static constexpr int kStages = (kFixed + 4 * kStageBytes + 4 * 1024 <= 216 * 1024) ? 4
-                                 : (kFixed + 3 * kStageBytes + 3 * 1024 <= 216 * 1024) ? 3 : 2;
+  static constexpr int kStages = (kFixed + 4 * kPerStage <= 216 * 1024) ? 4
+                                 : (kFixed + 3 * kPerStage <= 216 * 1024) ? 3 : 2;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKBytes;
   static constexpr int kDSOff = kKBytes + kVBytes;
   static constexpr int kDQOff = kDSOff + kDSBytes;
   static constexpr int kStageOff = kDQOff + kDQStageBytes;
   static constexpr int kVecOff = kStageOff + kStages * kStageBytes;  // 1 KB per stage
-  static constexpr int kBarOff = kVecOff + kStages * 1024;
+  static constexpr int kBiasOff = kVecOff + kStages * 1024;
+  static constexpr int kBarOff = kBiasOff + kStages * kBiasBytes;
   static constexpr int kBytes = kBarOff + 512;
   static constexpr int kAlloc = (kBytes + 1024 > 118 * 1024) ? kBytes + 1024 : 118 * 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
   // tensor memory: dV, dK accumulators; two S^T buffers (P^T is written back
   // over its own S^T as packed bf16); dP^T; dQ^T (atomic mode, d_qk <= 128)
   static constexpr uint32_t kColDV = 0;
@@ -77,9 +82,50 @@ struct StageVec {  // per query tile: log2-LSE, D, and (general path) ids / posi
   int32_t qpos[kBwdQ];
 };
 
+// The bias tile of one dK/dV step (query rows [q0, q0 + 64) of head h, keys
+// [kj0, kj0 + 128)), read by the 64 vector-loader threads a step ahead: thread
+// t holds pieces f = 64 k + t, piece f = 16 bytes (8 keys) of row f / 16 at
+// key 8 (f % 16).  Rows past Sq and keys past Skv are 0.  16-byte loads when
+// every bias row starts 16-byte aligned, else element by element.
+template <class E>
+__device__ __forceinline__ void bias_tile_load(const KernelArgs& a, int b, int h, int q0, int kj0,
+                                               int t, uint4 (&bv)[16]) {
+  const int bb = a.bias_b > 1 ? b : 0, bh = a.bias_h > 1 ? h : 0;
+  const int64_t slice = ((int64_t)bb * a.bias_h + bh) * a.Sq;
+  const int64_t total = (int64_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
+  const bool vec = (a.Skv % 8) == 0 && (reinterpret_cast<uintptr_t>(a.bias) & 15u) == 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int f = k * 64 + t;
+    const int i = q0 + (f >> 4), key = kj0 + (f & 15) * 8;
+    bv[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (i >= a.Sq || key >= a.Skv) continue;
+    const int64_t e0 = (slice + i) * a.Skv + key;
+    if (vec) {
+      if (ATTN_CHECK(a, span_ok(e0, 8, total), 0x750a)) bv[k] = sm103::ld_nc_v4(a.bias + e0);
+    } else {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (key + e < a.Skv && ATTN_CHECK(a, span_ok(e0 + e, 1, total), 0x750b))
+          w[e >> 1] |= static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(a.bias + e0 + e))
+                       << ((e & 1) * 16);
+      bv[k] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+__device__ __forceinline__ void bias_tile_store(uint8_t* tile, int t, const uint4 (&bv)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int f = k * 64 + t;
+    sm103::st_shared_v4(sm103::smem_u32(tile + (f >> 4) * 256 + (f & 15) * 16), bv[k].x, bv[k].y,
+                        bv[k].z, bv[k].w);
+  }
+}
+
 template <class E, int DQK, int DV, bool ATOMIC, bool HAS_BIAS, int DBIAS>
 __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ KernelArgs a) {
-  using L = DkdvLayout<DQK, DV, ATOMIC>;
+  using L = DkdvLayout<DQK, DV, ATOMIC, HAS_BIAS>;
   constexpr int NS = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -219,9 +265,14 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
             const int h = g * G + hh;
             for (int s = 0; s < nq; ++s, ++st) {
               const int stage = st % NS;
+              // the step's bias tile, loaded before the wait for its stage so
+              // that the load time overlaps the wait
+              uint4 bv[16];
+              if (HAS_BIAS) bias_tile_load<E>(a, b, h, q_lo + s * kBwdQ, w.t * kTile, t, bv);
               if (st >= (uint32_t)NS &&
                   !(ok = mbar_wait_warp(&bars->qd_empty[stage], ((st / NS) - 1) & 1)))
                 break;
+              if (HAS_BIAS) bias_tile_store(sm + L::kBiasOff + stage * L::kBiasBytes, t, bv);
               const int i = q_lo + s * kBwdQ + t;
               const bool in = i < a.Sq;
               const int64_t vi = ((int64_t)b * a.Hq + h) * a.Sq + i;
@@ -411,11 +462,12 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
               }
               if (j == 0 && half == 0) ATTN_TL(40, cur);
               const StageVec& V = vec[stage];
-              if (HAS_BIAS && row_ok) {
-                const bf16* bp = a.bias + (bias_base + q0 + c0h) * a.Skv + kj;
+              if (HAS_BIAS && row_ok) {  // this key's column of the step's bias tile
+                const bf16* bt =
+                    reinterpret_cast<const bf16*>(sm + L::kBiasOff + stage * L::kBiasBytes) + j;
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
-                  if (q0 + c0h + c < a.Sq) x[c] += E::ld(bp + (int64_t)c * a.Skv) * kLog2eP;
+                  if (q0 + c0h + c < a.Sq) x[c] += E::ld(bt + (c0h + c) * kTile) * kLog2eP;
               }
               // validity of this thread's 32 query columns, as a bitmask
               uint32_t vbits;
@@ -1061,7 +1113,7 @@ cudaError_t set_smem(K kern, int bytes) {
 
 template <class E, int DQK, int DV, bool AT, bool HB, int DB>
 cudaError_t dkdv_go(const KernelArgs& a, int nsm, cudaStream_t st) {
-  using L = DkdvLayout<DQK, DV, AT>;
+  using L = DkdvLayout<DQK, DV, AT, HB>;
   auto kern = dkdv_kernel<E, DQK, DV, AT, HB, DB>;
   cudaError_t e = set_smem(kern, L::kAlloc);
   if (e != cudaSuccess) return e;
