@@ -1006,14 +1006,20 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
         Di = a.Dvec[vi];
       }
       const bf16* bias_row = nullptr;
+      int64_t bias_e = 0;  // element index of the row's first key
       if (HAS_BIAS && row_ok) {
         const int bb = a.bias_b > 1 ? b : 0, bh = a.bias_h > 1 ? h : 0;
-        bias_row = a.bias + (((int64_t)bb * a.bias_h + bh) * a.Sq + i) * a.Skv;
+        bias_e = (((int64_t)bb * a.bias_h + bh) * a.Sq + i) * a.Skv;
+        bias_row = a.bias + bias_e;
+        prefetch_bias_l2(a, bias_e + kv_lo, min(kTile, a.Skv - kv_lo));
       }
       for (int j = 0; j < n; ++j) {
         const uint32_t k = kt + j;
         const int k0 = kv_lo + j * kTile;
         float x[kTile];
+        // the next key tile's bias row segment toward L2 while this one runs
+        if (HAS_BIAS && row_ok && j + 1 < n)
+          prefetch_bias_l2(a, bias_e + k0 + kTile, min(kTile, a.Skv - k0 - kTile));
         if (!(ok = mbar_wait_warp(&bars->s_full, k & 1))) break;
         tc_fence_after();
 #pragma unroll
@@ -1026,13 +1032,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ Kern
         }
         tc_fence_before();
         mbar_arrive(&bars->s_free);
-        if (HAS_BIAS && row_ok) {
-          const bf16* bp = bias_row + k0;
-          const int nv = min(kTile, a.Skv - k0);
-#pragma unroll
-          for (int c = 0; c < kTile; ++c)
-            if (c < nv) x[c] += E::ld(bp + c) * kLog2eP;
-        }
+        if (HAS_BIAS && row_ok) add_bias_row<E>(x, bias_row + k0, min(kTile, a.Skv - k0));
         uint64_t vb[2];
         kv_valid_bits(a, general, b, k0, rlo, rhi, my_id, my_pos, vb);
 #pragma unroll

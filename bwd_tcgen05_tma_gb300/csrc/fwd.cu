@@ -83,28 +83,6 @@ __device__ __forceinline__ FwdItem fwd_item(const KernelArgs& a, int idx) {
   return it;
 }
 
-// Adds bias[i, k0 + c] * log2(e) to x[c] for c < nvalid (row pointer given).
-template <class E>
-__device__ __forceinline__ void add_bias_row(float (&x)[kTile], const bf16* row, int nvalid) {
-  const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
-#pragma unroll
-  for (int c = 0; c < kTile; c += 8) {
-    if (vec && c + 8 <= nvalid) {
-      const uint4 u = ld_nc_v4(row + c);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[c + 2 * e] += E::lo(w[e]) * kLog2e;
-        x[c + 2 * e + 1] += E::hi(w[e]) * kLog2e;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (c + e < nvalid) x[c + e] += E::ld(row + c + e) * kLog2e;
-    }
-  }
-}
-
 template <class E, int DQK, int DV, bool HAS_BIAS>
 __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ KernelArgs a) {
   using L = FwdLayout<DQK, DV>;
@@ -334,6 +312,9 @@ __global__ void __launch_bounds__(256, 1) fwd_kernel(const __grid_constant__ Ker
         const int sb = k & 1;
         const int k0 = w.kv_lo + j * kTile;
         float x[kTile];
+        // the next key tile's bias row segment toward L2 while this one runs
+        if (HAS_BIAS && row_ok && j + 1 < w.n)
+          prefetch_bias_lines(a, (bias_row - a.bias) + k0 + kTile, min(kTile, a.Skv - k0 - kTile));
         if (!(ok = mbar_wait_warp(&bars->s_full[sb], (k >> 1) & 1))) break;
         tc_fence_after();
 #pragma unroll
