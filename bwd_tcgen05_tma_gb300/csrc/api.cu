@@ -619,7 +619,6 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
   // otherwise 64-row query tiles
   const bool tile128 = !atomic && p->d_qk <= 128 && p->d_v <= 128;
   const int qrows = tile128 ? kTile : kBwdQ;
-  a.dkdv_bq = qrows;
   if (!make_map(&a.tm_q, mt, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, qrows) ||
       !make_map(&a.tm_k, mt, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
       !make_map(&a.tm_v, mt, r.v, p->d_v, p->Hkv, (int64_t)p->B * p->Skv, r.v_token_stride, kTile) ||
@@ -668,13 +667,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* o, const void* d_o, c
         cudaStreamWaitEvent(st, ax->join, 0) != cudaSuccess)
       s = ATTN_ERR_CUDA;
   }
-  if (s != ATTN_OK) return s;
-  if (a.dbias_mode == 2) {
-    trace(ATTN_TRACE_DBIAS, false, st);
-    if (launch_dbias_convert(a, st) != cudaSuccess) return ATTN_ERR_CUDA;
-    trace(ATTN_TRACE_DBIAS, true, st);
-  }
-  return ATTN_OK;
+  return s;
 }
 
 attn_status_t attn_read_status(const void* ws, void* stream, attn_stats_t* stats) {

@@ -287,7 +287,6 @@ struct KernelArgs {
   int grad_st32;       // 1: dQ/dK/dV rows start 32-byte aligned (256-bit stores)
   int dkdv_batch_loop;  // 1: one dK/dV work item loops over every batch row
   int dkdv_head_loop;   // 1: one dK/dV work item loops over every KV head
-  int dkdv_bq;          // query-tile rows of the dK/dV pass in use (128 or 64)
 
   // FP8 (E4M3) forward: tm_q / tm_k map the one-byte Q and K, tm_v the
   // transposed V in the workspace (planes of [128 d][vt_pad keys])
@@ -599,12 +598,15 @@ __device__ __forceinline__ void prefetch_bias_lines(const KernelArgs& a, int64_t
   for (uintptr_t p = lo; p < hi; p += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Broadcast dBias (an fp32 accumulator summed over batch rows and/or heads):
-// the dK/dV pass that owns KV tile t writes the query rows its BQ-row query
-// tiles cover, [q_lo, q_lo + nq * BQ) within [0, Sq), for every batch row it
-// visits.  The first (batch row, head) of a work item to reach a row stores
-// it, the later ones add to it, and the conversion writes 0 where no pass
-// wrote, so the accumulator needs no clearing.
+// Broadcast dBias (summed over batch rows and/or heads).  Every (batch row,
+// head) that adds into one dBias row of KV tile t runs in the same dK/dV work
+// item, in a fixed order, and writes the query rows its BQ-row query tiles
+// cover, [q_lo, q_lo + nq * BQ) within [0, Sq).  For each row, the first of
+// them stores dS into the fp32 accumulator (or, if it is also the last, the
+// finished bf16 value into dBias), the ones in between add to the
+// accumulator, and the last adds and writes the finished value to dBias.
+// So the accumulator is never cleared and never converted: dBias is cleared
+// before the pass, and rows no step writes stay 0.
 //
 // Rows [i0, i0 + 32) of the current (batch row b, head g * G + hh) step that
 // an earlier step of the same work item has written already, as a bit mask.
@@ -622,18 +624,50 @@ __device__ __forceinline__ uint32_t dbias_rows_written_before(const KernelArgs& 
   }
   return seen;
 }
-
-// Whether any dK/dV step wrote query row i of accumulator slice bb for KV
-// tile t (the batch rows summed into slice bb: bb itself, or all of them when
-// the bias is broadcast over the batch).
-__device__ __forceinline__ bool dbias_row_written(const KernelArgs& a, int bb, int i, int t) {
-  const int b0 = a.bias_b > 1 ? bb : 0, b1 = a.bias_b > 1 ? bb + 1 : a.B;
-  for (int b = b0; b < b1; ++b) {
-    const int2 r = a.kv_tile_range[b * a.n_kt + t];
-    if (r.y > r.x && i >= r.x && i < r.x + ((r.y - r.x + a.dkdv_bq - 1) / a.dkdv_bq) * a.dkdv_bq)
-      return true;
+// One thread's share of a step: dS of key kj for the 32 query rows [r0, r0 +
+// 32) (rows past Sq skipped), accumulator row brow0 + c.  A step must call it
+// even where its dS is 0, or a row's first store or last write is lost.  Eight
+// loads in flight before their stores (a store between two loads would
+// serialise them: the addresses may alias).
+template <class E>
+__device__ __forceinline__ void dbias_acc_rows(const KernelArgs& a, int64_t brow0, int kj, int r0,
+                                               uint32_t seen, uint32_t later, const float (&ds)[32]) {
+  float* acc_p = a.dbias_acc + brow0 * a.Skv + kj;
+  bf16* out_p = a.dbias + brow0 * a.Skv + kj;
+#pragma unroll
+  for (int c8 = 0; c8 < 32; c8 += 8) {
+    float acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      acc[c] = (r0 + c8 + c < a.Sq && ((seen >> (c8 + c)) & 1u)) ? acc_p[(int64_t)(c8 + c) * a.Skv]
+                                                                   : 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (r0 + c8 + c >= a.Sq) continue;
+      const int64_t o = (int64_t)(c8 + c) * a.Skv;
+      if ((later >> (c8 + c)) & 1u)
+        acc_p[o] = acc[c] + ds[c8 + c];
+      else
+        E::st(out_p + o, acc[c] + ds[c8 + c]);
+    }
   }
-  return false;
+}
+
+// ... and that a later step of the item (batch rows up to b1, KV heads up to
+// g1, G query heads per KV head) will write again.
+template <int BQ>
+__device__ __forceinline__ uint32_t dbias_rows_written_after(const KernelArgs& a, int b, int b1, int g,
+                                                             int g1, int hh, int G, int t, int i0) {
+  if (a.bias_h == 1 && (g < g1 - 1 || hh < G - 1)) return ~0u;  // the item's last head will
+  uint32_t later = 0u;
+  if (a.bias_b == 1) {
+    for (int bp = b + 1; bp < b1; ++bp) {
+      int q_lo;
+      const int nq = dkdv_q_tiles<BQ>(a, bp, t, q_lo);
+      if (nq > 0) later |= static_cast<uint32_t>(range_bits64(q_lo - i0, q_lo + nq * BQ - i0));
+    }
+  }
+  return later;
 }
 
 
@@ -682,6 +716,5 @@ cudaError_t launch_bwd_dkdv128(const KernelArgs& a, int num_sms, cudaStream_t st
 // Deterministic dQ pass with Q, dO and dS as tensor-memory operands (d_qk, d_v <= 128).
 cudaError_t launch_bwd_dq128(const KernelArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_dq_convert(const KernelArgs& a, cudaStream_t st);
-cudaError_t launch_dbias_convert(const KernelArgs& a, cudaStream_t st);
 
 }  // namespace attn

@@ -23,7 +23,8 @@
 //                tiles visited in a fixed order, dQ accumulated in tensor
 //                memory (recomputes S and dP: two more GEMMs than atomic mode).
 //   dq_convert   fp32 dQ accumulator -> bf16 / fp16 in the caller's layout.
-//   dbias_convert fp32 broadcast-bias gradient -> bf16 / fp16.
+// A broadcast dBias is summed in an fp32 accumulator and finished (rounded to
+// bf16 / fp16) inside the dK/dV pass by the last step that adds to each row.
 //
 // Gradient formulas: TransformerEngine PR #3516 (fused-attention backward:
 // Q/K/V and optional bias gradients from the saved output and dO); dK/dV of a
@@ -162,38 +163,6 @@ __global__ void dq_convert_kernel(const KernelArgs a) {
   }
 }
 
-template <class E>
-__global__ void dbias_convert_kernel(const KernelArgs a) {
-  // Elements no dK/dV step wrote are 0 and are not read (the accumulator is
-  // not cleared).  With Skv a multiple of 4, four elements of one row per
-  // thread and step: one 16-byte load, one 8-byte store (both buffers are
-  // 16-byte aligned, and the four share a KV tile); otherwise one by one.
-  const int64_t n = (int64_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t t0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  const int64_t plane = (int64_t)a.bias_h * a.Sq * a.Skv;
-  auto written = [&](int64_t v) -> bool {
-    const int64_t row = v / a.Skv;
-    const int j = static_cast<int>(v - row * a.Skv);
-    const int i = static_cast<int>(row % a.Sq);
-    return dbias_row_written(a, static_cast<int>(v / plane), i, j / kTile);
-  };
-  if (a.Skv % 4 == 0) {
-    const int64_t n4 = n / 4;
-    for (int64_t v = t0; v < n4; v += stride) {
-      uint2 o = make_uint2(0u, 0u);
-      if (written(4 * v)) {
-        const float4 x = reinterpret_cast<const float4*>(a.dbias_acc)[v];
-        o.x = E::pack(x.x, x.y);
-        o.y = E::pack(x.z, x.w);
-      }
-      reinterpret_cast<uint2*>(a.dbias)[v] = o;
-    }
-  } else {
-    for (int64_t v = t0; v < n; v += stride) E::st(a.dbias + v, written(v) ? a.dbias_acc[v] : 0.f);
-  }
-}
-
 int blocks_for(int64_t n, int per_block) {
   const int64_t b = (n + per_block - 1) / per_block;
   return static_cast<int>(b < 4096 ? (b > 0 ? b : 1) : 4096);
@@ -206,11 +175,13 @@ cudaError_t launch_bwd_pre(const KernelArgs& a, int zero_dq_acc, cudaStream_t st
     e = cudaMemsetAsync(a.dq_acc, 0, (size_t)a.B * a.Sq * a.Hq * a.d_qk * sizeof(float), st);
     if (e != cudaSuccess) return e;
   }
+  // dBias rows no dK/dV step writes stay 0; the fp32 accumulator of a
+  // broadcast dBias is never cleared (see dbias_rows_written_before)
   const size_t nb = (size_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
-  if (a.dbias_mode == 1) {
+  if (a.dbias_mode != 0) {
     e = cudaMemsetAsync(a.dbias, 0, nb * sizeof(bf16), st);
     if (e != cudaSuccess) return e;
-  }  // the fp32 accumulator of a broadcast dBias is not cleared: see dbias_row_written
+  }
   const int mode = zero_dq_acc ? 0 : 1;
   if (a.Hq > kPreMaxH) return cudaErrorInvalidValue;  // rejected on the host before launch
   const int64_t ntok = (int64_t)a.B * a.Sq;
@@ -245,14 +216,6 @@ cudaError_t launch_sink_reduce(const KernelArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_dbias_convert(const KernelArgs& a, cudaStream_t st) {
-  const int64_t n = (int64_t)a.bias_b * a.bias_h * a.Sq * a.Skv;
-  if (a.elem_f16)
-    dbias_convert_kernel<ElemF16><<<blocks_for(n, 256), 256, 0, st>>>(a);
-  else
-    dbias_convert_kernel<ElemBf16><<<blocks_for(n, 256), 256, 0, st>>>(a);
-  return cudaGetLastError();
-}
 
 }  // namespace attn
 

@@ -562,25 +562,10 @@ __global__ void __launch_bounds__(512, 1) dkdv_kernel(const __grid_constant__ Ke
                   for (int c = 0; c < 32; ++c)
                     if (q0 + c0h + c < a.Sq) E::st(dp + (int64_t)c * a.Skv, x[c]);
                 } else {
-                  float* dp = a.dbias_acc + (bias_base + q0 + c0h) * a.Skv + kj;
-                  // rows no earlier step of this item wrote start from 0 (the
-                  // accumulator is not cleared); eight loads in flight before
-                  // their stores (a store between two loads would serialise
-                  // them: the addresses may alias)
-                  const uint32_t seen =
-                      dbias_rows_written_before<kBwdQ>(a, w.b0, b, w.g0, g, hh, w.t, q0 + c0h);
-#pragma unroll
-                  for (int c8 = 0; c8 < 32; c8 += 8) {
-                    float acc[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                      acc[c] = (q0 + c0h + c8 + c < a.Sq && ((seen >> (c8 + c)) & 1u))
-                                   ? dp[(int64_t)(c8 + c) * a.Skv]
-                                   : 0.f;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                      if (q0 + c0h + c8 + c < a.Sq) dp[(int64_t)(c8 + c) * a.Skv] = acc[c] + x[c8 + c];
-                  }
+                  dbias_acc_rows<E>(a, bias_base + q0 + c0h, kj, q0 + c0h,
+                                    dbias_rows_written_before<kBwdQ>(a, w.b0, b, w.g0, g, hh, w.t, q0 + c0h),
+                                    dbias_rows_written_after<kBwdQ>(a, b, w.b1, g, w.g1, hh, G, w.t, q0 + c0h),
+                                    x);
                 }
               }
               mbar_arrive(&bars->qd_empty[stage]);

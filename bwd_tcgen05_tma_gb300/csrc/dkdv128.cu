@@ -499,11 +499,25 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
               const uint32_t dp_tm = tmem + lane_base + L::kColDP + c0h;
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
-                if (none[q]) {  // P = 0, so dS = 0 (dBias already holds zeros)
+                if (none[q]) {  // P = 0, so dS = 0
                   uint32_t pk[16];
 #pragma unroll
                   for (int e = 0; e < 16; ++e) pk[e] = 0u;
                   tmem_st32x32b_x16(dp_tm + q * 16, pk);
+                  // a per-slice dBias already holds zeros; a summed one still
+                  // needs its first store or last write of these rows
+                  if (DBIAS == 2 && row_ok &&
+                      ATTN_CHECK(a, dbias_ok(a, bias_base + qh + q * 32, kj) &&
+                                        dbias_ok(a, bias_base + min(qh + q * 32 + 31, a.Sq - 1), kj),
+                                 0x7309)) {
+                    float zero[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) zero[c] = 0.f;
+                    dbias_acc_rows<E>(a, bias_base + qh + q * 32, kj, qh + q * 32,
+                                      dbias_rows_written_before<kQ>(a, w.b0, b, w.g0, g, hh, w.t, qh + q * 32),
+                                      dbias_rows_written_after<kQ>(a, b, w.b1, g, w.g1, hh, G, w.t, qh + q * 32),
+                                      zero);
+                  }
                   continue;
                 }
                 uint32_t u[32];
@@ -553,26 +567,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                     for (int c = 0; c < 32; ++c)
                       if (qh + q * 32 + c < a.Sq) E::st(dpb + (int64_t)c * a.Skv, ds[c]);
                   } else {
-                    float* dpb = a.dbias_acc + (bias_base + qh + q * 32) * a.Skv + kj;
-                    // rows no earlier step of this item wrote start from 0 (the
-                    // accumulator is not cleared); eight loads in flight before
-                    // their stores (a store between two loads would serialise
-                    // them: the addresses may alias)
-                    const uint32_t seen =
-                        dbias_rows_written_before<kQ>(a, w.b0, b, w.g0, g, hh, w.t, qh + q * 32);
-#pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) {
-                      float acc[8];
-#pragma unroll
-                      for (int c = 0; c < 8; ++c)
-                        acc[c] = (qh + q * 32 + c8 + c < a.Sq && ((seen >> (c8 + c)) & 1u))
-                                     ? dpb[(int64_t)(c8 + c) * a.Skv]
-                                     : 0.f;
-#pragma unroll
-                      for (int c = 0; c < 8; ++c)
-                        if (qh + q * 32 + c8 + c < a.Sq)
-                          dpb[(int64_t)(c8 + c) * a.Skv] = acc[c] + ds[c8 + c];
-                    }
+                    dbias_acc_rows<E>(a, bias_base + qh + q * 32, kj, qh + q * 32,
+                                      dbias_rows_written_before<kQ>(a, w.b0, b, w.g0, g, hh, w.t, qh + q * 32),
+                                      dbias_rows_written_after<kQ>(a, b, w.b1, g, w.g1, hh, G, w.t, qh + q * 32),
+                                      ds);
                   }
                 }
               }

@@ -328,7 +328,8 @@ typedef enum {
                               second stream (see attn_bwd) its events span
                               from the end of the preprocess to the end of
                               the dQ pass, overlapping the dK/dV pass */
-  ATTN_TRACE_DBIAS = 5     /* broadcast dBias conversion */
+  ATTN_TRACE_DBIAS = 5     /* not recorded: a broadcast dBias is finished
+                              inside the dK/dV pass */
 } attn_trace_slot_t;
 attn_status_t attn_set_trace_events(void* const* events);
 

@@ -168,6 +168,29 @@ def test_bias_shapes_and_reduction(bias_shape):
     check_backward(case, ref, g, db)
 
 
+@pytest.mark.parametrize("dq_mode,bias_shape,d_qk", [
+    ("deterministic", (1, 1), 128), ("deterministic", (1, 4), 128), ("deterministic", (2, 1), 128),
+    ("atomic", (1, 1), 128), ("deterministic", (1, 1), 192)])
+def test_backward_reads_no_stale_workspace(dq_mode, bias_shape, d_qk):
+    """The backward reads nothing of its workspace that the same call did not
+    write first: filled with 0xFF bytes (NaN as fp32) beforehand, it gives the
+    oracle's gradients, including a dBias summed over broadcast batch rows and
+    heads through an accumulator that is never cleared."""
+    from gpu_util import DevCase, check_backward
+
+    Hq, Hkv = (4, 2) if d_qk == 128 else (2, 2)
+    case = I.synth("ws", B=2, Sq=300, Skv=520, Hq=Hq, Hkv=Hkv, d_qk=d_qk, d_v=128,
+                   layout="HD_HD_HD", fmt="THD_SEGMENTS", causal=False, seed=33, seg=(60, 200),
+                   kv_seg=(60, 300), bias_shape=(bias_shape[0], Hq if bias_shape[1] > 1 else 1,
+                                                 300, 520))
+    ref = _ref(case)
+    d = DevCase(case, dq_mode=dq_mode)
+    d.forward()
+    d.ws_bwd.fill_(0xFF)
+    g, db = d.backward()
+    check_backward(case, ref, g, db)
+
+
 def test_deterministic_mode_bit_reproducible():
     from gpu_util import DevCase
 
