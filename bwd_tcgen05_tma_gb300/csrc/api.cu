@@ -520,7 +520,9 @@ attn_status_t attn_fwd(const attn_params_t* p, void* o, float* lse, void* ws, si
     a.fp8_dv = p->descale_v;
     if (!make_map8(&a.tm_q, r.q, p->d_qk, p->Hq, (int64_t)p->B * p->Sq, r.q_token_stride, kTile) ||
         !make_map8(&a.tm_k, r.k, p->d_qk, p->Hkv, (int64_t)p->B * p->Skv, r.k_token_stride, kTile) ||
-        !make_map_vt(&a.tm_v, a.vt, a.vt_pad, p->d_v, (int64_t)p->B * p->Hkv))
+        !make_map_vt(&a.tm_v, a.vt, a.vt_pad, p->d_v, (int64_t)p->B * p->Hkv) ||
+        !make_map_4d(&a.tm_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, o, p->d_v, p->Hq, p->Sq, p->B,
+                     (int64_t)p->Hq * p->d_v, kTile))
       return ATTN_ERR_CUDA;
     a.o = static_cast<bf16*>(o);
     a.lse = lse;

@@ -22,9 +22,15 @@
 //            O   += P8(j) V(j)      B = V(j)^T, K-major: a transposed copy of V
 //                                   made once per call by vt_transpose_kernel
 //
-// Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 4-7 softmax and
-// epilogue.  S is double-buffered in tensor memory, so the tensor core works
-// on S(j+1) while the softmax warps read S(j).
+// Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 4-11 softmax and
+// epilogue.  Each query row is shared by two softmax threads, one per key
+// half of the tile (64 keys each, warps 4-7 and 8-11), so a thread's chain
+// per tile is half a row and a tile's exponentials spread over eight warps;
+// with the maximum fixed before the second pass, the two halves meet only
+// twice per item (the row maximum after pass 1, the row sum at the end).  S
+// is double-buffered in tensor memory, so the tensor core works on S(j+1)
+// while the softmax warps read S(j).  Q of the next item loads during this
+// one (two stages), and O leaves through shared memory by TMA stores.
 #include <cmath>
 
 #include "attn_internal.cuh"
@@ -38,13 +44,17 @@ constexpr float kPScale = 256.f;  // P8 = E4M3(256 p)
 
 struct F8Layout {
   static constexpr int kT = kTile * kTile;  // one 128 x 128 tile of one-byte elements
-  static constexpr int kKStages = 3, kVStages = 2, kPStages = 2;
+  // Q of the next item loads during this one (stage = item parity)
+  static constexpr int kQStages = 2, kKStages = 3, kVStages = 2, kPStages = 2;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kT;
+  static constexpr int kKOff = kQOff + kQStages * kT;
   static constexpr int kVOff = kKOff + kKStages * kT;
   static constexpr int kPOff = kVOff + kVStages * kT;
-  static constexpr int kBarOff = kPOff + kPStages * kT;
-  static constexpr int kBytes = kBarOff + 1024;  // barriers, then the item ring at +256
+  // O in bf16 for the TMA store: two 64-column boxes of 16 KB, 128-byte swizzled
+  static constexpr int kOOff = kPOff + kPStages * kT;
+  static constexpr int kBarOff = kOOff + 2 * 16384;
+  static constexpr int kXchOff = kBarOff + 1024;  // row exchange slots [set][half][row]
+  static constexpr int kBytes = kXchOff + 2048;   // barriers, then the item ring at +256
   static constexpr int kAlloc = kBytes + 1024;   // slack to align the window to 1 KB
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
   // above half of the SM's shared memory, so two CTAs (each taking all of
@@ -55,10 +65,11 @@ struct F8Layout {
 };
 
 struct F8Bars {
-  uint64_t q_full, q_empty, o_full, o_empty, drain;
+  uint64_t q_full[2], q_empty[2], o_full, o_empty, drain, stg_full, stg_free;
   uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
 };
+static_assert(sizeof(F8Bars) + 8 <= 256, "barriers, tensor-memory holder and flag before the ring");
 
 // item = (query tile w = b * n_qt + t, head h), numbered w * Hq + h
 struct F8Item {
@@ -89,15 +100,43 @@ __device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// The 128 scores of this thread's row (one S buffer) in fp32, raw (before
-// the scale): four loads, one wait.
-__device__ __forceinline__ void load_row(uint32_t s_tm, uint32_t (&u)[4][32]) {
+// The 64 scores of this thread's half row (one S buffer) in fp32, raw
+// (before the scale): two loads, one wait.
+__device__ __forceinline__ void load_half_row(uint32_t s_tm, uint32_t (&u)[2][32]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) tmem_ld32x32b_x32(s_tm + q * 32, u[q]);
+  for (int q = 0; q < 2; ++q) tmem_ld32x32b_x32(s_tm + q * 32, u[q]);
   tmem_ld_wait(u);
 }
 
-__global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__ KernelArgs a) {
+// An empty exchange slot: a NaN payload the arithmetic never produces (the
+// GPU's own NaN results are all 0x7fffffff).
+constexpr uint32_t kXchEmpty = 0x7fa5a5a5u;
+
+// Row exchange between the two threads of one query row: each writes its
+// value into its own slot and takes the other's, leaving that slot empty.
+// Slots alternate between two sets, so a thread's next write to a set comes
+// after its partner has emptied it (the partner's write in between orders
+// them).  The wait is bounded like every other wait.
+__device__ __forceinline__ void xch_put(uint32_t* slot, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(v) : "memory");
+}
+__device__ __forceinline__ bool xch_take(uint32_t* slot, uint32_t& v) {
+  const uint32_t addr = smem_u32(slot);
+  uint64_t t0 = 0;
+  for (uint32_t n = 0;; ++n) {
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    if (v != kXchEmpty) break;
+    if ((n & 255u) == 255u) {
+      const uint64_t t = globaltimer_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > 2000000000ull) return false;
+    }
+  }
+  asm volatile("st.relaxed.cta.shared::cta.b32 [%0], %1;" ::"r"(addr), "r"(kXchEmpty) : "memory");
+  return true;
+}
+
+__global__ void __launch_bounds__(384, 1) fwd_fp8_kernel(const __grid_constant__ KernelArgs a) {
   using L = F8Layout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -106,14 +145,19 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + L::kBarOff + sizeof(F8Bars));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   ItemRing* ring = reinterpret_cast<ItemRing*>(sm + L::kBarOff + 256);
+  uint32_t* xch = reinterpret_cast<uint32_t*>(sm + L::kXchOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_items = a.B * a.n_qt * a.Hq;
 
   if (tid == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+    }
     mbar_init(&bars->o_full, 1);
-    mbar_init(&bars->o_empty, 128);
+    mbar_init(&bars->o_empty, 256);
+    mbar_init(&bars->stg_full, 256);  // every softmax thread's share of O staged
+    mbar_init(&bars->stg_free, 1);    // the previous O store has read the staging
     mbar_init(&bars->drain, 1);
     for (int s = 0; s < L::kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
@@ -123,14 +167,15 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_empty[s], 128);
-      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->s_empty[s], 256);
+      mbar_init(&bars->p_full[s], 256);
       mbar_init(&bars->p_empty[s], 1);
     }
-    ring_init(ring, 1 + 128);  // MMA issuer + softmax warpgroup
+    ring_init(ring, 1 + 256);  // MMA issuer + the softmax threads
     *abort_flag = 0;
     mbar_fence_init();
   }
+  for (int i = tid; i < 512; i += blockDim.x) xch[i] = kXchEmpty;
   if (warp == 1) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
@@ -161,12 +206,13 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
           break;
         const F8Item w = f8_item(a, idx);
         if (w.n == 0) continue;
-        if (it > 0 && !(ok = mbar_wait(&bars->q_empty, (it - 1) & 1))) break;
+        const int qs = it & 1;
+        if (it >= 2 && !(ok = mbar_wait(&bars->q_empty[qs], ((it >> 1) - 1) & 1))) break;
         const int qrow = w.b * a.Sq + w.t * kTile;
-        mbar_arrive_expect_tx(&bars->q_full, L::kT);
+        mbar_arrive_expect_tx(&bars->q_full[qs], L::kT);
         if (ATTN_CHECK(a, tma_box_ok(0, kTile, a.d_qk, 1, w.h, a.Hq, qrow, kTile,
                                      (int64_t)a.B * a.Sq, false), 0x7901))
-          tma_load_3d(sm + L::kQOff, &a.tm_q, &bars->q_full, 0, w.h, qrow);
+          tma_load_3d(sm + L::kQOff + qs * L::kT, &a.tm_q, &bars->q_full[qs], 0, w.h, qrow);
         ++it;
         const int g = w.h / (a.Hq / a.Hkv);
         for (int t2 = 0; t2 < 2 * w.n && ok; ++t2) {
@@ -181,6 +227,7 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
           if (ATTN_CHECK(a, tma_box_ok(0, kTile, a.d_qk, 1, g, a.Hkv, krow, kTile,
                                        (int64_t)a.B * a.Skv, false), 0x7902))
             tma_load_3d(sm + L::kKOff + s * L::kT, &a.tm_k, &bars->k_full[s], 0, g, krow);
+          ATTN_TL(1, kc);
           ++kc;
           if (t2 >= w.n) {
             const int s2 = vc % L::kVStages;
@@ -202,8 +249,9 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
         *abort_flag = 1;
       }
       if (*abort_flag) {  // let copies in flight land before the CTA exits
-        if (it > 0) mbar_wait(&bars->q_full, (it - 1) & 1, 100000000ull);
-        for (uint32_t u = (kc > 3u ? kc - 3u : 0u); u < kc; ++u)
+        for (uint32_t u = (it > 2u ? it - 2u : 0u); u < it; ++u)
+          mbar_wait(&bars->q_full[u & 1], (u >> 1) & 1, 100000000ull);
+        for (uint32_t u = (kc > (uint32_t)L::kKStages ? kc - L::kKStages : 0u); u < kc; ++u)
           mbar_wait(&bars->k_full[u % L::kKStages], (u / L::kKStages) & 1, 100000000ull);
         for (uint32_t u = (vc > 2u ? vc - 2u : 0u); u < vc; ++u)
           mbar_wait(&bars->v_full[u % L::kVStages], (u / L::kVStages) & 1, 100000000ull);
@@ -222,15 +270,17 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
     const uint64_t p_desc = sdesc_sw128(smem_u32(sm + L::kPOff), 16, 1024);
     uint32_t T = 0, kc = 0, vc = 0, pc = 0, it = 0;
     bool ok = true;
+    uint32_t q_off = 0;  // the current item's Q stage, in 16-byte units
     auto issue_s = [&]() -> bool {
       const int s = kc % L::kKStages, sb = T & 1;
       if (!mbar_wait_warp(&bars->k_full[s], (kc / L::kKStages) & 1)) return false;
       if (T >= 2 && !mbar_wait_warp(&bars->s_empty[sb], ((T >> 1) - 1) & 1)) return false;
       tc_fence_after();
       const uint64_t kd = k_desc + static_cast<uint32_t>((s * L::kT) >> 4);
-      mma_f8_ss4_warp(tm + L::kColS + sb * kTile, q_desc, kd, idesc, 0u);
+      mma_f8_ss4_warp(tm + L::kColS + sb * kTile, q_desc + q_off, kd, idesc, 0u);
       mma_commit_warp(&bars->s_full[sb]);
       mma_commit_warp(&bars->k_empty[s]);
+      ATTN_TL(10, T);
       ++kc;
       ++T;
       return true;
@@ -242,13 +292,14 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
         break;
       const int n = warp_uniform(f8_item(a, idx).n);
       if (n == 0) continue;
-      if (!(ok = mbar_wait_warp(&bars->q_full, it & 1))) break;
+      q_off = static_cast<uint32_t>(((it & 1) * L::kT) >> 4);
+      if (!(ok = mbar_wait_warp(&bars->q_full[it & 1], (it >> 1) & 1))) break;
       if (!(ok = issue_s())) break;
       for (int t2 = 0; t2 < 2 * n && ok; ++t2) {
         if (t2 + 1 < 2 * n) {
           if (!(ok = issue_s())) break;
         } else {
-          mma_commit_warp(&bars->q_empty);  // every S of this item is issued
+          mma_commit_warp(&bars->q_empty[it & 1]);  // every S of this item is issued
         }
         if (t2 < n) continue;
         const int j = t2 - n, pb = pc & 1, s2 = vc % L::kVStages;
@@ -261,6 +312,7 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
         mma_f8_ss4_warp(tm + L::kColO, pd, vd, idesc, j > 0 ? 1u : 0u);
         mma_commit_warp(&bars->p_empty[pb]);
         mma_commit_warp(&bars->v_empty[s2]);
+        ATTN_TL(11, pc);
         ++pc;
         ++vc;
       }
@@ -276,11 +328,24 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
     mbar_wait(&bars->drain, 0, 200000000ull);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int r = tid - 128;  // TMEM lane = query row
+    // thread (r, hf): query row r (TMEM lane r), keys [64 hf, 64 hf + 64) of
+    // each tile, value dims [64 hf, 64 hf + 64) of O
+    const int hf = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t p_addr = smem_u32(sm + L::kPOff);
-    uint32_t T = 0, pc = 0, it = 0;
+    uint32_t T = 0, pc = 0, it = 0, xc = 0;
     bool ok = true;
+    // swap v with the other half's thread of this row (warp-uniform result)
+    auto exchange = [&](float v, float& other) -> bool {
+      const uint32_t set = xc & 1;
+      ++xc;
+      xch_put(xch + (set * 2 + hf) * 128 + r, __float_as_uint(v));
+      uint32_t t = 0;
+      const bool got = xch_take(xch + (set * 2 + (hf ^ 1)) * 128 + r, t);
+      other = __uint_as_float(t);
+      return __all_sync(0xffffffffu, got);
+    };
     for (uint32_t rn = 0;; ++rn) {
       int32_t idx;
       if (!ok || __any_sync(0xffffffffu, *abort_flag != 0) || !(ok = ring_pop(ring, rn, idx)) ||
@@ -290,16 +355,16 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
       const int i = w.t * kTile + r;
       const bool row_ok = i < a.Sq;
       const int64_t grow = (int64_t)w.b * a.Sq + i;
-      bf16* orow = a.o + (grow * a.Hq + w.h) * kTile;
+      bf16* orow = a.o + (grow * a.Hq + w.h) * kTile + hf * 64;  // this half's 64 dims
       float* lse_out = a.lse + ((int64_t)w.b * a.Hq + w.h) * a.Sq + i;
       if (w.n == 0) {
-        if (row_ok && ATTN_CHECK(a, span_ok(orow - a.o, kTile, (int64_t)a.B * a.Sq * a.Hq * kTile) &&
+        if (row_ok && ATTN_CHECK(a, span_ok(orow - a.o, 64, (int64_t)a.B * a.Sq * a.Hq * kTile) &&
                                         span_ok(lse_out - a.lse, 1, (int64_t)a.B * a.Hq * a.Sq),
                                  0x7904)) {
 #pragma unroll
-          for (int c = 0; c < kTile; c += 8)
+          for (int c = 0; c < 64; c += 8)
             *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-          *lse_out = -INFINITY;
+          if (hf == 0) *lse_out = -INFINITY;
         }
         continue;
       }
@@ -314,9 +379,11 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
           my_pos = a.q_pos[grow];
         }
       }
-      auto valid = [&](int j, uint64_t (&vb)[2]) {
+      // validity of this thread's 64 keys of tile j
+      auto valid = [&](int j) -> uint64_t {
+        uint64_t vb[2];
         kv_valid_bits(a, general, w.b, w.kv_lo + j * kTile, rlo, rhi, my_id, my_pos, vb);
-        if (!row_ok) vb[0] = vb[1] = 0ull;
+        return row_ok ? vb[hf] : 0ull;
       };
       // pass 1: the row maximum of the raw scores over valid keys (the scale
       // is positive, so the maximum of the scaled scores is the scaled one)
@@ -324,19 +391,19 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
       for (int j = 0; j < w.n; ++j) {
-        uint64_t vb[2];
-        valid(j, vb);
+        const uint64_t vb = valid(j);
         const int sb = T & 1;
         if (!(ok = mbar_wait_warp(&bars->s_full[sb], (T >> 1) & 1))) break;
+        if (lane == 0) ATTN_TL(20 + (warp - 4), T);
         tc_fence_after();
-        uint32_t u[4][32];
-        load_row(tmem + lane_base + L::kColS + sb * kTile, u);
+        uint32_t u[2][32];
+        load_half_row(tmem + lane_base + L::kColS + sb * kTile + hf * 64, u);
         tc_fence_before();
         mbar_arrive(&bars->s_empty[sb]);
         ++T;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t m32 = static_cast<uint32_t>(vb[q >> 1] >> ((q & 1) * 32));
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t m32 = static_cast<uint32_t>(vb >> (q * 32));
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float x0 = (m32 & (1u << e)) ? __uint_as_float(u[q][e]) : -INFINITY;
@@ -346,27 +413,30 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
         }
       }
       if (!ok) break;
-      const float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      float mraw = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      float mo;
+      if (!(ok = exchange(mraw, mo))) break;
+      mraw = fmaxf(mraw, mo);  // the row's maximum, the same value in both halves
       const float m = mraw * a.fp8_sc2;  // log2 units (-inf: no valid key)
       const float m_use = (m == -INFINITY) ? 0.f : m;
       // pass 2: P8 = E4M3(256 exp2(s - m)) into shared memory, l = sum of p
       float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       for (int j = 0; j < w.n; ++j) {
-        uint64_t vb[2];
-        valid(j, vb);
+        const uint64_t vb = valid(j);
         const int sb = T & 1, pb = pc & 1;
         if (!(ok = mbar_wait_warp(&bars->s_full[sb], (T >> 1) & 1))) break;
+        if (lane == 0) ATTN_TL(20 + (warp - 4), T);
         tc_fence_after();
-        uint32_t u[4][32];
-        load_row(tmem + lane_base + L::kColS + sb * kTile, u);
+        uint32_t u[2][32];
+        load_half_row(tmem + lane_base + L::kColS + sb * kTile + hf * 64, u);
         tc_fence_before();
         mbar_arrive(&bars->s_empty[sb]);
         ++T;
-        uint32_t pw[32];  // 128 E4M3 codes, key order
+        uint32_t pw[16];  // this half's 64 E4M3 codes, key order
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t m32 = static_cast<uint32_t>(vb[q >> 1] >> ((q & 1) * 32));
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t m32 = static_cast<uint32_t>(vb >> (q * 32));
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             float p[4];
@@ -386,56 +456,93 @@ __global__ void __launch_bounds__(256, 1) fwd_fp8_kernel(const __grid_constant__
         // the stage's previous P (two tiles back) has been read by its P V
         if (pc >= 2 && !(ok = mbar_wait_warp(&bars->p_empty[pb], ((pc >> 1) - 1) & 1))) break;
         // row r of the K-major, 128-byte-swizzled P tile: 16-byte chunk c
-        // (keys 16 c .. 16 c + 15) at chunk c ^ (r % 8)
+        // (keys 16 c .. 16 c + 15) at chunk c ^ (r % 8); this half writes
+        // chunks 4 hf .. 4 hf + 3
         const uint32_t prow = p_addr + pb * L::kT + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(prow + ((c ^ (r & 7)) << 4), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
-                       pw[4 * c + 3]);
+        for (int c = 0; c < 4; ++c)
+          st_shared_v4(prow + (((4 * hf + c) ^ (r & 7)) << 4), pw[4 * c], pw[4 * c + 1],
+                       pw[4 * c + 2], pw[4 * c + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
+        if (lane == 0) ATTN_TL(30 + (warp - 4), pc);
         mbar_arrive(&bars->p_full[pb]);
         ++pc;
       }
       if (!ok) break;
-      const float l = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
+      const float lh = (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
+      float lo;
+      if (!(ok = exchange(lh, lo))) break;
+      const float l = hf == 0 ? lh + lo : lo + lh;  // one order in both halves
       // epilogue: O = descale_v * acc / (256 l), LSE = m + log2 l (natural log out)
+      if (lane == 0 && warp == 4) ATTN_TL(40, it);
       if (!(ok = mbar_wait_warp(&bars->o_full, it & 1))) break;
+      if (lane == 0 && warp == 4) ATTN_TL(41, it);
       tc_fence_after();
       const float inv = (l > 0.f) ? a.fp8_dv / (kPScale * l) : 0.f;
-      const bool store = row_ok && ATTN_CHECK(a, span_ok(orow - a.o, kTile,
-                                                         (int64_t)a.B * a.Sq * a.Hq * kTile),
-                                              0x7905);
+      // the staging is free once the previous item's O store has read it
+      // (the thread that issued that store waits for the read, then releases)
+      if (it > 0) {
+        if (tid == 128) {
+          bulk_wait_read_all();
+          mbar_arrive(&bars->stg_free);
+        }
+        if (!(ok = mbar_wait_warp(&bars->stg_free, (it - 1) & 1))) break;
+      }
+      // this half's 64 dims of O in bf16 into box hf of the staging, laid out
+      // as the store map's 128-byte-swizzled boxes: 16-byte chunk c of row r
+      // at chunk c ^ (r % 8)
+      const uint32_t stg_row = smem_u32(sm + L::kOOff + hf * 16384 + r * 128);
 #pragma unroll
-      for (int q = 0; q < kTile / 32; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t o[32];
-        tmem_ld32x32b_x32(tmem + lane_base + L::kColO + q * 32, o);
+        tmem_ld32x32b_x32(tmem + lane_base + L::kColO + hf * 64 + q * 32, o);
         tmem_ld_wait(o);
-        if (store) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[c + 0]) * inv, __uint_as_float(o[c + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + q * 32 + c) = v;
-          }
+        for (int c = 0; c < 4; ++c) {
+          const int e8 = c * 8;
+          st_shared_v4(stg_row + (static_cast<uint32_t>((q * 4 + c) ^ (r & 7)) << 4),
+                       pack_bf16x2(__uint_as_float(o[e8 + 0]) * inv, __uint_as_float(o[e8 + 1]) * inv),
+                       pack_bf16x2(__uint_as_float(o[e8 + 2]) * inv, __uint_as_float(o[e8 + 3]) * inv),
+                       pack_bf16x2(__uint_as_float(o[e8 + 4]) * inv, __uint_as_float(o[e8 + 5]) * inv),
+                       pack_bf16x2(__uint_as_float(o[e8 + 6]) * inv, __uint_as_float(o[e8 + 7]) * inv));
         }
       }
-      if (row_ok && ATTN_CHECK(a, span_ok(lse_out - a.lse, 1, (int64_t)a.B * a.Hq * a.Sq), 0x7906))
-        *lse_out = (l > 0.f) ? (m + __log2f(l)) * kLn2f : -INFINITY;
-      if (a.max_logit && ATTN_CHECK(a, span_ok((int64_t)w.b * a.Hq + w.h, 1, (int64_t)a.B * a.Hq),
-                                    0x7907))
-        warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + w.h, m);
+      // every row of the tile staged: one thread stores both boxes (rows past
+      // the batch row's end are clipped by the map)
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->stg_full);
+      bool sok = true;
+      if (tid == 128) {
+        sok = mbar_wait(&bars->stg_full, it & 1);
+        if (sok) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            if (ATTN_CHECK(a, tma_box_ok(c * 64, 64, a.d_v, 2, w.h, a.Hq, w.t * kTile, kTile, a.Sq,
+                                         true) && w.b >= 0 && w.b < a.B, 0x7905))
+              tma_store_4d(&a.tm_o, sm + L::kOOff + c * 16384, c * 64, w.h, w.t * kTile, w.b);
+          bulk_commit_group();
+        }
+      }
+      if (!(ok = __all_sync(0xffffffffu, sok))) break;
+      if (hf == 0) {
+        if (row_ok &&
+            ATTN_CHECK(a, span_ok(lse_out - a.lse, 1, (int64_t)a.B * a.Hq * a.Sq), 0x7906))
+          *lse_out = (l > 0.f) ? (m + __log2f(l)) * kLn2f : -INFINITY;
+        if (a.max_logit && ATTN_CHECK(a, span_ok((int64_t)w.b * a.Hq + w.h, 1, (int64_t)a.B * a.Hq),
+                                      0x7907))
+          warp_max_logit(a.max_logit + (int64_t)w.b * a.Hq + w.h, m);
+      }
       tc_fence_before();
       mbar_arrive(&bars->o_empty);
+      if (lane == 0 && warp == 4) ATTN_TL(42, it);
       ++it;
     }
     if (!ok) {
-      if (lane == 0) report_timeout(a, 0x930 + (warp & 3));
+      if (lane == 0) report_timeout(a, 0x930 + (warp - 4));
       *abort_flag = 1;
     }
+    if (tid == 128) bulk_wait_all();  // the last O store has read shared memory and landed
   }
   tc_fence_before();
   __syncthreads();
@@ -492,7 +599,19 @@ cudaError_t launch_fwd_fp8(const KernelArgs& a, int nsm, cudaStream_t st) {
   const int items = a.B * a.n_qt * a.Hq;
   const int grid = items < nsm ? items : nsm;
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(fwd_fp8_kernel, dim3(grid), dim3(256), L::kAlloc, st, a);
+  return launch_pdl(fwd_fp8_kernel, dim3(grid), dim3(384), L::kAlloc, st, a);
 }
 
 }  // namespace attn
+
+#ifdef ATTN_TIMELINE
+// Debug builds only: timeline of this translation unit's kernels.
+extern "C" int attn_debug_timeline_f8(unsigned long long* out, int cap) {
+  cudaDeviceSynchronize();
+  const int n = cap < attn::kTimelineCap ? cap : attn::kTimelineCap;
+  cudaMemcpyFromSymbol(out, attn::g_timeline, sizeof(unsigned long long) * n);
+  static unsigned long long zeros[attn::kTimelineCap];
+  cudaMemcpyToSymbol(attn::g_timeline, zeros, sizeof(zeros));
+  return n;
+}
+#endif
