@@ -191,6 +191,24 @@ def test_backward_reads_no_stale_workspace(dq_mode, bias_shape, d_qk):
     check_backward(case, ref, g, db)
 
 
+@pytest.mark.parametrize("dq_mode,d_qk", [("deterministic", 192), ("atomic", 128),
+                                         ("deterministic", 128)])
+def test_bias_rows_not_16_byte_aligned(dq_mode, d_qk):
+    """A key count that is not a multiple of 8 leaves bias rows off 16-byte
+    boundaries: the bias tile and row loads take their element-wise paths."""
+    from gpu_util import DevCase, check_backward, check_forward
+
+    case = I.synth("xu", B=2, Sq=300, Skv=517, Hq=2, Hkv=2, d_qk=d_qk, d_v=128,
+                   layout="HD_HD_HD", fmt="THD_SEGMENTS", causal=False, seed=34, seg=(60, 200),
+                   kv_seg=(60, 300), bias_shape=(1, 2, 300, 517))
+    ref = _ref(case)
+    d = DevCase(case, dq_mode=dq_mode)
+    o, lse = d.forward()
+    check_forward(case, ref, o, lse)
+    g, db = d.backward()
+    check_backward(case, ref, g, db)
+
+
 def test_deterministic_mode_bit_reproducible():
     from gpu_util import DevCase
 
