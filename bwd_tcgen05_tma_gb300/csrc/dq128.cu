@@ -388,14 +388,25 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
           const uint32_t m32 = static_cast<uint32_t>(vbits >> (q * 32));
           none[q] = __all_sync(0xffffffffu, m32 == 0u);
           const bool all = __all_sync(0xffffffffu, m32 == 0xffffffffu);
+          // P stays in registers, so the S buffer goes back to the MMA warp
+          // once the second chunk of S is loaded: S(j+1) does not wait for the
+          // exponentials of that chunk
           if (none[q]) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) pp[q * 16 + e] = 0u;
+            if (q == 1) {
+              tc_fence_before();
+              mbar_arrive(&bars->s_free);
+            }
             continue;
           }
           uint32_t u[32];
           tmem_ld32x32b_x32(s_tm + q * 32, u);
           tmem_ld_wait(u);
+          if (q == 1) {
+            tc_fence_before();
+            mbar_arrive(&bars->s_free);
+          }
           float x[32];
           if (HAS_BIAS) {
 #pragma unroll
@@ -427,8 +438,6 @@ __global__ void __launch_bounds__(512, 1) dq128_kernel(const __grid_constant__ K
 #pragma unroll
           for (int e = 0; e < 16; ++e) pp[q * 16 + e] = E::pack(x[2 * e], x[2 * e + 1]);
         }
-        tc_fence_before();
-        mbar_arrive(&bars->s_free);
         // dS = P (dP - D), packed bf16 over this thread's own dP columns
         if (!(ok = mbar_wait_warp(&bars->dp_full, k & 1))) break;
         tc_fence_after();
