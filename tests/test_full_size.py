@@ -140,3 +140,49 @@ def test_full_size_sampled(name, dq_mode):
         e = rel(np.concatenate([x.ravel() for x in got[key]]),
                 np.concatenate([x.ravel() for x in ref[key]]))
         assert e <= tol[key], f"{name} {dq_mode}: {key} rel err {e}"
+
+
+def test_full_size_fp8_forward_sampled():
+    """The E4M3 forward on the full packed THD GQA workload (E4M3 codes of its
+    inputs, descale factors 1), as the bench runs it, against the oracle's
+    E4M3 forward on sampled query rows of every head.  A row's O and LSE
+    depend only on that row (P is quantised against the row's own final
+    maximum), so the oracle run on the sampled rows alone is exact."""
+    import bench
+    from conftest import oracle_mask, oracle_metadata
+    from oracle import attn_ref as R
+
+    case = I.workload("thd_gqa")
+    prob = bench.Problem(case, "deterministic")
+    f8 = bench.Fp8Forward(case, prob)
+    f8.fwd()
+    f8.check_status()
+    torch.cuda.synchronize()
+
+    B, Sq, Skv, Hq, Hkv = case.B, case.Sq, case.Skv, case.Hq, case.Hkv
+    vals = {key: I.e4m3_value(I.e4m3_codes(x)) for key, x in case.buffers.items()}
+    q8, k8, v8 = R.unpack_layout(case.layout, vals, B, Sq, Skv, Hq, Hkv, case.d_qk, case.d_v)
+    qi, qp, ki, kp = oracle_metadata(case)
+    o_dev = f8.o.view(B, Sq, Hq, case.d_v)
+    rng = np.random.default_rng(11)
+    got = {"o": [], "lse": []}
+    ref = {"o": [], "lse": []}
+    for b in sorted({0, B - 1}):
+        rows = sample_query_rows(qi[b], rng)
+        ro, rl = R.attention_forward_fp8(q8[b:b + 1, rows], k8[b:b + 1], v8[b:b + 1], 1.0, 1.0,
+                                         1.0, qi[b:b + 1, rows], qp[b:b + 1, rows], ki[b:b + 1],
+                                         kp[b:b + 1], oracle_mask(case), case.scale)
+        go = o_dev[b, rows].float().cpu().numpy()        # [rows, Hq, d_v]
+        gl = f8.lse[b][:, rows].cpu().numpy()            # [Hq, rows]
+        fin = np.isfinite(rl[0])                         # [Hq, rows]
+        assert np.array_equal(np.isfinite(gl), fin), "LSE finiteness"
+        fin_o = fin.T                                    # [rows, Hq]
+        assert np.all(go[~fin_o] == 0.0), "rows without keys give O = 0"
+        got["o"].append(go[fin_o])
+        ref["o"].append(ro[0][fin_o])
+        got["lse"].append(gl[fin])
+        ref["lse"].append(rl[0][fin])
+    for key, tol in (("o", TOL_O), ("lse", TOL_LSE)):
+        e = rel(np.concatenate([x.ravel() for x in got[key]]),
+                np.concatenate([x.ravel() for x in ref[key]]))
+        assert e <= tol, f"E4M3 forward: {key} rel err {e}"

@@ -157,3 +157,35 @@ def test_planted_mistakes_are_caught():
     np.testing.assert_allclose(o[0, 0, 0], want, rtol=1e-14)
     p = np.array([1.0, 1.3 / 256])
     assert not np.allclose(R.e4m3_round(p) @ v[0, :, 0] / l, want, rtol=1e-6)  # no 256 scale
+
+
+def test_fp8_forward_rows_are_independent():
+    """The full-size GPU test runs the E4M3 oracle on sampled query rows only:
+    a row's O and LSE depend on that row alone (P is quantised against the
+    row's own maximum), so the oracle on a subset of rows gives the full run's
+    values for them, up to float64 summation order."""
+    import sys
+    import os
+
+    sys.path.insert(0, os.path.dirname(__file__))
+    from conftest import oracle_mask, oracle_metadata
+
+    from bwd_tcgen05_tma_gb300 import inputs as I
+
+    case = I.synth("rows", B=2, Sq=300, Skv=300, Hq=4, Hkv=2, d_qk=128, d_v=128, layout="3HD",
+                   fmt="THD_SEGMENTS", causal=True, seed=5, seg=(30, 160), pad_frac=0.05)
+    vals = {k: I.e4m3_value(I.e4m3_codes(x)) for k, x in case.buffers.items()}
+    q8, k8, v8 = R.unpack_layout(case.layout, vals, case.B, case.Sq, case.Skv, case.Hq,
+                                 case.Hkv, 128, 128)
+    qi, qp, ki, kp = oracle_metadata(case)
+    fo, fl = R.attention_forward_fp8(q8, k8, v8, 1.0, 1.0, 1.0, qi, qp, ki, kp,
+                                     oracle_mask(case), case.scale)
+    rows = [0, 7, 61, 150, 299]
+    for b in range(case.B):
+        ro, rl = R.attention_forward_fp8(q8[b:b + 1, rows], k8[b:b + 1], v8[b:b + 1], 1.0, 1.0,
+                                         1.0, qi[b:b + 1, rows], qp[b:b + 1, rows], ki[b:b + 1],
+                                         kp[b:b + 1], oracle_mask(case), case.scale)
+        np.testing.assert_allclose(ro[0], fo[b, rows], rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(np.isfinite(rl[0]), np.isfinite(fl[b][:, rows]))
+        fin = np.isfinite(rl[0])
+        np.testing.assert_allclose(rl[0][fin], fl[b][:, rows][fin], rtol=0, atol=1e-12)
