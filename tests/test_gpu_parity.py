@@ -69,6 +69,22 @@ def test_forward_matches_oracle(name, force_general):
         assert d.fwd_stats.path == 1
 
 
+@pytest.mark.parametrize("force_general", [False, True])
+def test_forward_many_items_per_cta(force_general):
+    """More (query tile, head pair) items than CTAs, so each CTA runs several
+    in a row, and key ranges whose last tile is used only in its first half
+    (those items take an odd number of 64-key steps)."""
+    from gpu_util import DevCase, check_forward
+
+    case = I.synth("thd_many", B=2, Sq=2048, Skv=2048, Hq=32, Hkv=8, d_qk=128, d_v=128,
+                   layout="3HD", fmt="THD_SEGMENTS", causal=True, seed=21, seg=(40, 500),
+                   pad_frac=0.05)
+    ref = _ref(case)
+    d = DevCase(case, force_general=force_general)
+    o, lse = d.forward()
+    check_forward(case, ref, o, lse)
+
+
 def test_fast_path_taken_for_matching_metadata():
     from gpu_util import DevCase
 
