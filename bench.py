@@ -354,12 +354,9 @@ def launches_per_step(case):
     """Kernels of this library launched per step (memsets excluded): the
     metadata kernel before the forward (one cooperative launch; the backward
     reuses its results); the forward; preprocess, dK/dV pass and dQ pass or
-    conversion; the broadcast dBias conversion when one is needed."""
+    dQ conversion.  A broadcast dBias is finished inside the dK/dV pass."""
     meta = 1
     bwd = 3
-    if case.bias is not None and ((case.bias.shape[0] == 1 and case.B > 1) or
-                                  (case.bias.shape[1] == 1 and case.Hq > 1)):
-        bwd += 1
     return meta + 1 + bwd
 
 
