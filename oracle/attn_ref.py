@@ -304,8 +304,8 @@ def attention_forward_fp8(q8, k8, v8, descale_q, descale_k, descale_v, id_q, pos
                           pos_kv, causal, scale, row_block=256):
     """O [B,Sq,Hq,d_v] and LSE [B,Hq,Sq] of the FP8 forward.
 
-    The pages define attention in bf16 only; SURVEY's next step is an FP8
-    forward of the same computation.  Reading taken (the plainest one that
+    The pages define attention in bf16 only; this is an FP8 forward of the
+    same computation, the adjacent precision.  Reading taken (the plainest one that
     keeps every product in the 8-bit format):
 
       inputs      q8, k8, v8 hold E4M3 values; the tensors they stand for are
