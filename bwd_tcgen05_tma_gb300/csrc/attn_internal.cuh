@@ -211,7 +211,8 @@ struct ChunkInfo {
   int32_t min_pos;  // over tokens with nonzero id
   int32_t max_pos;
   int32_t uniform;  // 1: all 64 tokens exist and carry the same nonzero id
-  int32_t pad[3];
+  int32_t consec;   // 1: uniform, and token k of the chunk sits at position min_pos + k
+  int32_t pad[2];
 };
 
 // Everything a kernel needs; passed by value as a __grid_constant__ parameter
@@ -369,6 +370,78 @@ __device__ __forceinline__ int2 band_queries_of_key(const KernelArgs& a, int j, 
 // Validity of the 128 keys [k0, k0 + 128) of batch row b for one query row, as
 // two 64-bit masks.  Fast path: the row's key range [rlo, rhi).  General path:
 // same nonzero segment id and a key position inside the row's band.
+// Validity bits of the 64 tokens of one chunk for a token of the other side
+// with nonzero segment id `id` whose band admits the positions [p.x, p.y],
+// from the chunk's summary alone.  False when the summary does not decide
+// it; the caller then compares token by token.
+__device__ __forceinline__ bool chunk_bits(const ChunkInfo& c, int id, int2 p, uint64_t& bits) {
+  if (c.max_id == 0 || id < c.min_id || id > c.max_id || c.max_pos < p.x || c.min_pos > p.y) {
+    bits = 0ull;  // no token carries the id, or none sits inside the band
+    return true;
+  }
+  if (!c.uniform) return false;
+  // every token carries the id (min_id <= id <= max_id == min_id)
+  if (c.min_pos >= p.x && c.max_pos <= p.y) {
+    bits = ~0ull;
+    return true;
+  }
+  if (!c.consec) return false;
+  // token k at position min_pos + k: the band keeps k in [p.x - min_pos, p.y - min_pos]
+  const int lo = p.x <= c.min_pos ? 0 : p.x - c.min_pos;
+  const int hi = p.y >= c.max_pos ? 64 : p.y - c.min_pos + 1;
+  bits = range_bits64(lo, hi);
+  return true;
+}
+
+// General path of kv_valid_bits, out of line: the fast path's loops keep
+// their registers and code to themselves.
+static __device__ __noinline__ ulonglong2 kv_valid_bits_general(const KernelArgs& a, int b, int k0,
+                                                         int my_id, int my_pos) {
+  uint64_t vb[2] = {0ull, 0ull};
+  if (my_id == 0) return make_ulonglong2(0ull, 0ull);
+  const int2 kp = band_key_pos(a, my_pos);
+  const int nkc = (a.Skv + kChunk - 1) / kChunk;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {  // the tile's two 64-key halves
+    const int kh = k0 + hh * 64;
+    if (kh >= a.Skv) continue;
+    if ((kh % kChunk) == 0 && chunk_bits(a.kv_chunk[b * nkc + kh / kChunk], my_id, kp, vb[hh]))
+      continue;
+    const int32_t* kid = a.kv_id + (int64_t)b * a.Skv + kh;
+    const int32_t* kpos = a.kv_pos + (int64_t)b * a.Skv + kh;
+    const int nv = min(64, a.Skv - kh);
+    const bool vec = ((reinterpret_cast<uintptr_t>(kid) & 15u) == 0);
+    uint64_t v64 = 0ull;
+#pragma unroll
+    for (int c = 0; c < 64; c += 4) {
+      int ids[4], pss[4];
+      if (vec && c + 4 <= nv) {
+        const int4 t1 = __ldg(reinterpret_cast<const int4*>(kid + c));
+        const int4 t2 = __ldg(reinterpret_cast<const int4*>(kpos + c));
+        ids[0] = t1.x; ids[1] = t1.y; ids[2] = t1.z; ids[3] = t1.w;
+        pss[0] = t2.x; pss[1] = t2.y; pss[2] = t2.z; pss[3] = t2.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ids[e] = (c + e < nv) ? __ldg(kid + c + e) : -1;
+          pss[e] = (c + e < nv) ? __ldg(kpos + c + e) : 0;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool v = (ids[e] == my_id) & (pss[e] >= kp.x) & (pss[e] <= kp.y);
+        v64 |= static_cast<uint64_t>(v) << (c + e);
+      }
+    }
+    vb[hh] = v64;
+  }
+  return make_ulonglong2(vb[0], vb[1]);
+}
+
+// Validity of the 128 keys [k0, k0 + 128) of batch row b for one query row,
+// as two 64-bit words.  Fast path: the row's key range [rlo, rhi).  General
+// path: same nonzero segment id and a key position inside the row's band,
+// from the key chunks' summaries where they decide it.
 __device__ __forceinline__ void kv_valid_bits(const KernelArgs& a, bool general, int b, int k0,
                                               int rlo, int rhi, int my_id, int my_pos,
                                               uint64_t (&vb)[2]) {
@@ -377,44 +450,9 @@ __device__ __forceinline__ void kv_valid_bits(const KernelArgs& a, bool general,
     vb[1] = range_bits64(rlo - k0 - 64, rhi - k0 - 64);
     return;
   }
-  vb[0] = vb[1] = 0ull;
-  if (my_id == 0) return;
-  const int2 kp = band_key_pos(a, my_pos);
-  const int nkc = (a.Skv + kChunk - 1) / kChunk;
-  if (k0 + kTile <= a.Skv && (k0 % kChunk) == 0) {
-    const ChunkInfo c0 = a.kv_chunk[b * nkc + k0 / kChunk];
-    const ChunkInfo c1 = a.kv_chunk[b * nkc + k0 / kChunk + 1];
-    if (c0.uniform && c1.uniform && c0.min_id == my_id && c1.min_id == my_id &&
-        min(c0.min_pos, c1.min_pos) >= kp.x && max(c0.max_pos, c1.max_pos) <= kp.y) {
-      vb[0] = vb[1] = ~0ull;
-      return;
-    }
-  }
-  const int32_t* kid = a.kv_id + (int64_t)b * a.Skv + k0;
-  const int32_t* kpos = a.kv_pos + (int64_t)b * a.Skv + k0;
-  const int nv = min(kTile, a.Skv - k0);
-  const bool vec = ((reinterpret_cast<uintptr_t>(kid) & 15u) == 0);
-#pragma unroll
-  for (int c = 0; c < kTile; c += 4) {
-    int ids[4], pss[4];
-    if (vec && c + 4 <= nv) {
-      const int4 t1 = __ldg(reinterpret_cast<const int4*>(kid + c));
-      const int4 t2 = __ldg(reinterpret_cast<const int4*>(kpos + c));
-      ids[0] = t1.x; ids[1] = t1.y; ids[2] = t1.z; ids[3] = t1.w;
-      pss[0] = t2.x; pss[1] = t2.y; pss[2] = t2.z; pss[3] = t2.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        ids[e] = (c + e < nv) ? __ldg(kid + c + e) : -1;
-        pss[e] = (c + e < nv) ? __ldg(kpos + c + e) : 0;
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const bool v = (ids[e] == my_id) & (pss[e] >= kp.x) & (pss[e] <= kp.y);
-      vb[(c + e) >> 6] |= static_cast<uint64_t>(v) << ((c + e) & 63);
-    }
-  }
+  const ulonglong2 r = kv_valid_bits_general(a, b, k0, my_id, my_pos);
+  vb[0] = r.x;
+  vb[1] = r.y;
 }
 
 __device__ __forceinline__ bool path_general(const KernelArgs& a) {

@@ -400,15 +400,10 @@ __global__ void __launch_bounds__(512, 1) dkdv128_kernel(const __grid_constant__
                 vbits = row_ok ? range_bits64(qlo - qh, qhi - qh) : 0ull;
               } else {
                 vbits = 0ull;
-                bool full = false;
-                if (row_ok && my_id != 0 && qh + 64 <= a.Sq && (qh % kChunk) == 0) {
-                  const ChunkInfo ci = a.q_chunk[b * nqc + qh / kChunk];
-                  full = ci.uniform && ci.min_id == my_id && ci.min_pos >= my_qp.x &&
-                         ci.max_pos <= my_qp.y;
-                }
-                if (full) {
-                  vbits = ~0ull;
-                } else if (row_ok && my_id != 0) {
+                bool known = false;  // decided by the query chunk's summary
+                if (row_ok && my_id != 0 && qh < a.Sq && (qh % kChunk) == 0)
+                  known = chunk_bits(a.q_chunk[b * nqc + qh / kChunk], my_id, my_qp, vbits);
+                if (!known && row_ok && my_id != 0) {
                   // per-token compare; every lane of the warp reads the same query row
                   const int32_t* qid = a.q_id + (int64_t)b * a.Sq;
                   const int32_t* qps = a.q_pos + (int64_t)b * a.Sq;

@@ -59,10 +59,10 @@ __device__ __forceinline__ uint64_t kv_bits64(const KernelArgs& a, bool general,
   if (!general) return range_bits64(rlo - kh, rhi - kh);
   if (my_id == 0 || kh >= a.Skv) return 0ull;
   const int2 kp = band_key_pos(a, my_pos);
-  if (kh + kChunk <= a.Skv && (kh % kChunk) == 0) {
+  if ((kh % kChunk) == 0) {
     const int nkc = (a.Skv + kChunk - 1) / kChunk;
-    const ChunkInfo c = a.kv_chunk[b * nkc + kh / kChunk];
-    if (c.uniform && c.min_id == my_id && c.min_pos >= kp.x && c.max_pos <= kp.y) return ~0ull;
+    uint64_t bits;
+    if (chunk_bits(a.kv_chunk[b * nkc + kh / kChunk], my_id, kp, bits)) return bits;
   }
   // every lane of the warp reads the same keys
   const int32_t* kid = a.kv_id + (int64_t)b * a.Skv + kh;

@@ -289,7 +289,15 @@ __device__ ChunkInfo chunk_info_warp(const int32_t* id, const int32_t* pos, int 
   ci.min_pos = pmn;
   ci.max_pos = pmx;
   ci.uniform = (!has0 && mx != 0 && mn == mx) ? 1 : 0;
-  ci.pad[0] = ci.pad[1] = ci.pad[2] = 0;
+  // consecutive positions: token c0 + k at min_pos + k (read only when uniform,
+  // so every token exists)
+  bool cons = true;
+  if (ci.uniform) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) cons &= pos[c0 + lane + 32 * k] == pmn + lane + 32 * k;
+  }
+  ci.consec = (__all_sync(0xffffffffu, cons) && ci.uniform) ? 1 : 0;
+  ci.pad[0] = ci.pad[1] = 0;
   return ci;
 }
 
