@@ -155,6 +155,39 @@ def test_backward_matches_oracle(name, dq_mode):
     assert d.bwd_stats.dq_mode == expect
 
 
+@pytest.mark.parametrize("shape,window", [("strided", None), ("strided", (90, None)),
+                                          ("shifted", None), ("shifted", (90, None))])
+def test_general_path_position_shapes(shape, window):
+    """Positions that are not offsets from 0 (the general path, reason 6):
+    strided (2 x offset, so no chunk has consecutive positions and every chunk
+    the band cuts is tested token by token) or shifted by 5 (consecutive, so
+    chunk summaries decide the cut chunks), with a causal mask and a causal
+    window in position units."""
+    from gpu_util import DevCase, check_backward, check_forward
+
+    case = I.synth("pos", B=2, Sq=1000, Skv=1000, Hq=4, Hkv=2, d_qk=128, d_v=128, layout="3HD",
+                   fmt="THD_SEGMENTS", causal=True, seed=23, seg=(40, 400), pad_frac=0.05)
+    ids = case.q_ids
+    starts = np.concatenate([np.ones((ids.shape[0], 1), bool), ids[:, 1:] != ids[:, :-1]], axis=1)
+    run = np.cumsum(starts, axis=1)
+    offs = np.zeros_like(ids)
+    for b in range(ids.shape[0]):
+        first = np.maximum.accumulate(np.where(starts[b], np.arange(ids.shape[1]), 0))
+        offs[b] = np.arange(ids.shape[1]) - first
+    pos = 2 * offs + (run % 3) if shape == "strided" else offs + 5
+    pos = np.where(ids != 0, pos, 0).astype(np.int32)
+    case.q_pos = pos
+    case.kv_pos = pos.copy()
+    case.window = window
+    ref = _ref(case)
+    d = DevCase(case)
+    o, lse = d.forward()
+    assert d.fwd_stats.path == 1 and d.fwd_stats.reason == 6
+    check_forward(case, ref, o, lse)
+    g, db = d.backward()
+    check_backward(case, ref, g, db)
+
+
 @pytest.mark.parametrize("name", ["thd_gqa_3hd", "cross_bias_192", "tiny"])
 def test_backward_general_path(name):
     from gpu_util import DevCase, check_backward
