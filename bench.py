@@ -55,6 +55,8 @@ def parse():
                          "path applies, to measure what not taking it costs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the other named workloads measured after the headline one")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the deterministic-mode and per-pass side measurements")
     return ap.parse_args()
@@ -170,7 +172,7 @@ class ClockSampler:
 class Problem:
     """Device buffers of one workload plus the C-ABI parameter block."""
 
-    def __init__(self, case, dq_mode, force_general=False):
+    def __init__(self, case, dq_mode, force_general=False, pin=True):
         import numpy as np
         import torch
 
@@ -185,15 +187,16 @@ class Problem:
         def i32(x):
             return None if x is None else torch.from_numpy(np.ascontiguousarray(x, np.int32))
 
-        # host copies (pinned) and device copies of every input
-        self.host_in = {k: bf(v).pin_memory() for k, v in c.buffers.items()}
-        self.host_in["do"] = bf(c.do.reshape(c.B * c.Sq, c.Hq, c.d_v)).pin_memory()
+        # host copies (pinned for the end-to-end steps) and device copies of every input
+        pm = (lambda t: t.pin_memory()) if pin else (lambda t: t)
+        self.host_in = {k: pm(bf(v)) for k, v in c.buffers.items()}
+        self.host_in["do"] = pm(bf(c.do.reshape(c.B * c.Sq, c.Hq, c.d_v)))
         if c.bias is not None:
-            self.host_in["bias"] = bf(c.bias).pin_memory()
+            self.host_in["bias"] = pm(bf(c.bias))
         for k in ("q_ids", "q_pos", "kv_ids", "kv_pos"):
             t = i32(getattr(c, k))
             if t is not None:
-                self.host_in[k] = t.pin_memory()
+                self.host_in[k] = pm(t)
         self.dev = {k: v.cuda() for k, v in self.host_in.items()}
         d = self.dev
         if c.layout == "3HD":
@@ -523,6 +526,48 @@ def timed(fn, steps, stream, barrier):
     return e0.elapsed_time(e1) / steps
 
 
+# the other named workloads, measured after the headline one in the same run
+# (timed steps each: about half a second of work or less)
+OTHER_WORKLOADS = (("bshd", 200), ("cross_bias", 20), ("long_kv", 10))
+
+
+def other_workloads(args, stream, barrier, max_over_ranks, world, peaks):
+    """fwd+bwd TFLOP/s of every other named workload and of the headline one
+    with the general masking path forced, deterministic dQ, each against the
+    measured peak for its timed region's length (burst up to 0.5 s)."""
+    import gc
+
+    import torch
+
+    from bwd_tcgen05_tma_gb300 import flops as F
+    from bwd_tcgen05_tma_gb300 import inputs as I
+
+    out = {}
+    runs = [(args.workload + "_general_path", args.workload, True, 100)]
+    runs += [(n, n, False, k) for n, k in OTHER_WORKLOADS]
+    for key, name, force_general, steps in runs:
+        try:
+            case = I.workload(name)
+            f_fwd, f_bwd, _ = F.attention_flops(case)
+            p = Problem(case, "deterministic", force_general, pin=False)
+            for _ in range(3):
+                p.step()
+            t = max_over_ranks(timed(p.step, steps, stream, barrier))
+            st = p.check_status()
+            v = aggregate_tflops(world, f_fwd + f_bwd, t)
+            pk = ("bf16_tflops_sustained" if t * steps * 1e-3 > 0.5 and
+                  "bf16_tflops_sustained" in peaks else "bf16_tflops")
+            out[key] = {"workload": WORKLOAD_DESC.get(name, name), "value": v, "unit": "TFLOP/s",
+                        "ms_per_step": t, "steps": steps, "pct_of_peak": v / float(peaks[pk]),
+                        "peak_basis": pk, "path": "fast" if st.path == 0 else "general"}
+            del p, case
+        except Exception as e:  # a failure here must not cost the headline line
+            out[key] = {"error": f"{type(e).__name__}: {e}"[:200]}
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     from bwd_tcgen05_tma_gb300 import inputs as I
@@ -697,6 +742,11 @@ def main():
         line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s",
                                 "cores": cpu_cores(), "kind": "oracle", "sample": desc,
                                 "seconds": dt}
+    if (not args.no_extras and not args.no_other_workloads and world == 1 and
+            args.workload == "thd_gqa" and not args.force_general):
+        del prob
+        line["other_workloads"] = other_workloads(args, stream, barrier, max_over_ranks, world,
+                                                  peaks)
     if rank == 0:
         print(json.dumps(line), flush=True)
     rk.close()
