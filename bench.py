@@ -80,7 +80,7 @@ KERNEL_SOURCES = {
     "bwd_pre": ("bwd.cu",),
     "fwd_fp8": ("fwd_fp8.cu",),
 }
-COMMON_SOURCES = ("attn_internal.cuh", "sm103_ptx.cuh", "debug_checks.h")
+COMMON_SOURCES = ("attn_internal.cuh", "chunk_mask.h", "sm103_ptx.cuh", "debug_checks.h")
 
 
 def source_hash(kernel):

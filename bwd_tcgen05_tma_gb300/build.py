@@ -24,7 +24,7 @@ LIB = os.path.join(HERE, "libattn_sm103.so")
 LIB_DEBUG = os.path.join(HERE, "libattn_sm103_debug.so")
 SOURCES = ["api.cu", "meta.cu", "fwd.cu", "bwd.cu", "bwd_bf16.cu", "bwd_f16.cu", "dkdv128.cu",
            "dq128.cu", "fwd2t.cu", "fwd_fp8.cu"]
-HEADERS = ["attn_internal.cuh", "sm103_ptx.cuh", "bwd_passes.cuh", "debug_checks.h",
+HEADERS = ["attn_internal.cuh", "chunk_mask.h", "sm103_ptx.cuh", "bwd_passes.cuh", "debug_checks.h",
            os.path.join("..", "..", "include", "attn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

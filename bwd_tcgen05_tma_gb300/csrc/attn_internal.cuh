@@ -8,6 +8,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "chunk_mask.h"
 #include "debug_checks.h"
 #include "sm103_ptx.cuh"
 
@@ -330,16 +331,7 @@ __device__ __forceinline__ void store16_elems(bf16* dst, const uint32_t (&w)[8],
   }
 }
 
-// Bit c set for lo <= c < hi, c in [0, 64).  Masks are applied with selects on
-// these bits so the element loops stay branch-free.
-__device__ __forceinline__ uint64_t range_bits64(int lo, int hi) {
-  lo = lo < 0 ? 0 : lo;
-  hi = hi > 64 ? 64 : hi;
-  if (hi <= lo) return 0ull;
-  const uint64_t upper = (hi >= 64) ? ~0ull : ((1ull << hi) - 1ull);
-  const uint64_t lower = (lo <= 0) ? 0ull : ((1ull << lo) - 1ull);
-  return upper & ~lower;
-}
+using attn_mask::range_bits64;
 
 __device__ __forceinline__ bool path_general(const KernelArgs& a);
 
@@ -372,25 +364,11 @@ __device__ __forceinline__ int2 band_queries_of_key(const KernelArgs& a, int j, 
 // same nonzero segment id and a key position inside the row's band.
 // Validity bits of the 64 tokens of one chunk for a token of the other side
 // with nonzero segment id `id` whose band admits the positions [p.x, p.y],
-// from the chunk's summary alone.  False when the summary does not decide
-// it; the caller then compares token by token.
+// from the chunk's summary alone (attn_mask::chunk_decide).  False when the
+// summary does not decide it; the caller then compares token by token.
 __device__ __forceinline__ bool chunk_bits(const ChunkInfo& c, int id, int2 p, uint64_t& bits) {
-  if (c.max_id == 0 || id < c.min_id || id > c.max_id || c.max_pos < p.x || c.min_pos > p.y) {
-    bits = 0ull;  // no token carries the id, or none sits inside the band
-    return true;
-  }
-  if (!c.uniform) return false;
-  // every token carries the id (min_id <= id <= max_id == min_id)
-  if (c.min_pos >= p.x && c.max_pos <= p.y) {
-    bits = ~0ull;
-    return true;
-  }
-  if (!c.consec) return false;
-  // token k at position min_pos + k: the band keeps k in [p.x - min_pos, p.y - min_pos]
-  const int lo = p.x <= c.min_pos ? 0 : p.x - c.min_pos;
-  const int hi = p.y >= c.max_pos ? 64 : p.y - c.min_pos + 1;
-  bits = range_bits64(lo, hi);
-  return true;
+  return attn_mask::chunk_decide(c.min_id, c.max_id, c.min_pos, c.max_pos, c.uniform, c.consec,
+                                 id, p.x, p.y, &bits);
 }
 
 // General path of kv_valid_bits, out of line: the fast path's loops keep
